@@ -1,0 +1,370 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 KV-cached decoder step.
+
+Default workload: GPT-2-124M-shaped fp32 decoder, batch 32, 128-token prompts,
+decode positions 128..255 (the teacher-forced 128-step workload), contiguous
+KV cache. One bench step = one batched decode step (every row of the hot path:
+embed, norm+QKV+RoPE/kv_write, paged attention, O+residual, norm+FFN, final
+norm + tied head + argmax), replayed as one CUDA graph. Decode positions cycle
+through the workload's 128 steps, so every 128 bench steps are exactly one pass
+of the workload.
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+sample of the same workload (test infrastructure, never the product path).
+
+Prints one JSON line (rank 0). Multi-GPU: launched by torchrun, one replica per
+rank (the decode batch shards by sequence; no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+BASELINE_METRIC = "decode tok/s at batch B and prefill tok/s; % of GB300 HBM BW / bf16 TC peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic work per unit (decode step)
+# ------------------------------------------------------------------------------------------------
+
+def weight_bytes(s: wl.ModelShape) -> int:
+    """Projection weights read once per step, including the tied head (vocab x d)."""
+    return (s.n_layers * s.layer_params() + s.vocab * s.d_model) * s.elt_bytes
+
+
+def gemv_bytes(s: wl.ModelShape, B: int) -> int:
+    """Projection kernels: weights once, plus activations in (fp32/bf16) and outputs out."""
+    a = s.elt_bytes
+    d, F, qkv, hq = s.d_model, s.d_ff, s.qkv_dim, s.n_heads * s.head_dim
+    per_layer = B * (d * a + qkv * 4)             # qkv: x in, q (fp32) / k,v out
+    per_layer += B * (hq * a + 2 * d * 4)         # o: x in, residual read+write
+    per_layer += B * (d * a + F * a)              # up
+    per_layer += B * (F * a + 2 * d * 4)          # down
+    return weight_bytes(s) + s.n_layers * per_layer + B * d * a
+
+
+def attn_bytes(s: wl.ModelShape, ctx: np.ndarray) -> int:
+    """Decode attention: K and V of every cached position (incl. the new one) once per layer."""
+    kv = int(ctx.sum()) * s.n_kv_heads * s.head_dim * s.elt_bytes * 2 * s.n_layers
+    qo = len(ctx) * s.n_heads * s.head_dim * (4 + s.elt_bytes) * s.n_layers
+    return kv + qo
+
+
+def step_bytes(s: wl.ModelShape, ctx: np.ndarray) -> int:
+    return gemv_bytes(s, len(ctx)) + attn_bytes(s, ctx)
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ------------------------------------------------------------------------------------------------
+
+def oracle_decode_rate(W: wl.Workload, steps: int, warmup: int = 0, n_seq: int = 1, weights=None):
+    """Time the float64 oracle, as it stands, on `steps` decode steps of `n_seq` sequences.
+
+    Prefill is untimed; positions cycle through the workload's decode positions exactly
+    as the GPU bench does. Returns (tok/s, seconds, description).
+    """
+    import oracle
+    w = weights or wl.make_weights(W.model, scale=W.weight_scale)
+    model = oracle.OracleModel(w)
+    prompts = wl.draw_prompts(W.lengths(), W.model.vocab)
+    stream = wl.draw_stream(W.batch, max(W.decode_steps, 1), W.model.vocab)
+    period = max(W.decode_steps, 1)
+    seqs = []
+    for b in range(n_seq):
+        s = oracle.Sequence(model)
+        s.prefill(prompts[b])
+        seqs.append((s, list(s.k), list(s.v), s.length))
+    done = 0
+    t0 = None
+    for i in range(warmup + steps):
+        if i == warmup:
+            t0 = time.perf_counter()
+        j = i % period
+        for b, (s, k0, v0, L0) in enumerate(seqs):
+            if j == 0:
+                s.k, s.v, s.length = list(k0), list(v0), L0
+            s.step(int(stream[j, b]))
+        if i >= warmup:
+            done += n_seq
+    dt = time.perf_counter() - t0
+    desc = (f"float64 NumPy oracle, KV-cached mode, {n_seq} of {W.batch} sequences, {steps} decode steps "
+            f"(positions {int(W.lengths()[0])}..{int(W.lengths()[0]) + period - 1} cycled), prefill untimed")
+    return done / dt, dt, desc
+
+
+def gpu_id_for_smi(local: int) -> str:
+    """nvidia-smi --id of this process's GPU (its UUID when torch reports one)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local)
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, W):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    rate, dt, desc = oracle_decode_rate(W, args.steps, args.warmup, n_seq=1)
+    line = {"impl": "reference", "metric": BASELINE_METRIC, "metric_detail": f"decode tok/s at batch {W.batch}",
+            "value": rate, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": W.name, "batch": W.batch, "prompt_len": int(W.lengths()[0]),
+                       "decode_steps_cycled": W.decode_steps},
+            "cpu_baseline": {"value": rate, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": rate, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+def run_decode_bench(args, W):
+    import torch
+    import torch.distributed as dist
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    s = W.model
+    host_w = wl.make_weights(s, scale=W.weight_scale)
+    period = W.decode_steps
+    run = WorkloadRun(W, host_weights=host_w)
+    B = run.B
+    stream_np = wl.draw_stream(B, period, s.vocab)
+    toks = torch.from_numpy(stream_np).cuda()
+    run.prefill()
+    torch.cuda.synchronize()
+
+    def step(i):
+        run.decode(toks[i % period], i % period)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    launches_per_step = run.dec.last_launch_count()
+
+    # ---- timed region: K graph replays, barrier + synchronize on both sides
+    st = run.stream
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id_for_smi(local)) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record(st)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(st)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = B * args.steps * world
+    value = tokens / (ms / 1000.0)
+    assert run.dec.error_flags() == 0, "device error flags set during the bench"
+
+    # ---- per-kernel durations (CUDA events around every launch, one pass of the workload)
+    run.dec.set_profiling(True)
+    run.dec.kernel_stats(reset=True)
+    for i in range(period):
+        step(i)
+    stats = run.dec.kernel_stats(reset=True)
+    run.dec.set_profiling(False)
+    fam = {}
+    for name, (n, t) in stats.items():
+        f = "gemv" if name.startswith("gemv") else "gemm_tc" if name.startswith("gemm_tc") else \
+            "gemm_simt" if name.startswith("gemm_simt") else name
+        a = fam.setdefault(f, [0, 0.0])
+        a[0] += n
+        a[1] += t
+    dom = max(fam, key=lambda k: fam[k][1])
+    pk, pk_kind = peaks()
+    ctx_steps = np.stack([run.lengths + j + 1 for j in range(period)])          # keys read per step
+    if dom == "gemv":
+        alg = gemv_bytes(s, B) * period
+    elif dom == "attn_decode":
+        alg = sum(attn_bytes(s, c) for c in ctx_steps)
+    else:
+        alg = None
+    dom_ms = fam[dom][1]
+    achieved = alg / (dom_ms / 1000.0) / 1e9 if alg else None
+    roof = {"bound": "hbm", "kernel": dom, "launches": fam[dom][0], "achieved": achieved, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "traffic": None,
+            "peak_source": f"hbm_gbs of {pk_kind}",
+            "alg_bytes_per_launch": (alg / fam[dom][0]) if alg else None,
+            "avg_launch_us": 1000.0 * dom_ms / fam[dom][0]}
+    step_alg = float(np.mean([step_bytes(s, c) for c in ctx_steps]))
+    step_gbs = step_alg / (ms / args.steps / 1000.0) / 1e9
+    kernel_share = {k: round(v[1] / sum(x[1] for x in fam.values()), 4) for k, v in sorted(fam.items())}
+
+    # ---- end to end through the C ABI with host buffers (H2D inputs, D2H ids, every step)
+    n_e2e = min(args.steps, 2 * period)
+    tok_h = [np.ascontiguousarray(stream_np[j]) for j in range(period)]
+    pos_h = [np.ascontiguousarray((run.lengths + j).astype(np.int32)) for j in range(period)]
+    tables_h = None if W.contiguous_kv else np.ascontiguousarray(run.tables_np, dtype=np.int32)
+    ids_h = np.zeros(B, np.int32)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        j = i % period
+        run.dec.decode_step_host(tok_h[j], pos_h[j], tables_h, ids_h)
+    e2e_s = time.perf_counter() - t0
+    h2d = B * 4 * 2 + (0 if tables_h is None else tables_h.nbytes)
+    e2e = {"value": B * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * 4,
+           "steps": n_e2e, "api": "llm_decode_step_host"}
+
+    line = {"metric": BASELINE_METRIC, "metric_detail": f"decode tok/s at batch {B}", "value": value,
+            "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
+            "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]),
+                       "decode_positions": f"{int(run.lengths.min())}..{int(run.lengths.max()) + period - 1} cycled",
+                       "kv": "contiguous" if W.contiguous_kv else "paged16",
+                       "l2": "inputs larger than L2: %.0f MB weights + %.0f MB KV per step" % (
+                           weight_bytes(s) / 1e6, attn_bytes(s, ctx_steps[-1]) / 1e6),
+                       "graph": "one CUDA graph per step"},
+            "roofline": roof,
+            "step_roofline": {"alg_bytes_per_step": step_alg, "achieved_gbs": step_gbs,
+                              "frac": step_gbs / pk["hbm_gbs"], "peak_source": f"hbm_gbs of {pk_kind}"},
+            "kernel_share": kernel_share,
+            "gpu_launches": launches_per_step * args.steps,
+            "launches_per_step": launches_per_step,
+            "e2e": e2e,
+            "clocks": clk.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del run
+        rate, dt, desc = oracle_decode_rate(W, args.cpu_steps, 0, n_seq=1, weights=host_w)
+        line["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1280)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=wl.W_GPT2_F32_B32.name, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-steps", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    W = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, W)
+    if W.mode == "prefill" or W.decode_steps == 0:
+        ap.error("prefill workloads: see --workload; this bench times decode steps")
+    return run_decode_bench(args, W)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

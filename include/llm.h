@@ -1,0 +1,205 @@
+/*
+ * llm.h — C ABI of the GB300 KV-cached decoder step (libllm.so).
+ *
+ * One library, one GPU. It computes the forward step of a decoder-only
+ * transformer in two variants:
+ *   - GPT-2: learned position embeddings, LayerNorm, multi-head causal attention,
+ *     GELU-tanh FFN with the tanh argument clamped to +-15, tied LM head
+ *     ("bare-metal-llm", sections "Picking the model", "What got built", "The bug
+ *     worth telling"; "batch_forge", GELU overflow paragraph);
+ *   - Llama: RMSNorm, RoPE, grouped-query attention, SwiGLU FFN, tied embeddings,
+ *     no biases ("rvllm-metal", section "What the kernels do").
+ * Prefill and batched single-token decode both end in a greedy argmax on the
+ * GPU, so one int32 per sequence leaves the device ("rvllm-metal", "What the
+ * kernels do", last paragraph). The KV cache is paged with 16-token blocks found
+ * through a per-sequence block table ("rvllm-metal", "What the kernels do":
+ * kv_write into the paged cache, division and modulo of the position).
+ *
+ * Conventions for every call:
+ *   - Pointer arguments are DEVICE pointers unless the argument says HOST.
+ *   - The caller owns weights, inputs and outputs; the library never frees them
+ *     and keeps weight pointers (no copy) from llm_create to llm_destroy.
+ *   - The handle owns its KV pool and workspace, allocated in llm_create.
+ *   - Work is enqueued on the handle's stream and returns before it runs (except
+ *     where a call says it synchronises). A handle must not be used from two
+ *     host threads at once.
+ *   - Every call checks its arguments on the host before any launch and returns
+ *     a status; nothing is launched when the status is not LLM_OK. Errors that
+ *     only the device can see (a token id, position or block id out of range,
+ *     a NaN logit) set bits in the handle's device error word, skip the bad
+ *     access and never trap; read them with llm_get_error_flags.
+ *   - llm_last_error() gives a one-line message for the last non-OK status
+ *     returned on the calling thread.
+ */
+#ifndef LLM_H
+#define LLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LLM_OK = 0,
+  LLM_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, inconsistent config */
+  LLM_ERR_OUT_OF_RANGE = 2,  /* a size beyond what the handle was created for */
+  LLM_ERR_NO_DEVICE = 3,     /* no CUDA device, or not a compute capability 10.3 device */
+  LLM_ERR_UNSUPPORTED = 4,   /* a config this build does not implement (e.g. head_dim != 64) */
+  LLM_ERR_OOM = 5,           /* device allocation failed in llm_create */
+  LLM_ERR_CUDA = 6,          /* a CUDA runtime call failed */
+  LLM_ERR_DEVICE_FLAG = 7    /* llm_get_error_flags found a device-side error bit set */
+} llm_status;
+
+enum { LLM_ARCH_GPT2 = 0, LLM_ARCH_LLAMA = 1 };
+enum { LLM_DTYPE_F32 = 0, LLM_DTYPE_BF16 = 1 };
+
+/* Bits of the device error word (llm_get_error_flags). */
+#define LLM_FLAG_BAD_TOKEN     0x01u  /* token id outside [0, vocab) */
+#define LLM_FLAG_BAD_POSITION  0x02u  /* position outside [0, n_ctx) or beyond the block table */
+#define LLM_FLAG_BAD_BLOCK     0x04u  /* block-table entry outside [0, num_kv_blocks) */
+#define LLM_FLAG_NAN_LOGIT     0x08u  /* a logit was NaN (argmax then returns the first NaN index) */
+#define LLM_FLAG_WAIT_TIMEOUT  0x10u  /* a bounded device-side wait gave up */
+
+typedef struct {
+  int arch;               /* LLM_ARCH_GPT2 or LLM_ARCH_LLAMA */
+  int dtype;              /* LLM_DTYPE_F32 or LLM_DTYPE_BF16: weights, KV cache and GEMM operands */
+  int n_layers;
+  int d_model;
+  int n_heads;            /* query heads */
+  int n_kv_heads;         /* KV heads; n_heads % n_kv_heads == 0 (GPT-2: equal) */
+  int head_dim;           /* must be 64 */
+  int d_ff;               /* FFN width F */
+  int vocab;
+  int n_ctx;              /* GPT-2: rows of the position table; Llama: largest position + 1 */
+  float norm_eps;         /* LayerNorm / RMSNorm epsilon, inside the square root */
+  float rope_theta;       /* Llama only */
+  int kv_block_size;      /* tokens per KV block; must be 16 */
+  int num_kv_blocks;      /* physical blocks per layer in the pool (ignored when contiguous_kv) */
+  int max_batch;          /* largest B of a decode step or prefill call */
+  int max_blocks_per_seq; /* row length of a block table */
+  int max_prefill_tokens; /* rows of one prefill chunk (workspace size); >= the longest prompt */
+  int contiguous_kv;      /* 1: sequence b owns slots [b*max_blocks_per_seq*16, ...), tables ignored */
+} llm_config;
+
+/*
+ * Weights: DEVICE pointers, element type given by config.dtype (fp32 or bf16),
+ * row-major. Per-layer fields are HOST arrays of n_layers device pointers; the
+ * library copies those arrays. Absent tensors are NULL (all biases and ln*_b /
+ * pos_emb for Llama). Shapes, d = d_model, H = n_heads, Hkv = n_kv_heads,
+ * hd = head_dim, F = d_ff:
+ *   tok_emb [vocab][d]            token embedding, also the tied LM head
+ *   pos_emb [n_ctx][d]            GPT-2 learned positions
+ *   ln1_w/ln1_b [d]               pre-attention norm gain / bias
+ *   w_qkv [(H+2Hkv)*hd][d]        rows: all q heads, then k heads, then v heads
+ *   b_qkv [(H+2Hkv)*hd]
+ *   w_o   [d][H*hd],  b_o [d]
+ *   ln2_w/ln2_b [d]
+ *   w_up  GPT-2: [F][d]; Llama: [2F][d] with gate rows 0..F-1 then up rows F..2F-1
+ *   b_up  [F] (GPT-2)
+ *   w_down [d][F], b_down [d]
+ *   lnf_w/lnf_b [d]               final norm
+ */
+typedef struct {
+  const void* tok_emb;
+  const void* pos_emb;
+  const void* const* ln1_w;
+  const void* const* ln1_b;
+  const void* const* w_qkv;
+  const void* const* b_qkv;
+  const void* const* w_o;
+  const void* const* b_o;
+  const void* const* ln2_w;
+  const void* const* ln2_b;
+  const void* const* w_up;
+  const void* const* b_up;
+  const void* const* w_down;
+  const void* const* b_down;
+  const void* lnf_w;
+  const void* lnf_b;
+} llm_weights;
+
+typedef struct llm_handle llm_handle;
+
+/* Validate the config, check the device (compute capability 10.3), copy the
+ * per-layer pointer arrays, allocate the KV pool
+ * (2 * n_layers * num_kv_blocks * n_kv_heads * 16 * head_dim elements of dtype,
+ * laid out [layer][block][kv_head][16][head_dim], K and V in separate pools)
+ * and the workspace. cuda_stream is a cudaStream_t (NULL = the legacy default
+ * stream, which disables CUDA-graph replay). Errors: INVALID_ARG, UNSUPPORTED,
+ * NO_DEVICE, OOM, CUDA. On error *out is NULL and nothing is leaked. */
+llm_status llm_create(const llm_config* config, const llm_weights* weights, void* cuda_stream,
+                      llm_handle** out);
+
+/* Free the pool, workspace and cached graphs (synchronises the stream). NULL is a no-op. */
+void llm_destroy(llm_handle* h);
+
+/* Prompt prefill from position 0 ("rvllm-metal", sections "The matmul pain story"
+ * and "Numbers": the whole prompt goes through at once).
+ *   tokens        device int32 [sum(lengths)], the prompts packed back to back
+ *   lengths       HOST int32 [B], each in [1, max_prefill_tokens] and, for GPT-2, <= n_ctx
+ *   block_tables  device int32 [B][max_blocks_per_seq] physical block ids (ignored
+ *                 when contiguous_kv); the first ceil(len/16) entries must be valid
+ *   next_ids      device int32 [B]: argmax of the last position's logits
+ *   logits        device float [B][vocab] last-position logits, or NULL
+ * Writes K/V of every prompt position into the pool. Sequences are processed in
+ * chunks of at most max_prefill_tokens rows. Errors: INVALID_ARG, OUT_OF_RANGE. */
+llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* lengths, const int32_t* block_tables,
+                       int B, int32_t* next_ids, float* logits);
+
+/* One batched decode step ("rvllm-metal", section "What the kernels do").
+ *   tokens        device int32 [B], the token fed to each sequence
+ *   positions     device int32 [B], its position = the sequence's context length before
+ *                 this step; K/V are written at that slot and attention covers 0..positions[b]
+ *   block_tables  device int32 [B][max_blocks_per_seq] (ignored when contiguous_kv)
+ *   next_ids      device int32 [B]
+ *   logits        device float [B][vocab], or NULL
+ * The first call for a given B captures the step in a CUDA graph (when the
+ * stream allows it); later calls replay it. Errors: INVALID_ARG, OUT_OF_RANGE. */
+llm_status llm_decode_step(llm_handle* h, const int32_t* tokens, const int32_t* positions,
+                           const int32_t* block_tables, int B, int32_t* next_ids, float* logits);
+
+/* The same step from HOST buffers: copies tokens, positions and (unless NULL or
+ * contiguous_kv) block_tables to the device, runs llm_decode_step, copies
+ * next_ids (and logits when not NULL) back, and synchronises the stream before
+ * returning. All five pointers are HOST memory (pinned or pageable). */
+llm_status llm_decode_step_host(llm_handle* h, const int32_t* tokens, const int32_t* positions,
+                                const int32_t* block_tables, int B, int32_t* next_ids, float* logits);
+
+/* Synchronise the stream, return the device error word in *flags and clear it.
+ * Returns LLM_ERR_DEVICE_FLAG when any bit was set, LLM_OK otherwise. */
+llm_status llm_get_error_flags(llm_handle* h, uint32_t* flags);
+
+/* Per-kernel timing. While enabled, steps run without graph replay and every
+ * launch is bracketed by CUDA events on the handle's stream. */
+typedef struct {
+  char name[48];
+  int launches;
+  double total_ms;
+} llm_kernel_stat;
+
+llm_status llm_set_profiling(llm_handle* h, int enable);
+/* Synchronise, then fill up to max entries (one per kernel name) with the times
+ * accumulated since profiling was enabled or last reset; *n gets the count. */
+llm_status llm_get_kernel_stats(llm_handle* h, llm_kernel_stat* out, int max, int* n, int reset);
+/* Kernel launches issued by the most recent llm_decode_step / llm_prefill call. */
+llm_status llm_last_launch_count(llm_handle* h, int* n);
+/* enable = 1 (default): decode steps are captured once per B and replayed as CUDA
+ * graphs; 0: every launch is issued eagerly. Graphs need a non-default stream. */
+llm_status llm_set_graphs(llm_handle* h, int enable);
+
+/* Projection kernel choice: 0 = by row count (default), 1 = CUDA-core weight-stream
+ * GEMV, 2 = CUDA-core tiled GEMM, 3 = tcgen05 tensor-core GEMM (bf16 models; falls
+ * back to 2 where it does not apply). For tests that force every kernel on every
+ * shape. Drops cached graphs. Errors: INVALID_ARG for another value. */
+llm_status llm_set_linear_variant(llm_handle* h, int variant);
+
+const char* llm_status_string(llm_status s);
+const char* llm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLM_H */

@@ -1,0 +1,63 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path and the oracle on the
+same seeded inputs and compare them element by element."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import workloads as wl
+
+# Acceptance: max-abs logit error 2e-3 (fp32 weights) / 3e-2 (bf16 weights); argmax ids
+# equal wherever the oracle's top-1/top-2 margin exceeds 1e-3.
+LOGIT_TOL = {wl.DTYPE_F32: 2e-3, wl.DTYPE_BF16: 3e-2}
+MARGIN = 1e-3
+
+
+def check_logits(z_gpu: np.ndarray, z_ref: np.ndarray, dtype: int, what: str = "") -> float:
+    z_gpu = np.asarray(z_gpu, dtype=np.float64)
+    assert z_gpu.shape == z_ref.shape, (z_gpu.shape, z_ref.shape)
+    assert np.all(np.isfinite(z_gpu)), f"{what}: non-finite logits"
+    err = float(np.abs(z_gpu - z_ref).max())
+    assert err <= LOGIT_TOL[dtype], f"{what}: max-abs logit error {err:.3e} > {LOGIT_TOL[dtype]:.0e}"
+    return err
+
+
+def check_ids(ids_gpu, z_ref_rows, what: str = "") -> int:
+    """Greedy ids must match where the oracle has a clear winner; returns the number checked."""
+    n = 0
+    for i, (g, z) in enumerate(zip(np.asarray(ids_gpu).reshape(-1), z_ref_rows)):
+        if oracle.top2_margin(z) > MARGIN:
+            assert int(g) == oracle.argmax_rule(z), f"{what}: id mismatch at row {i}: {g} vs {oracle.argmax_rule(z)}"
+            n += 1
+    return n
+
+
+def oracle_teacher(model: oracle.OracleModel, prompt, stream) -> np.ndarray:
+    """Logits after the prompt and after each teacher-forced token: [1 + len(stream), V]."""
+    return oracle.teacher_forced(model, prompt, stream)
+
+
+def run_gpu_teacher(run, stream_tokens: np.ndarray, rows=None, variant: int = 0, graphs: bool = True):
+    """Prefill then teacher-forced decode on the GPU.
+
+    stream_tokens [S, B] int32. Returns (ids [1+S, B], logits [1+S, len(rows), V]) on the host.
+    """
+    import torch
+    B, V = run.B, run.shape.vocab
+    rows = list(range(B)) if rows is None else list(rows)
+    if variant:
+        run.dec.set_linear_variant(variant)
+    run.dec.set_graphs(graphs)
+    logits = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    ids, zs = [], []
+    run.prefill(logits)
+    torch.cuda.synchronize()
+    ids.append(run.next_ids.cpu().numpy().copy())
+    zs.append(logits[rows].cpu().numpy())
+    toks = torch.from_numpy(np.ascontiguousarray(stream_tokens, dtype=np.int32)).cuda()
+    for s in range(stream_tokens.shape[0]):
+        run.decode(toks[s], s, logits)
+        torch.cuda.synchronize()
+        ids.append(run.next_ids.cpu().numpy().copy())
+        zs.append(logits[rows].cpu().numpy())
+    return np.stack(ids), np.stack(zs)

@@ -1,0 +1,236 @@
+"""CUDA path vs float64 oracle, element by element, through the C ABI (GPU only)."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from parity_util import LOGIT_TOL, check_ids, check_logits, oracle_teacher, run_gpu_teacher
+
+pytestmark = pytest.mark.gpu
+
+# Small shapes: several 64-wide tiles, ragged tails (vocab 1000, lengths 5/17/70), 2 layers.
+SMALL_GPT2 = wl.ModelShape("small-gpt2", wl.ARCH_GPT2, wl.DTYPE_F32, 2, 192, 3, 3, 64, 512, 1000, 128)
+SMALL_GPT2_BF16 = replace(SMALL_GPT2, name="small-gpt2-bf16", dtype=wl.DTYPE_BF16)
+SMALL_LLAMA = wl.ModelShape("small-llama", wl.ARCH_LLAMA, wl.DTYPE_BF16, 2, 384, 6, 2, 64, 320, 1024, 512)
+SMALL_LLAMA_F32 = replace(SMALL_LLAMA, name="small-llama-f32", dtype=wl.DTYPE_F32)
+SMALL = [SMALL_GPT2, SMALL_GPT2_BF16, SMALL_LLAMA, SMALL_LLAMA_F32]
+LENGTHS = np.array([5, 17, 70], dtype=np.int32)
+STEPS = 6
+
+
+def small_workload(shape, contiguous=False, shuffle=True):
+    return wl.Workload("small", shape, batch=len(LENGTHS), prompt_len=0, decode_steps=STEPS, mode="teacher",
+                       contiguous_kv=contiguous, shuffle_tables=shuffle)
+
+
+@pytest.fixture(scope="module")
+def small_models():
+    out = {}
+    for s in SMALL:
+        w = wl.make_weights(s, scale=2.0, perturb=True)
+        out[s.name] = (w, oracle.OracleModel(w))
+    return out
+
+
+def _oracle_rows(model, run, stream):
+    return [oracle_teacher(model, run.prompts[b], stream[:, b]) for b in range(run.B)]
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["gemv", "simt"])
+@pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
+def test_small_model_matches_oracle(gpu_lib, small_models, shape, variant):
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, model = small_models[shape.name]
+    run = WorkloadRun(small_workload(shape), host_weights=w, lengths=LENGTHS)
+    stream = wl.draw_stream(run.B, STEPS, shape.vocab)
+    ids, z = run_gpu_teacher(run, stream, variant=variant)
+    assert run.dec.error_flags() == 0
+    ref = _oracle_rows(model, run, stream)
+    for b in range(run.B):
+        check_logits(z[:, b], ref[b], shape.dtype, f"{shape.name} seq {b}")
+        check_ids(ids[:, b], ref[b], f"{shape.name} seq {b}")
+    run.close()
+
+
+def test_graph_replay_equals_eager_bitwise(gpu_lib, small_models):
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, _ = small_models[SMALL_LLAMA.name]
+    stream = wl.draw_stream(len(LENGTHS), STEPS, SMALL_LLAMA.vocab)
+    outs = []
+    for graphs in (True, False):
+        run = WorkloadRun(small_workload(SMALL_LLAMA), host_weights=w, lengths=LENGTHS)
+        outs.append(run_gpu_teacher(run, stream, graphs=graphs))
+        run.close()
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+
+
+def test_block_table_layout_does_not_change_results(gpu_lib, small_models):
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, _ = small_models[SMALL_GPT2.name]
+    stream = wl.draw_stream(len(LENGTHS), STEPS, SMALL_GPT2.vocab)
+    outs = []
+    for contiguous, shuffle in ((False, True), (False, False), (True, False)):
+        run = WorkloadRun(small_workload(SMALL_GPT2, contiguous, shuffle), host_weights=w, lengths=LENGTHS)
+        outs.append(run_gpu_teacher(run, stream))
+        run.close()
+    for o in outs[1:]:
+        np.testing.assert_array_equal(outs[0][0], o[0])
+        np.testing.assert_array_equal(outs[0][1], o[1])
+
+
+def test_sequence_result_independent_of_batch(gpu_lib, small_models):
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, _ = small_models[SMALL_LLAMA.name]
+    stream = wl.draw_stream(len(LENGTHS), STEPS, SMALL_LLAMA.vocab)
+    run = WorkloadRun(small_workload(SMALL_LLAMA), host_weights=w, lengths=LENGTHS)
+    ids3, z3 = run_gpu_teacher(run, stream, variant=1)
+    run.close()
+    run1 = WorkloadRun(small_workload(SMALL_LLAMA), host_weights=w, lengths=LENGTHS, batch=1)
+    ids1, z1 = run_gpu_teacher(run1, stream[:, :1], variant=1)
+    run1.close()
+    np.testing.assert_array_equal(ids1[:, 0], ids3[:, 0])
+    np.testing.assert_array_equal(z1[:, 0], z3[:, 0])
+
+
+def test_host_buffer_entry_point_matches_device_call(gpu_lib, small_models):
+    import torch
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, _ = small_models[SMALL_LLAMA.name]
+    stream = wl.draw_stream(len(LENGTHS), 2, SMALL_LLAMA.vocab)
+    a = WorkloadRun(small_workload(SMALL_LLAMA), host_weights=w, lengths=LENGTHS)
+    ids_dev, z_dev = run_gpu_teacher(a, stream)
+    a.close()
+    b = WorkloadRun(small_workload(SMALL_LLAMA), host_weights=w, lengths=LENGTHS)
+    b.prefill()
+    torch.cuda.synchronize()
+    tables = np.ascontiguousarray(b.tables_np, dtype=np.int32)
+    for s in range(2):
+        ids = np.zeros(b.B, np.int32)
+        z = np.zeros((b.B, SMALL_LLAMA.vocab), np.float32)
+        pos = (b.lengths + s).astype(np.int32)
+        b.dec.decode_step_host(np.ascontiguousarray(stream[s]), pos, tables, ids, z)
+        np.testing.assert_array_equal(ids, ids_dev[s + 1])
+        np.testing.assert_array_equal(z, z_dev[s + 1])
+    b.close()
+
+
+def test_device_error_flags_and_host_status(gpu_lib, small_models):
+    import torch
+    import transformer_decoder_forward_gb300 as L
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, _ = small_models[SMALL_GPT2.name]
+    run = WorkloadRun(small_workload(SMALL_GPT2), host_weights=w, lengths=LENGTHS)
+    run.prefill()
+    assert run.dec.error_flags() == 0
+    dev = "cuda"
+    # token id out of range
+    bad_tok = torch.tensor([5, SMALL_GPT2.vocab + 3, 1], dtype=torch.int32, device=dev)
+    run.decode(bad_tok, 0)
+    assert run.dec.error_flags() & L.FLAG_BAD_TOKEN
+    # position beyond the learned position table and the block table
+    pos = torch.tensor([5, 10_000, 70], dtype=torch.int32, device=dev)
+    ok_tok = torch.tensor([1, 2, 3], dtype=torch.int32, device=dev)
+    with torch.cuda.stream(run.stream):
+        run.dec.decode_step(ok_tok, pos, run.tables, run.next_ids)
+    assert run.dec.error_flags() & L.FLAG_BAD_POSITION
+    # block id outside the pool
+    bad_tables = run.tables.clone()
+    bad_tables[1, :] = 1 << 20
+    with torch.cuda.stream(run.stream):
+        run.dec.decode_step(ok_tok, run.step_positions[0], bad_tables, run.next_ids)
+    assert run.dec.error_flags() & L.FLAG_BAD_BLOCK
+    assert run.dec.error_flags() == 0
+    # host-side status codes: nothing is launched
+    big = torch.zeros(run.B + 1, dtype=torch.int32, device=dev)
+    with pytest.raises(L.LLMError) as e:
+        run.dec.decode_step(big, big, run.tables, big)
+    assert e.value.status == 2
+    with pytest.raises(L.LLMError) as e:
+        run.dec.prefill(run.tokens, [0, 1, 1], run.tables, run.next_ids)
+    assert e.value.status == 1
+    with pytest.raises(L.LLMError) as e:
+        run.dec.prefill(run.tokens, [SMALL_GPT2.n_ctx + 1], run.tables, run.next_ids)
+    assert e.value.status == 2
+    run.close()
+
+
+# ------------------------------------------------------------------------------------------------
+# the five workloads at their full sizes, in the launch configuration the bench uses
+# ------------------------------------------------------------------------------------------------
+
+def test_gpt2_124m_fp32_b1_greedy_stream(gpu_lib):
+    """8 prompt ids, 16 greedy steps: the oracle's greedy stream is fed back (teacher forcing)."""
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    W = wl.W_GPT2_F32_B1
+    w = wl.make_weights(W.model)
+    model = oracle.OracleModel(w)
+    run = WorkloadRun(W, host_weights=w)
+    ids_ref, z_ref = oracle.greedy_generate(model, run.prompts[0], W.decode_steps)
+    stream = ids_ref[:-1].reshape(-1, 1).astype(np.int32)
+    ids, z = run_gpu_teacher(run, stream)
+    check_logits(z[:, 0], z_ref, W.model.dtype, W.name)
+    assert check_ids(ids[:, 0], z_ref, W.name) >= 1
+    assert run.dec.error_flags() == 0
+    run.close()
+
+
+@pytest.mark.parametrize("W", [wl.W_GPT2_F32_B32, wl.W_GPT2_F32_B32_X8], ids=["x1", "x8"])
+def test_gpt2_124m_fp32_b32_teacher_forced(gpu_lib, W):
+    """32 sequences x (128 prompt + 128 teacher-forced steps), contiguous KV; oracle on a sample."""
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w = wl.make_weights(W.model, scale=W.weight_scale)
+    model = oracle.OracleModel(w)
+    run = WorkloadRun(W, host_weights=w)
+    stream = wl.draw_stream(run.B, W.decode_steps, W.model.vocab)
+    rows = [0, 13, 31]
+    ids, z = run_gpu_teacher(run, stream, rows=rows)
+    assert run.dec.error_flags() == 0
+    for i, b in enumerate(rows):
+        ref = oracle_teacher(model, run.prompts[b], stream[:, b])
+        check_logits(z[:, i], ref, W.model.dtype, f"{W.name} seq {b}")
+        check_ids(ids[:, b], ref, f"{W.name} seq {b}")
+    if W.weight_scale == 8.0:
+        assert model.stats["max_gelu_arg"] > 15.0
+    run.close()
+
+
+def test_smollm2_360m_bf16_b64_decode(gpu_lib):
+    """64 sequences of 64..2048 tokens in shuffled paged blocks, one decode step; oracle on 3."""
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    W = wl.W_SMOLLM2_B64
+    w = wl.make_weights(W.model)
+    model = oracle.OracleModel(w)
+    run = WorkloadRun(W, host_weights=w)
+    stream = wl.draw_stream(run.B, 1, W.model.vocab)
+    lens = run.lengths
+    rows = [int(np.argmin(lens)), int(np.argmax(lens)), 7]
+    ids, z = run_gpu_teacher(run, stream, rows=rows)
+    assert run.dec.error_flags() == 0
+    for i, b in enumerate(rows):
+        ref = oracle_teacher(model, run.prompts[b], stream[:, b])
+        check_logits(z[:, i], ref, W.model.dtype, f"{W.name} seq {b}")
+        check_ids(ids[:, b], ref, f"{W.name} seq {b}")
+    run.close()
+
+
+def test_gpt2_124m_bf16_prefill_16x1024(gpu_lib):
+    import torch
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    W = wl.W_GPT2_BF16_PREFILL
+    w = wl.make_weights(W.model)
+    model = oracle.OracleModel(w)
+    run = WorkloadRun(W, host_weights=w)
+    logits = torch.empty((run.B, W.model.vocab), dtype=torch.float32, device="cuda")
+    run.prefill(logits)
+    torch.cuda.synchronize()
+    assert run.dec.error_flags() == 0
+    ids = run.next_ids.cpu().numpy()
+    z = logits.cpu().numpy()
+    for b in (0, 15):
+        ref = oracle.forward_full(model, run.prompts[b], last_only=True)
+        check_logits(z[b:b + 1], ref, W.model.dtype, f"{W.name} seq {b}")
+        check_ids(ids[b:b + 1], ref, f"{W.name} seq {b}")
+    run.close()

@@ -1,0 +1,219 @@
+"""Python binding of libllm.so: the GB300 KV-cached decoder step.
+
+Argument marshalling only. Every step of the forward pass runs in the CUDA
+library; PyTorch provides device memory and streams. Loading fails loudly when
+the library is missing or the device is not a GB300: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libllm.so")
+
+LLM_OK = 0
+STATUS = {0: "LLM_OK", 1: "LLM_ERR_INVALID_ARG", 2: "LLM_ERR_OUT_OF_RANGE", 3: "LLM_ERR_NO_DEVICE",
+          4: "LLM_ERR_UNSUPPORTED", 5: "LLM_ERR_OOM", 6: "LLM_ERR_CUDA", 7: "LLM_ERR_DEVICE_FLAG"}
+FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+
+EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_decode_step", "llm_decode_step_host",
+           "llm_get_error_flags", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
+           "llm_set_graphs", "llm_set_linear_variant", "llm_status_string", "llm_last_error"]
+
+
+class LLMError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class LLMConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("arch", "dtype", "n_layers", "d_model", "n_heads", "n_kv_heads",
+                                             "head_dim", "d_ff", "vocab", "n_ctx")] + \
+               [("norm_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
+               [(n, ctypes.c_int) for n in ("kv_block_size", "num_kv_blocks", "max_batch", "max_blocks_per_seq",
+                                             "max_prefill_tokens", "contiguous_kv")]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class LLMWeights(ctypes.Structure):
+    _fields_ = [("tok_emb", ctypes.c_void_p), ("pos_emb", ctypes.c_void_p)] + \
+               [(n, _PP) for n in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b",
+                                   "w_up", "b_up", "w_down", "b_down")] + \
+               [("lnf_w", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p)]
+
+
+class KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libllm.so once. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m transformer_decoder_forward_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i32p = ctypes.c_void_p, ctypes.c_void_p
+    lib.llm_create.argtypes = [ctypes.POINTER(LLMConfig), ctypes.POINTER(LLMWeights), vp, ctypes.POINTER(vp)]
+    lib.llm_destroy.argtypes = [vp]
+    lib.llm_destroy.restype = None
+    lib.llm_prefill.argtypes = [vp, i32p, ctypes.POINTER(ctypes.c_int32), i32p, ctypes.c_int, i32p, vp]
+    lib.llm_decode_step.argtypes = [vp, i32p, i32p, i32p, ctypes.c_int, i32p, vp]
+    lib.llm_decode_step_host.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp]
+    lib.llm_get_error_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.llm_set_profiling.argtypes = [vp, ctypes.c_int]
+    lib.llm_get_kernel_stats.argtypes = [vp, ctypes.POINTER(KernelStat), ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                         ctypes.c_int]
+    lib.llm_last_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    lib.llm_set_graphs.argtypes = [vp, ctypes.c_int]
+    lib.llm_set_linear_variant.argtypes = [vp, ctypes.c_int]
+    lib.llm_status_string.argtypes = [ctypes.c_int]
+    lib.llm_status_string.restype = ctypes.c_char_p
+    lib.llm_last_error.argtypes = []
+    lib.llm_last_error.restype = ctypes.c_char_p
+    for name in ("llm_create", "llm_prefill", "llm_decode_step", "llm_decode_step_host", "llm_get_error_flags",
+                 "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
+                 "llm_set_linear_variant"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != LLM_OK:
+        raise LLMError(status, (_lib.llm_last_error() or b"").decode())
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def upload_weights(w, device: str = "cuda"):
+    """Copy a ``workloads.Weights`` host model to device tensors (fp32 or bf16). Returns a dict of tensors."""
+    import torch
+
+    def dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    out = {"tok_emb": dev(w.tok_emb), "pos_emb": dev(w.pos_emb), "lnf_w": dev(w.lnf_w), "lnf_b": dev(w.lnf_b)}
+    for k in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b", "w_up", "b_up", "w_down", "b_down"):
+        out[k] = [dev(a) for a in getattr(w, k)]
+    return out
+
+
+class Decoder:
+    """One libllm handle over device-resident weights.
+
+    ``shape`` is a ``workloads.ModelShape``; ``dev_w`` the dict from ``upload_weights``.
+    All tensors passed to the step methods are CUDA tensors (int32 ids/positions/tables,
+    float32 logits), except ``lengths`` of prefill, which is host data.
+    """
+
+    def __init__(self, shape, dev_w, *, max_batch: int, max_blocks_per_seq: int, num_kv_blocks: int = 0,
+                 max_prefill_tokens: int = 4096, contiguous_kv: bool = False, stream=None):
+        import torch
+        self.lib = load()
+        self.shape = shape
+        self.dev_w = dev_w
+        self.stream = stream if stream is not None else torch.cuda.Stream()
+        c = LLMConfig(arch=shape.arch, dtype=shape.dtype, n_layers=shape.n_layers, d_model=shape.d_model,
+                      n_heads=shape.n_heads, n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim,
+                      d_ff=shape.d_ff, vocab=shape.vocab, n_ctx=shape.n_ctx, norm_eps=shape.norm_eps,
+                      rope_theta=shape.rope_theta, kv_block_size=16, num_kv_blocks=num_kv_blocks,
+                      max_batch=max_batch, max_blocks_per_seq=max_blocks_per_seq,
+                      max_prefill_tokens=max_prefill_tokens, contiguous_kv=int(contiguous_kv))
+        self.config = c
+        L = shape.n_layers
+        self._arrays = []
+
+        def arr(name):
+            lst = dev_w.get(name)
+            if lst is None or all(t is None for t in lst):
+                return None
+            a = (ctypes.c_void_p * L)(*[_ptr(t) for t in lst])
+            self._arrays.append(a)
+            return ctypes.cast(a, _PP)
+
+        w = LLMWeights(tok_emb=_ptr(dev_w["tok_emb"]), pos_emb=_ptr(dev_w["pos_emb"]),
+                       lnf_w=_ptr(dev_w["lnf_w"]), lnf_b=_ptr(dev_w["lnf_b"]))
+        for k in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b", "w_up", "b_up", "w_down",
+                  "b_down"):
+            setattr(w, k, arr(k))
+        handle = ctypes.c_void_p()
+        torch.cuda.synchronize()
+        _check(self.lib.llm_create(ctypes.byref(c), ctypes.byref(w), ctypes.c_void_p(self.stream.cuda_stream),
+                                   ctypes.byref(handle)))
+        self.handle = handle
+
+    # ---- steps ---------------------------------------------------------------------------
+    def prefill(self, tokens, lengths: Sequence[int], block_tables, next_ids, logits=None) -> None:
+        lens = (ctypes.c_int32 * len(lengths))(*[int(x) for x in lengths])
+        _check(self.lib.llm_prefill(self.handle, _ptr(tokens), lens, _ptr(block_tables), len(lengths),
+                                    _ptr(next_ids), _ptr(logits)))
+
+    def decode_step(self, tokens, positions, block_tables, next_ids, logits=None) -> None:
+        _check(self.lib.llm_decode_step(self.handle, _ptr(tokens), _ptr(positions), _ptr(block_tables),
+                                        int(tokens.numel()), _ptr(next_ids), _ptr(logits)))
+
+    def decode_step_host(self, tokens: np.ndarray, positions: np.ndarray, block_tables: Optional[np.ndarray],
+                         next_ids: np.ndarray, logits: Optional[np.ndarray] = None) -> None:
+        """Host-buffer variant: numpy int32 inputs, numpy int32 / float32 outputs (synchronous)."""
+        def p(a):
+            return None if a is None else a.ctypes.data
+        _check(self.lib.llm_decode_step_host(self.handle, p(tokens), p(positions), p(block_tables), len(tokens),
+                                             p(next_ids), p(logits)))
+
+    # ---- diagnostics ---------------------------------------------------------------------
+    def error_flags(self) -> int:
+        f = ctypes.c_uint32(0)
+        st = self.lib.llm_get_error_flags(self.handle, ctypes.byref(f))
+        if st not in (LLM_OK, 7):
+            _check(st)
+        return int(f.value)
+
+    def set_profiling(self, on: bool) -> None:
+        _check(self.lib.llm_set_profiling(self.handle, int(on)))
+
+    def set_graphs(self, on: bool) -> None:
+        _check(self.lib.llm_set_graphs(self.handle, int(on)))
+
+    def set_linear_variant(self, v: int) -> None:
+        """0 auto, 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM."""
+        _check(self.lib.llm_set_linear_variant(self.handle, int(v)))
+
+    def kernel_stats(self, reset: bool = True):
+        buf = (KernelStat * 64)()
+        n = ctypes.c_int(0)
+        _check(self.lib.llm_get_kernel_stats(self.handle, buf, 64, ctypes.byref(n), int(reset)))
+        return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n.value)}
+
+    def last_launch_count(self) -> int:
+        n = ctypes.c_int(0)
+        _check(self.lib.llm_last_launch_count(self.handle, ctypes.byref(n)))
+        return n.value
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            self.lib.llm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

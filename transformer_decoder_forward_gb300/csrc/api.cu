@@ -1,0 +1,679 @@
+// C ABI of the decoder step: handle, workspace, step orchestration, CUDA graphs.
+//
+// A decode step is one CUDA graph: the pages record a whole forward pass into
+// one command buffer and submit it once ("bare-metal-llm", section "What it
+// taught me"; "rvllm-metal", section "You record work, then you submit it").
+// Kernel parameters are fixed in a graph, so the per-call pointers (tokens,
+// positions, block tables, outputs) travel through one device-resident
+// StepArgs struct that the graph's first node rewrites; each replay only
+// updates that node's parameters. Nothing is rebuilt per step on the host (the
+// pages list per-step host-built tables as a weakness, "What's basic about it").
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/llm.h"
+#include "attention.cuh"
+#include "linear.cuh"
+#include "misc.cuh"
+
+using namespace llm;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+llm_status fail(llm_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+#define CUDA_TRY(expr)                                                                          \
+  do {                                                                                          \
+    cudaError_t _e = (expr);                                                                    \
+    if (_e != cudaSuccess)                                                                      \
+      return fail(LLM_ERR_CUDA, std::string(#expr) + ": " + cudaGetErrorString(_e));           \
+  } while (0)
+
+struct LayerW {
+  const void *ln1_w, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o, *ln2_w, *ln2_b, *w_up, *b_up, *w_down, *b_down;
+};
+
+struct GraphEntry {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t args_node = nullptr;
+  int launches = 0;
+};
+
+struct ProfRec {
+  std::string name;
+  cudaEvent_t a, b;
+};
+
+struct Stat {
+  int launches = 0;
+  double ms = 0.0;
+};
+
+}  // namespace
+
+struct llm_handle {
+  llm_config cfg{};
+  int dev = 0, num_sms = 0;
+  cudaStream_t stream = nullptr;
+  int wdt = DT_F32, adt = DT_F32;
+  size_t welt = 4;
+  const void *tok_emb = nullptr, *pos_emb = nullptr, *lnf_w = nullptr, *lnf_b = nullptr;
+  std::vector<LayerW> layers;
+  // KV pool
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  size_t layer_kv_elems = 0;
+  int num_blocks = 0;
+  // workspace
+  int max_rows = 0;
+  float* h = nullptr;
+  void* xn = nullptr;
+  float* q = nullptr;
+  void* att = nullptr;
+  void* ff = nullptr;
+  int split = 128, max_splits = 1;
+  float* attn_po = nullptr;
+  float* attn_ml = nullptr;
+  int head_tiles = 0;
+  float* head_val = nullptr;
+  int* head_idx = nullptr;
+  float* gemv_part = nullptr;
+  size_t gemv_part_elems = 0;
+  unsigned* counters = nullptr;
+  int counters_len = 0;
+  unsigned* flags = nullptr;
+  StepArgs* d_args = nullptr;
+  int* d_row_pos = nullptr;
+  int* d_row_seq = nullptr;
+  int* d_last_row = nullptr;
+  int4* d_items = nullptr;
+  int max_items = 0;
+  // host-buffer entry point staging
+  int* d_host_tokens = nullptr;
+  int* d_host_pos = nullptr;
+  int* d_host_tables = nullptr;
+  int* d_host_ids = nullptr;
+  float* d_host_logits = nullptr;
+  // execution options
+  bool use_graphs = true;
+  bool pdl = false;
+  int lin_variant = LIN_AUTO;
+  std::map<int, GraphEntry> graphs;
+  // profiling
+  bool profiling = false;
+  std::vector<ProfRec> prof;
+  std::vector<cudaEvent_t> event_pool;
+  size_t event_next = 0;
+  std::map<std::string, Stat> stats;
+  int launch_counter = 0;
+  int last_launches = 0;
+  std::vector<void*> allocations;
+};
+
+namespace {
+
+template <typename T>
+llm_status dev_alloc(llm_handle* h, T** p, size_t count) {
+  *p = nullptr;
+  if (count == 0) count = 1;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(LLM_ERR_OOM, "cudaMalloc of " + std::to_string(count * sizeof(T)) + " bytes failed");
+  }
+  h->allocations.push_back(*p);
+  e = cudaMemset(*p, 0, count * sizeof(T));
+  if (e != cudaSuccess) return fail(LLM_ERR_CUDA, cudaGetErrorString(e));
+  return LLM_OK;
+}
+
+void free_all(llm_handle* h) {
+  for (auto& kv : h->graphs) {
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    if (kv.second.graph) cudaGraphDestroy(kv.second.graph);
+  }
+  h->graphs.clear();
+  for (auto ev : h->event_pool) cudaEventDestroy(ev);
+  h->event_pool.clear();
+  for (void* p : h->allocations) cudaFree(p);
+  h->allocations.clear();
+}
+
+cudaEvent_t next_event(llm_handle* h) {
+  if (h->event_next >= h->event_pool.size()) {
+    cudaEvent_t e;
+    cudaEventCreate(&e);
+    h->event_pool.push_back(e);
+  }
+  return h->event_pool[h->event_next++];
+}
+
+// Every kernel launch goes through here: counts it and, when profiling, brackets it with events.
+template <typename F>
+llm_status run(llm_handle* h, const char* name, F&& f) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (h->profiling) {
+    a = next_event(h);
+    b = next_event(h);
+    cudaEventRecord(a, h->stream);
+  }
+  cudaError_t e = f();
+  if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string(name) + ": " + cudaGetErrorString(e));
+  if (h->profiling) {
+    cudaEventRecord(b, h->stream);
+    h->prof.push_back({name, a, b});
+  }
+  h->launch_counter++;
+  return LLM_OK;
+}
+
+#define RUN(name, expr)                              \
+  do {                                               \
+    llm_status _s = run(h, name, [&]() { return (expr); }); \
+    if (_s != LLM_OK) return _s;                     \
+  } while (0)
+
+int pick_variant(const llm_handle* h, const LinearParams& p) {
+  if (h->lin_variant != LIN_AUTO) return h->lin_variant;
+  if (p.M <= 64) return LIN_GEMV;
+  if (gemm_tc_supported(p)) return LIN_TC;
+  return LIN_SIMT;
+}
+
+llm_status linear(llm_handle* h, const char* tag, LinearParams p) {
+  p.part = h->gemv_part;
+  p.part_elems = h->gemv_part_elems;
+  p.counters = h->counters;
+  p.counters_len = h->counters_len;
+  int v = pick_variant(h, p);
+  if (v == LIN_TC && !gemm_tc_supported(p)) v = LIN_SIMT;
+  std::string name = std::string(v == LIN_GEMV ? "gemv_" : v == LIN_TC ? "gemm_tc_" : "gemm_simt_") + tag;
+  if (v == LIN_GEMV) RUN(name.c_str(), launch_gemv(p, h->num_sms, h->stream, h->pdl));
+  else if (v == LIN_TC) RUN(name.c_str(), launch_gemm_tc(p, h->num_sms, h->stream, h->pdl));
+  else RUN(name.c_str(), launch_gemm_simt(p, h->stream, h->pdl));
+  return LLM_OK;
+}
+
+KVLayer kv_layer(const llm_handle* h, int l) {
+  KVLayer kv;
+  kv.k = static_cast<char*>(h->k_pool) + (size_t)l * h->layer_kv_elems * h->welt;
+  kv.v = static_cast<char*>(h->v_pool) + (size_t)l * h->layer_kv_elems * h->welt;
+  kv.num_blocks = h->num_blocks;
+  kv.n_kv_heads = h->cfg.n_kv_heads;
+  kv.mbps = h->cfg.max_blocks_per_seq;
+  kv.contiguous = h->cfg.contiguous_kv;
+  return kv;
+}
+
+Epilogue base_epi(const llm_handle* h) {
+  Epilogue e;
+  memset(&e, 0, sizeof(e));
+  e.act_dtype = h->adt;
+  e.args = h->d_args;
+  e.flags = h->flags;
+  return e;
+}
+
+// The kernels of one forward pass over M rows (decode: M = B, one row per
+// sequence; prefill chunk: the packed prompt rows), reading d_args.
+// items != 0 selects prefill attention over `n_items` work items.
+llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_items) {
+  const llm_config& c = h->cfg;
+  const int d = c.d_model, H = c.n_heads, Hkv = c.n_kv_heads, F = c.d_ff;
+  const bool gpt2 = c.arch == LLM_ARCH_GPT2;
+  const int qkv_n = (H + 2 * Hkv) * HD;
+
+  EmbedParams ep{h->tok_emb, gpt2 ? h->pos_emb : nullptr, h->d_args, h->h, M, d, c.vocab, c.n_ctx, h->flags};
+  RUN("embed", launch_embed(ep, h->wdt, h->stream, h->pdl));
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& w = h->layers[l];
+    NormParams np{h->h, w.ln1_w, gpt2 ? w.ln1_b : nullptr, h->xn, h->d_args, M, d, gpt2 ? 1 : 0, 0, c.norm_eps};
+    RUN("norm", launch_norm(np, h->wdt, h->adt, h->stream, h->pdl));
+
+    LinearParams lp;
+    memset(&lp, 0, sizeof(lp));
+    lp.wdt = h->wdt; lp.xdt = h->adt; lp.adt = h->adt;
+    lp.M = M;
+    // QKV + RoPE + kv_write
+    lp.W = w.w_qkv; lp.X = h->xn; lp.N = qkv_n; lp.K = d; lp.ldx = d; lp.swiglu = 0;
+    lp.epi = base_epi(h);
+    lp.epi.kind = EPI_QKV;
+    lp.epi.bias = w.b_qkv;
+    lp.epi.q_out = h->q;
+    lp.epi.kv = kv_layer(h, l);
+    lp.epi.n_heads = H;
+    lp.epi.rope = gpt2 ? 0 : 1;
+    lp.epi.rope_theta = c.rope_theta;
+    { llm_status s_ = linear(h, "qkv", lp); if (s_ != LLM_OK) return s_; }
+
+    // attention
+    if (!prefill) {
+      AttnDecodeParams ap;
+      memset(&ap, 0, sizeof(ap));
+      ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.B = B; ap.n_heads = H;
+      ap.split = h->split; ap.max_splits = h->max_splits; ap.part_o = h->attn_po; ap.part_ml = h->attn_ml;
+      ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
+      RUN("attn_decode", launch_attn_decode(ap, h->wdt, h->stream, h->pdl));
+      h->launch_counter++;   // split + merge
+    } else {
+      AttnPrefillParams ap;
+      memset(&ap, 0, sizeof(ap));
+      ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.items = h->d_items; ap.n_items = n_items;
+      ap.n_heads = H; ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
+      RUN("attn_prefill", launch_attn_prefill(ap, h->wdt, h->stream, h->pdl));
+    }
+
+    // out projection + residual
+    lp.W = w.w_o; lp.X = h->att; lp.N = d; lp.K = H * HD; lp.ldx = H * HD;
+    lp.epi = base_epi(h);
+    lp.epi.kind = EPI_RESID; lp.epi.bias = w.b_o; lp.epi.resid = h->h; lp.epi.ld_resid = d;
+    { llm_status s_ = linear(h, "o", lp); if (s_ != LLM_OK) return s_; }
+
+    NormParams np2{h->h, w.ln2_w, gpt2 ? w.ln2_b : nullptr, h->xn, h->d_args, M, d, gpt2 ? 1 : 0, 0, c.norm_eps};
+    RUN("norm", launch_norm(np2, h->wdt, h->adt, h->stream, h->pdl));
+
+    // FFN up (+gate) with the activation
+    lp.W = w.w_up; lp.X = h->xn; lp.N = F; lp.K = d; lp.ldx = d; lp.swiglu = gpt2 ? 0 : 1;
+    lp.epi = base_epi(h);
+    lp.epi.kind = gpt2 ? EPI_GELU : EPI_SWIGLU; lp.epi.bias = w.b_up; lp.epi.out = h->ff; lp.epi.ld_out = F;
+    { llm_status s_ = linear(h, "up", lp); if (s_ != LLM_OK) return s_; }
+
+    // FFN down + residual
+    lp.W = w.w_down; lp.X = h->ff; lp.N = d; lp.K = F; lp.ldx = F; lp.swiglu = 0;
+    lp.epi = base_epi(h);
+    lp.epi.kind = EPI_RESID; lp.epi.bias = w.b_down; lp.epi.resid = h->h; lp.epi.ld_resid = d;
+    { llm_status s_ = linear(h, "down", lp); if (s_ != LLM_OK) return s_; }
+  }
+
+  // final norm on each sequence's last row, tied LM head + argmax partials, argmax reduce
+  NormParams nf{h->h, h->lnf_w, gpt2 ? h->lnf_b : nullptr, h->xn, h->d_args, B, d, gpt2 ? 1 : 0, prefill ? 1 : 0,
+                c.norm_eps};
+  RUN("norm", launch_norm(nf, h->wdt, h->adt, h->stream, h->pdl));
+  LinearParams hp;
+  memset(&hp, 0, sizeof(hp));
+  hp.wdt = h->wdt; hp.xdt = h->adt; hp.adt = h->adt;
+  hp.W = h->tok_emb; hp.X = h->xn; hp.M = B; hp.N = c.vocab; hp.K = d; hp.ldx = d;
+  hp.epi = base_epi(h);
+  hp.epi.kind = EPI_HEAD; hp.epi.part_val = h->head_val; hp.epi.part_idx = h->head_idx; hp.epi.vocab = c.vocab;
+  { llm_status s_ = linear(h, "head", hp); if (s_ != LLM_OK) return s_; }
+  ArgmaxParams amp{h->head_val, h->head_idx, h->head_tiles, h->d_args, h->flags};
+  RUN("argmax", launch_argmax(amp, B, h->stream, h->pdl));
+  return LLM_OK;
+}
+
+llm_status check_handle(llm_handle* h) {
+  if (!h) return fail(LLM_ERR_INVALID_ARG, "handle is NULL");
+  cudaError_t e = cudaSetDevice(h->dev);
+  if (e != cudaSuccess) return fail(LLM_ERR_CUDA, cudaGetErrorString(e));
+  return LLM_OK;
+}
+
+void begin_call(llm_handle* h) { h->launch_counter = 0; }
+void end_call(llm_handle* h) { h->last_launches = h->launch_counter; }
+
+bool stream_capturable(cudaStream_t s) { return s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread; }
+
+}  // namespace
+
+extern "C" {
+
+const char* llm_status_string(llm_status s) {
+  switch (s) {
+    case LLM_OK: return "ok";
+    case LLM_ERR_INVALID_ARG: return "invalid argument";
+    case LLM_ERR_OUT_OF_RANGE: return "out of range";
+    case LLM_ERR_NO_DEVICE: return "no suitable CUDA device";
+    case LLM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LLM_ERR_OOM: return "out of device memory";
+    case LLM_ERR_CUDA: return "CUDA error";
+    case LLM_ERR_DEVICE_FLAG: return "device error flag set";
+  }
+  return "unknown status";
+}
+
+const char* llm_last_error(void) { return g_last_error.c_str(); }
+
+llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_stream, llm_handle** out) {
+  if (!out) return fail(LLM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfgp || !wp) return fail(LLM_ERR_INVALID_ARG, "config or weights is NULL");
+  const llm_config c = *cfgp;
+  if (c.arch != LLM_ARCH_GPT2 && c.arch != LLM_ARCH_LLAMA) return fail(LLM_ERR_INVALID_ARG, "bad arch");
+  if (c.dtype != LLM_DTYPE_F32 && c.dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_INVALID_ARG, "bad dtype");
+  if (c.n_layers <= 0 || c.d_model <= 0 || c.n_heads <= 0 || c.n_kv_heads <= 0 || c.d_ff <= 0 || c.vocab <= 0 ||
+      c.n_ctx <= 0 || c.max_batch <= 0 || c.max_blocks_per_seq <= 0 || c.max_prefill_tokens <= 0)
+    return fail(LLM_ERR_INVALID_ARG, "sizes must be positive");
+  if (c.head_dim != HD) return fail(LLM_ERR_UNSUPPORTED, "head_dim must be 64");
+  if (c.kv_block_size != KVB) return fail(LLM_ERR_UNSUPPORTED, "kv_block_size must be 16");
+  if (c.n_heads % c.n_kv_heads != 0) return fail(LLM_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
+  if (c.n_heads / c.n_kv_heads > 8) return fail(LLM_ERR_UNSUPPORTED, "at most 8 query heads per KV head");
+  if (c.d_model > 8192) return fail(LLM_ERR_UNSUPPORTED, "d_model above 8192");
+  if (c.d_model % 8 != 0 || c.d_ff % 8 != 0) return fail(LLM_ERR_UNSUPPORTED, "d_model and d_ff must be multiples of 8");
+  if (c.arch == LLM_ARCH_LLAMA && !(c.rope_theta > 0.0f)) return fail(LLM_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if (!c.contiguous_kv && c.num_kv_blocks <= 0) return fail(LLM_ERR_INVALID_ARG, "num_kv_blocks must be positive");
+  const bool gpt2 = c.arch == LLM_ARCH_GPT2;
+  if (!wp->tok_emb || (gpt2 && !wp->pos_emb) || !wp->lnf_w || (gpt2 && !wp->lnf_b))
+    return fail(LLM_ERR_INVALID_ARG, "missing embedding or final-norm weights");
+  if (!wp->ln1_w || !wp->w_qkv || !wp->w_o || !wp->ln2_w || !wp->w_up || !wp->w_down)
+    return fail(LLM_ERR_INVALID_ARG, "missing per-layer weight arrays");
+  if (gpt2 && (!wp->ln1_b || !wp->ln2_b || !wp->b_qkv || !wp->b_o || !wp->b_up || !wp->b_down))
+    return fail(LLM_ERR_INVALID_ARG, "GPT-2 needs all bias arrays");
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return fail(LLM_ERR_NO_DEVICE, "no CUDA device");
+  }
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return fail(LLM_ERR_NO_DEVICE, "cannot query device");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(LLM_ERR_NO_DEVICE, "this build runs on compute capability 10.3 (GB300) only");
+
+  llm_handle* h = new llm_handle();
+  h->cfg = c;
+  h->dev = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->stream = static_cast<cudaStream_t>(cuda_stream);
+  h->wdt = h->adt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
+  h->welt = c.dtype == LLM_DTYPE_F32 ? 4 : 2;
+  h->tok_emb = wp->tok_emb;
+  h->pos_emb = gpt2 ? wp->pos_emb : nullptr;
+  h->lnf_w = wp->lnf_w;
+  h->lnf_b = gpt2 ? wp->lnf_b : nullptr;
+  h->layers.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    LayerW& w = h->layers[l];
+    w.ln1_w = wp->ln1_w[l]; w.ln1_b = wp->ln1_b ? wp->ln1_b[l] : nullptr;
+    w.w_qkv = wp->w_qkv[l]; w.b_qkv = wp->b_qkv ? wp->b_qkv[l] : nullptr;
+    w.w_o = wp->w_o[l]; w.b_o = wp->b_o ? wp->b_o[l] : nullptr;
+    w.ln2_w = wp->ln2_w[l]; w.ln2_b = wp->ln2_b ? wp->ln2_b[l] : nullptr;
+    w.w_up = wp->w_up[l]; w.b_up = wp->b_up ? wp->b_up[l] : nullptr;
+    w.w_down = wp->w_down[l]; w.b_down = wp->b_down ? wp->b_down[l] : nullptr;
+    if (!gpt2) { w.ln1_b = w.b_qkv = w.b_o = w.ln2_b = w.b_up = w.b_down = nullptr; }
+    if (!w.ln1_w || !w.w_qkv || !w.w_o || !w.ln2_w || !w.w_up || !w.w_down ||
+        (gpt2 && (!w.ln1_b || !w.b_qkv || !w.b_o || !w.ln2_b || !w.b_up || !w.b_down))) {
+      delete h;
+      return fail(LLM_ERR_INVALID_ARG, "NULL weight pointer in layer " + std::to_string(l));
+    }
+  }
+
+  const int H = c.n_heads, Hkv = c.n_kv_heads, d = c.d_model, F = c.d_ff;
+  h->num_blocks = c.contiguous_kv ? c.max_batch * c.max_blocks_per_seq : c.num_kv_blocks;
+  h->layer_kv_elems = (size_t)h->num_blocks * Hkv * KVB * HD;
+  h->max_rows = std::max(c.max_batch, c.max_prefill_tokens);
+  const int max_ctx = std::min(c.n_ctx, c.max_blocks_per_seq * KVB);
+  h->max_splits = std::max(1, (max_ctx + h->split - 1) / h->split);
+  h->head_tiles = (c.vocab + TILE_N - 1) / TILE_N;
+  h->max_items = c.max_prefill_tokens / 64 + c.max_batch + 1;
+  const size_t act = h->welt;
+  const size_t R = h->max_rows;
+  llm_status st = LLM_OK;
+#define ALLOC(ptr, T, n)                                                         \
+  do {                                                                           \
+    st = dev_alloc(h, reinterpret_cast<T**>(&(ptr)), (size_t)(n));               \
+    if (st != LLM_OK) { free_all(h); delete h; return st; }                      \
+  } while (0)
+  ALLOC(h->k_pool, char, (size_t)c.n_layers * h->layer_kv_elems * h->welt);
+  ALLOC(h->v_pool, char, (size_t)c.n_layers * h->layer_kv_elems * h->welt);
+  ALLOC(h->h, float, R * d);
+  ALLOC(h->xn, char, R * d * act);
+  ALLOC(h->q, float, R * H * HD);
+  ALLOC(h->att, char, R * H * HD * act);
+  ALLOC(h->ff, char, R * F * act);
+  ALLOC(h->attn_po, float, (size_t)c.max_batch * H * h->max_splits * HD);
+  ALLOC(h->attn_ml, float, (size_t)c.max_batch * H * h->max_splits * 2);
+  ALLOC(h->head_val, float, (size_t)h->head_tiles * R);
+  ALLOC(h->head_idx, int, (size_t)h->head_tiles * R);
+  h->gemv_part_elems = (size_t)8 << 20;
+  ALLOC(h->gemv_part, float, h->gemv_part_elems);
+  h->counters_len = 16384;
+  ALLOC(h->counters, unsigned, h->counters_len);
+  ALLOC(h->flags, unsigned, 1);
+  ALLOC(h->d_args, StepArgs, 1);
+  ALLOC(h->d_row_pos, int, R);
+  ALLOC(h->d_row_seq, int, R);
+  ALLOC(h->d_last_row, int, c.max_batch);
+  ALLOC(h->d_items, int4, h->max_items);
+  ALLOC(h->d_host_tokens, int, c.max_batch);
+  ALLOC(h->d_host_pos, int, c.max_batch);
+  ALLOC(h->d_host_tables, int, (size_t)c.max_batch * c.max_blocks_per_seq);
+  ALLOC(h->d_host_ids, int, c.max_batch);
+  ALLOC(h->d_host_logits, float, (size_t)c.max_batch * c.vocab);
+#undef ALLOC
+  if (!stream_capturable(h->stream)) h->use_graphs = false;
+  if (const char* env = getenv("LLM_NO_GRAPH")) h->use_graphs = h->use_graphs && env[0] != '1';
+  if (const char* env = getenv("LLM_PDL")) h->pdl = env[0] == '1';
+  *out = h;
+  return LLM_OK;
+}
+
+void llm_destroy(llm_handle* h) {
+  if (!h) return;
+  cudaSetDevice(h->dev);
+  cudaStreamSynchronize(h->stream);
+  free_all(h);
+  delete h;
+}
+
+llm_status llm_decode_step(llm_handle* h, const int32_t* tokens, const int32_t* positions, const int32_t* tables,
+                           int B, int32_t* next_ids, float* logits) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  if (B <= 0) return fail(LLM_ERR_INVALID_ARG, "B must be positive");
+  if (B > h->cfg.max_batch) return fail(LLM_ERR_OUT_OF_RANGE, "B exceeds max_batch");
+  if (!tokens || !positions || !next_ids) return fail(LLM_ERR_INVALID_ARG, "NULL tokens/positions/next_ids");
+  if (!tables && !h->cfg.contiguous_kv) return fail(LLM_ERR_INVALID_ARG, "NULL block_tables");
+  StepArgs a{tokens, positions, nullptr, tables, next_ids, logits, nullptr, B, B};
+  begin_call(h);
+  if (!h->use_graphs || h->profiling) {
+    CUDA_TRY(launch_set_args(h->d_args, a, h->stream));
+    h->launch_counter++;
+    st = enqueue_forward(h, B, B, false, 0);
+    end_call(h);
+    return st;
+  }
+  auto it = h->graphs.find(B);
+  if (it == h->graphs.end()) {
+    GraphEntry ge;
+    CUDA_TRY(cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = launch_set_args(h->d_args, a, h->stream);
+    h->launch_counter++;
+    llm_status fs = e == cudaSuccess ? enqueue_forward(h, B, B, false, 0) : LLM_ERR_CUDA;
+    cudaGraph_t g = nullptr;
+    cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
+    if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("set_args: ") + cudaGetErrorString(e));
+    if (fs != LLM_OK) { if (g) cudaGraphDestroy(g); return fs; }
+    if (ee != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("end capture: ") + cudaGetErrorString(ee));
+    size_t nroots = 0;
+    CUDA_TRY(cudaGraphGetRootNodes(g, nullptr, &nroots));
+    std::vector<cudaGraphNode_t> roots(nroots);
+    CUDA_TRY(cudaGraphGetRootNodes(g, roots.data(), &nroots));
+    if (nroots != 1) { cudaGraphDestroy(g); return fail(LLM_ERR_CUDA, "captured step has more than one root"); }
+    ge.graph = g;
+    ge.args_node = roots[0];
+    CUDA_TRY(cudaGraphInstantiate(&ge.exec, g, 0));
+    ge.launches = h->launch_counter;
+    it = h->graphs.emplace(B, ge).first;
+  }
+  cudaKernelNodeParams kp;
+  memset(&kp, 0, sizeof(kp));
+  StepArgs* dst = h->d_args;
+  void* params[2] = {&dst, &a};
+  kp.func = const_cast<void*>(set_args_kernel());
+  kp.gridDim = dim3(1);
+  kp.blockDim = dim3(1);
+  kp.kernelParams = params;
+  CUDA_TRY(cudaGraphExecKernelNodeSetParams(it->second.exec, it->second.args_node, &kp));
+  CUDA_TRY(cudaGraphLaunch(it->second.exec, h->stream));
+  h->launch_counter = it->second.launches;
+  end_call(h);
+  return LLM_OK;
+}
+
+llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* lengths, const int32_t* tables, int B,
+                       int32_t* next_ids, float* logits) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  const llm_config& c = h->cfg;
+  if (B <= 0) return fail(LLM_ERR_INVALID_ARG, "B must be positive");
+  if (B > c.max_batch) return fail(LLM_ERR_OUT_OF_RANGE, "B exceeds max_batch");
+  if (!tokens || !lengths || !next_ids) return fail(LLM_ERR_INVALID_ARG, "NULL tokens/lengths/next_ids");
+  if (!tables && !c.contiguous_kv) return fail(LLM_ERR_INVALID_ARG, "NULL block_tables");
+  for (int b = 0; b < B; ++b) {
+    const int L = lengths[b];
+    if (L <= 0) return fail(LLM_ERR_INVALID_ARG, "prompt length must be positive");
+    if (L > c.max_prefill_tokens) return fail(LLM_ERR_OUT_OF_RANGE, "prompt longer than max_prefill_tokens");
+    if (L > c.n_ctx) return fail(LLM_ERR_OUT_OF_RANGE, "prompt longer than n_ctx");
+    if ((L + KVB - 1) / KVB > c.max_blocks_per_seq) return fail(LLM_ERR_OUT_OF_RANGE, "prompt needs more blocks than max_blocks_per_seq");
+  }
+  begin_call(h);
+  size_t tok_off = 0;
+  int s0 = 0;
+  while (s0 < B) {
+    int s1 = s0, rows = 0;
+    while (s1 < B && rows + lengths[s1] <= c.max_prefill_tokens) rows += lengths[s1++];
+    const int nb = s1 - s0;
+    std::vector<int> row_pos(rows), row_seq(rows), last_row(nb);
+    std::vector<int4> items;
+    int r = 0;
+    for (int b = s0; b < s1; ++b) {
+      const int L = lengths[b];
+      for (int t = 0; t < L; ++t) { row_pos[r + t] = t; row_seq[r + t] = b; }
+      for (int q0 = 0; q0 < L; q0 += 64) items.push_back(make_int4(b, q0, r + q0, L));
+      r += L;
+      last_row[b - s0] = r - 1;
+    }
+    if ((int)items.size() > h->max_items) { end_call(h); return fail(LLM_ERR_OUT_OF_RANGE, "too many attention tiles"); }
+    CUDA_TRY(cudaMemcpyAsync(h->d_row_pos, row_pos.data(), rows * sizeof(int), cudaMemcpyHostToDevice, h->stream));
+    CUDA_TRY(cudaMemcpyAsync(h->d_row_seq, row_seq.data(), rows * sizeof(int), cudaMemcpyHostToDevice, h->stream));
+    CUDA_TRY(cudaMemcpyAsync(h->d_last_row, last_row.data(), nb * sizeof(int), cudaMemcpyHostToDevice, h->stream));
+    CUDA_TRY(cudaMemcpyAsync(h->d_items, items.data(), items.size() * sizeof(int4), cudaMemcpyHostToDevice, h->stream));
+    StepArgs a{tokens + tok_off, h->d_row_pos, h->d_row_seq, tables, next_ids + s0,
+               logits ? logits + (size_t)s0 * c.vocab : nullptr, h->d_last_row, rows, nb};
+    CUDA_TRY(launch_set_args(h->d_args, a, h->stream));
+    h->launch_counter++;
+    st = enqueue_forward(h, rows, nb, true, (int)items.size());
+    if (st != LLM_OK) { end_call(h); return st; }
+    tok_off += rows;
+    s0 = s1;
+  }
+  end_call(h);
+  return LLM_OK;
+}
+
+llm_status llm_decode_step_host(llm_handle* h, const int32_t* tokens, const int32_t* positions,
+                                const int32_t* tables, int B, int32_t* next_ids, float* logits) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  if (B <= 0) return fail(LLM_ERR_INVALID_ARG, "B must be positive");
+  if (B > h->cfg.max_batch) return fail(LLM_ERR_OUT_OF_RANGE, "B exceeds max_batch");
+  if (!tokens || !positions || !next_ids) return fail(LLM_ERR_INVALID_ARG, "NULL tokens/positions/next_ids");
+  const bool need_tables = !h->cfg.contiguous_kv;
+  if (need_tables && !tables) return fail(LLM_ERR_INVALID_ARG, "NULL block_tables");
+  CUDA_TRY(cudaMemcpyAsync(h->d_host_tokens, tokens, B * sizeof(int), cudaMemcpyHostToDevice, h->stream));
+  CUDA_TRY(cudaMemcpyAsync(h->d_host_pos, positions, B * sizeof(int), cudaMemcpyHostToDevice, h->stream));
+  if (need_tables)
+    CUDA_TRY(cudaMemcpyAsync(h->d_host_tables, tables, (size_t)B * h->cfg.max_blocks_per_seq * sizeof(int),
+                             cudaMemcpyHostToDevice, h->stream));
+  st = llm_decode_step(h, h->d_host_tokens, h->d_host_pos, need_tables ? h->d_host_tables : nullptr, B,
+                       h->d_host_ids, logits ? h->d_host_logits : nullptr);
+  if (st != LLM_OK) return st;
+  CUDA_TRY(cudaMemcpyAsync(next_ids, h->d_host_ids, B * sizeof(int), cudaMemcpyDeviceToHost, h->stream));
+  if (logits)
+    CUDA_TRY(cudaMemcpyAsync(logits, h->d_host_logits, (size_t)B * h->cfg.vocab * sizeof(float),
+                             cudaMemcpyDeviceToHost, h->stream));
+  CUDA_TRY(cudaStreamSynchronize(h->stream));
+  return LLM_OK;
+}
+
+llm_status llm_get_error_flags(llm_handle* h, uint32_t* flags) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  if (!flags) return fail(LLM_ERR_INVALID_ARG, "flags is NULL");
+  CUDA_TRY(cudaStreamSynchronize(h->stream));
+  unsigned v = 0;
+  CUDA_TRY(cudaMemcpy(&v, h->flags, sizeof(v), cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(h->flags, 0, sizeof(unsigned)));
+  *flags = v;
+  return v ? fail(LLM_ERR_DEVICE_FLAG, "device error flags 0x" + std::to_string(v)) : LLM_OK;
+}
+
+llm_status llm_set_profiling(llm_handle* h, int enable) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  h->profiling = enable != 0;
+  return LLM_OK;
+}
+
+llm_status llm_get_kernel_stats(llm_handle* h, llm_kernel_stat* out, int max, int* n, int reset) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  if (!n || (max > 0 && !out)) return fail(LLM_ERR_INVALID_ARG, "NULL output");
+  CUDA_TRY(cudaStreamSynchronize(h->stream));
+  for (auto& r : h->prof) {
+    float ms = 0.0f;
+    CUDA_TRY(cudaEventElapsedTime(&ms, r.a, r.b));
+    Stat& s = h->stats[r.name];
+    s.launches++;
+    s.ms += ms;
+  }
+  h->prof.clear();
+  h->event_next = 0;
+  int i = 0;
+  for (auto& kv : h->stats) {
+    if (i >= max) break;
+    memset(&out[i], 0, sizeof(out[i]));
+    strncpy(out[i].name, kv.first.c_str(), sizeof(out[i].name) - 1);
+    out[i].launches = kv.second.launches;
+    out[i].total_ms = kv.second.ms;
+    ++i;
+  }
+  *n = i;
+  if (reset) h->stats.clear();
+  return LLM_OK;
+}
+
+llm_status llm_last_launch_count(llm_handle* h, int* n) {
+  if (!h || !n) return fail(LLM_ERR_INVALID_ARG, "NULL argument");
+  *n = h->last_launches;
+  return LLM_OK;
+}
+
+llm_status llm_set_graphs(llm_handle* h, int enable) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  h->use_graphs = enable != 0 && stream_capturable(h->stream);
+  return LLM_OK;
+}
+
+llm_status llm_set_linear_variant(llm_handle* h, int variant) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  if (variant < LIN_AUTO || variant > LIN_TC) return fail(LLM_ERR_INVALID_ARG, "variant must be 0..3");
+  CUDA_TRY(cudaStreamSynchronize(h->stream));
+  for (auto& kv : h->graphs) {
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    if (kv.second.graph) cudaGraphDestroy(kv.second.graph);
+  }
+  h->graphs.clear();
+  h->lin_variant = variant;
+  return LLM_OK;
+}
+
+}  // extern "C"

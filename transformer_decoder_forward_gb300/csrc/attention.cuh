@@ -1,0 +1,40 @@
+// Causal attention over the paged KV cache (declarations).
+#pragma once
+#include "common.cuh"
+
+namespace llm {
+
+// Decode: one query row per sequence, keys 0..positions[b].
+struct AttnDecodeParams {
+  const float* q;           // [B][H*64] fp32, RoPE already applied
+  KVLayer kv;
+  const StepArgs* args;     // positions, block tables
+  int B;
+  int n_heads;
+  int split;                // tokens per split (multiple of 16)
+  int max_splits;           // grid.y
+  float* part_o;            // [B][H][max_splits][64]
+  float* part_ml;           // [B][H][max_splits][2]  (running max, sum of exp)
+  void* out;                // [B][H*64] in the activation dtype
+  int out_dtype;
+  unsigned* flags;
+};
+
+// Prefill: packed rows; a work item is (sequence, first query position, row of that
+// query, sequence length); keys of sequence s are positions 0..len-1 in the pool.
+struct AttnPrefillParams {
+  const float* q;           // [rows][H*64] fp32
+  KVLayer kv;
+  const StepArgs* args;     // block tables
+  const int4* items;        // {seq, q_pos0, row0, len}
+  int n_items;
+  int n_heads;
+  void* out;                // [rows][H*64] activation dtype
+  int out_dtype;
+  unsigned* flags;
+};
+
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, int kv_dtype, cudaStream_t s, bool pdl);
+cudaError_t launch_attn_prefill(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl);
+
+}  // namespace llm

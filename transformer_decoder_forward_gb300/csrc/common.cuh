@@ -1,0 +1,175 @@
+// Shared device-side definitions of the decoder-step kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace llm {
+
+enum : int { DT_F32 = 0, DT_BF16 = 1 };
+enum : int { ARCH_GPT2 = 0, ARCH_LLAMA = 1 };
+constexpr int HD = 64;          // head_dim (the only supported value)
+constexpr int KVB = 16;         // tokens per KV block
+
+// Device error word bits (mirrors LLM_FLAG_* in include/llm.h).
+constexpr unsigned FLAG_BAD_TOKEN = 0x01u;
+constexpr unsigned FLAG_BAD_POSITION = 0x02u;
+constexpr unsigned FLAG_BAD_BLOCK = 0x04u;
+constexpr unsigned FLAG_NAN_LOGIT = 0x08u;
+constexpr unsigned FLAG_WAIT_TIMEOUT = 0x10u;
+
+typedef __nv_bfloat16 bf16;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ void set_flag(unsigned* flags, unsigned bit) {
+  if (flags) atomicOr(flags, bit);
+}
+
+// 16-byte global loads. Weights are read once per step: stream them past L1.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// Unpack 16 bytes into floats: 4 for fp32, 8 for bf16.
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+};
+template <> struct Vec16<bf16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Greedy-argmax order: NaN ranks above every number (lowest index among NaNs),
+// otherwise larger value wins and ties go to the lower index.
+__device__ __forceinline__ bool argmax_better(float a, int ia, float b, int ib) {
+  const bool na = a != a, nb = b != b;
+  if (na || nb) return na && (!nb || ia < ib);
+  return a > b || (a == b && ia < ib);
+}
+
+// Programmatic dependent launch: wait for the producer grid / let the consumer start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Per-call pointers that change from step to step. A graph replays with fixed
+// kernel parameters, so kernels read these through one device-resident struct
+// that the first node of the step rewrites.
+struct StepArgs {
+  const int* tokens;        // [M]
+  const int* positions;     // [M] position of each row
+  const int* row_seq;       // [M] sequence of each row, or nullptr (row m is sequence m)
+  const int* block_tables;  // [B][mbps]
+  int* next_ids;            // [B]
+  float* logits;            // [B][V] or nullptr
+  const int* last_row;      // [B] row of each sequence's last token, or nullptr (row b)
+  int M;
+  int B;
+};
+
+// Paged KV pool of one layer: [block][kv_head][16][64], element type = weight dtype.
+struct KVLayer {
+  void* k;
+  void* v;
+  int num_blocks;
+  int n_kv_heads;
+  int mbps;        // max blocks per sequence (block-table row length)
+  int contiguous;  // sequence s owns blocks [s*mbps, (s+1)*mbps)
+};
+
+// Physical block holding logical position `pos` of sequence `seq`, or -1 (and a flag).
+__device__ __forceinline__ int kv_block(const KVLayer& kv, const int* tables, int seq, int pos, unsigned* flags) {
+  const int lb = pos >> 4;
+  if (pos < 0 || lb >= kv.mbps) { set_flag(flags, FLAG_BAD_POSITION); return -1; }
+  const int pb = kv.contiguous ? seq * kv.mbps + lb : tables[(size_t)seq * kv.mbps + lb];
+  if (pb < 0 || pb >= kv.num_blocks) { set_flag(flags, FLAG_BAD_BLOCK); return -1; }
+  return pb;
+}
+__device__ __forceinline__ size_t kv_offset(const KVLayer& kv, int pb, int g, int slot) {
+  return (((size_t)pb * kv.n_kv_heads + g) * KVB + slot) * HD;
+}
+
+// What a projection kernel does with its output tile.
+enum : int {
+  EPI_STORE_F32 = 0,  // out_f32[m][n] = y + b
+  EPI_STORE_ACT = 1,  // out[m][n] = act(y + b) in the activation dtype
+  EPI_RESID = 2,      // resid[m][n] += y + b              (fp32 residual stream)
+  EPI_GELU = 3,       // out[m][n] = gelu_tanh_clamped(y + b) (activation dtype)
+  EPI_SWIGLU = 4,     // out[m][j] = silu(gate_j) * up_j; tile columns = 32 gate rows + 32 up rows
+  EPI_QKV = 5,        // q -> q_out (fp32, RoPE'd), k/v -> KV pool slot of the row
+  EPI_HEAD = 6,       // logits (optional) + per-tile argmax partials
+};
+
+struct Epilogue {
+  int kind;
+  int act_dtype;        // DT_F32 / DT_BF16 for `out`
+  const void* bias;     // [N] in the weight dtype, or nullptr
+  void* out;            // STORE / GELU / SWIGLU output
+  int ld_out;
+  float* resid;         // RESID
+  int ld_resid;
+  // QKV
+  float* q_out;         // [M][H*64]
+  KVLayer kv;
+  int n_heads;
+  int rope;             // 1: rotate q and k (Llama)
+  float rope_theta;
+  // HEAD
+  float* part_val;      // [n_tiles][M]
+  int* part_idx;
+  int vocab;
+  // shared
+  const StepArgs* args;
+  unsigned* flags;
+};
+
+// Row r of the SwiGLU tile: tile columns 0..31 are gate rows, 32..63 the matching up rows.
+__device__ __forceinline__ int swiglu_row(int n0_half, int c, int d_ff) {
+  return c < 32 ? n0_half + c : d_ff + n0_half + (c - 32);
+}
+
+__device__ __forceinline__ float gelu_tanh_clamped(float x) {
+  const float kC = 0.7978845608028654f;   // sqrt(2/pi)
+  float u = kC * (x + 0.044715f * x * x * x);
+  u = fminf(15.0f, fmaxf(-15.0f, u));
+  return 0.5f * x * (1.0f + tanhf(u));
+}
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+}  // namespace llm

@@ -1,0 +1,37 @@
+// Projection kernels y = x . W^T with fused epilogues (declarations + parameters).
+#pragma once
+#include "common.cuh"
+
+namespace llm {
+
+// Tile columns per output tile: 64 = one head (keeps RoPE pairs and SwiGLU gate/up in one tile).
+constexpr int TILE_N = 64;
+
+struct LinearParams {
+  const void* W;        // [rows][K] weight, dtype wdt
+  const void* X;        // [M][ldx] activations, dtype xdt
+  int M, N, K, ldx;     // N: output columns of the epilogue (d_ff for SWIGLU)
+  int wdt, xdt, adt;    // weight / input / activation-output dtypes
+  int swiglu;           // 1: tile t reads gate rows t*32.. and up rows F + t*32..
+  Epilogue epi;
+  // split-K workspace for the GEMV path
+  float* part;          // fp32 partial sums
+  size_t part_elems;
+  unsigned* counters;   // per-tile arrival tickets (all zero between launches)
+  int counters_len;
+};
+
+inline int linear_tiles(const LinearParams& p) {
+  return p.swiglu ? (p.N + 31) / 32 : (p.N + TILE_N - 1) / TILE_N;
+}
+
+// Variants. AUTO picks by M; the others force one kernel (tests sweep all of them).
+enum : int { LIN_AUTO = 0, LIN_GEMV = 1, LIN_SIMT = 2, LIN_TC = 3 };
+
+// Each returns cudaSuccess or the launch error; `name` receives the kernel family name.
+cudaError_t launch_gemv(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
+cudaError_t launch_gemm_simt(const LinearParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_gemm_tc(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
+bool gemm_tc_supported(const LinearParams& p);
+
+}  // namespace llm

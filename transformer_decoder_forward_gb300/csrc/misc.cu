@@ -1,0 +1,181 @@
+// Embedding gather, row norms, greedy-argmax reduction and the step-argument node.
+#include "misc.cuh"
+
+namespace llm {
+
+namespace {
+
+constexpr int ROW_THREADS = 256;
+constexpr int MAX_PER_THREAD = 32;   // d_model <= 8192
+
+// h[m] = tok_emb[token] (+ pos_emb[position] for GPT-2): "bare-metal-llm", section
+// "What got built" (embedding lookup) and "Picking the model" (learned positions).
+template <typename WT>
+__global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
+  const int m = blockIdx.x;
+  pdl_wait();
+  const StepArgs* a = p.args;
+  int tok = a->tokens[m];
+  const int pos = a->positions[m];
+  if (tok < 0 || tok >= p.vocab) {
+    if (threadIdx.x == 0) set_flag(p.flags, FLAG_BAD_TOKEN);
+    tok = -1;
+  }
+  bool pos_ok = pos >= 0 && pos < p.n_ctx;
+  if (!pos_ok && threadIdx.x == 0) set_flag(p.flags, FLAG_BAD_POSITION);
+  const WT* te = reinterpret_cast<const WT*>(p.tok_emb) + (size_t)(tok < 0 ? 0 : tok) * p.d;
+  const WT* pe = p.pos_emb ? reinterpret_cast<const WT*>(p.pos_emb) + (size_t)(pos_ok ? pos : 0) * p.d : nullptr;
+  pdl_trigger();
+  for (int i = threadIdx.x; i < p.d; i += ROW_THREADS) {
+    float v = tok < 0 ? 0.0f : to_f32(te[i]);
+    if (pe && pos_ok) v += to_f32(pe[i]);
+    p.h[(size_t)m * p.d + i] = v;
+  }
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int w = 0; w < ROW_THREADS / 32; ++w) t += red[w];
+  return t;
+}
+
+// LayerNorm ((x - mean) / sqrt(var + eps) * g + b, biased variance) or RMSNorm
+// (x / sqrt(mean(x^2) + eps) * g), one row per CTA, warp-shuffle reductions
+// ("rvllm-metal", section "How a GPU runs your kernel": one threadgroup per row,
+// simd_sum then a small cross-group sum).
+template <typename WT, typename AT>
+__global__ void __launch_bounds__(ROW_THREADS) k_norm(const NormParams p) {
+  __shared__ float red[ROW_THREADS / 32];
+  const int r = blockIdx.x;
+  pdl_wait();
+  int src = r;
+  if (p.use_last_row && p.args->last_row) src = p.args->last_row[r];
+  const float* x = p.h + (size_t)src * p.d;
+  float v[MAX_PER_THREAD];
+  int n = 0;
+  float s = 0.0f;
+  for (int i = threadIdx.x; i < p.d; i += ROW_THREADS, ++n) {
+    v[n] = x[i];
+    s += v[n];
+  }
+  float mean = 0.0f, scale;
+  if (p.layer_norm) {
+    mean = block_sum(s, red) / p.d;
+    float q = 0.0f;
+    for (int j = 0; j < n; ++j) q += (v[j] - mean) * (v[j] - mean);
+    const float var = block_sum(q, red) / p.d;
+    scale = 1.0f / sqrtf(var + p.eps);
+  } else {
+    float q = 0.0f;
+    for (int j = 0; j < n; ++j) q += v[j] * v[j];
+    const float ms = block_sum(q, red) / p.d;
+    scale = 1.0f / sqrtf(ms + p.eps);
+  }
+  pdl_trigger();
+  const WT* gw = reinterpret_cast<const WT*>(p.g);
+  const WT* bw = reinterpret_cast<const WT*>(p.b);
+  AT* out = reinterpret_cast<AT*>(p.out) + (size_t)r * p.d;
+  n = 0;
+  for (int i = threadIdx.x; i < p.d; i += ROW_THREADS, ++n) {
+    float y = (v[n] - mean) * scale * to_f32(gw[i]);
+    if (bw) y += to_f32(bw[i]);
+    out[i] = from_f32<AT>(y);
+  }
+}
+
+// next_ids[b] = argmax over the per-tile partials of row b ("rvllm-metal", section
+// "What the kernels do": a GPU argmax so one integer per sequence comes back).
+__global__ void __launch_bounds__(ROW_THREADS) k_argmax_reduce(const ArgmaxParams p) {
+  __shared__ float sv[ROW_THREADS / 32];
+  __shared__ int si[ROW_THREADS / 32];
+  const int b = blockIdx.x;
+  pdl_wait();
+  const StepArgs* a = p.args;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int t = threadIdx.x; t < p.n_tiles; t += ROW_THREADS) {
+    const float v = p.part_val[(size_t)t * a->B + b];
+    const int i = p.part_idx[(size_t)t * a->B + b];
+    if (argmax_better(v, i, best, bi)) { best = v; bi = i; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (argmax_better(ov, oi, best, bi)) { best = ov; bi = oi; }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { sv[warp] = best; si[warp] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < ROW_THREADS / 32; ++w)
+      if (argmax_better(sv[w], si[w], best, bi)) { best = sv[w]; bi = si[w]; }
+    if (best != best) set_flag(p.flags, FLAG_NAN_LOGIT);
+    a->next_ids[b] = bi;
+  }
+}
+
+__global__ void k_set_args(StepArgs* dst, StepArgs v) { *dst = v; }
+
+template <typename WT>
+cudaError_t embed_t(const EmbedParams& p, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t c = make_launch_cfg(dim3(p.M), dim3(ROW_THREADS), 0, s, attr, pdl);
+  return cudaLaunchKernelEx(&c, k_embed<WT>, p);
+}
+template <typename WT, typename AT>
+cudaError_t norm_t(const NormParams& p, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t c = make_launch_cfg(dim3(p.rows), dim3(ROW_THREADS), 0, s, attr, pdl);
+  return cudaLaunchKernelEx(&c, k_norm<WT, AT>, p);
+}
+
+}  // namespace
+
+cudaLaunchConfig_t make_launch_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr,
+                                   bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
+}
+
+cudaError_t launch_embed(const EmbedParams& p, int wdt, cudaStream_t s, bool pdl) {
+  if (p.M <= 0) return cudaSuccess;
+  return wdt == DT_F32 ? embed_t<float>(p, s, pdl) : embed_t<bf16>(p, s, pdl);
+}
+
+cudaError_t launch_norm(const NormParams& p, int wdt, int adt, cudaStream_t s, bool pdl) {
+  if (p.rows <= 0) return cudaSuccess;
+  if (p.d > ROW_THREADS * MAX_PER_THREAD) return cudaErrorInvalidValue;
+  if (wdt == DT_F32) return adt == DT_F32 ? norm_t<float, float>(p, s, pdl) : norm_t<float, bf16>(p, s, pdl);
+  return adt == DT_F32 ? norm_t<bf16, float>(p, s, pdl) : norm_t<bf16, bf16>(p, s, pdl);
+}
+
+cudaError_t launch_argmax(const ArgmaxParams& p, int B, cudaStream_t s, bool pdl) {
+  if (B <= 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t c = make_launch_cfg(dim3(B), dim3(ROW_THREADS), 0, s, attr, pdl);
+  return cudaLaunchKernelEx(&c, k_argmax_reduce, p);
+}
+
+cudaError_t launch_set_args(StepArgs* dst, const StepArgs& v, cudaStream_t s) {
+  k_set_args<<<1, 1, 0, s>>>(dst, v);
+  return cudaGetLastError();
+}
+
+const void* set_args_kernel() { return reinterpret_cast<const void*>(&k_set_args); }
+
+}  // namespace llm
