@@ -190,8 +190,8 @@ def test_gpt2_124m_fp32_b32_teacher_forced(gpu_lib, W):
     assert run.dec.error_flags() == 0
     for i, b in enumerate(rows):
         ref = oracle_teacher(model, run.prompts[b], stream[:, b])
-        check_logits(z[:, i], ref, W.model.dtype, f"{W.name} seq {b}")
-        check_ids(ids[:, b], ref, f"{W.name} seq {b}")
+        check_logits(z[:, i], ref, W.model.dtype, f"{W.name} seq {b}", scale=W.weight_scale)
+        check_ids(ids[:, b], ref, f"{W.name} seq {b}", scale=W.weight_scale)
     if W.weight_scale == 8.0:
         assert model.stats["max_gelu_arg"] > 15.0
     run.close()
