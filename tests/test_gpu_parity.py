@@ -67,6 +67,30 @@ def test_graph_replay_equals_eager_bitwise(gpu_lib, small_models):
     np.testing.assert_array_equal(outs[0][1], outs[1][1])
 
 
+def test_programmatic_launch_does_not_change_results(gpu_lib, small_models):
+    """Kernels launched with programmatic dependent launch (the default) and without it agree bitwise."""
+    import subprocess
+    import sys
+    code = ("import sys, numpy as np; sys.path.insert(0, 'tests'); sys.path.insert(0, '.');"
+            "import workloads as wl; from test_gpu_parity import *;"
+            "from transformer_decoder_forward_gb300.runner import WorkloadRun;"
+            "w = wl.make_weights(SMALL_LLAMA, scale=2.0, perturb=True);"
+            "run = WorkloadRun(small_workload(SMALL_LLAMA), host_weights=w, lengths=LENGTHS);"
+            "ids, z = run_gpu_teacher(run, wl.draw_stream(len(LENGTHS), STEPS, SMALL_LLAMA.vocab));"
+            "np.save(sys.argv[1], z); np.save(sys.argv[1] + '.ids', ids)")
+    import os
+    import tempfile
+    d = tempfile.mkdtemp()
+    outs = []
+    for flag in ("1", "0"):
+        f = os.path.join(d, f"z{flag}.npy")
+        env = dict(os.environ, LLM_PDL=flag)
+        subprocess.run([sys.executable, "-c", code, f], check=True, env=env, cwd=os.path.dirname(os.path.dirname(__file__)) or ".")
+        outs.append((np.load(f), np.load(f + ".ids.npy")))
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+
+
 def test_block_table_layout_does_not_change_results(gpu_lib, small_models):
     from transformer_decoder_forward_gb300.runner import WorkloadRun
     w, _ = small_models[SMALL_GPT2.name]

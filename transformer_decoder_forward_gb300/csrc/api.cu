@@ -109,7 +109,7 @@ struct llm_handle {
   float* d_host_logits = nullptr;
   // execution options
   bool use_graphs = true;
-  bool pdl = false;
+  bool pdl = true;   // programmatic dependent launch between the step's kernels
   int lin_variant = LIN_AUTO;
   std::map<int, GraphEntry> graphs;
   // profiling
@@ -458,7 +458,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
 #undef ALLOC
   if (!stream_capturable(h->stream)) h->use_graphs = false;
   if (const char* env = getenv("LLM_NO_GRAPH")) h->use_graphs = h->use_graphs && env[0] != '1';
-  if (const char* env = getenv("LLM_PDL")) h->pdl = env[0] == '1';
+  if (const char* env = getenv("LLM_PDL")) h->pdl = env[0] != '0';
   *out = h;
   return LLM_OK;
 }

@@ -25,53 +25,92 @@ constexpr int MAX_G = 8;
 constexpr int MAX_SPLIT = 256;
 constexpr float SM_SCALE = 0.125f;   // 1/sqrt(64)
 
+// smem for one split: K and V blocks (split/16 blocks of 16 x 64 elements each), then a
+// small fixed area. The whole split is in flight at once: one thread issues a TMA bulk
+// copy per KV block (16 contiguous token rows of one head) onto a single mbarrier.
+template <typename KT>
+__host__ __device__ constexpr size_t attn_decode_smem(int split) {
+  return 2 * (size_t)split * HD * sizeof(KT);
+}
+
 template <typename KT>
 __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDecodeParams p) {
+  extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ __align__(16) float qs[MAX_G][HD];
   __shared__ float sc[MAX_G][MAX_SPLIT];
   __shared__ __align__(16) float ored[AD_THREADS / 32][MAX_G][HD];
   __shared__ float red[AD_THREADS / 32][MAX_G];
   __shared__ float stat[2][MAX_G];
+  __shared__ int blk_ok[MAX_SPLIT / KVB];
+  __shared__ __align__(8) uint64_t bar;
 
   constexpr int EPL = 16 / sizeof(KT);    // elements per 16-byte load
   constexpr int LPT = HD / EPL;           // lanes per token row: 16 (fp32) or 8 (bf16)
   constexpr int TPW = 32 / LPT;           // token rows per warp load
   constexpr int NWARP = AD_THREADS / 32;
+  constexpr unsigned BLK_BYTES = KVB * HD * sizeof(KT);
 
   const int Hkv = p.kv.n_kv_heads, H = p.n_heads, G = H / Hkv;
   const int b = blockIdx.x / Hkv, g = blockIdx.x - b * Hkv, sp = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();
+  KT* Ks = reinterpret_cast<KT*>(dyn);
+  KT* Vs = Ks + (size_t)p.split * HD;
+  pdl_wait();   // the new token's K/V is written by the projection that precedes this kernel
   const StepArgs* a = p.args;
   const int pos = a->positions[b];
   const int ctx = pos + 1;
   const int t0 = sp * p.split;
   if (t0 >= ctx) return;
   const int nt = min(p.split, ctx - t0);
+  const int nb = (nt + KVB - 1) / KVB;
 
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const KT* kbase = reinterpret_cast<const KT*>(p.kv.k);
+    const KT* vbase = reinterpret_cast<const KT*>(p.kv.v);
+    int pbs[MAX_SPLIT / KVB];
+    unsigned bytes = 0;
+    for (int i = 0; i < nb; ++i) {
+      pbs[i] = kv_block(p.kv, a->block_tables, b, t0 + i * KVB, p.flags);
+      blk_ok[i] = pbs[i] >= 0;
+      if (pbs[i] >= 0) bytes += 2 * BLK_BYTES;
+    }
+    mbar_arrive_expect_tx(&bar, bytes);
+    for (int i = 0; i < nb; ++i) {
+      if (pbs[i] < 0) continue;
+      const size_t off = kv_offset(p.kv, pbs[i], g, 0);
+      bulk_g2s(Ks + (size_t)i * KVB * HD, kbase + off, BLK_BYTES, &bar);
+      bulk_g2s(Vs + (size_t)i * KVB * HD, vbase + off, BLK_BYTES, &bar);
+    }
+  }
   for (int i = tid; i < G * HD; i += AD_THREADS) {
     const int j = i / HD, d = i - j * HD;
     qs[j][d] = p.q[(size_t)b * H * HD + (size_t)(g * G + j) * HD + d] * SM_SCALE;
   }
+  const bool ok = mbar_wait(&bar, 0, p.flags);
   __syncthreads();
+  if (!ok) {
+    // the copies may still be landing: give them one more bounded wait before leaving
+    mbar_wait(&bar, 0, p.flags);
+    return;
+  }
+  pdl_trigger();
 
-  const KT* kbase = reinterpret_cast<const KT*>(p.kv.k);
-  const KT* vbase = reinterpret_cast<const KT*>(p.kv.v);
   const int sub = lane / LPT, li = lane - sub * LPT;
-
-  // ---- scores: LPT lanes per token, 16-byte loads along the head dimension
+  // ---- scores: LPT lanes per token row, 16-byte shared loads along the head dimension
   for (int tb = warp * TPW; tb < nt; tb += NWARP * TPW) {
     const int t = tb + sub;
     float kf[EPL];
+    const bool valid = t < nt && blk_ok[t / KVB];
+    if (valid) {
+      Vec16<KT>::unpack(*reinterpret_cast<const uint4*>(Ks + (size_t)t * HD + li * EPL), kf);
+    } else {
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) kf[e] = 0.0f;
-    if (t < nt) {
-      const int pt = t0 + t;
-      const int pb = kv_block(p.kv, a->block_tables, b, pt, p.flags);
-      if (pb >= 0) {
-        const uint4 u = ldg16(kbase + kv_offset(p.kv, pb, g, pt & (KVB - 1)) + li * EPL);
-        Vec16<KT>::unpack(u, kf);
-      }
+      for (int e = 0; e < EPL; ++e) kf[e] = 0.0f;
     }
     for (int j = 0; j < G; ++j) {
       float d = 0.0f;
@@ -79,7 +118,7 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
       for (int e = 0; e < EPL; ++e) d = fmaf(kf[e], qs[j][li * EPL + e], d);
 #pragma unroll
       for (int o = LPT / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      if (li == 0 && t < nt) sc[j][t] = d;
+      if (li == 0 && t < nt) sc[j][t] = valid ? d : -INFINITY;
     }
   }
   __syncthreads();
@@ -102,12 +141,11 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
     const float m = stat[0][j];
     float l = 0.0f;
     for (int t = tid; t < nt; t += AD_THREADS) {
-      const float e = expf(sc[j][t] - m);
+      const float e = m == -INFINITY ? 0.0f : expf(sc[j][t] - m);
       sc[j][t] = e;
       l += e;
     }
     l = warp_sum(l);
-    __syncthreads();
     if (lane == 0) red[warp][j] = l;
   }
   __syncthreads();
@@ -126,11 +164,9 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[j][e] = 0.0f;
   for (int t = tg; t < nt; t += NTG) {
-    const int pt = t0 + t;
-    const int pb = kv_block(p.kv, a->block_tables, b, pt, nullptr);
-    if (pb < 0) continue;
+    if (!blk_ok[t / KVB]) continue;
     float vf[EPL];
-    Vec16<KT>::unpack(ldg16(vbase + kv_offset(p.kv, pb, g, pt & (KVB - 1)) + dg * EPL), vf);
+    Vec16<KT>::unpack(*reinterpret_cast<const uint4*>(Vs + (size_t)t * HD + dg * EPL), vf);
 #pragma unroll
     for (int j = 0; j < MAX_G; ++j) {
       if (j < G) {
@@ -159,7 +195,6 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
       for (int e = 0; e < EPL; ++e) ored[warp][j][dg * EPL + e] = acc[j][e];
   }
   __syncthreads();
-  pdl_trigger();
   for (int i = tid; i < G * HD; i += AD_THREADS) {
     const int j = i / HD, d = i - j * HD;
     float o = 0.0f;
@@ -185,7 +220,7 @@ __global__ void __launch_bounds__(HD) k_attn_decode_merge(const AttnDecodeParams
   for (int s = 0; s < ns; ++s) m = fmaxf(m, ml[2 * s]);
   float l = 0.0f, o = 0.0f;
   for (int s = 0; s < ns; ++s) {
-    const float w = expf(ml[2 * s] - m);
+    const float w = m == -INFINITY ? 0.0f : expf(ml[2 * s] - m);
     l = fmaf(w, ml[2 * s + 1], l);
     o = fmaf(w, po[s * HD + d], o);
   }
@@ -344,8 +379,16 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, 
 
 template <typename KT, typename AT>
 cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
+  const size_t smem = attn_decode_smem<KT>(p.split);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_split<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)attn_decode_smem<KT>(MAX_SPLIT));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t c1 = make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(AD_THREADS), 0, s, attr, pdl);
+  cudaLaunchConfig_t c1 = make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(AD_THREADS), smem, s, attr, pdl);
   cudaError_t e = cudaLaunchKernelEx(&c1, k_attn_decode_split<KT>, p);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[1];

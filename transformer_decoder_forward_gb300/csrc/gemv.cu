@@ -3,74 +3,148 @@
 // Decode is memory bound: every step reads all weights once and does little
 // arithmetic per byte ("rvllm-metal", section "The matmul pain story"). The
 // pages' linear_small gives one simdgroup per output and re-reads the
-// activations per output; here the activations of all M rows sit in shared
+// activations per output; here the activations of up to 32 rows sit in shared
 // memory and every weight element loaded (16-byte streaming loads, 8 lanes
-// covering 128 contiguous bytes of a row) is used for all M rows.
+// covering 128 contiguous bytes of a row) is used for all of them.
 //
-// CTA = 256 threads = 8 warps; warp w owns tile columns 8w..8w+7; in a warp,
-// lane = 4 row groups x 8 k-lanes and each thread holds 2 weight rows.
-// Small matrices split K across CTAs (the pages' linear_mma_small splits K
-// across simdgroups for the same reason: too few output tiles to fill the
-// GPU); partial tiles go to a workspace and the last CTA to arrive for a tile
-// sums them in split order (deterministic) and runs the epilogue.
+// CTA = 256 threads = 8 warps and owns 64 output columns (one head: RoPE pairs,
+// SwiGLU gate/up pairs and argmax tiles stay inside the CTA); warp w owns
+// columns 8w..8w+7; in a warp, lane = 4 row groups x 8 k-lanes and each thread
+// holds 2 weight rows.
+//
+// Small matrices split K across the CTAs of a thread-block cluster (the pages'
+// linear_mma_small splits K across simdgroups because too few output tiles
+// fill the GPU). Partials stay in shared memory; after a cluster barrier each
+// CTA sums a slice of the rows over all ranks in rank order through
+// distributed shared memory (deterministic, no global round trip) and runs the
+// epilogue for that slice. The split depends on the weight shape only, so a
+// row's arithmetic never depends on how many rows share the launch.
+//
+// Weights do not depend on earlier kernels: before waiting on its producer
+// (programmatic dependent launch) a CTA already warms L2 with its weight slice
+// and loads its first weight vectors into registers.
+#include <cooperative_groups.h>
+
 #include <algorithm>
 
 #include "epilogue.cuh"
 #include "linear.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace llm {
 
 namespace {
 
 constexpr int GEMV_THREADS = 256;
-constexpr int TL_LD = TILE_N + 1;   // padded row stride of the output tile in smem
+constexpr int TL_LD = TILE_N + 1;   // padded row stride of the output tiles in smem
+constexpr int GEMV_MT = 32;         // rows per CTA (larger M uses grid.z)
+constexpr int U = 2;                // weight vectors per row in flight per thread and stage
+
+template <typename XT, int VEC>
+__device__ __forceinline__ void lds_x(const XT* p, float* f);
+template <>
+__device__ __forceinline__ void lds_x<float, 4>(const float* p, float* f) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void lds_x<float, 8>(const float* p, float* f) {
+  lds_x<float, 4>(p, f);
+  lds_x<float, 4>(p + 4, f + 4);
+}
+template <>
+__device__ __forceinline__ void lds_x<bf16, 8>(const bf16* p, float* f) {
+  Vec16<bf16>::unpack(*reinterpret_cast<const uint4*>(p), f);
+}
+template <>
+__device__ __forceinline__ void lds_x<bf16, 4>(const bf16* p, float* f) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  f[0] = __uint_as_float(u.x << 16); f[1] = __uint_as_float(u.x & 0xffff0000u);
+  f[2] = __uint_as_float(u.y << 16); f[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+
+__host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+template <typename XT>
+__host__ __device__ constexpr size_t gemv_smem(int MT, int kcta) {
+  return align16((size_t)MT * (kcta + 16 / sizeof(XT)) * sizeof(XT)) + 2 * (size_t)MT * TL_LD * sizeof(float);
+}
 
 template <typename WT, typename XT, typename AT, int MT>
-__global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int kc, int ks_total) {
-  extern __shared__ __align__(16) float smem[];
+__global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int kcta, int ks_total) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   constexpr int VEC = Vec16<WT>::N;
+  constexpr int STRIDE = 8 * VEC;
+  constexpr int XE = 16 / sizeof(XT);      // x elements per 16 bytes
   const int tile = blockIdx.x, ks = blockIdx.y, mbase = blockIdx.z * MT;
   const int mcount = min(MT, p.M - mbase);
-  const int k0 = ks * kc;
-  const int kcl = min(kc, p.K - k0);
-  const int ldxs = kc + 4;
-  float* xs = smem;                       // [MT][ldxs]
-  float* tl = smem + MT * ldxs;           // [MT][TL_LD]
-  const int F = p.N;                      // SWIGLU: output width = d_ff
+  const int k0 = ks * kcta;
+  const int kcl = max(0, min(kcta, p.K - k0));
+  const int ldxs = kcta + XE;
+  XT* xs = reinterpret_cast<XT*>(smem_raw);                                          // [MT][ldxs]
+  float* tl = reinterpret_cast<float*>(smem_raw + align16((size_t)MT * ldxs * sizeof(XT)));  // [MT][TL_LD]
+  float* red = tl + MT * TL_LD;                                                      // [MT][TL_LD]
+  const int F = p.N;
 
-  // Weights do not depend on earlier kernels: warm L2 with this CTA's rows before waiting.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 3, kl = lane & 7;
   const WT* W = reinterpret_cast<const WT*>(p.W);
-  int wrow[2];
+  const WT* wp[2];
   bool rvalid[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int c = warp * 8 + g * 2 + r;   // tile column
-    int row, outcol;
+    int row;
     if (p.swiglu) {
-      outcol = tile * 32 + (c & 31);
       row = swiglu_row(tile * 32, c, F);
-      rvalid[r] = outcol < F;
+      rvalid[r] = tile * 32 + (c & 31) < F;
     } else {
       row = tile * TILE_N + c;
       rvalid[r] = row < p.N;
     }
-    wrow[r] = rvalid[r] ? row : 0;
+    wp[r] = W + (size_t)(rvalid[r] ? row : 0) * p.K + k0;
   }
-  if (kl == 0) {
+
+  // ---- before the dependency wait: weights only
+  const bool vec_ok = (p.K % VEC) == 0;
+  const int kvec_end = vec_ok ? (kcl / VEC) * VEC : 0;
+  if (threadIdx.x < TILE_N && kvec_end > 0 && ((p.K * sizeof(WT)) % 16) == 0) {
+    const int c = threadIdx.x;
+    const int row = p.swiglu ? swiglu_row(tile * 32, c, F) : tile * TILE_N + c;
+    const bool ok = p.swiglu ? (tile * 32 + (c & 31) < F) : row < p.N;
+    if (ok) bulk_prefetch_l2(W + (size_t)row * p.K + k0, (unsigned)(kvec_end * sizeof(WT)));
+  }
+  uint4 wa[U][2], wb[U][2];
+  auto load_w = [&](uint4 (&w)[U][2], int kbase) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
-      if (rvalid[r] && kcl > 0)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(W + (size_t)wrow[r] * p.K + k0));
-  }
+    for (int u = 0; u < U; ++u) {
+      const int kk = kbase + u * STRIDE;
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        w[u][r] = (rvalid[r] && kk < kvec_end) ? ldg_stream16(wp[r] + kk) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  load_w(wa, kl * VEC);
+  pdl_trigger();
   pdl_wait();
 
-  // Stage this CTA's slice of X (rows mbase.., columns k0..k0+kcl) as fp32.
+  // ---- stage this CTA's slice of X (rows mbase.., columns k0..k0+kcl)
   const XT* X = reinterpret_cast<const XT*>(p.X);
-  for (int i = threadIdx.x; i < mcount * kcl; i += GEMV_THREADS) {
-    const int m = i / kcl, k = i - m * kcl;
-    xs[m * ldxs + k] = to_f32(X[(size_t)(mbase + m) * p.ldx + k0 + k]);
+  const bool x_vec = ((p.ldx % XE) == 0) && ((k0 % XE) == 0) && ((kcl % XE) == 0);
+  if (x_vec) {
+    const int chunks = kcl / XE;
+    for (int i = threadIdx.x; i < mcount * chunks; i += GEMV_THREADS) {
+      const int m = i / chunks, c = i - m * chunks;
+      cp_async16(xs + (size_t)m * ldxs + c * XE, X + (size_t)(mbase + m) * p.ldx + k0 + c * XE);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+  } else {
+    for (int i = threadIdx.x; i < mcount * kcl; i += GEMV_THREADS) {
+      const int m = i / kcl, k = i - m * kcl;
+      xs[(size_t)m * ldxs + k] = X[(size_t)(mbase + m) * p.ldx + k0 + k];
+    }
   }
   __syncthreads();
 
@@ -80,67 +154,50 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[r][m] = 0.0f;
 
-  const bool vec_ok = (p.K % VEC) == 0;
-  const int kvec_end = vec_ok ? (kcl / VEC) * VEC : 0;
-  constexpr int U = MT <= 8 ? 4 : 2;
-  constexpr int STRIDE = 8 * VEC;
-  const WT* wp0 = W + (size_t)wrow[0] * p.K + k0;
-  const WT* wp1 = W + (size_t)wrow[1] * p.K + k0;
-
-  auto fma_chunk = [&](const uint4& w0, const uint4& w1, int k) {
+  auto fma_vec = [&](const uint4& w0, const uint4& w1, int k) {
     float f0[VEC], f1[VEC];
     Vec16<WT>::unpack(w0, f0);
     Vec16<WT>::unpack(w1, f1);
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (m < mcount) {
-        const float* xr = xs + m * ldxs + k;
+        float xv[VEC];
+        lds_x<XT, VEC>(xs + (size_t)m * ldxs + k, xv);
 #pragma unroll
-        for (int j = 0; j < VEC; j += 4) {
-          const float4 xv = *reinterpret_cast<const float4*>(xr + j);
-          acc[0][m] = fmaf(f0[j], xv.x, acc[0][m]);
-          acc[0][m] = fmaf(f0[j + 1], xv.y, acc[0][m]);
-          acc[0][m] = fmaf(f0[j + 2], xv.z, acc[0][m]);
-          acc[0][m] = fmaf(f0[j + 3], xv.w, acc[0][m]);
-          acc[1][m] = fmaf(f1[j], xv.x, acc[1][m]);
-          acc[1][m] = fmaf(f1[j + 1], xv.y, acc[1][m]);
-          acc[1][m] = fmaf(f1[j + 2], xv.z, acc[1][m]);
-          acc[1][m] = fmaf(f1[j + 3], xv.w, acc[1][m]);
+        for (int j = 0; j < VEC; ++j) {
+          acc[0][m] = fmaf(f0[j], xv[j], acc[0][m]);
+          acc[1][m] = fmaf(f1[j], xv[j], acc[1][m]);
         }
       }
     }
   };
 
-  int k = kl * VEC;
-  for (; k + (U - 1) * STRIDE + VEC <= kvec_end; k += U * STRIDE) {
-    uint4 w0[U], w1[U];
+  for (int k = kl * VEC; k < kvec_end; k += U * STRIDE) {
+    load_w(wb, k + U * STRIDE);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (k + u * STRIDE < kvec_end) fma_vec(wa[u][0], wa[u][1], k + u * STRIDE);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      w0[u] = rvalid[0] ? ldg_stream16(wp0 + k + u * STRIDE) : make_uint4(0, 0, 0, 0);
-      w1[u] = rvalid[1] ? ldg_stream16(wp1 + k + u * STRIDE) : make_uint4(0, 0, 0, 0);
+      wa[u][0] = wb[u][0];
+      wa[u][1] = wb[u][1];
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) fma_chunk(w0[u], w1[u], k + u * STRIDE);
-  }
-  for (; k + VEC <= kvec_end; k += STRIDE) {
-    const uint4 w0 = rvalid[0] ? ldg_stream16(wp0 + k) : make_uint4(0, 0, 0, 0);
-    const uint4 w1 = rvalid[1] ? ldg_stream16(wp1 + k) : make_uint4(0, 0, 0, 0);
-    fma_chunk(w0, w1, k);
   }
   // scalar tail (K not a multiple of the vector width)
   for (int kk = kvec_end + kl; kk < kcl; kk += 8) {
-    const float a0 = rvalid[0] ? to_f32(wp0[kk]) : 0.0f;
-    const float a1 = rvalid[1] ? to_f32(wp1[kk]) : 0.0f;
+    const float a0 = rvalid[0] ? to_f32(wp[0][kk]) : 0.0f;
+    const float a1 = rvalid[1] ? to_f32(wp[1][kk]) : 0.0f;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (m < mcount) {
-        acc[0][m] = fmaf(a0, xs[m * ldxs + kk], acc[0][m]);
-        acc[1][m] = fmaf(a1, xs[m * ldxs + kk], acc[1][m]);
+        const float x = to_f32(xs[(size_t)m * ldxs + kk]);
+        acc[0][m] = fmaf(a0, x, acc[0][m]);
+        acc[1][m] = fmaf(a1, x, acc[1][m]);
       }
     }
   }
 
-  // reduce over the 8 k-lanes
+  // ---- reduce over the 8 k-lanes
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
 #pragma unroll
@@ -152,65 +209,56 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
       if (kl == 0 && m < mcount) tl[m * TL_LD + warp * 8 + g * 2 + r] = v;
     }
   }
-  __syncthreads();
 
   const int n0 = p.swiglu ? tile * 32 : tile * TILE_N;
-  if (ks_total > 1) {
-    const int ldp = gridDim.x * TILE_N;
-    float* part = p.part + ((size_t)ks * p.M + mbase) * ldp + (size_t)tile * TILE_N;
-    for (int i = threadIdx.x; i < mcount * TILE_N; i += GEMV_THREADS) {
-      const int m = i / TILE_N, c = i - m * TILE_N;
-      part[(size_t)m * ldp + c] = tl[m * TL_LD + c];
-    }
-    __threadfence();
+  if (ks_total == 1) {
     __syncthreads();
-    __shared__ unsigned ticket;
-    unsigned* ctr = p.counters + blockIdx.z * gridDim.x + tile;
-    if (threadIdx.x == 0) ticket = atomicAdd(ctr, 1u);
-    __syncthreads();
-    if (ticket != (unsigned)ks_total - 1) return;
-    __threadfence();
-    const float* base = p.part + (size_t)mbase * ldp + (size_t)tile * TILE_N;
-    for (int i = threadIdx.x; i < mcount * TILE_N; i += GEMV_THREADS) {
-      const int m = i / TILE_N, c = i - m * TILE_N;
-      float s = 0.0f;
-      for (int j = 0; j < ks_total; ++j) s += __ldcg(base + ((size_t)j * p.M + m) * ldp + c);
-      tl[m * TL_LD + c] = s;
-    }
-    if (threadIdx.x == 0) *ctr = 0u;
-    __syncthreads();
+    run_epilogue<WT, AT>(p.epi, tl, TL_LD, mbase, mcount, n0, TILE_N, p.N);
+    return;
   }
-  pdl_trigger();
-  run_epilogue<WT, AT>(p.epi, tl, TL_LD, mbase, mcount, n0, TILE_N, p.N);
+  // ---- split-K reduction across the cluster through distributed shared memory
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int rank = (int)cluster.block_rank();
+  const int rp = (mcount + ks_total - 1) / ks_total;
+  const int r0 = min(mcount, rank * rp), r1 = min(mcount, r0 + rp);
+  for (int i = threadIdx.x; i < (r1 - r0) * TILE_N; i += GEMV_THREADS) {
+    const int m = r0 + i / TILE_N, c = i % TILE_N;
+    float s = 0.0f;
+#pragma unroll 8
+    for (int j = 0; j < ks_total; ++j) s += cluster.map_shared_rank(tl, j)[m * TL_LD + c];
+    red[(m - r0) * TL_LD + c] = s;
+  }
+  cluster.sync();   // every rank has finished reading the others' partials
+  if (r1 > r0) run_epilogue<WT, AT>(p.epi, red, TL_LD, mbase + r0, r1 - r0, n0, TILE_N, p.N);
+}
+
+// K split (cluster size) from the weight shape only: enough CTAs to cover the SMs and an
+// activation slice of at most 64 KB for 32 rows.
+template <typename WT, typename XT>
+void gemv_split(int tiles, int K, int num_sms, int* ks_out, int* kcta_out) {
+  constexpr int STRIDE = 8 * Vec16<WT>::N;
+  const int kmax = (64 * 1024) / (GEMV_MT * (int)sizeof(XT));
+  int ks = 1;
+  while (ks < 8 && (tiles * ks < num_sms || (K + ks - 1) / ks > kmax) && K / (ks * 2) >= STRIDE) ks *= 2;
+  int kcta = (K + ks - 1) / ks;
+  kcta = ((kcta + STRIDE - 1) / STRIDE) * STRIDE;
+  *ks_out = (K + kcta - 1) / kcta;
+  *kcta_out = kcta;
 }
 
 template <typename WT, typename XT, typename AT, int MT>
 cudaError_t launch_t(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
-  constexpr int VEC = Vec16<WT>::N;
   const int tiles = linear_tiles(p);
   const int zch = (p.M + MT - 1) / MT;
-  // Split K from the weight shape alone (never from M), so a row's arithmetic does not
-  // depend on how many other rows share the launch: split until the tiles cover the GPU
-  // twice (keeping >= 2 vector steps per lane) and at most KC_MAX columns per split.
-  constexpr int KC_MAX = 512;
-  const int step = 8 * VEC;
-  int ks = 1;
-  const int want = 2 * num_sms;
-  while (tiles * ks < want && (p.K / (ks * 2)) >= 2 * step) ks *= 2;
-  ks = std::max(ks, (p.K + KC_MAX - 1) / KC_MAX);
-  int kc = (p.K + ks - 1) / ks;
-  kc = ((kc + step - 1) / step) * step;
-  ks = (p.K + kc - 1) / kc;
-  auto smem_bytes = [&](int kcv) { return (size_t)(MT * (kcv + 4) + MT * TL_LD) * sizeof(float); };
-  if (ks > 1) {
-    const size_t need = (size_t)ks * p.M * tiles * TILE_N;
-    if (need > p.part_elems || tiles * zch > p.counters_len) return cudaErrorInvalidValue;
-  }
-  const size_t smem = smem_bytes(kc);
+  int ks, kcta;
+  gemv_split<WT, XT>(tiles, p.K, num_sms, &ks, &kcta);
+  const size_t smem = gemv_smem<XT>(MT, kcta);
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
   auto kern = k_gemv<WT, XT, AT, MT>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -219,12 +267,23 @@ cudaError_t launch_t(const LinearParams& p, int num_sms, cudaStream_t s, bool pd
   cfg.blockDim = dim3(GEMV_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (ks > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = ks;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, p, kc, ks);
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, p, kcta, ks);
 }
 
 template <typename WT, typename XT, typename AT>
@@ -234,15 +293,13 @@ cudaError_t launch_m(const LinearParams& p, int num_sms, cudaStream_t s, bool pd
   if (p.M <= 4) return launch_t<WT, XT, AT, 4>(p, num_sms, s, pdl);
   if (p.M <= 8) return launch_t<WT, XT, AT, 8>(p, num_sms, s, pdl);
   if (p.M <= 16) return launch_t<WT, XT, AT, 16>(p, num_sms, s, pdl);
-  return launch_t<WT, XT, AT, 32>(p, num_sms, s, pdl);
+  return launch_t<WT, XT, AT, GEMV_MT>(p, num_sms, s, pdl);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
-  // weight dtype == activation dtype in this library: fp32 model -> fp32 activations,
-  // bf16 model -> bf16 activations. X may also be fp32 for a bf16 model (tests).
   if (p.wdt == DT_F32) {
     if (p.xdt != DT_F32) return cudaErrorInvalidValue;
     return p.adt == DT_F32 ? launch_m<float, float, float>(p, num_sms, s, pdl)

@@ -6,7 +6,6 @@ namespace llm {
 namespace {
 
 constexpr int ROW_THREADS = 256;
-constexpr int MAX_PER_THREAD = 32;   // d_model <= 8192
 
 // h[m] = tok_emb[token] (+ pos_emb[position] for GPT-2): "bare-metal-llm", section
 // "What got built" (embedding lookup) and "Picking the model" (learned positions).
@@ -14,6 +13,7 @@ template <typename WT>
 __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
   const int m = blockIdx.x;
   pdl_wait();
+  pdl_trigger();
   const StepArgs* a = p.args;
   int tok = a->tokens[m];
   const int pos = a->positions[m];
@@ -25,7 +25,6 @@ __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
   if (!pos_ok && threadIdx.x == 0) set_flag(p.flags, FLAG_BAD_POSITION);
   const WT* te = reinterpret_cast<const WT*>(p.tok_emb) + (size_t)(tok < 0 ? 0 : tok) * p.d;
   const WT* pe = p.pos_emb ? reinterpret_cast<const WT*>(p.pos_emb) + (size_t)(pos_ok ? pos : 0) * p.d : nullptr;
-  pdl_trigger();
   for (int i = threadIdx.x; i < p.d; i += ROW_THREADS) {
     float v = tok < 0 ? 0.0f : to_f32(te[i]);
     if (pe && pos_ok) v += to_f32(pe[i]);
@@ -33,59 +32,54 @@ __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
   }
 }
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  v = warp_sum(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = 0.0f;
-#pragma unroll
-  for (int w = 0; w < ROW_THREADS / 32; ++w) t += red[w];
-  return t;
-}
-
 // LayerNorm ((x - mean) / sqrt(var + eps) * g + b, biased variance) or RMSNorm
-// (x / sqrt(mean(x^2) + eps) * g), one row per CTA, warp-shuffle reductions
-// ("rvllm-metal", section "How a GPU runs your kernel": one threadgroup per row,
-// simd_sum then a small cross-group sum).
+// (x / sqrt(mean(x^2) + eps) * g): one warp per row, warp-shuffle reductions
+// ("rvllm-metal", section "How a GPU runs your kernel": simd_sum, then no
+// threadgroup round trip is needed when one simdgroup owns the row). The row is
+// read with 16-byte loads; the variance pass re-reads it from L1.
+constexpr int NORM_ROWS = 8;   // rows (warps) per CTA
+
 template <typename WT, typename AT>
-__global__ void __launch_bounds__(ROW_THREADS) k_norm(const NormParams p) {
-  __shared__ float red[ROW_THREADS / 32];
-  const int r = blockIdx.x;
+__global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * NORM_ROWS + warp;
   pdl_wait();
+  pdl_trigger();
+  if (r >= p.rows) return;
   int src = r;
   if (p.use_last_row && p.args->last_row) src = p.args->last_row[r];
   const float* x = p.h + (size_t)src * p.d;
-  float v[MAX_PER_THREAD];
-  int n = 0;
-  float s = 0.0f;
-  for (int i = threadIdx.x; i < p.d; i += ROW_THREADS, ++n) {
-    v[n] = x[i];
-    s += v[n];
-  }
-  float mean = 0.0f, scale;
+  const int d4 = p.d >> 2;   // d is a multiple of 8
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  float mean = 0.0f;
   if (p.layer_norm) {
-    mean = block_sum(s, red) / p.d;
-    float q = 0.0f;
-    for (int j = 0; j < n; ++j) q += (v[j] - mean) * (v[j] - mean);
-    const float var = block_sum(q, red) / p.d;
-    scale = 1.0f / sqrtf(var + p.eps);
-  } else {
-    float q = 0.0f;
-    for (int j = 0; j < n; ++j) q += v[j] * v[j];
-    const float ms = block_sum(q, red) / p.d;
-    scale = 1.0f / sqrtf(ms + p.eps);
+    float s = 0.0f;
+    for (int i = lane; i < d4; i += 32) {
+      const float4 v = x4[i];
+      s += (v.x + v.y) + (v.z + v.w);
+    }
+    mean = warp_sum(s) / p.d;
   }
-  pdl_trigger();
+  float q = 0.0f;
+  for (int i = lane; i < d4; i += 32) {
+    const float4 v = x4[i];
+    const float a = v.x - mean, b = v.y - mean, c = v.z - mean, e = v.w - mean;
+    q += (a * a + b * b) + (c * c + e * e);
+  }
+  const float scale = 1.0f / sqrtf(warp_sum(q) / p.d + p.eps);
   const WT* gw = reinterpret_cast<const WT*>(p.g);
   const WT* bw = reinterpret_cast<const WT*>(p.b);
   AT* out = reinterpret_cast<AT*>(p.out) + (size_t)r * p.d;
-  n = 0;
-  for (int i = threadIdx.x; i < p.d; i += ROW_THREADS, ++n) {
-    float y = (v[n] - mean) * scale * to_f32(gw[i]);
-    if (bw) y += to_f32(bw[i]);
-    out[i] = from_f32<AT>(y);
+  for (int i = lane; i < d4; i += 32) {
+    const float4 v = x4[i];
+    const float xv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = 4 * i + j;
+      float y = (xv[j] - mean) * scale * to_f32(gw[c]);
+      if (bw) y += to_f32(bw[c]);
+      out[c] = from_f32<AT>(y);
+    }
   }
 }
 
@@ -132,7 +126,8 @@ cudaError_t embed_t(const EmbedParams& p, cudaStream_t s, bool pdl) {
 template <typename WT, typename AT>
 cudaError_t norm_t(const NormParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t c = make_launch_cfg(dim3(p.rows), dim3(ROW_THREADS), 0, s, attr, pdl);
+  cudaLaunchConfig_t c = make_launch_cfg(dim3((p.rows + NORM_ROWS - 1) / NORM_ROWS), dim3(NORM_ROWS * 32), 0, s,
+                                         attr, pdl);
   return cudaLaunchKernelEx(&c, k_norm<WT, AT>, p);
 }
 
@@ -159,7 +154,7 @@ cudaError_t launch_embed(const EmbedParams& p, int wdt, cudaStream_t s, bool pdl
 
 cudaError_t launch_norm(const NormParams& p, int wdt, int adt, cudaStream_t s, bool pdl) {
   if (p.rows <= 0) return cudaSuccess;
-  if (p.d > ROW_THREADS * MAX_PER_THREAD) return cudaErrorInvalidValue;
+  if (p.d % 8 != 0) return cudaErrorInvalidValue;
   if (wdt == DT_F32) return adt == DT_F32 ? norm_t<float, float>(p, s, pdl) : norm_t<float, bf16>(p, s, pdl);
   return adt == DT_F32 ? norm_t<bf16, float>(p, s, pdl) : norm_t<bf16, bf16>(p, s, pdl);
 }
