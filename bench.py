@@ -353,7 +353,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=wl.W_GPT2_F32_B32.name, choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--cpu-steps", type=int, default=128)
+    ap.add_argument("--cpu-steps", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -195,6 +195,17 @@ llm_status llm_set_graphs(llm_handle* h, int enable);
  * shape. Drops cached graphs. Errors: INVALID_ARG for another value. */
 llm_status llm_set_linear_variant(llm_handle* h, int variant);
 
+/* Test and diagnostic entry point (no handle): one projection with a chosen kernel,
+ *   y[m][n] = sum_k x[m][k] * w[n][k] (+ bias[n]),  m < M, n < N,
+ * x DEVICE [M][K] and w DEVICE [N][K] row-major in `dtype` (LLM_DTYPE_F32 or
+ * LLM_DTYPE_BF16), bias DEVICE [N] in `dtype` or NULL, y DEVICE float [M][N].
+ * variant: 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM (bf16 only;
+ * K and the row strides must be multiples of 8). Enqueued on `cuda_stream`.
+ * Errors: INVALID_ARG (bad sizes, NULL, K % 8 for variant 3), UNSUPPORTED
+ * (variant 3 with fp32), CUDA. */
+llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const void* w, const void* bias, float* y,
+                         int variant, void* cuda_stream);
+
 const char* llm_status_string(llm_status s);
 const char* llm_last_error(void);
 

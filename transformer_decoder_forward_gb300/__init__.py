@@ -22,7 +22,7 @@ FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIM
 
 EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_decode_step", "llm_decode_step_host",
            "llm_get_error_flags", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
-           "llm_set_graphs", "llm_set_linear_variant", "llm_status_string", "llm_last_error"]
+           "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_status_string", "llm_last_error"]
 
 
 class LLMError(RuntimeError):
@@ -78,13 +78,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_last_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.llm_set_graphs.argtypes = [vp, ctypes.c_int]
     lib.llm_set_linear_variant.argtypes = [vp, ctypes.c_int]
+    lib.llm_op_linear.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int, vp]
     lib.llm_status_string.argtypes = [ctypes.c_int]
     lib.llm_status_string.restype = ctypes.c_char_p
     lib.llm_last_error.argtypes = []
     lib.llm_last_error.restype = ctypes.c_char_p
     for name in ("llm_create", "llm_prefill", "llm_decode_step", "llm_decode_step_host", "llm_get_error_flags",
                  "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
-                 "llm_set_linear_variant"):
+                 "llm_set_linear_variant", "llm_op_linear"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -97,6 +98,20 @@ def _check(status: int) -> None:
 
 def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
+
+
+def op_linear(x, w, bias, y, variant: int, stream=None) -> None:
+    """y = x . w^T (+ bias) with one chosen projection kernel (tests / diagnostics).
+
+    x [M, K], w [N, K] (both float32 or both bfloat16 CUDA tensors), bias [N] or None, y float32 [M, N]."""
+    import torch
+    lib = load()
+    dtype = 1 if w.dtype == torch.bfloat16 else 0
+    M, K = x.shape
+    N = w.shape[0]
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.llm_op_linear(dtype, M, N, K, _ptr(x), _ptr(w), _ptr(bias), _ptr(y), int(variant),
+                             ctypes.c_void_p(s.cuda_stream)))
 
 
 def upload_weights(w, device: str = "cuda"):

@@ -84,7 +84,7 @@ struct llm_handle {
   float* q = nullptr;
   void* att = nullptr;
   void* ff = nullptr;
-  int split = 128, max_splits = 1;
+  int split = 64, max_splits = 1;
   float* attn_po = nullptr;
   float* attn_ml = nullptr;
   int head_tiles = 0;
@@ -361,7 +361,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   if (c.kv_block_size != KVB) return fail(LLM_ERR_UNSUPPORTED, "kv_block_size must be 16");
   if (c.n_heads % c.n_kv_heads != 0) return fail(LLM_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
   if (c.n_heads / c.n_kv_heads > 8) return fail(LLM_ERR_UNSUPPORTED, "at most 8 query heads per KV head");
-  if (c.d_model > 8192) return fail(LLM_ERR_UNSUPPORTED, "d_model above 8192");
+  if (c.d_model > 2048) return fail(LLM_ERR_UNSUPPORTED, "d_model above 2048");
   if (c.d_model % 8 != 0 || c.d_ff % 8 != 0) return fail(LLM_ERR_UNSUPPORTED, "d_model and d_ff must be multiples of 8");
   if (c.arch == LLM_ARCH_LLAMA && !(c.rope_theta > 0.0f)) return fail(LLM_ERR_INVALID_ARG, "rope_theta must be > 0");
   if (!c.contiguous_kv && c.num_kv_blocks <= 0) return fail(LLM_ERR_INVALID_ARG, "num_kv_blocks must be positive");
@@ -659,6 +659,34 @@ llm_status llm_set_graphs(llm_handle* h, int enable) {
   llm_status st = check_handle(h);
   if (st != LLM_OK) return st;
   h->use_graphs = enable != 0 && stream_capturable(h->stream);
+  return LLM_OK;
+}
+
+llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const void* w, const void* bias, float* y,
+                         int variant, void* cuda_stream) {
+  if (M <= 0 || N <= 0 || K <= 0) return fail(LLM_ERR_INVALID_ARG, "sizes must be positive");
+  if (!x || !w || !y) return fail(LLM_ERR_INVALID_ARG, "NULL x, w or y");
+  if (dtype != LLM_DTYPE_F32 && dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_INVALID_ARG, "bad dtype");
+  if (variant < LIN_GEMV || variant > LIN_TC) return fail(LLM_ERR_INVALID_ARG, "variant must be 1..3");
+  if (variant == LIN_TC && dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_UNSUPPORTED, "tcgen05 path is bf16 only");
+  if (variant == LIN_TC && K % 8 != 0) return fail(LLM_ERR_INVALID_ARG, "tcgen05 path needs K % 8 == 0");
+  int dev = 0, nsm = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+  LinearParams p;
+  memset(&p, 0, sizeof(p));
+  p.W = w; p.X = x; p.M = M; p.N = N; p.K = K; p.ldx = K;
+  p.wdt = p.xdt = dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
+  p.adt = p.wdt;
+  p.epi.kind = EPI_STORE_F32;
+  p.epi.bias = bias;
+  p.epi.out = y;
+  p.epi.ld_out = N;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = variant == LIN_GEMV ? launch_gemv(p, nsm, s, false)
+                  : variant == LIN_SIMT ? launch_gemm_simt(p, s, false)
+                                        : launch_gemm_tc(p, nsm, s, false);
+  if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("llm_op_linear: ") + cudaGetErrorString(e));
   return LLM_OK;
 }
 

@@ -22,7 +22,7 @@ namespace {
 
 constexpr int AD_THREADS = 128;
 constexpr int MAX_G = 8;
-constexpr int MAX_SPLIT = 256;
+constexpr int MAX_SPLIT = 128;
 constexpr float SM_SCALE = 0.125f;   // 1/sqrt(64)
 
 // smem for one split: K and V blocks (split/16 blocks of 16 x 64 elements each), then a

@@ -108,18 +108,21 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   uint32_t ok;
+  // suspend hint 1000 ns: a failed poll sleeps at most ~1 us
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
-// Bounded wait: every spin in this library gives up after a fixed number of polls
-// (each try_wait itself suspends for a while), sets FLAG_WAIT_TIMEOUT and returns false.
-constexpr unsigned WAIT_POLLS = 1u << 22;
+// Bounded wait: every spin in this library gives up after ~2^31 SM clock cycles (about
+// one second), sets FLAG_WAIT_TIMEOUT and returns false.
+constexpr long long WAIT_CYCLES = 1ll << 31;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsigned* flags) {
-  for (unsigned i = 0; i < WAIT_POLLS; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (clock64() - t0 < WAIT_CYCLES)
     if (mbar_try_wait(bar, parity)) return true;
   set_flag(flags, FLAG_WAIT_TIMEOUT);
   return false;

@@ -1,10 +1,275 @@
-// tcgen05 / TMEM tensor-core projection (bf16 operands, fp32 accumulation).
+// tcgen05 / TMEM tensor-core projection for many rows (prefill), bf16 operands,
+// fp32 accumulation, fused epilogues.
+//
+// Prefill is arithmetic bound ("rvllm-metal", section "The matmul pain story":
+// lots of rows, a tiled kernel staging slices of x and W). On sm_103a the tile
+// is a 5th-generation tensor-core contraction:
+//   - TMA (cp.async.bulk.tensor, 128-byte swizzle) stages 128 x 64 slices of
+//     x (rows) and 128 x 64 slices of W into a 4-stage shared-memory ring, each
+//     stage guarded by a "full" and an "empty" mbarrier;
+//   - one elected thread issues tcgen05.mma (M = 128, N = 128, K = 16, bf16 in,
+//     fp32 accumulate) into a 128 x 128 fp32 accumulator in tensor memory, and
+//     tcgen05.commit releases each stage once the MMAs that read it finish;
+//   - after the last commit, four warps read the accumulator back with
+//     tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = tile rows), stage it as
+//     an fp32 tile in shared memory and run the shared epilogue per 64-column
+//     sub-tile (bias, GELU / SwiGLU, RoPE + kv_write, residual add).
+// Every wait is bounded (FLAG_WAIT_TIMEOUT) and the tensor memory is always freed.
+#include <cuda.h>
+
+#include "epilogue.cuh"
 #include "linear.cuh"
 
 namespace llm {
 
-bool gemm_tc_supported(const LinearParams&) { return false; }
+namespace {
 
-cudaError_t launch_gemm_tc(const LinearParams&, int, cudaStream_t, bool) { return cudaErrorNotSupported; }
+constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_THREADS = 128;
+constexpr int A_STAGE = TC_BM * TC_BK * 2;   // bytes
+constexpr int B_STAGE = TC_BN * TC_BK * 2;
+constexpr int OT_LD = TC_BN + 1;
+constexpr size_t TC_SMEM = 1024 + (size_t)TC_STAGES * (A_STAGE + B_STAGE) + 256;
+
+// ---- tcgen05 / TMA wrappers -------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, rows of 64 bf16 (128 bytes) written by
+// TMA with the 128-byte swizzle, 8-row groups 1024 bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
+  const uint32_t a = smem_u32(p);
+  uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;              // swizzle: 128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A/B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <typename AT>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    k_gemm_tc(const LinearParams p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sA = base;
+  unsigned char* sB = base + TC_STAGES * A_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + TC_STAGES * (A_STAGE + B_STAGE));
+  uint64_t* empty = full + TC_STAGES;
+  uint64_t* done = empty + TC_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_n = blockIdx.x, tile_m = blockIdx.y;
+  const int m0 = tile_m * TC_BM;
+  const int kiters = (p.K + TC_BK - 1) / TC_BK;
+  const int F = p.N;
+
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, TC_BN);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    mbar_fence_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    for (int i = 0; i < kiters; ++i) {
+      const int s = i % TC_STAGES;
+      if (i >= TC_STAGES && !mbar_wait(&empty[s], ((i / TC_STAGES) - 1) & 1, p.epi.flags)) break;
+      mbar_arrive_expect_tx(&full[s], A_STAGE + B_STAGE);
+      const int kc = i * TC_BK;
+      tma_load_2d(sA + s * A_STAGE, &tmA, kc, m0, &full[s]);
+      unsigned char* b = sB + s * B_STAGE;
+      if (p.swiglu) {
+        // two 64-column sub-tiles, each 32 gate rows then the 32 matching up rows
+        for (int sub = 0; sub < 2; ++sub) {
+          const int j0 = (tile_n * 2 + sub) * 32;
+          tma_load_2d(b + (sub * 64) * 128, &tmB, kc, j0, &full[s]);
+          tma_load_2d(b + (sub * 64 + 32) * 128, &tmB, kc, F + j0, &full[s]);
+        }
+      } else {
+        tma_load_2d(b, &tmB, kc, tile_n * TC_BN, &full[s]);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
+    for (int i = 0; i < kiters; ++i) {
+      const int s = i % TC_STAGES;
+      if (!mbar_wait(&full[s], (i / TC_STAGES) & 1, p.epi.flags)) break;
+      tc_fence_after();
+      const uint64_t da = sw128_desc(sA + s * A_STAGE);
+      const uint64_t db = sw128_desc(sB + s * B_STAGE);
+#pragma unroll
+      for (int kk = 0; kk < TC_BK / 16; ++kk)   // 16 bf16 = 32 bytes per MMA step
+        tc_mma(tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(&empty[s]);
+    }
+    tc_commit(done);
+  }
+  // ---- epilogue: all four warps
+  ok = mbar_wait(done, 0, p.epi.flags);
+  if (!ok) ok = mbar_wait(done, 0, p.epi.flags);   // one more bounded wait for the MMAs in flight
+  tc_fence_after();
+  float* ot = reinterpret_cast<float*>(base);   // [128][OT_LD] over the drained pipeline buffers
+  const int row = warp * 32 + lane;
+  __syncwarp();   // lanes 0 of warps 0/1 come from the producer / MMA loops: reconverge for tcgen05.ld
+  if (ok) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) ot[row * OT_LD + c0 + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TC_BN);
+  }
+  pdl_trigger();
+  if (!ok) return;
+  const int mrows = min(TC_BM, p.M - m0);
+#pragma unroll 1
+  for (int sub = 0; sub < TC_BN / 64; ++sub) {
+    const int n0 = p.swiglu ? (tile_n * 2 + sub) * 32 : tile_n * TC_BN + sub * 64;
+    if (!p.swiglu && n0 >= p.N) break;
+    run_epilogue<bf16, AT>(p.epi, ot + sub * 64, OT_LD, m0, mrows, n0, 64, p.N);
+  }
+}
+
+// ---- host side -------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix with row stride ld (elements);
+// box = 64 columns x box_rows rows, 128-byte swizzle, out-of-bounds reads fill zero.
+bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const LinearParams& p) {
+  if (p.wdt != DT_BF16 || p.xdt != DT_BF16) return false;
+  if (p.K % 8 != 0 || p.ldx % 8 != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(p.W) | reinterpret_cast<uintptr_t>(p.X)) & 15) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_tc(const LinearParams& p, int /*num_sms*/, cudaStream_t s, bool pdl) {
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
+  if (!gemm_tc_supported(p)) return cudaErrorNotSupported;
+  CUtensorMap ma, mb;
+  const int wrows = p.swiglu ? 2 * p.N : p.N;
+  if (!make_map(&ma, p.X, p.M, p.K, p.ldx, TC_BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, p.W, wrows, p.K, p.K, p.swiglu ? 32 : TC_BN)) return cudaErrorInvalidValue;
+  const int tiles_n = p.swiglu ? (p.N + 63) / 64 : (p.N + TC_BN - 1) / TC_BN;
+  const int tiles_m = (p.M + TC_BM - 1) / TC_BM;
+  auto kern = p.adt == DT_BF16 ? k_gemm_tc<bf16> : k_gemm_tc<float>;
+  static bool attr_set[2] = {false, false};
+  bool& set = attr_set[p.adt == DT_BF16 ? 1 : 0];
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles_n, tiles_m);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = TC_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p, ma, mb);
+}
 
 }  // namespace llm

@@ -38,7 +38,7 @@ namespace {
 
 constexpr int GEMV_THREADS = 256;
 constexpr int TL_LD = TILE_N + 1;   // padded row stride of the output tiles in smem
-constexpr int GEMV_MT = 32;         // rows per CTA (larger M uses grid.z)
+constexpr int GEMV_MT = 16;         // rows per CTA (larger M: more CTAs along grid.x)
 constexpr int U = 2;                // weight vectors per row in flight per thread and stage
 
 template <typename XT, int VEC>
@@ -77,7 +77,9 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
   constexpr int VEC = Vec16<WT>::N;
   constexpr int STRIDE = 8 * VEC;
   constexpr int XE = 16 / sizeof(XT);      // x elements per 16 bytes
-  const int tile = blockIdx.x, ks = blockIdx.y, mbase = blockIdx.z * MT;
+  // grid.x = row chunk (fastest, so the chunks sharing a weight slice run together), grid.y = K split,
+  // grid.z = output tile
+  const int tile = blockIdx.z, ks = blockIdx.y, mbase = blockIdx.x * MT;
   const int mcount = min(MT, p.M - mbase);
   const int k0 = ks * kcta;
   const int kcl = max(0, min(kcta, p.K - k0));
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
 }
 
 // K split (cluster size) from the weight shape only: enough CTAs to cover the SMs and an
-// activation slice of at most 64 KB for 32 rows.
+// activation slice of at most 64 KB for a full row chunk.
 template <typename WT, typename XT>
 void gemv_split(int tiles, int K, int num_sms, int* ks_out, int* kcta_out) {
   constexpr int STRIDE = 8 * Vec16<WT>::N;
@@ -263,7 +265,8 @@ cudaError_t launch_t(const LinearParams& p, int num_sms, cudaStream_t s, bool pd
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles, ks, zch);
+  if (tiles > 65535) return cudaErrorInvalidValue;
+  cfg.gridDim = dim3(zch, ks, tiles);
   cfg.blockDim = dim3(GEMV_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -292,7 +295,6 @@ cudaError_t launch_m(const LinearParams& p, int num_sms, cudaStream_t s, bool pd
   if (p.M <= 2) return launch_t<WT, XT, AT, 2>(p, num_sms, s, pdl);
   if (p.M <= 4) return launch_t<WT, XT, AT, 4>(p, num_sms, s, pdl);
   if (p.M <= 8) return launch_t<WT, XT, AT, 8>(p, num_sms, s, pdl);
-  if (p.M <= 16) return launch_t<WT, XT, AT, 16>(p, num_sms, s, pdl);
   return launch_t<WT, XT, AT, GEMV_MT>(p, num_sms, s, pdl);
 }
 

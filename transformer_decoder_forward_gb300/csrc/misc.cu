@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
 // threadgroup round trip is needed when one simdgroup owns the row). The row is
 // read with 16-byte loads; the variance pass re-reads it from L1.
 constexpr int NORM_ROWS = 8;   // rows (warps) per CTA
+constexpr int NORM_NV = 16;    // float4 per lane held in registers: d <= 16 * 128 = 2048
 
 template <typename WT, typename AT>
 __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
@@ -48,35 +49,38 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
   if (r >= p.rows) return;
   int src = r;
   if (p.use_last_row && p.args->last_row) src = p.args->last_row[r];
-  const float* x = p.h + (size_t)src * p.d;
+  const float4* x4 = reinterpret_cast<const float4*>(p.h + (size_t)src * p.d);
   const int d4 = p.d >> 2;   // d is a multiple of 8
-  const float4* x4 = reinterpret_cast<const float4*>(x);
-  float mean = 0.0f;
-  if (p.layer_norm) {
-    float s = 0.0f;
-    for (int i = lane; i < d4; i += 32) {
-      const float4 v = x4[i];
-      s += (v.x + v.y) + (v.z + v.w);
-    }
-    mean = warp_sum(s) / p.d;
+  float4 v[NORM_NV];
+  float s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < NORM_NV; ++j) {
+    const int i = lane + 32 * j;
+    v[j] = i < d4 ? x4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
   }
+  const float mean = p.layer_norm ? warp_sum(s) / p.d : 0.0f;
   float q = 0.0f;
-  for (int i = lane; i < d4; i += 32) {
-    const float4 v = x4[i];
-    const float a = v.x - mean, b = v.y - mean, c = v.z - mean, e = v.w - mean;
-    q += (a * a + b * b) + (c * c + e * e);
+#pragma unroll
+  for (int j = 0; j < NORM_NV; ++j) {
+    if (lane + 32 * j < d4) {
+      const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, e = v[j].w - mean;
+      q += (a * a + b * b) + (c * c + e * e);
+    }
   }
   const float scale = 1.0f / sqrtf(warp_sum(q) / p.d + p.eps);
   const WT* gw = reinterpret_cast<const WT*>(p.g);
   const WT* bw = reinterpret_cast<const WT*>(p.b);
   AT* out = reinterpret_cast<AT*>(p.out) + (size_t)r * p.d;
-  for (int i = lane; i < d4; i += 32) {
-    const float4 v = x4[i];
-    const float xv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = 4 * i + j;
-      float y = (xv[j] - mean) * scale * to_f32(gw[c]);
+  for (int j = 0; j < NORM_NV; ++j) {
+    const int i = lane + 32 * j;
+    if (i >= d4) continue;
+    const float xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int c = 4 * i + t;
+      float y = (xv[t] - mean) * scale * to_f32(gw[c]);
       if (bw) y += to_f32(bw[c]);
       out[c] = from_f32<AT>(y);
     }
@@ -154,7 +158,7 @@ cudaError_t launch_embed(const EmbedParams& p, int wdt, cudaStream_t s, bool pdl
 
 cudaError_t launch_norm(const NormParams& p, int wdt, int adt, cudaStream_t s, bool pdl) {
   if (p.rows <= 0) return cudaSuccess;
-  if (p.d % 8 != 0) return cudaErrorInvalidValue;
+  if (p.d % 8 != 0 || p.d > NORM_NV * 128) return cudaErrorInvalidValue;
   if (wdt == DT_F32) return adt == DT_F32 ? norm_t<float, float>(p, s, pdl) : norm_t<float, bf16>(p, s, pdl);
   return adt == DT_F32 ? norm_t<bf16, float>(p, s, pdl) : norm_t<bf16, bf16>(p, s, pdl);
 }
