@@ -206,6 +206,26 @@ llm_status llm_set_linear_variant(llm_handle* h, int variant);
 llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const void* w, const void* bias, float* y,
                          int variant, void* cuda_stream);
 
+/* Test and diagnostic entry point (no handle): one layer of batched decode attention
+ * over a paged KV pool, the split-K kernel pair of llm_decode_step ("rvllm-metal",
+ * section "What the kernels do": scores, -inf mask, softmax, probs @ V, reading the
+ * paged cache). Row b attends with its n_heads query heads (GQA: head h uses KV head
+ * h / (n_heads / n_kv_heads)) over positions 0..positions[b]:
+ *   q             DEVICE float [B][n_heads * 64] (already rotated for Llama)
+ *   k_pool/v_pool DEVICE [num_blocks][n_kv_heads][16][64] in kv_dtype (LLM_DTYPE_*)
+ *   positions     DEVICE int32 [B]
+ *   block_tables  DEVICE int32 [B][max_blocks_per_seq], slot = table[pos / 16] * 16 + pos % 16
+ *   out           DEVICE float [B][n_heads * 64]
+ * Its split partials live in device scratch that this call allocates and frees
+ * stream-ordered (cudaMallocAsync / cudaFreeAsync) on cuda_stream. Device-side range
+ * errors (a position or block id out of range) are skipped, not reported.
+ * Errors: INVALID_ARG (NULL, sizes, n_heads % n_kv_heads, more than 8 query heads per
+ * KV head), OOM, CUDA. */
+llm_status llm_op_attention_decode(int kv_dtype, int B, int n_heads, int n_kv_heads, const float* q,
+                                   const void* k_pool, const void* v_pool, int num_blocks, const int32_t* positions,
+                                   const int32_t* block_tables, int max_blocks_per_seq, float* out,
+                                   void* cuda_stream);
+
 const char* llm_status_string(llm_status s);
 const char* llm_last_error(void);
 

@@ -43,3 +43,56 @@ def test_linear_kernel_matches_oracle(gpu_lib, variant, bf16, M, N, K):
     tol = 1e-6 + 4 * K * 2.0 ** -23 * scale
     assert np.all(np.isfinite(got))
     assert np.all(np.abs(got - ref) <= tol), float(np.abs(got - ref).max())
+
+
+# ------------------------------------------------------------------------------------------------
+# decode attention over a shuffled paged pool, against the oracle's causal attention
+# ------------------------------------------------------------------------------------------------
+
+def make_attention_case(B, H, Hkv, ctx_max, bf16, seed):
+    """Random q and a shuffled paged K/V pool; returns host and device views."""
+    import torch
+    r = np.random.default_rng(seed)
+    pos = r.integers(0, ctx_max, size=B).astype(np.int32)
+    pos[0] = ctx_max - 1                                  # one row at the maximum context
+    if B > 1:
+        pos[1] = 0                                        # one row with a single key
+    ctx = pos + 1
+    mbps = wl.blocks_needed(int(ctx.max()))
+    tables, nblk = wl.make_block_tables(ctx, mbps, shuffle=True, seed=seed)
+    tables = np.where(tables < 0, 0, tables).astype(np.int32)
+    k = r.standard_normal((nblk, Hkv, 16, 64), dtype=np.float32)
+    v = r.standard_normal((nblk, Hkv, 16, 64), dtype=np.float32)
+    q = r.standard_normal((B, H * 64), dtype=np.float32) * np.float32(0.5)
+    if bf16:
+        k, v = (wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(a)) for a in (k, v))
+    dt = torch.bfloat16 if bf16 else torch.float32
+    dev = dict(q=torch.from_numpy(q).cuda(), k=torch.from_numpy(k).cuda().to(dt), v=torch.from_numpy(v).cuda().to(dt),
+               pos=torch.from_numpy(pos).cuda(), tables=torch.from_numpy(tables).cuda())
+    return q, k, v, pos, tables, dev
+
+
+def oracle_decode_attention(q, k, v, pos, tables, H, Hkv):
+    from oracle import causal_attention
+    out = []
+    for b in range(len(pos)):
+        t = np.arange(pos[b] + 1)
+        blk = tables[b, t // 16]
+        kk = k[blk, :, t % 16, :].astype(np.float64)     # [T, Hkv, 64]
+        vv = v[blk, :, t % 16, :].astype(np.float64)
+        qq = q[b].reshape(1, H, 64).astype(np.float64)
+        out.append(causal_attention(qq, kk, vv, np.array([pos[b]]))[0])
+    return np.stack(out)
+
+
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+@pytest.mark.parametrize("B,H,Hkv,ctx", [(1, 12, 12, 1), (3, 12, 12, 200), (5, 15, 5, 2049), (4, 8, 1, 700),
+                                         (64, 25, 25, 300)])
+def test_decode_attention_matches_oracle(gpu_lib, bf16, B, H, Hkv, ctx):
+    import torch
+    q, k, v, pos, tables, d = make_attention_case(B, H, Hkv, ctx, bf16, seed=B + H + ctx)
+    out = torch.full((B, H * 64), float("nan"), dtype=torch.float32, device="cuda")
+    gpu_lib.op_attention_decode(d["q"], d["k"], d["v"], d["pos"], d["tables"], out, Hkv)
+    torch.cuda.synchronize()
+    ref = oracle_decode_attention(q, k, v, pos, tables, H, Hkv)
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=2e-5)

@@ -22,7 +22,8 @@ FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIM
 
 EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_decode_step", "llm_decode_step_host",
            "llm_get_error_flags", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
-           "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_status_string", "llm_last_error"]
+           "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode", "llm_status_string",
+           "llm_last_error"]
 
 
 class LLMError(RuntimeError):
@@ -79,13 +80,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_set_graphs.argtypes = [vp, ctypes.c_int]
     lib.llm_set_linear_variant.argtypes = [vp, ctypes.c_int]
     lib.llm_op_linear.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int, vp]
+    lib.llm_op_attention_decode.argtypes = [ctypes.c_int] * 4 + [vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp]
     lib.llm_status_string.argtypes = [ctypes.c_int]
     lib.llm_status_string.restype = ctypes.c_char_p
     lib.llm_last_error.argtypes = []
     lib.llm_last_error.restype = ctypes.c_char_p
     for name in ("llm_create", "llm_prefill", "llm_decode_step", "llm_decode_step_host", "llm_get_error_flags",
                  "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
-                 "llm_set_linear_variant", "llm_op_linear"):
+                 "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -112,6 +114,19 @@ def op_linear(x, w, bias, y, variant: int, stream=None) -> None:
     s = stream if stream is not None else torch.cuda.current_stream()
     _check(lib.llm_op_linear(dtype, M, N, K, _ptr(x), _ptr(w), _ptr(bias), _ptr(y), int(variant),
                              ctypes.c_void_p(s.cuda_stream)))
+
+
+def op_attention_decode(q, k_pool, v_pool, positions, block_tables, out, n_kv_heads: int, stream=None) -> None:
+    """Paged decode attention of one layer (tests / diagnostics). See llm_op_attention_decode."""
+    import torch
+    lib = load()
+    fn = lib.llm_op_attention_decode
+    kv_dtype = 1 if k_pool.dtype == torch.bfloat16 else 0
+    B, HD = q.shape
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(fn(kv_dtype, B, HD // 64, int(n_kv_heads), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                       k_pool.shape[0], _ptr(positions), _ptr(block_tables), block_tables.shape[1],
+                                       _ptr(out), ctypes.c_void_p(s.cuda_stream)))
 
 
 def upload_weights(w, device: str = "cuda"):

@@ -19,6 +19,7 @@
 #include <vector>
 
 #include "../../include/llm.h"
+#include "api_internal.h"
 #include "attention.cuh"
 #include "linear.cuh"
 #include "misc.cuh"
@@ -63,6 +64,8 @@ struct Stat {
 };
 
 }  // namespace
+
+llm_status llm_internal_fail(llm_status s, const std::string& msg) { return fail(s, msg); }
 
 struct llm_handle {
   llm_config cfg{};
@@ -687,6 +690,56 @@ llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const vo
                   : variant == LIN_SIMT ? launch_gemm_simt(p, s, false)
                                         : launch_gemm_tc(p, nsm, s, false);
   if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("llm_op_linear: ") + cudaGetErrorString(e));
+  return LLM_OK;
+}
+
+llm_status llm_op_attention_decode(int kv_dtype, int B, int n_heads, int n_kv_heads, const float* q,
+                                   const void* k_pool, const void* v_pool, int num_blocks, const int32_t* positions,
+                                   const int32_t* block_tables, int max_blocks_per_seq, float* out,
+                                   void* cuda_stream) {
+  if (B <= 0 || n_heads <= 0 || n_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(LLM_ERR_INVALID_ARG, "sizes must be positive");
+  if (!q || !k_pool || !v_pool || !positions || !block_tables || !out)
+    return fail(LLM_ERR_INVALID_ARG, "NULL pointer argument");
+  if (kv_dtype != LLM_DTYPE_F32 && kv_dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_INVALID_ARG, "bad kv_dtype");
+  if (n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > 8)
+    return fail(LLM_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads, at most 8 per KV head");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const int split = 64;
+  const int max_splits = (max_blocks_per_seq * KVB + split - 1) / split;
+  const size_t part_o = (size_t)B * n_heads * max_splits * HD, part_ml = (size_t)B * n_heads * max_splits * 2;
+  char* scratch = nullptr;
+  const size_t bytes = 256 + (part_o + part_ml) * sizeof(float);
+  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(LLM_ERR_OOM, "cudaMallocAsync of the attention scratch failed");
+  }
+  StepArgs* args = reinterpret_cast<StepArgs*>(scratch);
+  StepArgs a{nullptr, positions, nullptr, block_tables, nullptr, nullptr, nullptr, B, B};
+  AttnDecodeParams p;
+  memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.kv.k = const_cast<void*>(k_pool);
+  p.kv.v = const_cast<void*>(v_pool);
+  p.kv.num_blocks = num_blocks;
+  p.kv.n_kv_heads = n_kv_heads;
+  p.kv.mbps = max_blocks_per_seq;
+  p.kv.contiguous = 0;
+  p.args = args;
+  p.B = B;
+  p.n_heads = n_heads;
+  p.split = split;
+  p.max_splits = max_splits;
+  p.part_o = reinterpret_cast<float*>(scratch + 256);
+  p.part_ml = p.part_o + part_o;
+  p.out = out;
+  p.out_dtype = DT_F32;
+  p.flags = nullptr;
+  cudaError_t e = launch_set_args(args, a, s);
+  if (e == cudaSuccess) e = launch_attn_decode(p, kv_dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16, s, false);
+  cudaError_t ef = cudaFreeAsync(scratch, s);
+  if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("llm_op_attention_decode: ") + cudaGetErrorString(e));
+  if (ef != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("cudaFreeAsync: ") + cudaGetErrorString(ef));
   return LLM_OK;
 }
 
