@@ -226,6 +226,24 @@ llm_status llm_op_attention_decode(int kv_dtype, int B, int n_heads, int n_kv_he
                                    const int32_t* block_tables, int max_blocks_per_seq, float* out,
                                    void* cuda_stream);
 
+/* llm_op_attention_decode for callers that cannot allocate device memory (code inside
+ * someone else's stream capture, or a process whose allocator owns all of HBM). The
+ * pages have no counterpart of this entry point. Same arguments, layouts and result as
+ * llm_op_attention_decode, but no cudaMalloc / cudaFree / allocating call of any
+ * library: the scratch (a 256-byte argument block plus B * n_heads * ceil(max_blocks_per_seq
+ * * 16 / 64) * 264 bytes of split partials) lives in one fixed 4 MiB __device__ array that
+ * every GPU loading the library holds until the process exits.
+ *   - The first call on a device resolves the array's device address (cudaGetSymbolAddress)
+ *     for that device; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents: calls whose
+ *     execution overlaps on the GPU (other streams, other threads) race on it.
+ * Errors: as llm_op_attention_decode, plus OUT_OF_RANGE when the scratch needed exceeds
+ * the array (nothing is launched), UNSUPPORTED for device ordinals above 63. */
+llm_status llm_op_attention_decode_noalloc(int kv_dtype, int B, int n_heads, int n_kv_heads, const float* q,
+                                           const void* k_pool, const void* v_pool, int num_blocks,
+                                           const int32_t* positions, const int32_t* block_tables,
+                                           int max_blocks_per_seq, float* out, void* cuda_stream);
+
 const char* llm_status_string(llm_status s);
 const char* llm_last_error(void);
 

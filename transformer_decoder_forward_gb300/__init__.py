@@ -22,8 +22,8 @@ FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIM
 
 EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_decode_step", "llm_decode_step_host",
            "llm_get_error_flags", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
-           "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode", "llm_status_string",
-           "llm_last_error"]
+           "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode", "llm_op_attention_decode_noalloc",
+           "llm_status_string", "llm_last_error"]
 
 
 class LLMError(RuntimeError):
@@ -81,13 +81,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_set_linear_variant.argtypes = [vp, ctypes.c_int]
     lib.llm_op_linear.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int, vp]
     lib.llm_op_attention_decode.argtypes = [ctypes.c_int] * 4 + [vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp]
+    lib.llm_op_attention_decode_noalloc.argtypes = lib.llm_op_attention_decode.argtypes
     lib.llm_status_string.argtypes = [ctypes.c_int]
     lib.llm_status_string.restype = ctypes.c_char_p
     lib.llm_last_error.argtypes = []
     lib.llm_last_error.restype = ctypes.c_char_p
     for name in ("llm_create", "llm_prefill", "llm_decode_step", "llm_decode_step_host", "llm_get_error_flags",
                  "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
-                 "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode"):
+                 "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode",
+                 "llm_op_attention_decode_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -116,11 +118,15 @@ def op_linear(x, w, bias, y, variant: int, stream=None) -> None:
                              ctypes.c_void_p(s.cuda_stream)))
 
 
-def op_attention_decode(q, k_pool, v_pool, positions, block_tables, out, n_kv_heads: int, stream=None) -> None:
-    """Paged decode attention of one layer (tests / diagnostics). See llm_op_attention_decode."""
+def op_attention_decode(q, k_pool, v_pool, positions, block_tables, out, n_kv_heads: int, stream=None,
+                        noalloc: bool = False) -> None:
+    """Paged decode attention of one layer (tests / diagnostics). See llm_op_attention_decode.
+
+    noalloc=True calls llm_op_attention_decode_noalloc: the same kernels with their scratch in a
+    fixed device array instead of memory allocated per call."""
     import torch
     lib = load()
-    fn = lib.llm_op_attention_decode
+    fn = lib.llm_op_attention_decode_noalloc if noalloc else lib.llm_op_attention_decode
     kv_dtype = 1 if k_pool.dtype == torch.bfloat16 else 0
     B, HD = q.shape
     s = stream if stream is not None else torch.cuda.current_stream()
