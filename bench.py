@@ -77,6 +77,18 @@ def step_bytes(s: wl.ModelShape, ctx: np.ndarray) -> int:
     return gemv_bytes(s, len(ctx)) + attn_bytes(s, ctx)
 
 
+def prefill_gemm_flops(s: wl.ModelShape, lengths: np.ndarray) -> float:
+    """Projection flops of one prefill: 2 * rows * (layer params) plus the head on the last rows."""
+    rows = float(lengths.sum())
+    return 2.0 * rows * s.n_layers * s.layer_params() + 2.0 * len(lengths) * s.vocab * s.d_model
+
+
+def prefill_attn_flops(s: wl.ModelShape, lengths: np.ndarray) -> float:
+    """Causal attention flops: q.k and p.v over the (T+1)T/2 visible pairs of every head."""
+    pairs = float(sum(int(L) * (int(L) + 1) // 2 for L in lengths))
+    return 4.0 * pairs * s.head_dim * s.n_heads * s.n_layers
+
+
 # ------------------------------------------------------------------------------------------------
 # clocks
 # ------------------------------------------------------------------------------------------------
@@ -196,6 +208,26 @@ def run_reference(args, W):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    if W.mode == "prefill" or W.decode_steps == 0:
+        import oracle
+        w = wl.make_weights(W.model, scale=W.weight_scale)
+        model = oracle.OracleModel(w)
+        prompt = wl.draw_prompts(W.lengths(), W.model.vocab)[0]
+        n = max(1, min(args.steps, 3))
+        t0 = time.perf_counter()
+        for _ in range(n):
+            oracle.forward_full(model, prompt, last_only=True)
+        dt = time.perf_counter() - t0
+        rate = n * len(prompt) / dt
+        desc = f"float64 NumPy oracle, stateless forward of 1 of {W.batch} prompts ({len(prompt)} tokens), {n} times"
+        line = {"impl": "reference", "metric": BASELINE_METRIC, "metric_detail": "prefill tok/s", "value": rate,
+                "unit": "tok/s", "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": 1000.0 * dt / n,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": W.name, "batch": W.batch, "prompt_len": len(prompt)},
+                "cpu_baseline": {"value": rate, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc},
+                "e2e": {"value": rate, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
     rate, dt, desc = oracle_decode_rate(W, args.steps, args.warmup, n_seq=1)
     line = {"impl": "reference", "metric": BASELINE_METRIC, "metric_detail": f"decode tok/s at batch {W.batch}",
             "value": rate, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -274,16 +306,20 @@ def run_decode_bench(args, W):
     stats = run.dec.kernel_stats(reset=True)
     run.dec.set_profiling(False)
     fam = {}
+    kinds = {}
     for name, (n, t) in stats.items():
-        f = "gemv" if name.startswith("gemv") else "gemm_tc" if name.startswith("gemm_tc") else \
-            "gemm_simt" if name.startswith("gemm_simt") else name
+        # every projection kernel (CUDA-core GEMV or tcgen05) is one family: they share the
+        # weight-stream roofline
+        f = "proj" if name.startswith(("gemv", "gemm")) else name
+        if f == "proj":
+            kinds[name.split("_")[0] + ("_" + name.split("_")[1] if name.startswith("gemm") else "")] = 1
         a = fam.setdefault(f, [0, 0.0])
         a[0] += n
         a[1] += t
     dom = max(fam, key=lambda k: fam[k][1])
     pk, pk_kind = peaks()
     ctx_steps = np.stack([run.lengths + j + 1 for j in range(period)])          # keys read per step
-    if dom == "gemv":
+    if dom == "proj":
         alg = gemv_bytes(s, B) * period
     elif dom == "attn_decode":
         alg = sum(attn_bytes(s, c) for c in ctx_steps)
@@ -291,7 +327,8 @@ def run_decode_bench(args, W):
         alg = None
     dom_ms = fam[dom][1]
     achieved = alg / (dom_ms / 1000.0) / 1e9 if alg else None
-    roof = {"bound": "hbm", "kernel": dom, "launches": fam[dom][0], "achieved": achieved, "peak": pk["hbm_gbs"],
+    roof = {"bound": "hbm", "kernel": dom if dom != "proj" else "proj (" + "+".join(sorted(kinds)) + ")",
+            "launches": fam[dom][0], "achieved": achieved, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "traffic": None,
             "peak_source": f"hbm_gbs of {pk_kind}",
             "alg_bytes_per_launch": (alg / fam[dom][0]) if alg else None,
@@ -346,6 +383,113 @@ def run_decode_bench(args, W):
     return 0
 
 
+def run_prefill_bench(args, W):
+    """One step = one prefill of the whole batch (every row of the hot path, attention over the
+    full causal prompt, K/V written into the paged pool, last-position argmax)."""
+    import torch
+    import torch.distributed as dist
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    s = W.model
+    host_w = wl.make_weights(s, scale=W.weight_scale)
+    run = WorkloadRun(W, host_weights=host_w)
+    B = run.B
+    tokens_total = int(run.lengths.sum())
+    for _ in range(args.warmup):
+        run.prefill()
+    torch.cuda.synchronize()
+    launches_per_step = run.dec.last_launch_count()
+    st = run.stream
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id_for_smi(local)) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record(st)
+        for _ in range(args.steps):
+            run.prefill()
+        ev1.record(st)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = tokens_total * args.steps * world / (ms / 1000.0)
+    assert run.dec.error_flags() == 0, "device error flags set during the bench"
+    # per-kernel durations over one more prefill
+    run.dec.set_profiling(True)
+    run.dec.kernel_stats(reset=True)
+    run.prefill()
+    stats = run.dec.kernel_stats(reset=True)
+    run.dec.set_profiling(False)
+    fam = {}
+    for name, (n, t) in stats.items():
+        f = "gemm_tc" if name.startswith("gemm_tc") else ("proj" if name.startswith(("gemv", "gemm")) else name)
+        a = fam.setdefault(f, [0, 0.0])
+        a[0] += n
+        a[1] += t
+    pk, pk_kind = peaks()
+    gem = fam.get("gemm_tc", [0, 0.0])
+    gflops = prefill_gemm_flops(s, run.lengths)
+    achieved = gflops / (gem[1] / 1000.0) / 1e12 if gem[1] > 0 else None
+    roof = {"bound": "tensor", "kernel": "gemm_tc (tcgen05 projections)", "launches": gem[0], "achieved": achieved,
+            "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": (achieved / pk["bf16_tflops"]) if achieved else None,
+            "traffic": None, "peak_source": f"bf16_tflops (burst) of {pk_kind}",
+            "alg_flops_per_launch": gflops / gem[0] if gem[0] else None,
+            "avg_launch_us": 1000.0 * gem[1] / gem[0] if gem[0] else None}
+    total = sum(v[1] for v in fam.values())
+    kernel_share = {k: round(v[1] / total, 4) for k, v in sorted(fam.items())}
+    # end to end: host token ids in, next ids out, through the C ABI
+    tok_h = torch.from_numpy(np.concatenate(run.prompts).astype(np.int32)).pin_memory()
+    ids_h = torch.zeros(B, dtype=torch.int32).pin_memory()
+    n_e2e = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        with torch.cuda.stream(st):
+            run.tokens.copy_(tok_h, non_blocking=True)
+            run.dec.prefill(run.tokens, [int(x) for x in run.lengths], run.tables, run.next_ids)
+            ids_h.copy_(run.next_ids, non_blocking=True)
+        st.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": tokens_total * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": int(tok_h.numel() * 4),
+           "d2h_bytes_per_step": B * 4, "steps": n_e2e, "api": "llm_prefill (pinned host ids in, ids out)"}
+    line = {"metric": BASELINE_METRIC, "metric_detail": f"prefill tok/s, {B} x {int(run.lengths[0])} tokens",
+            "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
+            "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]), "kv": "paged16",
+                       "l2": "inputs larger than L2: %.0f MB activations per step" % (tokens_total * s.d_model * 4 / 1e6)},
+            "roofline": roof,
+            "attention_flops_per_step": prefill_attn_flops(s, run.lengths),
+            "gemm_flops_per_step": gflops,
+            "kernel_share": kernel_share, "gpu_launches": launches_per_step * args.steps,
+            "launches_per_step": launches_per_step, "e2e": e2e, "clocks": clk.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        model = oracle.OracleModel(host_w)
+        t0 = time.perf_counter()
+        oracle.forward_full(model, run.prompts[0], last_only=True)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": int(run.lengths[0]) / dt, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"float64 NumPy oracle, 1 of {B} prompts ({int(run.lengths[0])} tokens), "
+                                          "stateless forward", "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -362,7 +506,7 @@ def main():
     if args.impl == "reference":
         return run_reference(args, W)
     if W.mode == "prefill" or W.decode_steps == 0:
-        ap.error("prefill workloads: see --workload; this bench times decode steps")
+        return run_prefill_bench(args, W)
     return run_decode_bench(args, W)
 
 

@@ -190,19 +190,22 @@ llm_status llm_last_launch_count(llm_handle* h, int* n);
 llm_status llm_set_graphs(llm_handle* h, int enable);
 
 /* Projection kernel choice: 0 = by row count (default), 1 = CUDA-core weight-stream
- * GEMV, 2 = CUDA-core tiled GEMM, 3 = tcgen05 tensor-core GEMM (bf16 models; falls
- * back to 2 where it does not apply). For tests that force every kernel on every
- * shape. Drops cached graphs. Errors: INVALID_ARG for another value. */
+ * GEMV, 2 = CUDA-core tiled GEMM, 3 = tcgen05 GEMM with the activation rows on the
+ * MMA's M side (bf16 models; falls back to 2 where it does not apply), 4 = tcgen05
+ * GEMM with the weight rows on the MMA's M side (at most 256 activation rows; bf16,
+ * or fp32 as three tf32 products; falls back to 3 / 2). For tests that force every
+ * kernel on every shape. Drops cached graphs. Errors: INVALID_ARG for another value. */
 llm_status llm_set_linear_variant(llm_handle* h, int variant);
 
 /* Test and diagnostic entry point (no handle): one projection with a chosen kernel,
  *   y[m][n] = sum_k x[m][k] * w[n][k] (+ bias[n]),  m < M, n < N,
  * x DEVICE [M][K] and w DEVICE [N][K] row-major in `dtype` (LLM_DTYPE_F32 or
  * LLM_DTYPE_BF16), bias DEVICE [N] in `dtype` or NULL, y DEVICE float [M][N].
- * variant: 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM (bf16 only;
- * K and the row strides must be multiples of 8). Enqueued on `cuda_stream`.
- * Errors: INVALID_ARG (bad sizes, NULL, K % 8 for variant 3), UNSUPPORTED
- * (variant 3 with fp32), CUDA. */
+ * variant: 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM (bf16 only),
+ * 4 tcgen05 GEMM with the weights on the MMA's M side (M <= 256; bf16, or fp32 as
+ * three tf32 products). Variants 3 and 4 need K % 8 == 0. Enqueued on `cuda_stream`.
+ * Errors: INVALID_ARG (bad sizes, NULL, K % 8 for variants 3/4, M > 256 for 4),
+ * UNSUPPORTED (variant 3 with fp32), CUDA. */
 llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const void* w, const void* bias, float* y,
                          int variant, void* cuda_stream);
 

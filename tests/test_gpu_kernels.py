@@ -21,7 +21,7 @@ def _inputs(M, N, K, bf16, seed):
     return x, w, b
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3], ids=["gemv", "simt", "tcgen05"])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4], ids=["gemv", "simt", "tcgen05", "tcgen05-swap"])
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_linear_kernel_matches_oracle(gpu_lib, variant, bf16, M, N, K):
@@ -30,6 +30,8 @@ def test_linear_kernel_matches_oracle(gpu_lib, variant, bf16, M, N, K):
         pytest.skip("tcgen05 path is bf16 only")
     if variant == 1 and M > 64:
         pytest.skip("the weight-stream GEMV serves decode row counts")
+    if variant == 4 and M > 256:
+        pytest.skip("weights-on-M path serves at most 256 rows")
     x, w, b = _inputs(M, N, K, bf16, seed=M * 7 + N + K)
     dt = torch.bfloat16 if bf16 else torch.float32
     tx, tw, tb = (torch.from_numpy(a).cuda().to(dt) for a in (x, w, b))
@@ -38,9 +40,11 @@ def test_linear_kernel_matches_oracle(gpu_lib, variant, bf16, M, N, K):
     torch.cuda.synchronize()
     ref = OracleModel.linear(x.astype(np.float64), w.astype(np.float64), b.astype(np.float64))
     got = y.cpu().numpy()
-    # fp32 accumulation over K terms of size |x||w|: bound by K * 2^-23 * sum|x w| (+ margin)
+    # fp32 accumulation over K terms of size |x||w|: bound by K * 2^-23 * sum|x w| (+ margin).
+    # The fp32 tensor-core path sums three tf32 products; the dropped low*low term and the
+    # tf32 rounding of the low parts add about 2^-20 relative per product.
     scale = np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T + np.abs(b)
-    tol = 1e-6 + 4 * K * 2.0 ** -23 * scale
+    tol = 1e-6 + 4 * K * 2.0 ** -23 * scale + (2.0 ** -19 * scale if (variant == 4 and not bf16) else 0)
     assert np.all(np.isfinite(got))
     assert np.all(np.abs(got - ref) <= tol), float(np.abs(got - ref).max())
 

@@ -38,7 +38,7 @@ def _oracle_rows(model, run, stream):
     return [oracle_teacher(model, run.prompts[b], stream[:, b]) for b in range(run.B)]
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3], ids=["gemv", "simt", "tcgen05"])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4], ids=["gemv", "simt", "tcgen05", "tcgen05-swap"])
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
 def test_small_model_matches_oracle(gpu_lib, small_models, shape, variant):
     from transformer_decoder_forward_gb300.runner import WorkloadRun
@@ -258,3 +258,22 @@ def test_gpt2_124m_bf16_prefill_16x1024(gpu_lib):
         check_logits(z[b:b + 1], ref, W.model.dtype, f"{W.name} seq {b}")
         check_ids(ids[b:b + 1], ref, f"{W.name} seq {b}")
     run.close()
+
+
+def test_gpt2_xl_bf16_b256_ctx1024(gpu_lib):
+    """256 sequences: 960-token prompts in shuffled paged blocks, then 64 teacher-forced decode
+    steps up to position 1023 (context 1024); the oracle recomputes two sampled sequences."""
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    W = wl.W_GPT2XL_B256
+    w = wl.make_weights(W.model)
+    run = WorkloadRun(W, host_weights=w)
+    stream = wl.draw_stream(run.B, W.decode_steps, W.model.vocab)
+    rows = [0, 255]
+    ids, z = run_gpu_teacher(run, stream, rows=rows)
+    assert run.dec.error_flags() == 0
+    run.close()
+    model = oracle.OracleModel(w)
+    for i, b in enumerate(rows):
+        ref = oracle_teacher(model, run.prompts[b], stream[:, b])
+        check_logits(z[:, i], ref, W.model.dtype, f"{W.name} seq {b}")
+        check_ids(ids[:, b], ref, f"{W.name} seq {b}")

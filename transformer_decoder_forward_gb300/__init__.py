@@ -229,7 +229,7 @@ class Decoder:
         _check(self.lib.llm_set_graphs(self.handle, int(on)))
 
     def set_linear_variant(self, v: int) -> None:
-        """0 auto, 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM."""
+        """0 auto, 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM, 4 tcgen05 weights-on-M GEMM."""
         _check(self.lib.llm_set_linear_variant(self.handle, int(v)))
 
     def kernel_stats(self, reset: bool = True):

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -93,10 +94,6 @@ struct llm_handle {
   int head_tiles = 0;
   float* head_val = nullptr;
   int* head_idx = nullptr;
-  float* gemv_part = nullptr;
-  size_t gemv_part_elems = 0;
-  unsigned* counters = nullptr;
-  int counters_len = 0;
   unsigned* flags = nullptr;
   StepArgs* d_args = nullptr;
   int* d_row_pos = nullptr;
@@ -104,6 +101,7 @@ struct llm_handle {
   int* d_last_row = nullptr;
   int4* d_items = nullptr;
   int max_items = 0;
+  float2* d_rope = nullptr;   // RoPE inverse frequencies, split (hi, lo)
   // host-buffer entry point staging
   int* d_host_tokens = nullptr;
   int* d_host_pos = nullptr;
@@ -174,7 +172,10 @@ llm_status run(llm_handle* h, const char* name, F&& f) {
     cudaEventRecord(a, h->stream);
   }
   cudaError_t e = f();
-  if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string(name) + ": " + cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    cudaGetLastError();   // a failed launch must not be reported again by the next call
+    return fail(LLM_ERR_CUDA, std::string(name) + ": " + cudaGetErrorString(e));
+  }
   if (h->profiling) {
     cudaEventRecord(b, h->stream);
     h->prof.push_back({name, a, b});
@@ -191,21 +192,20 @@ llm_status run(llm_handle* h, const char* name, F&& f) {
 
 int pick_variant(const llm_handle* h, const LinearParams& p) {
   if (h->lin_variant != LIN_AUTO) return h->lin_variant;
+  if (p.M <= 256 && gemm_tc_swap_supported(p)) return LIN_TC_SWAP;
   if (p.M <= 64) return LIN_GEMV;
   if (gemm_tc_supported(p)) return LIN_TC;
   return LIN_SIMT;
 }
 
 llm_status linear(llm_handle* h, const char* tag, LinearParams p) {
-  p.part = h->gemv_part;
-  p.part_elems = h->gemv_part_elems;
-  p.counters = h->counters;
-  p.counters_len = h->counters_len;
   int v = pick_variant(h, p);
+  if (v == LIN_TC_SWAP && !gemm_tc_swap_supported(p)) v = gemm_tc_supported(p) ? LIN_TC : LIN_SIMT;
   if (v == LIN_TC && !gemm_tc_supported(p)) v = LIN_SIMT;
-  std::string name = std::string(v == LIN_GEMV ? "gemv_" : v == LIN_TC ? "gemm_tc_" : "gemm_simt_") + tag;
+  std::string name = std::string(v == LIN_GEMV ? "gemv_" : v == LIN_TC ? "gemm_tc_" : v == LIN_TC_SWAP ? "gemm_tcs_" : "gemm_simt_") + tag;
   if (v == LIN_GEMV) RUN(name.c_str(), launch_gemv(p, h->num_sms, h->stream, h->pdl));
   else if (v == LIN_TC) RUN(name.c_str(), launch_gemm_tc(p, h->num_sms, h->stream, h->pdl));
+  else if (v == LIN_TC_SWAP) RUN(name.c_str(), launch_gemm_tc_swap(p, h->num_sms, h->stream, h->pdl));
   else RUN(name.c_str(), launch_gemm_simt(p, h->stream, h->pdl));
   return LLM_OK;
 }
@@ -230,6 +230,19 @@ Epilogue base_epi(const llm_handle* h) {
   return e;
 }
 
+// y = Norm(h) . W^T: the norm kernel writes xn (activation dtype), then the projection.
+llm_status norm_linear(llm_handle* h, const char* tag, LinearParams p, const void* g, const void* b,
+                       bool last_row) {
+  const llm_config& c = h->cfg;
+  const bool gpt2 = c.arch == LLM_ARCH_GPT2;
+  NormParams np{h->h, g, gpt2 ? b : nullptr, h->xn, h->d_args, p.M, c.d_model, gpt2 ? 1 : 0, last_row ? 1 : 0,
+                c.norm_eps};
+  RUN("norm", launch_norm(np, h->wdt, h->adt, h->stream, h->pdl));
+  p.X = h->xn;
+  p.ldx = c.d_model;
+  return linear(h, tag, p);
+}
+
 // The kernels of one forward pass over M rows (decode: M = B, one row per
 // sequence; prefill chunk: the packed prompt rows), reading d_args.
 // items != 0 selects prefill attention over `n_items` work items.
@@ -244,15 +257,12 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
 
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& w = h->layers[l];
-    NormParams np{h->h, w.ln1_w, gpt2 ? w.ln1_b : nullptr, h->xn, h->d_args, M, d, gpt2 ? 1 : 0, 0, c.norm_eps};
-    RUN("norm", launch_norm(np, h->wdt, h->adt, h->stream, h->pdl));
-
     LinearParams lp;
     memset(&lp, 0, sizeof(lp));
     lp.wdt = h->wdt; lp.xdt = h->adt; lp.adt = h->adt;
     lp.M = M;
-    // QKV + RoPE + kv_write
-    lp.W = w.w_qkv; lp.X = h->xn; lp.N = qkv_n; lp.K = d; lp.ldx = d; lp.swiglu = 0;
+    // norm + QKV + RoPE + kv_write
+    lp.W = w.w_qkv; lp.N = qkv_n; lp.K = d; lp.swiglu = 0;
     lp.epi = base_epi(h);
     lp.epi.kind = EPI_QKV;
     lp.epi.bias = w.b_qkv;
@@ -261,7 +271,8 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
     lp.epi.n_heads = H;
     lp.epi.rope = gpt2 ? 0 : 1;
     lp.epi.rope_theta = c.rope_theta;
-    { llm_status s_ = linear(h, "qkv", lp); if (s_ != LLM_OK) return s_; }
+    lp.epi.rope_tab = h->d_rope;
+    { llm_status s_ = norm_linear(h, "qkv", lp, w.ln1_w, w.ln1_b, false); if (s_ != LLM_OK) return s_; }
 
     // attention
     if (!prefill) {
@@ -286,14 +297,11 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
     lp.epi.kind = EPI_RESID; lp.epi.bias = w.b_o; lp.epi.resid = h->h; lp.epi.ld_resid = d;
     { llm_status s_ = linear(h, "o", lp); if (s_ != LLM_OK) return s_; }
 
-    NormParams np2{h->h, w.ln2_w, gpt2 ? w.ln2_b : nullptr, h->xn, h->d_args, M, d, gpt2 ? 1 : 0, 0, c.norm_eps};
-    RUN("norm", launch_norm(np2, h->wdt, h->adt, h->stream, h->pdl));
-
-    // FFN up (+gate) with the activation
-    lp.W = w.w_up; lp.X = h->xn; lp.N = F; lp.K = d; lp.ldx = d; lp.swiglu = gpt2 ? 0 : 1;
+    // norm + FFN up (+gate) with the activation
+    lp.W = w.w_up; lp.N = F; lp.K = d; lp.swiglu = gpt2 ? 0 : 1;
     lp.epi = base_epi(h);
     lp.epi.kind = gpt2 ? EPI_GELU : EPI_SWIGLU; lp.epi.bias = w.b_up; lp.epi.out = h->ff; lp.epi.ld_out = F;
-    { llm_status s_ = linear(h, "up", lp); if (s_ != LLM_OK) return s_; }
+    { llm_status s_ = norm_linear(h, "up", lp, w.ln2_w, w.ln2_b, false); if (s_ != LLM_OK) return s_; }
 
     // FFN down + residual
     lp.W = w.w_down; lp.X = h->ff; lp.N = d; lp.K = F; lp.ldx = F; lp.swiglu = 0;
@@ -303,16 +311,13 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
   }
 
   // final norm on each sequence's last row, tied LM head + argmax partials, argmax reduce
-  NormParams nf{h->h, h->lnf_w, gpt2 ? h->lnf_b : nullptr, h->xn, h->d_args, B, d, gpt2 ? 1 : 0, prefill ? 1 : 0,
-                c.norm_eps};
-  RUN("norm", launch_norm(nf, h->wdt, h->adt, h->stream, h->pdl));
   LinearParams hp;
   memset(&hp, 0, sizeof(hp));
   hp.wdt = h->wdt; hp.xdt = h->adt; hp.adt = h->adt;
-  hp.W = h->tok_emb; hp.X = h->xn; hp.M = B; hp.N = c.vocab; hp.K = d; hp.ldx = d;
+  hp.W = h->tok_emb; hp.M = B; hp.N = c.vocab; hp.K = d;
   hp.epi = base_epi(h);
   hp.epi.kind = EPI_HEAD; hp.epi.part_val = h->head_val; hp.epi.part_idx = h->head_idx; hp.epi.vocab = c.vocab;
-  { llm_status s_ = linear(h, "head", hp); if (s_ != LLM_OK) return s_; }
+  { llm_status s_ = norm_linear(h, "head", hp, h->lnf_w, h->lnf_b, prefill); if (s_ != LLM_OK) return s_; }
   ArgmaxParams amp{h->head_val, h->head_idx, h->head_tiles, h->d_args, h->flags};
   RUN("argmax", launch_argmax(amp, B, h->stream, h->pdl));
   return LLM_OK;
@@ -421,6 +426,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   h->layer_kv_elems = (size_t)h->num_blocks * Hkv * KVB * HD;
   h->max_rows = std::max(c.max_batch, c.max_prefill_tokens);
   const int max_ctx = std::min(c.n_ctx, c.max_blocks_per_seq * KVB);
+  h->split = attn_decode_split_for(c.max_batch, c.n_kv_heads, max_ctx, h->num_sms);
   h->max_splits = std::max(1, (max_ctx + h->split - 1) / h->split);
   h->head_tiles = (c.vocab + TILE_N - 1) / TILE_N;
   h->max_items = c.max_prefill_tokens / 64 + c.max_batch + 1;
@@ -443,10 +449,6 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   ALLOC(h->attn_ml, float, (size_t)c.max_batch * H * h->max_splits * 2);
   ALLOC(h->head_val, float, (size_t)h->head_tiles * R);
   ALLOC(h->head_idx, int, (size_t)h->head_tiles * R);
-  h->gemv_part_elems = (size_t)8 << 20;
-  ALLOC(h->gemv_part, float, h->gemv_part_elems);
-  h->counters_len = 16384;
-  ALLOC(h->counters, unsigned, h->counters_len);
   ALLOC(h->flags, unsigned, 1);
   ALLOC(h->d_args, StepArgs, 1);
   ALLOC(h->d_row_pos, int, R);
@@ -458,7 +460,27 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   ALLOC(h->d_host_tables, int, (size_t)c.max_batch * c.max_blocks_per_seq);
   ALLOC(h->d_host_ids, int, c.max_batch);
   ALLOC(h->d_host_logits, float, (size_t)c.max_batch * c.vocab);
+  ALLOC(h->d_rope, float2, HD / 2);
 #undef ALLOC
+  {
+    // inverse frequency theta^(-2d/64) of RoPE pair d, split into hi (11 significant bits:
+    // pos * hi is exact in fp32 for pos < 2^13) + lo, computed once here in double
+    float2 tab[HD / 2];
+    for (int d = 0; d < HD / 2; ++d) {
+      const double f = gpt2 ? 0.0 : pow((double)c.rope_theta, -2.0 * d / HD);
+      float hi = (float)f;
+      uint32_t bits;
+      memcpy(&bits, &hi, 4);
+      bits &= 0xFFFFE000u;   // keep 10 explicit mantissa bits (11 significant)
+      memcpy(&hi, &bits, 4);
+      tab[d] = make_float2(hi, (float)(f - (double)hi));
+    }
+    if (cudaMemcpy(h->d_rope, tab, sizeof(tab), cudaMemcpyHostToDevice) != cudaSuccess) {
+      free_all(h);
+      delete h;
+      return fail(LLM_ERR_CUDA, "copy of the RoPE table failed");
+    }
+  }
   if (!stream_capturable(h->stream)) h->use_graphs = false;
   if (const char* env = getenv("LLM_NO_GRAPH")) h->use_graphs = h->use_graphs && env[0] != '1';
   if (const char* env = getenv("LLM_PDL")) h->pdl = env[0] != '0';
@@ -670,9 +692,11 @@ llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const vo
   if (M <= 0 || N <= 0 || K <= 0) return fail(LLM_ERR_INVALID_ARG, "sizes must be positive");
   if (!x || !w || !y) return fail(LLM_ERR_INVALID_ARG, "NULL x, w or y");
   if (dtype != LLM_DTYPE_F32 && dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_INVALID_ARG, "bad dtype");
-  if (variant < LIN_GEMV || variant > LIN_TC) return fail(LLM_ERR_INVALID_ARG, "variant must be 1..3");
+  if (variant < LIN_GEMV || variant > LIN_TC_SWAP) return fail(LLM_ERR_INVALID_ARG, "variant must be 1..4");
   if (variant == LIN_TC && dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_UNSUPPORTED, "tcgen05 path is bf16 only");
-  if (variant == LIN_TC && K % 8 != 0) return fail(LLM_ERR_INVALID_ARG, "tcgen05 path needs K % 8 == 0");
+  if ((variant == LIN_TC || variant == LIN_TC_SWAP) && K % 8 != 0)
+    return fail(LLM_ERR_INVALID_ARG, "tcgen05 paths need K % 8 == 0");
+  if (variant == LIN_TC_SWAP && M > 256) return fail(LLM_ERR_INVALID_ARG, "weights-on-M tcgen05 path needs M <= 256");
   int dev = 0, nsm = 0;
   CUDA_TRY(cudaGetDevice(&dev));
   CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
@@ -688,7 +712,8 @@ llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const vo
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   cudaError_t e = variant == LIN_GEMV ? launch_gemv(p, nsm, s, false)
                   : variant == LIN_SIMT ? launch_gemm_simt(p, s, false)
-                                        : launch_gemm_tc(p, nsm, s, false);
+                  : variant == LIN_TC   ? launch_gemm_tc(p, nsm, s, false)
+                                        : launch_gemm_tc_swap(p, nsm, s, false);
   if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("llm_op_linear: ") + cudaGetErrorString(e));
   return LLM_OK;
 }
@@ -705,7 +730,10 @@ llm_status llm_op_attention_decode(int kv_dtype, int B, int n_heads, int n_kv_he
   if (n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > 8)
     return fail(LLM_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads, at most 8 per KV head");
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  const int split = 64;
+  int dev = 0, sms = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int split = attn_decode_split_for(B, n_kv_heads, max_blocks_per_seq * KVB, sms);
   const int max_splits = (max_blocks_per_seq * KVB + split - 1) / split;
   const size_t part_o = (size_t)B * n_heads * max_splits * HD, part_ml = (size_t)B * n_heads * max_splits * 2;
   char* scratch = nullptr;
@@ -746,7 +774,7 @@ llm_status llm_op_attention_decode(int kv_dtype, int B, int n_heads, int n_kv_he
 llm_status llm_set_linear_variant(llm_handle* h, int variant) {
   llm_status st = check_handle(h);
   if (st != LLM_OK) return st;
-  if (variant < LIN_AUTO || variant > LIN_TC) return fail(LLM_ERR_INVALID_ARG, "variant must be 0..3");
+  if (variant < LIN_AUTO || variant > LIN_TC_SWAP) return fail(LLM_ERR_INVALID_ARG, "variant must be 0..4");
   CUDA_TRY(cudaStreamSynchronize(h->stream));
   for (auto& kv : h->graphs) {
     if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);

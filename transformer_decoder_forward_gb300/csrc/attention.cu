@@ -22,188 +22,163 @@ namespace {
 
 constexpr int AD_THREADS = 128;
 constexpr int MAX_G = 8;
-constexpr int MAX_SPLIT = 128;
 constexpr float SM_SCALE = 0.125f;   // 1/sqrt(64)
 
-// smem for one split: K and V blocks (split/16 blocks of 16 x 64 elements each), then a
-// small fixed area. The whole split is in flight at once: one thread issues a TMA bulk
-// copy per KV block (16 contiguous token rows of one head) onto a single mbarrier.
-template <typename KT>
-__host__ __device__ constexpr size_t attn_decode_smem(int split) {
-  return 2 * (size_t)split * HD * sizeof(KT);
-}
-
-template <typename KT>
+// Decode attention, one CTA per (sequence b, KV head g, chunk of `split` tokens).
+// The chunk's 16-token KV blocks are dealt to the 4 warps in turn; each warp streams
+// its blocks with 16-byte loads (two blocks in flight) and keeps an online softmax
+// (running max, sum of exp, unnormalised output) for every query head of the group
+// in registers. A token row is LPT lanes wide (8 for bf16, 16 for fp32); the lanes
+// that score a token are the lanes that weight its value row, so no probability has
+// to be broadcast. At the end the 4 warps' states are merged in shared memory and the
+// chunk's (max, sum, output) goes to the split-K partial buffer.
+template <typename KT, int GMAX>
 __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDecodeParams p) {
-  extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ __align__(16) float qs[MAX_G][HD];
-  __shared__ float sc[MAX_G][MAX_SPLIT];
-  __shared__ __align__(16) float ored[AD_THREADS / 32][MAX_G][HD];
-  __shared__ float red[AD_THREADS / 32][MAX_G];
-  __shared__ float stat[2][MAX_G];
-  __shared__ int blk_ok[MAX_SPLIT / KVB];
-  __shared__ __align__(8) uint64_t bar;
-
   constexpr int EPL = 16 / sizeof(KT);    // elements per 16-byte load
-  constexpr int LPT = HD / EPL;           // lanes per token row: 16 (fp32) or 8 (bf16)
-  constexpr int TPW = 32 / LPT;           // token rows per warp load
-  constexpr int NWARP = AD_THREADS / 32;
-  constexpr unsigned BLK_BYTES = KVB * HD * sizeof(KT);
+  constexpr int LPT = HD / EPL;           // lanes per token row: 8 (bf16) or 16 (fp32)
+  constexpr int TG = 32 / LPT;            // token groups per warp: 4 or 2
+  constexpr int IT = KVB / TG;            // loads per lane per 16-token block: 4 or 8
+  constexpr int NW = AD_THREADS / 32;
+  __shared__ float s_m[NW][GMAX], s_l[NW][GMAX];
+  __shared__ __align__(16) float s_o[NW][GMAX][HD];
 
   const int Hkv = p.kv.n_kv_heads, H = p.n_heads, G = H / Hkv;
   const int b = blockIdx.x / Hkv, g = blockIdx.x - b * Hkv, sp = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  KT* Ks = reinterpret_cast<KT*>(dyn);
-  KT* Vs = Ks + (size_t)p.split * HD;
+  const int dg = lane % LPT, tg = lane / LPT;
   pdl_wait();   // the new token's K/V is written by the projection that precedes this kernel
   const StepArgs* a = p.args;
-  const int pos = a->positions[b];
-  const int ctx = pos + 1;
+  const int ctx = a->positions[b] + 1;
   const int t0 = sp * p.split;
   if (t0 >= ctx) return;
   const int nt = min(p.split, ctx - t0);
-  const int nb = (nt + KVB - 1) / KVB;
+  const int nblk = (nt + KVB - 1) / KVB;
 
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    const KT* kbase = reinterpret_cast<const KT*>(p.kv.k);
-    const KT* vbase = reinterpret_cast<const KT*>(p.kv.v);
-    int pbs[MAX_SPLIT / KVB];
-    unsigned bytes = 0;
-    for (int i = 0; i < nb; ++i) {
-      pbs[i] = kv_block(p.kv, a->block_tables, b, t0 + i * KVB, p.flags);
-      blk_ok[i] = pbs[i] >= 0;
-      if (pbs[i] >= 0) bytes += 2 * BLK_BYTES;
-    }
-    mbar_arrive_expect_tx(&bar, bytes);
-    for (int i = 0; i < nb; ++i) {
-      if (pbs[i] < 0) continue;
-      const size_t off = kv_offset(p.kv, pbs[i], g, 0);
-      bulk_g2s(Ks + (size_t)i * KVB * HD, kbase + off, BLK_BYTES, &bar);
-      bulk_g2s(Vs + (size_t)i * KVB * HD, vbase + off, BLK_BYTES, &bar);
+  float qf[GMAX][EPL], o[GMAX][EPL], m[GMAX], l[GMAX];
+#pragma unroll
+  for (int j = 0; j < GMAX; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      o[j][e] = 0.0f;
+      qf[j][e] = j < G ? p.q[(size_t)b * H * HD + (size_t)(g * G + j) * HD + dg * EPL + e] * SM_SCALE : 0.0f;
     }
   }
-  for (int i = tid; i < G * HD; i += AD_THREADS) {
-    const int j = i / HD, d = i - j * HD;
-    qs[j][d] = p.q[(size_t)b * H * HD + (size_t)(g * G + j) * HD + d] * SM_SCALE;
+  const KT* kbase = reinterpret_cast<const KT*>(p.kv.k);
+  const KT* vbase = reinterpret_cast<const KT*>(p.kv.v);
+
+  auto load_block = [&](int bi, uint4* kq, uint4* vq, bool& ok) {
+    const int pb = kv_block(p.kv, a->block_tables, b, t0 + bi * KVB, p.flags);
+    ok = pb >= 0;
+    const size_t off = kv_offset(p.kv, ok ? pb : 0, g, 0) + dg * EPL;
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const int t = it * TG + tg;
+      kq[it] = ok ? ldg16(kbase + off + (size_t)t * HD) : make_uint4(0, 0, 0, 0);
+      vq[it] = ok ? ldg16(vbase + off + (size_t)t * HD) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto consume = [&](int bi, const uint4* kq, const uint4* vq, bool ok) {
+    if (!ok) return;
+    float sc[GMAX][IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      float kf[EPL];
+      Vec16<KT>::unpack(kq[it], kf);
+      const bool valid = bi * KVB + it * TG + tg < nt;
+#pragma unroll
+      for (int j = 0; j < GMAX; ++j) {
+        float d = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) d = fmaf(kf[e], qf[j][e], d);
+#pragma unroll
+        for (int x = LPT / 2; x > 0; x >>= 1) d += __shfl_xor_sync(0xffffffffu, d, x);
+        sc[j][it] = valid ? d : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < GMAX; ++j) {
+      if (j >= G) continue;
+      float mb = sc[j][0];
+#pragma unroll
+      for (int it = 1; it < IT; ++it) mb = fmaxf(mb, sc[j][it]);
+#pragma unroll
+      for (int x = LPT; x < 32; x <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, x));
+      const float mn = fmaxf(m[j], mb);
+      const float alpha = m[j] == -INFINITY ? 0.0f : expf(m[j] - mn);
+      m[j] = mn;
+      l[j] *= alpha;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[j][e] *= alpha;
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        const float pr = sc[j][it] == -INFINITY ? 0.0f : expf(sc[j][it] - mn);
+        l[j] += pr;
+        float vf[EPL];
+        Vec16<KT>::unpack(vq[it], vf);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(pr, vf[e], o[j][e]);
+      }
+    }
+  };
+
+  // two blocks in flight per warp
+  uint4 ka[IT], va[IT], kb[IT], vb[IT];
+  bool oka = false, okb = false;
+  int bi = warp;
+  if (bi < nblk) load_block(bi, ka, va, oka);
+  for (; bi < nblk; bi += 2 * NW) {
+    const int bn = bi + NW;
+    if (bn < nblk) load_block(bn, kb, vb, okb);
+    consume(bi, ka, va, oka);
+    if (bn >= nblk) break;
+    const int bn2 = bn + NW;
+    if (bn2 < nblk) load_block(bn2, ka, va, oka);
+    consume(bn, kb, vb, okb);
   }
-  const bool ok = mbar_wait(&bar, 0, p.flags);
+
+  // warp: sum l and o over the token groups (m is warp-uniform)
+#pragma unroll
+  for (int j = 0; j < GMAX; ++j) {
+#pragma unroll
+    for (int x = LPT; x < 32; x <<= 1) {
+      l[j] += __shfl_xor_sync(0xffffffffu, l[j], x);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[j][e] += __shfl_xor_sync(0xffffffffu, o[j][e], x);
+    }
+  }
+  if (tg == 0) {
+#pragma unroll
+    for (int j = 0; j < GMAX; ++j) {
+      if (j >= G) continue;
+      if (dg == 0) {
+        s_m[warp][j] = m[j];
+        s_l[warp][j] = l[j];
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) s_o[warp][j][dg * EPL + e] = o[j][e];
+    }
+  }
   __syncthreads();
-  if (!ok) {
-    // the copies may still be landing: give them one more bounded wait before leaving
-    mbar_wait(&bar, 0, p.flags);
-    return;
-  }
   pdl_trigger();
-
-  const int sub = lane / LPT, li = lane - sub * LPT;
-  // ---- scores: LPT lanes per token row, 16-byte shared loads along the head dimension
-  for (int tb = warp * TPW; tb < nt; tb += NWARP * TPW) {
-    const int t = tb + sub;
-    float kf[EPL];
-    const bool valid = t < nt && blk_ok[t / KVB];
-    if (valid) {
-      Vec16<KT>::unpack(*reinterpret_cast<const uint4*>(Ks + (size_t)t * HD + li * EPL), kf);
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) kf[e] = 0.0f;
-    }
-    for (int j = 0; j < G; ++j) {
-      float d = 0.0f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) d = fmaf(kf[e], qs[j][li * EPL + e], d);
-#pragma unroll
-      for (int o = LPT / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      if (li == 0 && t < nt) sc[j][t] = valid ? d : -INFINITY;
-    }
-  }
-  __syncthreads();
-
-  // ---- softmax statistics of this split
-  for (int j = 0; j < G; ++j) {
-    float m = -INFINITY;
-    for (int t = tid; t < nt; t += AD_THREADS) m = fmaxf(m, sc[j][t]);
-    m = warp_max(m);
-    if (lane == 0) red[warp][j] = m;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float m = red[0][tid];
-    for (int w = 1; w < NWARP; ++w) m = fmaxf(m, red[w][tid]);
-    stat[0][tid] = m;
-  }
-  __syncthreads();
-  for (int j = 0; j < G; ++j) {
-    const float m = stat[0][j];
-    float l = 0.0f;
-    for (int t = tid; t < nt; t += AD_THREADS) {
-      const float e = m == -INFINITY ? 0.0f : expf(sc[j][t] - m);
-      sc[j][t] = e;
-      l += e;
-    }
-    l = warp_sum(l);
-    if (lane == 0) red[warp][j] = l;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float l = 0.0f;
-    for (int w = 0; w < NWARP; ++w) l += red[w][tid];
-    stat[1][tid] = l;
-  }
-
-  // ---- P . V: LPT lanes cover the head dimension, token groups stride the split
-  constexpr int NTG = AD_THREADS / LPT;
-  const int dg = tid % LPT, tg = tid / LPT;
-  float acc[MAX_G][EPL];
-#pragma unroll
-  for (int j = 0; j < MAX_G; ++j)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[j][e] = 0.0f;
-  for (int t = tg; t < nt; t += NTG) {
-    if (!blk_ok[t / KVB]) continue;
-    float vf[EPL];
-    Vec16<KT>::unpack(*reinterpret_cast<const uint4*>(Vs + (size_t)t * HD + dg * EPL), vf);
-#pragma unroll
-    for (int j = 0; j < MAX_G; ++j) {
-      if (j < G) {
-        const float pj = sc[j][t];
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[j][e] = fmaf(pj, vf[e], acc[j][e]);
-      }
-    }
-  }
-  // reduce token groups inside the warp (lanes differing above the LPT bits), then across warps
-#pragma unroll
-  for (int j = 0; j < MAX_G; ++j) {
-    if (j < G) {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        float v = acc[j][e];
-#pragma unroll
-        for (int o = LPT; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        acc[j][e] = v;
-      }
-    }
-  }
-  if (lane < LPT) {
-    for (int j = 0; j < G; ++j)
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) ored[warp][j][dg * EPL + e] = acc[j][e];
-  }
-  __syncthreads();
   for (int i = tid; i < G * HD; i += AD_THREADS) {
     const int j = i / HD, d = i - j * HD;
-    float o = 0.0f;
-    for (int w = 0; w < NWARP; ++w) o += ored[w][j][d];
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w][j]);
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float c = s_m[w][j] == -INFINITY ? 0.0f : expf(s_m[w][j] - M);
+      L = fmaf(c, s_l[w][j], L);
+      O = fmaf(c, s_o[w][j][d], O);
+    }
     const size_t hs = ((size_t)b * H + g * G + j) * p.max_splits + sp;
-    p.part_o[hs * HD + d] = o;
+    p.part_o[hs * HD + d] = O;
     if (d == 0) {
-      p.part_ml[hs * 2] = stat[0][j];
-      p.part_ml[hs * 2 + 1] = stat[1][j];
+      p.part_ml[hs * 2] = M;
+      p.part_ml[hs * 2 + 1] = L;
     }
   }
 }
@@ -377,19 +352,30 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, 
   return cfg;
 }
 
+}  // namespace
+
+int attn_decode_split_for(int B, int n_kv_heads, int max_ctx, int num_sms) {
+  if (const char* env = getenv("LLM_ATTN_SPLIT")) {
+    const int v = atoi(env);
+    if (v >= KVB && v % KVB == 0) return v;
+  }
+  // as long as possible (fewer partials to merge, longer streams per warp) while the grid
+  // of (sequence, KV head, chunk) CTAs is still several waves deep
+  int split = 1024;
+  while (split > 64 && (long long)B * n_kv_heads * ((max_ctx + split - 1) / split) < 8LL * num_sms) split /= 2;
+  return split;
+}
+
+namespace {
+
 template <typename KT, typename AT>
 cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
-  const size_t smem = attn_decode_smem<KT>(p.split);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_split<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)attn_decode_smem<KT>(MAX_SPLIT));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const int G = p.n_heads / p.kv.n_kv_heads;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t c1 = make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(AD_THREADS), smem, s, attr, pdl);
-  cudaError_t e = cudaLaunchKernelEx(&c1, k_attn_decode_split<KT>, p);
+  cudaLaunchConfig_t c1 = make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(AD_THREADS), 0, s, attr, pdl);
+  cudaError_t e = G == 1 ? cudaLaunchKernelEx(&c1, k_attn_decode_split<KT, 1>, p)
+                  : G <= 4 ? cudaLaunchKernelEx(&c1, k_attn_decode_split<KT, 4>, p)
+                           : cudaLaunchKernelEx(&c1, k_attn_decode_split<KT, 8>, p);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t c2 = make_cfg(dim3(p.B * p.n_heads), dim3(HD), 0, s, attr2, pdl);
@@ -415,8 +401,7 @@ cudaError_t prefill_t(const AttnPrefillParams& p, cudaStream_t s, bool pdl) {
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int kv_dtype, cudaStream_t s, bool pdl) {
   if (p.B <= 0) return cudaSuccess;
-  if (p.n_heads / p.kv.n_kv_heads > MAX_G || p.split > MAX_SPLIT || (p.split % KVB) != 0)
-    return cudaErrorInvalidValue;
+  if (p.n_heads / p.kv.n_kv_heads > MAX_G || p.split <= 0 || (p.split % KVB) != 0) return cudaErrorInvalidValue;
   if (kv_dtype == DT_F32)
     return p.out_dtype == DT_F32 ? decode_t<float, float>(p, s, pdl) : decode_t<float, bf16>(p, s, pdl);
   return p.out_dtype == DT_F32 ? decode_t<bf16, float>(p, s, pdl) : decode_t<bf16, bf16>(p, s, pdl);

@@ -34,6 +34,10 @@ struct AttnPrefillParams {
   unsigned* flags;
 };
 
+// Tokens per decode split for a batch of B sequences of up to max_ctx keys (a multiple of
+// 16; the environment variable LLM_ATTN_SPLIT overrides it).
+int attn_decode_split_for(int B, int n_kv_heads, int max_ctx, int num_sms);
+
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int kv_dtype, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_prefill(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl);
 

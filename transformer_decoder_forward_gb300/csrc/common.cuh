@@ -108,9 +108,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   uint32_t ok;
-  // suspend hint 1000 ns: a failed poll sleeps at most ~1 us
+  // no suspend-time hint: a hint lets a failed poll sleep for the whole hint even when the
+  // phase completes meanwhile, which put ~1 us on every pipeline hand-off
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
@@ -208,6 +209,7 @@ struct Epilogue {
   int n_heads;
   int rope;             // 1: rotate q and k (Llama)
   float rope_theta;
+  const float2* rope_tab;  // [HD/2] inverse frequency of pair d split as (hi, lo), hi with 11 significant bits
   // HEAD
   float* part_val;      // [n_tiles][M]
   int* part_idx;

@@ -1,5 +1,5 @@
 // Output-tile epilogues shared by every projection kernel (CUDA-core GEMV, SIMT
-// GEMM, tcgen05 GEMM). The producer leaves an fp32 tile tile[m][c] in shared
+// GEMM, tcgen05 GEMMs). The producer leaves an fp32 tile tile[m][c] in shared
 // memory (row stride ldt) holding y = x . W^T for rows m0.. and tile columns
 // c = 0..ncols-1, then every thread of the block calls run_epilogue().
 //
@@ -10,10 +10,16 @@
 //   SWIGLU  silu(gate) * up;
 //   QKV     bias, RoPE on q and k (Llama), kv_write of k and v into the paged cache;
 //   HEAD    tied-LM-head logits and a per-tile greedy argmax partial.
+//
+// Latency: the per-tile bias and the per-row KV slot are staged in shared memory
+// once, and read-modify-write loads are issued in batches before their stores, so a
+// thread never waits on one global round trip per element.
 #pragma once
 #include "common.cuh"
 
 namespace llm {
+
+constexpr int EPI_MAX_ROWS = 256;   // rows of one epilogue call (every projection tile fits)
 
 template <typename WT>
 __device__ __forceinline__ float bias_at(const void* b, int n) {
@@ -25,41 +31,98 @@ __device__ __forceinline__ void store_act(void* out, size_t i, float v) {
   reinterpret_cast<AT*>(out)[i] = from_f32<AT>(v);
 }
 
-// Angle of RoPE pair d at position pos, reduced to [-pi, pi] in double precision
-// so that large positions keep their accuracy in the float sincos.
-__device__ __forceinline__ void rope_sincos(int pos, int d, float theta, float* s, float* c) {
-  const double inv_freq = exp2(-(2.0 * d / HD) * log2((double)theta));
-  double a = (double)pos * inv_freq;
-  const double two_pi = 6.283185307179586476925;
-  a -= two_pi * rint(a / two_pi);
-  sincosf((float)a, s, c);
+// RoPE angle pos * inv_freq[d] reduced to about [-pi, pi] in fp32 without losing the
+// position's precision. inv_freq is split on the host into hi (11 significant bits, so
+// pos * hi is exact for pos < 2^13) + lo; 2*pi is split Cody-Waite style into three
+// floats so that k * 2*pi is subtracted exactly for the quotients that occur.
+__device__ __forceinline__ void rope_sincos(int pos, float2 f, float* s, float* c) {
+  const float p = (float)pos;
+  const float a_hi = p * f.x;                         // exact
+  const float a_lo = p * f.y;
+  const float k = rintf(a_hi * 0.15915494309189535f);   // 1 / (2 pi)
+  float r = fmaf(-k, 6.28125f, a_hi);                 // 2 pi = 6.28125 + c2 + c3 (c2, c3 floats)
+  r = fmaf(-k, 1.9353071693331003e-3f, r);
+  r = fmaf(-k, 1.0253376273028358e-11f, r);
+  r += a_lo;
+  sincosf(r, s, c);
 }
 
-// tile: fp32 [.., ldt] in shared memory. Rows m0 .. m0+mrows-1 of the launch,
-// tile columns 0..ncols-1 map to output column n0 + c (for SWIGLU: gate row n0 + c
-// for c < 32 and up row F + n0 + c - 32; output column n0 + c). N = output width.
+// tile: fp32 [.., ldt] in shared memory. Rows m0 .. m0+mrows-1 of the launch (mrows <=
+// EPI_MAX_ROWS), tile columns 0..ncols-1 (ncols <= 64) map to output column n0 + c (for
+// SWIGLU: gate row n0 + c for c < 32 and up row F + n0 + c - 32; output column n0 + c).
+// N = output width. Every thread of the block must call it (it synchronises the block).
 template <typename WT, typename AT>
 __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int m0, int mrows, int n0, int ncols,
                              int N) {
+  __shared__ float s_bias[64];
+  __shared__ int s_pos[EPI_MAX_ROWS];
+  __shared__ int s_blk[EPI_MAX_ROWS];
   const int tid = threadIdx.x, nth = blockDim.x;
+  __syncthreads();   // a previous call's readers are done with the staging arrays
+  if (tid < ncols) {
+    float b = 0.0f;
+    if (e.bias) {
+      if (e.kind == EPI_SWIGLU) {
+        const int j = n0 + (tid & 31);
+        if (j < N) b = bias_at<WT>(e.bias, tid < 32 ? j : N + j);
+      } else if (n0 + tid < N) {
+        b = bias_at<WT>(e.bias, n0 + tid);
+      }
+    }
+    s_bias[tid] = b;
+  }
+  if (e.kind == EPI_QKV) {
+    const StepArgs* a = e.args;
+    const int H = e.n_heads;
+    const bool kv_cols = n0 + ncols > H * HD;   // this tile holds k or v columns
+    for (int m = tid; m < mrows; m += nth) {
+      const int row = m0 + m;
+      const int pos = a->positions[row];
+      s_pos[m] = pos;
+      if (kv_cols) {
+        const int seq = a->row_seq ? a->row_seq[row] : row;
+        s_blk[m] = kv_block(e.kv, a->block_tables, seq, pos, e.flags);
+      }
+    }
+  }
+  __syncthreads();
+
   switch (e.kind) {
     case EPI_STORE_F32:
     case EPI_STORE_ACT:
-    case EPI_RESID:
     case EPI_GELU: {
       for (int i = tid; i < mrows * ncols; i += nth) {
         const int m = i / ncols, c = i - m * ncols, n = n0 + c;
         if (n >= N) continue;
-        const float y = tile[m * ldt + c] + bias_at<WT>(e.bias, n);
-        const size_t row = (size_t)(m0 + m);
-        if (e.kind == EPI_STORE_F32) {
-          reinterpret_cast<float*>(e.out)[row * e.ld_out + n] = y;
-        } else if (e.kind == EPI_STORE_ACT) {
-          store_act<AT>(e.out, row * e.ld_out + n, y);
-        } else if (e.kind == EPI_RESID) {
-          e.resid[row * e.ld_resid + n] += y;
-        } else {
-          store_act<AT>(e.out, row * e.ld_out + n, gelu_tanh_clamped(y));
+        const float y = tile[m * ldt + c] + s_bias[c];
+        const size_t o = (size_t)(m0 + m) * e.ld_out + n;
+        if (e.kind == EPI_STORE_F32) reinterpret_cast<float*>(e.out)[o] = y;
+        else if (e.kind == EPI_STORE_ACT) store_act<AT>(e.out, o, y);
+        else store_act<AT>(e.out, o, gelu_tanh_clamped(y));
+      }
+      break;
+    }
+    case EPI_RESID: {
+      // residual read-modify-write: issue a batch of loads, then the stores
+      constexpr int RB = 8;
+      const int total = mrows * ncols;
+      for (int i0 = 0; i0 < total; i0 += RB * nth) {
+        float hv[RB];
+        size_t ad[RB];
+        bool ok[RB];
+#pragma unroll
+        for (int j = 0; j < RB; ++j) {
+          const int i = i0 + j * nth + tid;
+          const int m = i / ncols, c = i - m * ncols;
+          ok[j] = i < total && n0 + c < N;
+          ad[j] = (size_t)(m0 + m) * e.ld_resid + n0 + c;
+          hv[j] = ok[j] ? e.resid[ad[j]] : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < RB; ++j) {
+          const int i = i0 + j * nth + tid;
+          const int m = i / ncols, c = i - m * ncols;
+          if (ok[j]) e.resid[ad[j]] = hv[j] + tile[m * ldt + c] + s_bias[c];
         }
       }
       break;
@@ -69,31 +132,28 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
       for (int i = tid; i < mrows * 32; i += nth) {
         const int m = i >> 5, c = i & 31, j = n0 + c;
         if (j >= N) continue;
-        const float g = tile[m * ldt + c] + bias_at<WT>(e.bias, j);
-        const float u = tile[m * ldt + 32 + c] + bias_at<WT>(e.bias, N + j);
+        const float g = tile[m * ldt + c] + s_bias[c];
+        const float u = tile[m * ldt + 32 + c] + s_bias[32 + c];
         store_act<AT>(e.out, (size_t)(m0 + m) * e.ld_out + j, silu_f(g) * u);
       }
       break;
     }
     case EPI_QKV: {
-      const StepArgs* a = e.args;
       const int H = e.n_heads, Hkv = e.kv.n_kv_heads;
-      // one thread per (row, head-column-pair) when rotating, per element otherwise
-      const int per_row = ncols;
-      for (int i = tid; i < mrows * per_row; i += nth) {
-        const int m = i / per_row, c = i - m * per_row, n = n0 + c;
+      for (int i = tid; i < mrows * ncols; i += nth) {
+        const int m = i / ncols, c = i - m * ncols, n = n0 + c;
         if (n >= N) continue;
         const int hh = n / HD, d = n - hh * HD;
         const int row = m0 + m;
-        const int pos = a->positions[row];
+        const int pos = s_pos[m];
         const bool is_q = hh < H, is_k = !is_q && hh < H + Hkv;
-        float v0 = tile[m * ldt + c] + bias_at<WT>(e.bias, n);
+        float v0 = tile[m * ldt + c] + s_bias[c];
         float v1 = 0.0f;
         if (e.rope && (is_q || is_k)) {
           if (d >= HD / 2) continue;                  // the partner thread writes this element
-          v1 = tile[m * ldt + c + HD / 2] + bias_at<WT>(e.bias, n + HD / 2);
+          v1 = tile[m * ldt + c + HD / 2] + s_bias[c + HD / 2];
           float s, co;
-          rope_sincos(pos, d, e.rope_theta, &s, &co);
+          rope_sincos(pos, e.rope_tab[d], &s, &co);
           const float r0 = v0 * co - v1 * s;
           const float r1 = v1 * co + v0 * s;
           v0 = r0;
@@ -105,8 +165,7 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
           if (e.rope) q[d + HD / 2] = v1;
           continue;
         }
-        const int seq = a->row_seq ? a->row_seq[row] : row;
-        const int pb = kv_block(e.kv, a->block_tables, seq, pos, e.flags);
+        const int pb = s_blk[m];
         if (pb < 0) continue;
         const int g = is_k ? hh - H : hh - H - Hkv;
         WT* dst = reinterpret_cast<WT*>(is_k ? e.kv.k : e.kv.v) + kv_offset(e.kv, pb, g, pos & (KVB - 1));
@@ -127,6 +186,7 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
       // per-row argmax over this tile's columns: one warp per row
       const int warp = tid >> 5, lane = tid & 31, nwarps = nth >> 5;
       const int tile_n = n0 / ncols;
+      const int B = a->B;
       for (int m = warp; m < mrows; m += nwarps) {
         float best = -INFINITY;
         int bi = 0x7fffffff;
@@ -143,7 +203,7 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
           if (argmax_better(ov, oi, best, bi)) { best = ov; bi = oi; }
         }
         if (lane == 0) {
-          const size_t slot = (size_t)tile_n * a->B + (m0 + m);
+          const size_t slot = (size_t)tile_n * B + (m0 + m);
           e.part_val[slot] = best;
           e.part_idx[slot] = bi;
         }

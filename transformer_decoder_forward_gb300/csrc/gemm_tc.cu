@@ -15,10 +15,9 @@
 //     an fp32 tile in shared memory and run the shared epilogue per 64-column
 //     sub-tile (bias, GELU / SwiGLU, RoPE + kv_write, residual add).
 // Every wait is bounded (FLAG_WAIT_TIMEOUT) and the tensor memory is always freed.
-#include <cuda.h>
-
 #include "epilogue.cuh"
 #include "linear.cuh"
+#include "tcgen05.cuh"
 
 namespace llm {
 
@@ -30,66 +29,6 @@ constexpr int A_STAGE = TC_BM * TC_BK * 2;   // bytes
 constexpr int B_STAGE = TC_BN * TC_BK * 2;
 constexpr int OT_LD = TC_BN + 1;
 constexpr size_t TC_SMEM = 1024 + (size_t)TC_STAGES * (A_STAGE + B_STAGE) + 256;
-
-// ---- tcgen05 / TMA wrappers -------------------------------------------------------------------
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, rows of 64 bf16 (128 bytes) written by
-// TMA with the 128-byte swizzle, 8-row groups 1024 bytes apart (stride byte offset).
-__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
-  const uint32_t a = smem_u32(p);
-  uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);
-  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
-  d |= (uint64_t)1 << 46;              // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;              // swizzle: 128B
-  return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32, A/B bf16, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
 
 template <typename AT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -198,41 +137,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 }
 
-// ---- host side -------------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-    else
-      cudaGetLastError();
-  }
-  return fn;
-}
-
-// 2-D bf16 tensor map over a row-major [rows][cols] matrix with row stride ld (elements);
-// box = 64 columns x box_rows rows, 128-byte swizzle, out-of-bounds reads fill zero.
-bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {
-  EncodeTiledFn f = encode_fn();
-  if (!f) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool gemm_tc_supported(const LinearParams& p) {
@@ -247,8 +151,8 @@ cudaError_t launch_gemm_tc(const LinearParams& p, int /*num_sms*/, cudaStream_t 
   if (!gemm_tc_supported(p)) return cudaErrorNotSupported;
   CUtensorMap ma, mb;
   const int wrows = p.swiglu ? 2 * p.N : p.N;
-  if (!make_map(&ma, p.X, p.M, p.K, p.ldx, TC_BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, p.W, wrows, p.K, p.K, p.swiglu ? 32 : TC_BN)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, p.X, DT_BF16, p.M, p.K, p.ldx, TC_BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, p.W, DT_BF16, wrows, p.K, p.K, p.swiglu ? 32 : TC_BN)) return cudaErrorInvalidValue;
   const int tiles_n = p.swiglu ? (p.N + 63) / 64 : (p.N + TC_BN - 1) / TC_BN;
   const int tiles_m = (p.M + TC_BM - 1) / TC_BM;
   auto kern = p.adt == DT_BF16 ? k_gemm_tc<bf16> : k_gemm_tc<float>;

@@ -1,0 +1,388 @@
+// Decode projection on tensor cores, weights on the MMA's M side ("swap-AB").
+//
+// A decode step multiplies a few rows of activations by every weight matrix, so it
+// streams all weights once per step and is memory bound ("rvllm-metal", section
+// "The matmul pain story"). The pages' answer is a simdgroup GEMV for 1-4 rows and
+// a K-split small-tile kernel for 5-16 rows. On sm_103a this kernel puts 128 weight
+// rows on the tcgen05 M side and the step's tokens on the N side (N = rows rounded
+// up to 16, at most 256):
+//   - warp 0, one lane: TMA producer. Before waiting on the previous kernel
+//     (programmatic dependent launch) it already issues the weight tiles of the
+//     first stages: weights never depend on earlier kernels.
+//   - warp 1, one lane: issues tcgen05.mma into a 128 x N fp32 TMEM accumulator.
+//   - warps 2-5: for fp32 models they split each staged operand tile into tf32
+//     high and low parts in a separate buffer and release the TMA stage at once,
+//     so the weight stream runs ahead of the conversion; the MMA sums
+//     W_hi.X_hi + W_hi.X_lo + W_lo.X_hi (three tf32 products, fp32-level accuracy).
+//     After the last MMA they read the accumulator with tcgen05.ld and stage it
+//     transposed (tokens x weight rows) for the shared epilogue.
+// Small matrices split K across a thread-block cluster; partial tiles are summed in
+// rank order through distributed shared memory. The split and the stage count
+// depend on the weight shape only. Every wait is bounded and TMEM is always freed.
+#include <cooperative_groups.h>
+
+#include <algorithm>
+#include <type_traits>
+
+#include "epilogue.cuh"
+#include "linear.cuh"
+#include "tcgen05.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace llm {
+
+namespace {
+
+constexpr int SW_THREADS = 192;
+constexpr int SW_ROWS = 128;                 // weight rows per tile (MMA M)
+constexpr int SW_A_BYTES = SW_ROWS * 128;    // one 128-byte K slice of 128 weight rows
+constexpr int SW_OT_LD = SW_ROWS + 1;
+constexpr int SW_MAX_KS = 8;                 // cluster size limit (portable)
+
+template <int NT, bool TF32>
+struct SwapCfg {
+  static constexpr int B_BYTES = NT * 128;
+  static constexpr int RAW = SW_A_BYTES + B_BYTES;      // one TMA stage: [W slice][X slice]
+  static constexpr int CONVB = 2 * RAW;                 // tf32: [W hi][X hi][W lo][X lo]
+  // TMA stages: bf16 keeps up to 4 within ~100 KB (a second CTA fits on the SM); tf32 keeps
+  // 4 raw stages plus 2 converted buffers (2 + 1 for the widest tiles).
+  static constexpr int NRAW = TF32 ? (NT <= 64 ? 4 : 2)
+                                   : (4 * RAW <= 100 * 1024 ? 4 : (3 * RAW <= 100 * 1024 ? 3 : 2));
+  static constexpr int NCONV = TF32 ? (NT <= 64 ? 2 : 1) : 0;
+  static constexpr size_t PIPE = (size_t)NRAW * RAW + (size_t)NCONV * CONVB;
+  static constexpr size_t OT = (size_t)NT * SW_OT_LD * 4;
+  static constexpr size_t RED = (size_t)((NT + 1) / 2) * SW_OT_LD * 4;   // ks >= 2: a rank reduces <= NT/2 rows
+  static constexpr size_t BODY = PIPE > OT + RED ? PIPE : OT + RED;
+  static constexpr size_t SMEM = 1024 + BODY + 256;
+  static constexpr int KE = TF32 ? 32 : 64;            // K elements per stage (128 bytes)
+  static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
+};
+
+// tf32 high part: the fp32 value rounded to 10 mantissa bits (to nearest, ties away, by an
+// integer add on the bit pattern) with its 13 low bits cleared, so it is exactly
+// representable in tf32 and the tensor core uses it unchanged; the low part x - hi is exact
+// in fp32 and at most 2^-11 |x|.
+__device__ __forceinline__ float hi13(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+__device__ __forceinline__ float4 tf32_hi(const float4& x) {
+  return make_float4(hi13(x.x), hi13(x.y), hi13(x.z), hi13(x.w));
+}
+
+template <typename AT, int NT, bool TF32>
+__global__ void __launch_bounds__(SW_THREADS, 1)
+    k_gemm_tc_swap(const LinearParams p, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmX, int kcta, int ks_total) {
+  using C = SwapCfg<NT, TF32>;
+  using WT = typename std::conditional<TF32, float, bf16>::type;   // weight / activation / KV type
+  constexpr int NR = C::NRAW, NC = C::NCONV > 0 ? C::NCONV : 1;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + C::BODY);   // TMA -> consumer, per raw stage
+  uint64_t* rfree = full + NR;                                      // consumer -> TMA, per raw stage
+  uint64_t* conv = rfree + NR;                                      // tf32: converter -> MMA
+  uint64_t* cfree = conv + NC;                                      // tf32: MMA -> converter
+  uint64_t* done = cfree + NC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  auto raw_a = [&](int r) { return base + (size_t)r * C::RAW; };
+  auto raw_b = [&](int r) { return base + (size_t)r * C::RAW + SW_A_BYTES; };
+  auto cv = [&](int c) { return base + (size_t)NR * C::RAW + (size_t)c * C::CONVB; };   // [A hi][B hi][A lo][B lo]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x, ks = blockIdx.y;
+  const int k0 = ks * kcta;
+  const int kend = min(p.K, k0 + kcta);
+  const int kiters = (kend - k0 + C::KE - 1) / C::KE;
+  const int F = p.N, M = p.M;
+  unsigned* flags = p.epi.flags;
+
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    for (int r = 0; r < NR; ++r) {
+      mbar_init(&full[r], 1);
+      mbar_init(&rfree[r], TF32 ? 4 : 1);
+    }
+    for (int c = 0; c < NC; ++c) {
+      mbar_init(&conv[c], 4);
+      mbar_init(&cfree[c], 1);
+    }
+    mbar_init(done, 1);
+    mbar_fence_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    auto load_w = [&](int r, int kc) {
+      unsigned char* a = raw_a(r);
+      if (p.swiglu) {
+        for (int sub = 0; sub < 2; ++sub) {
+          const int j0 = (tile * 2 + sub) * 32;
+          tma_load_2d(a + (sub * 64) * 128, &tmW, kc, j0, &full[r]);
+          tma_load_2d(a + (sub * 64 + 32) * 128, &tmW, kc, F + j0, &full[r]);
+        }
+      } else {
+        tma_load_2d(a, &tmW, kc, tile * SW_ROWS, &full[r]);
+      }
+    };
+    const int pre = min(NR, kiters);
+    for (int i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(&full[i], C::RAW);
+      load_w(i, k0 + i * C::KE);
+    }
+    pdl_wait();
+    for (int i = 0; i < pre; ++i) tma_load_2d(raw_b(i), &tmX, k0 + i * C::KE, 0, &full[i]);
+    for (int i = pre; i < kiters; ++i) {
+      const int r = i % NR;
+      if (!mbar_wait(&rfree[r], ((i / NR) - 1) & 1, flags)) break;
+      mbar_arrive_expect_tx(&full[r], C::RAW);
+      load_w(r, k0 + i * C::KE);
+      tma_load_2d(raw_b(r), &tmX, k0 + i * C::KE, 0, &full[r]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    pdl_wait();
+    constexpr uint32_t idesc = TF32 ? idesc_tf32(SW_ROWS, NT) : idesc_bf16(SW_ROWS, NT);
+    for (int i = 0; i < kiters; ++i) {
+      if constexpr (TF32) {
+        const int c = i % NC;
+        if (!mbar_wait(&conv[c], (i / NC) & 1, flags)) break;
+        tc_fence_after();
+        unsigned char* b = cv(c);
+        const uint64_t da = sw128_desc(b), db = sw128_desc(b + SW_A_BYTES);
+        const uint64_t dal = sw128_desc(b + C::RAW), dbl = sw128_desc(b + C::RAW + SW_A_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {   // 32 bytes of K per MMA
+          const uint64_t o = (uint64_t)(kk * 2);
+          tc_mma_tf32(tmem, da + o, db + o, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_tf32(tmem, da + o, dbl + o, idesc, 1u);
+          tc_mma_tf32(tmem, dal + o, db + o, idesc, 1u);
+        }
+        tc_commit(&cfree[c]);
+      } else {
+        const int r = i % NR;
+        if (!mbar_wait(&full[r], (i / NR) & 1, flags)) break;
+        tc_fence_after();
+        const uint64_t da = sw128_desc(raw_a(r)), db = sw128_desc(raw_b(r));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t o = (uint64_t)(kk * 2);
+          tc_mma(tmem, da + o, db + o, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&rfree[r]);
+      }
+    }
+    tc_commit(done);
+  } else if (warp >= 2) {
+    pdl_wait();
+    if constexpr (TF32) {
+      // ---- tf32 split: raw stage r -> converted buffer c, then release r to the producer
+      const int t = threadIdx.x - 64;   // 0..127
+      for (int i = 0; i < kiters; ++i) {
+        const int r = i % NR, c = i % NC;
+        if (!mbar_wait(&full[r], (i / NR) & 1, flags)) break;
+        if (i >= NC && !mbar_wait(&cfree[c], ((i / NC) - 1) & 1, flags)) break;
+        const float4* src = reinterpret_cast<const float4*>(raw_a(r));   // [W][X] contiguous
+        float4* hi = reinterpret_cast<float4*>(cv(c));
+        float4* lo = reinterpret_cast<float4*>(cv(c) + C::RAW);
+#pragma unroll 4
+        for (int j = t; j < C::RAW / 16; j += 128) {
+          const float4 x = src[j];
+          const float4 h = tf32_hi(x);
+          hi[j] = h;
+          lo[j] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&conv[c]);
+          mbar_arrive(&rfree[r]);
+        }
+      }
+    }
+  }
+
+  pdl_wait();   // every thread writes outputs in the epilogue: all of them pass the dependency wait
+  // ---- accumulator -> shared memory, transposed to [token][weight row]
+  bool ok = true;
+  float* ot = reinterpret_cast<float*>(base);
+  if (warp >= 2) {
+    ok = mbar_wait(done, 0, flags);
+    if (!ok) ok = mbar_wait(done, 0, flags);
+    tc_fence_after();
+    __syncwarp();
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    const int row = q * 32 + lane;          // weight row inside the tile
+    if (ok) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < NT; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < NT) ot[(c0 + j) * SW_OT_LD + row] = __uint_as_float(r[j]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  pdl_trigger();
+  ok = __syncthreads_and(warp < 2 ? 1 : (ok ? 1 : 0)) != 0;
+  if (!ok) {
+    if (ks_total > 1) {   // keep the cluster barriers matched
+      cg::this_cluster().sync();
+      cg::this_cluster().sync();
+    }
+    return;
+  }
+
+  auto epilogue = [&](const float* tl, int r0, int nrows) {
+#pragma unroll 1
+    for (int sub = 0; sub < SW_ROWS / 64; ++sub) {
+      const int n0 = p.swiglu ? (tile * 2 + sub) * 32 : tile * SW_ROWS + sub * 64;
+      if (!p.swiglu && n0 >= p.N) break;
+      run_epilogue<WT, AT>(p.epi, tl + sub * 64, SW_OT_LD, r0, nrows, n0, 64, p.N);
+    }
+  };
+  if (ks_total == 1) {
+    epilogue(ot, 0, M);
+    return;
+  }
+  // ---- split-K: rank r sums rows [r*rp, (r+1)*rp) of all ranks' partial tiles, in rank order
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int rank = (int)cluster.block_rank();
+  const int rp = (M + ks_total - 1) / ks_total;
+  const int r0 = min(M, rank * rp), r1 = min(M, r0 + rp);
+  float* red = ot + (size_t)NT * SW_OT_LD;
+  const float* src[SW_MAX_KS];
+#pragma unroll
+  for (int j = 0; j < SW_MAX_KS; ++j) src[j] = cluster.map_shared_rank(ot, j < ks_total ? j : 0);
+  for (int i = threadIdx.x; i < (r1 - r0) * SW_ROWS; i += SW_THREADS) {
+    const int m = r0 + i / SW_ROWS, c = i % SW_ROWS;
+    float v[SW_MAX_KS];
+#pragma unroll
+    for (int j = 0; j < SW_MAX_KS; ++j) v[j] = j < ks_total ? src[j][m * SW_OT_LD + c] : 0.0f;
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < SW_MAX_KS; ++j) s += v[j];
+    red[(m - r0) * SW_OT_LD + c] = s;
+  }
+  cluster.sync();
+  __syncthreads();
+  if (r1 > r0) epilogue(red, r0, r1 - r0);
+}
+
+template <typename AT, int NT, bool TF32>
+cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
+  using C = SwapCfg<NT, TF32>;
+  const int tiles = p.swiglu ? (p.N + 63) / 64 : (p.N + SW_ROWS - 1) / SW_ROWS;
+  const int wrows = p.swiglu ? 2 * p.N : p.N;
+  // K split from the weight shape only (never from M): the largest cluster size <= 8 whose
+  // grid still runs as one wave (the cluster occupancy the driver reports for this kernel),
+  // with at least two K stages per CTA.
+  auto kern = k_gemm_tc_swap<AT, NT, TF32>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  static int capacity[SW_MAX_KS + 1] = {0};   // CTAs of one wave per cluster size
+  auto wave = [&](int c) {
+    if (!capacity[c]) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(1, c);
+      q.blockDim = dim3(SW_THREADS);
+      q.dynamicSmemBytes = C::SMEM;
+      cudaLaunchAttribute a[1];
+      a[0].id = cudaLaunchAttributeClusterDimension;
+      a[0].val.clusterDim.x = 1;
+      a[0].val.clusterDim.y = c;
+      a[0].val.clusterDim.z = 1;
+      q.attrs = a;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = num_sms / c;
+      }
+      capacity[c] = n * c;
+    }
+    return capacity[c];
+  };
+  int ks = 1;
+  while (ks < SW_MAX_KS && tiles * ks * 2 <= wave(ks * 2) && p.K / (ks * 2) >= 2 * C::KE) ks *= 2;
+  int kcta = (p.K + ks - 1) / ks;
+  kcta = ((kcta + C::KE - 1) / C::KE) * C::KE;
+  ks = (p.K + kcta - 1) / kcta;
+  const int dt = TF32 ? DT_F32 : DT_BF16;
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, p.W, dt, wrows, p.K, p.K, p.swiglu ? 32 : SW_ROWS)) return cudaErrorInvalidValue;
+  if (!make_map(&mx, p.X, dt, p.M, p.K, p.ldx, NT)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles, ks);
+  cfg.blockDim = dim3(SW_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (ks > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = ks;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, p, mw, mx, kcta, ks);
+}
+
+template <typename AT, bool TF32>
+cudaError_t launch_at(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
+  if (p.M <= 16) return launch_nt<AT, 16, TF32>(p, num_sms, s, pdl);
+  if (p.M <= 32) return launch_nt<AT, 32, TF32>(p, num_sms, s, pdl);
+  if (p.M <= 64) return launch_nt<AT, 64, TF32>(p, num_sms, s, pdl);
+  if (p.M <= 128) return launch_nt<AT, 128, TF32>(p, num_sms, s, pdl);
+  return launch_nt<AT, 256, TF32>(p, num_sms, s, pdl);
+}
+
+}  // namespace
+
+bool gemm_tc_swap_supported(const LinearParams& p) {
+  if (p.M <= 0 || p.M > 256 || p.wdt != p.xdt || p.xnorm) return false;
+  if (p.K % 8 != 0 || p.ldx % 8 != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(p.W) | reinterpret_cast<uintptr_t>(p.X)) & 15) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_tc_swap(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
+  if (!gemm_tc_swap_supported(p)) return cudaErrorNotSupported;
+  const bool tf32 = p.wdt == DT_F32;
+  if (p.adt == DT_BF16)
+    return tf32 ? launch_at<bf16, true>(p, num_sms, s, pdl) : launch_at<bf16, false>(p, num_sms, s, pdl);
+  return tf32 ? launch_at<float, true>(p, num_sms, s, pdl) : launch_at<float, false>(p, num_sms, s, pdl);
+}
+
+}  // namespace llm

@@ -14,11 +14,7 @@ struct LinearParams {
   int wdt, xdt, adt;    // weight / input / activation-output dtypes
   int swiglu;           // 1: tile t reads gate rows t*32.. and up rows F + t*32..
   Epilogue epi;
-  // split-K workspace for the GEMV path
-  float* part;          // fp32 partial sums
-  size_t part_elems;
-  unsigned* counters;   // per-tile arrival tickets (all zero between launches)
-  int counters_len;
+  int xnorm;            // reserved: 0 (X is read as is)
 };
 
 inline int linear_tiles(const LinearParams& p) {
@@ -26,12 +22,18 @@ inline int linear_tiles(const LinearParams& p) {
 }
 
 // Variants. AUTO picks by M; the others force one kernel (tests sweep all of them).
-enum : int { LIN_AUTO = 0, LIN_GEMV = 1, LIN_SIMT = 2, LIN_TC = 3 };
+//   LIN_GEMV     CUDA-core weight-stream GEMV (decode)
+//   LIN_SIMT     CUDA-core tiled GEMM
+//   LIN_TC       tcgen05 GEMM, activations on the MMA's M side (prefill, bf16)
+//   LIN_TC_SWAP  tcgen05 GEMM, weights on the MMA's M side (decode, M <= 256; bf16, or fp32 as 3 x tf32)
+enum : int { LIN_AUTO = 0, LIN_GEMV = 1, LIN_SIMT = 2, LIN_TC = 3, LIN_TC_SWAP = 4 };
 
 // Each returns cudaSuccess or the launch error; `name` receives the kernel family name.
 cudaError_t launch_gemv(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
 cudaError_t launch_gemm_simt(const LinearParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_gemm_tc(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
 bool gemm_tc_supported(const LinearParams& p);
+cudaError_t launch_gemm_tc_swap(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
+bool gemm_tc_swap_supported(const LinearParams& p);
 
 }  // namespace llm

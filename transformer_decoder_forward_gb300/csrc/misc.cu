@@ -72,18 +72,24 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
   const WT* gw = reinterpret_cast<const WT*>(p.g);
   const WT* bw = reinterpret_cast<const WT*>(p.b);
   AT* out = reinterpret_cast<AT*>(p.out) + (size_t)r * p.d;
+  // gains / biases of this lane's columns: all loads issued before any store
+  float gv[NORM_NV][4], bv[NORM_NV][4];
+#pragma unroll
+  for (int j = 0; j < NORM_NV; ++j) {
+    const int i = lane + 32 * j;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      gv[j][t] = i < d4 ? to_f32(gw[4 * i + t]) : 0.0f;
+      bv[j][t] = (i < d4 && bw) ? to_f32(bw[4 * i + t]) : 0.0f;
+    }
+  }
 #pragma unroll
   for (int j = 0; j < NORM_NV; ++j) {
     const int i = lane + 32 * j;
     if (i >= d4) continue;
     const float xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int c = 4 * i + t;
-      float y = (xv[t] - mean) * scale * to_f32(gw[c]);
-      if (bw) y += to_f32(bw[c]);
-      out[c] = from_f32<AT>(y);
-    }
+    for (int t = 0; t < 4; ++t) out[4 * i + t] = from_f32<AT>((xv[t] - mean) * scale * gv[j][t] + bv[j][t]);
   }
 }
 
