@@ -56,8 +56,9 @@ def weight_bytes(s: wl.ModelShape) -> int:
 
 
 def gemv_bytes(s: wl.ModelShape, B: int) -> int:
-    """Projection kernels: weights once, plus activations in (fp32/bf16) and outputs out."""
-    a = s.elt_bytes
+    """Projection kernels: weights once, plus activations in and outputs out (4 bytes a value:
+    fp32, or a bf16 pair for bf16 weights)."""
+    a = 4
     d, F, qkv, hq = s.d_model, s.d_ff, s.qkv_dim, s.n_heads * s.head_dim
     per_layer = B * (d * a + qkv * 4)             # qkv: x in, q (fp32) / k,v out
     per_layer += B * (hq * a + 2 * d * 4)         # o: x in, residual read+write
@@ -68,8 +69,8 @@ def gemv_bytes(s: wl.ModelShape, B: int) -> int:
 
 def attn_bytes(s: wl.ModelShape, ctx: np.ndarray) -> int:
     """Decode attention: K and V of every cached position (incl. the new one) once per layer."""
-    kv = int(ctx.sum()) * s.n_kv_heads * s.head_dim * s.elt_bytes * 2 * s.n_layers
-    qo = len(ctx) * s.n_heads * s.head_dim * (4 + s.elt_bytes) * s.n_layers
+    kv = int(ctx.sum()) * s.n_kv_heads * s.head_dim * 4 * 2 * s.n_layers   # fp32 cache
+    qo = len(ctx) * s.n_heads * s.head_dim * (4 + 4) * s.n_layers
     return kv + qo
 
 
@@ -359,7 +360,10 @@ def run_decode_bench(args, W):
             "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
             "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]),
                        "decode_positions": f"{int(run.lengths.min())}..{int(run.lengths.max()) + period - 1} cycled",
-                       "kv": "contiguous" if W.contiguous_kv else "paged16",
+                       "kv": ("contiguous" if W.contiguous_kv else "paged16") + " fp32",
+                       "precision": ("fp32 weights" if s.dtype == wl.DTYPE_F32 else "bf16 weights")
+                       + ", fp32 KV cache and residual, fp32 accumulation"
+                       + ("" if s.dtype == wl.DTYPE_F32 else ", activations as bf16 (hi, lo) pairs"),
                        "l2": "inputs larger than L2: %.0f MB weights + %.0f MB KV per step" % (
                            weight_bytes(s) / 1e6, attn_bytes(s, ctx_steps[-1]) / 1e6),
                        "graph": "one CUDA graph per step"},

@@ -15,6 +15,14 @@
  * through a per-sequence block table ("rvllm-metal", "What the kernels do":
  * kv_write into the paged cache, division and modulo of the position).
  *
+ * Precision: only the weights take config.dtype. The residual stream, the KV cache
+ * and the logits are fp32 (the weights alone are half precision in "rvllm-metal",
+ * section "The matmul pain story"; its KV cache is F32, section "What's basic about
+ * it"); with bf16 weights the activations fed to a projection are kept as bf16
+ * (hi, lo) pairs, about 2^-17 relative, so the tensor cores take two bf16 products
+ * per step instead of rounding the activations to bf16. All arithmetic accumulates
+ * in fp32.
+ *
  * Conventions for every call:
  *   - Pointer arguments are DEVICE pointers unless the argument says HOST.
  *   - The caller owns weights, inputs and outputs; the library never frees them
@@ -64,7 +72,7 @@ enum { LLM_DTYPE_F32 = 0, LLM_DTYPE_BF16 = 1 };
 
 typedef struct {
   int arch;               /* LLM_ARCH_GPT2 or LLM_ARCH_LLAMA */
-  int dtype;              /* LLM_DTYPE_F32 or LLM_DTYPE_BF16: weights, KV cache and GEMM operands */
+  int dtype;              /* LLM_DTYPE_F32 or LLM_DTYPE_BF16: element type of the weights */
   int n_layers;
   int d_model;
   int n_heads;            /* query heads */
@@ -124,7 +132,7 @@ typedef struct llm_handle llm_handle;
 
 /* Validate the config, check the device (compute capability 10.3), copy the
  * per-layer pointer arrays, allocate the KV pool
- * (2 * n_layers * num_kv_blocks * n_kv_heads * 16 * head_dim elements of dtype,
+ * (2 * n_layers * num_kv_blocks * n_kv_heads * 16 * head_dim fp32 values,
  * laid out [layer][block][kv_head][16][head_dim], K and V in separate pools)
  * and the workspace. cuda_stream is a cudaStream_t (NULL = the legacy default
  * stream, which disables CUDA-graph replay). Errors: INVALID_ARG, UNSUPPORTED,
@@ -199,8 +207,11 @@ llm_status llm_set_linear_variant(llm_handle* h, int variant);
 
 /* Test and diagnostic entry point (no handle): one projection with a chosen kernel,
  *   y[m][n] = sum_k x[m][k] * w[n][k] (+ bias[n]),  m < M, n < N,
- * x DEVICE [M][K] and w DEVICE [N][K] row-major in `dtype` (LLM_DTYPE_F32 or
- * LLM_DTYPE_BF16), bias DEVICE [N] in `dtype` or NULL, y DEVICE float [M][N].
+ * w DEVICE [N][K] row-major in `dtype` (LLM_DTYPE_F32 or LLM_DTYPE_BF16), bias DEVICE
+ * [N] in `dtype` or NULL, y DEVICE float [M][N]. x DEVICE in the library's activation
+ * storage for that dtype: fp32 [M][K] for LLM_DTYPE_F32; for LLM_DTYPE_BF16 a bf16
+ * [M][2K] array whose row m holds hi[0..K) then lo[0..K), x[m][k] = hi[k] + lo[k]
+ * (the library keeps the activations of bf16-weight models as such pairs).
  * variant: 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM (bf16 only),
  * 4 tcgen05 GEMM with the weights on the MMA's M side (M <= 256; bf16, or fp32 as
  * three tf32 products). Variants 3 and 4 need K % 8 == 0. Enqueued on `cuda_stream`.

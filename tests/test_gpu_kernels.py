@@ -17,8 +17,18 @@ def _inputs(M, N, K, bf16, seed):
     w = (r.standard_normal((N, K), dtype=np.float32) * np.float32(0.05))
     b = r.standard_normal(N, dtype=np.float32) * np.float32(0.1)
     if bf16:
-        x, w, b = (wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(a)) for a in (x, w, b))
+        w, b = (wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(a)) for a in (w, b))
     return x, w, b
+
+
+def bf16_pair(x):
+    """The library's activation storage for bf16 weights: row m = bf16 hi[0..K) then lo[0..K),
+    hi = bf16(x), lo = bf16(x - hi). Returns (uint16 bits [M, 2K], the represented values hi + lo)."""
+    hi_bits = wl.f32_to_bf16_bits(x)
+    hi = wl.bf16_bits_to_f32(hi_bits)
+    lo_bits = wl.f32_to_bf16_bits((x - hi).astype(np.float32))
+    val = hi.astype(np.float64) + wl.bf16_bits_to_f32(lo_bits).astype(np.float64)
+    return np.concatenate([hi_bits, lo_bits], axis=1), val
 
 
 @pytest.mark.parametrize("variant", [1, 2, 3, 4], ids=["gemv", "simt", "tcgen05", "tcgen05-swap"])
@@ -34,16 +44,22 @@ def test_linear_kernel_matches_oracle(gpu_lib, variant, bf16, M, N, K):
         pytest.skip("weights-on-M path serves at most 256 rows")
     x, w, b = _inputs(M, N, K, bf16, seed=M * 7 + N + K)
     dt = torch.bfloat16 if bf16 else torch.float32
-    tx, tw, tb = (torch.from_numpy(a).cuda().to(dt) for a in (x, w, b))
+    tw, tb = (torch.from_numpy(a).cuda().to(dt) for a in (w, b))
+    if bf16:
+        bits, xv = bf16_pair(x)
+        tx = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    else:
+        xv = x.astype(np.float64)
+        tx = torch.from_numpy(x).cuda()
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     gpu_lib.op_linear(tx, tw, tb, y, variant)
     torch.cuda.synchronize()
-    ref = OracleModel.linear(x.astype(np.float64), w.astype(np.float64), b.astype(np.float64))
+    ref = OracleModel.linear(xv, w.astype(np.float64), b.astype(np.float64))
     got = y.cpu().numpy()
     # fp32 accumulation over K terms of size |x||w|: bound by K * 2^-23 * sum|x w| (+ margin).
     # The fp32 tensor-core path sums three tf32 products; the dropped low*low term and the
     # tf32 rounding of the low parts add about 2^-20 relative per product.
-    scale = np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T + np.abs(b)
+    scale = np.abs(xv) @ np.abs(w.astype(np.float64)).T + np.abs(b)
     tol = 1e-6 + 4 * K * 2.0 ** -23 * scale + (2.0 ** -19 * scale if (variant == 4 and not bf16) else 0)
     assert np.all(np.isfinite(got))
     assert np.all(np.abs(got - ref) <= tol), float(np.abs(got - ref).max())

@@ -107,12 +107,16 @@ def _ptr(t) -> Optional[int]:
 def op_linear(x, w, bias, y, variant: int, stream=None) -> None:
     """y = x . w^T (+ bias) with one chosen projection kernel (tests / diagnostics).
 
-    x [M, K], w [N, K] (both float32 or both bfloat16 CUDA tensors), bias [N] or None, y float32 [M, N]."""
+    w [N, K] float32 or bfloat16, bias [N] (w's dtype) or None, y float32 [M, N]. x is the
+    library's activation storage for w's dtype: float32 [M, K], or for bfloat16 weights a
+    bfloat16 [M, 2K] tensor whose row holds hi[0..K) then lo[0..K) (x = hi + lo)."""
     import torch
     lib = load()
     dtype = 1 if w.dtype == torch.bfloat16 else 0
-    M, K = x.shape
-    N = w.shape[0]
+    N, K = w.shape
+    M = x.shape[0]
+    if x.dtype != w.dtype or x.shape[1] != (2 * K if dtype == 1 else K):
+        raise ValueError("x must be float32 [M, K] for float32 weights, bfloat16 [M, 2K] for bfloat16 weights")
     s = stream if stream is not None else torch.cuda.current_stream()
     _check(lib.llm_op_linear(dtype, M, N, K, _ptr(x), _ptr(w), _ptr(bias), _ptr(y), int(variant),
                              ctypes.c_void_p(s.cuda_stream)))

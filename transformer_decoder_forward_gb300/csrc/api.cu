@@ -72,11 +72,12 @@ struct llm_handle {
   llm_config cfg{};
   int dev = 0, num_sms = 0;
   cudaStream_t stream = nullptr;
-  int wdt = DT_F32, adt = DT_F32;
-  size_t welt = 4;
+  int wdt = DT_F32;   // weights
+  int adt = DT_F32;   // activations between kernels: DT_F32, or DT_SPLIT (bf16 pairs) for bf16 weights
+  int act_mul = 1;    // row stride of an activation matrix in storage elements = act_mul * width
   const void *tok_emb = nullptr, *pos_emb = nullptr, *lnf_w = nullptr, *lnf_b = nullptr;
   std::vector<LayerW> layers;
-  // KV pool
+  // KV pool (fp32)
   void* k_pool = nullptr;
   void* v_pool = nullptr;
   size_t layer_kv_elems = 0;
@@ -212,8 +213,8 @@ llm_status linear(llm_handle* h, const char* tag, LinearParams p) {
 
 KVLayer kv_layer(const llm_handle* h, int l) {
   KVLayer kv;
-  kv.k = static_cast<char*>(h->k_pool) + (size_t)l * h->layer_kv_elems * h->welt;
-  kv.v = static_cast<char*>(h->v_pool) + (size_t)l * h->layer_kv_elems * h->welt;
+  kv.k = static_cast<float*>(h->k_pool) + (size_t)l * h->layer_kv_elems;
+  kv.v = static_cast<float*>(h->v_pool) + (size_t)l * h->layer_kv_elems;
   kv.num_blocks = h->num_blocks;
   kv.n_kv_heads = h->cfg.n_kv_heads;
   kv.mbps = h->cfg.max_blocks_per_seq;
@@ -230,7 +231,7 @@ Epilogue base_epi(const llm_handle* h) {
   return e;
 }
 
-// y = Norm(h) . W^T: the norm kernel writes xn (activation dtype), then the projection.
+// y = Norm(h) . W^T: the norm kernel writes xn (activation storage), then the projection.
 llm_status norm_linear(llm_handle* h, const char* tag, LinearParams p, const void* g, const void* b,
                        bool last_row) {
   const llm_config& c = h->cfg;
@@ -239,7 +240,7 @@ llm_status norm_linear(llm_handle* h, const char* tag, LinearParams p, const voi
                 c.norm_eps};
   RUN("norm", launch_norm(np, h->wdt, h->adt, h->stream, h->pdl));
   p.X = h->xn;
-  p.ldx = c.d_model;
+  p.ldx = h->act_mul * c.d_model;
   return linear(h, tag, p);
 }
 
@@ -281,18 +282,18 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
       ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.B = B; ap.n_heads = H;
       ap.split = h->split; ap.max_splits = h->max_splits; ap.part_o = h->attn_po; ap.part_ml = h->attn_ml;
       ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
-      RUN("attn_decode", launch_attn_decode(ap, h->wdt, h->stream, h->pdl));
+      RUN("attn_decode", launch_attn_decode(ap, DT_F32, h->stream, h->pdl));
       h->launch_counter++;   // split + merge
     } else {
       AttnPrefillParams ap;
       memset(&ap, 0, sizeof(ap));
       ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.items = h->d_items; ap.n_items = n_items;
       ap.n_heads = H; ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
-      RUN("attn_prefill", launch_attn_prefill(ap, h->wdt, h->stream, h->pdl));
+      RUN("attn_prefill", launch_attn_prefill(ap, DT_F32, h->stream, h->pdl));
     }
 
     // out projection + residual
-    lp.W = w.w_o; lp.X = h->att; lp.N = d; lp.K = H * HD; lp.ldx = H * HD;
+    lp.W = w.w_o; lp.X = h->att; lp.N = d; lp.K = H * HD; lp.ldx = h->act_mul * H * HD;
     lp.epi = base_epi(h);
     lp.epi.kind = EPI_RESID; lp.epi.bias = w.b_o; lp.epi.resid = h->h; lp.epi.ld_resid = d;
     { llm_status s_ = linear(h, "o", lp); if (s_ != LLM_OK) return s_; }
@@ -300,11 +301,12 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
     // norm + FFN up (+gate) with the activation
     lp.W = w.w_up; lp.N = F; lp.K = d; lp.swiglu = gpt2 ? 0 : 1;
     lp.epi = base_epi(h);
-    lp.epi.kind = gpt2 ? EPI_GELU : EPI_SWIGLU; lp.epi.bias = w.b_up; lp.epi.out = h->ff; lp.epi.ld_out = F;
+    lp.epi.kind = gpt2 ? EPI_GELU : EPI_SWIGLU; lp.epi.bias = w.b_up; lp.epi.out = h->ff;
+    lp.epi.ld_out = h->act_mul * F;
     { llm_status s_ = norm_linear(h, "up", lp, w.ln2_w, w.ln2_b, false); if (s_ != LLM_OK) return s_; }
 
     // FFN down + residual
-    lp.W = w.w_down; lp.X = h->ff; lp.N = d; lp.K = F; lp.ldx = F; lp.swiglu = 0;
+    lp.W = w.w_down; lp.X = h->ff; lp.N = d; lp.K = F; lp.ldx = h->act_mul * F; lp.swiglu = 0;
     lp.epi = base_epi(h);
     lp.epi.kind = EPI_RESID; lp.epi.bias = w.b_down; lp.epi.resid = h->h; lp.epi.ld_resid = d;
     { llm_status s_ = linear(h, "down", lp); if (s_ != LLM_OK) return s_; }
@@ -398,8 +400,11 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   h->dev = dev;
   h->num_sms = prop.multiProcessorCount;
   h->stream = static_cast<cudaStream_t>(cuda_stream);
-  h->wdt = h->adt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
-  h->welt = c.dtype == LLM_DTYPE_F32 ? 4 : 2;
+  // Only the weights take the model's dtype. Activations keep fp32 accuracy (bf16-weight
+  // models store them as bf16 pairs for the tensor cores) and the KV cache is fp32.
+  h->wdt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
+  h->adt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : DT_SPLIT;
+  h->act_mul = h->adt == DT_SPLIT ? 2 : 1;
   h->tok_emb = wp->tok_emb;
   h->pos_emb = gpt2 ? wp->pos_emb : nullptr;
   h->lnf_w = wp->lnf_w;
@@ -430,7 +435,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   h->max_splits = std::max(1, (max_ctx + h->split - 1) / h->split);
   h->head_tiles = (c.vocab + TILE_N - 1) / TILE_N;
   h->max_items = c.max_prefill_tokens / 64 + c.max_batch + 1;
-  const size_t act = h->welt;
+  const size_t act = 4;   // bytes per activation value: fp32, or a bf16 pair
   const size_t R = h->max_rows;
   llm_status st = LLM_OK;
 #define ALLOC(ptr, T, n)                                                         \
@@ -438,8 +443,8 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
     st = dev_alloc(h, reinterpret_cast<T**>(&(ptr)), (size_t)(n));               \
     if (st != LLM_OK) { free_all(h); delete h; return st; }                      \
   } while (0)
-  ALLOC(h->k_pool, char, (size_t)c.n_layers * h->layer_kv_elems * h->welt);
-  ALLOC(h->v_pool, char, (size_t)c.n_layers * h->layer_kv_elems * h->welt);
+  ALLOC(h->k_pool, float, (size_t)c.n_layers * h->layer_kv_elems);
+  ALLOC(h->v_pool, float, (size_t)c.n_layers * h->layer_kv_elems);
   ALLOC(h->h, float, R * d);
   ALLOC(h->xn, char, R * d * act);
   ALLOC(h->q, float, R * H * HD);
@@ -702,9 +707,10 @@ llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const vo
   CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
   LinearParams p;
   memset(&p, 0, sizeof(p));
-  p.W = w; p.X = x; p.M = M; p.N = N; p.K = K; p.ldx = K;
-  p.wdt = p.xdt = dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
-  p.adt = p.wdt;
+  p.W = w; p.X = x; p.M = M; p.N = N; p.K = K;
+  p.wdt = dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
+  p.xdt = p.adt = dtype == LLM_DTYPE_F32 ? DT_F32 : DT_SPLIT;
+  p.ldx = dtype == LLM_DTYPE_F32 ? K : 2 * K;
   p.epi.kind = EPI_STORE_F32;
   p.epi.bias = bias;
   p.epi.out = y;

@@ -14,6 +14,8 @@
 // online softmax: CTA (64 query rows, head) walks the causal key tiles.
 //
 // Scores are q.k / sqrt(64); masked keys get -inf so exp gives exactly 0.
+#include <type_traits>
+
 #include "attention.cuh"
 
 namespace llm {
@@ -201,7 +203,8 @@ __global__ void __launch_bounds__(HD) k_attn_decode_merge(const AttnDecodeParams
   }
   pdl_trigger();
   const float r = l > 0.0f ? o / l : 0.0f;
-  reinterpret_cast<AT*>(p.out)[(size_t)bh * HD + d] = from_f32<AT>(r);
+  const int ld = (std::is_same<AT, Split>::value ? 2 : 1) * p.n_heads * HD;
+  act_store<AT>(p.out, b, ld, (bh - b * p.n_heads) * HD + d, r);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -326,15 +329,16 @@ __global__ void __launch_bounds__(AP_THREADS) k_attn_prefill(const AttnPrefillPa
     }
   }
   pdl_trigger();
-  AT* out = reinterpret_cast<AT*>(p.out);
+  const int ld = (std::is_same<AT, Split>::value ? 2 : 1) * H * HD;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = ty * 4 + i;
     if (r >= nq) continue;
     const float inv = 1.0f / lrow[i];
+    float y[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      out[(size_t)(row0 + r) * H * HD + h * HD + tx * 4 + j] = from_f32<AT>(o[i][j] * inv);
+    for (int j = 0; j < 4; ++j) y[j] = o[i][j] * inv;
+    act_store4<AT>(p.out, row0 + r, ld, h * HD + tx * 4, y);
   }
 }
 
@@ -402,16 +406,18 @@ cudaError_t prefill_t(const AttnPrefillParams& p, cudaStream_t s, bool pdl) {
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int kv_dtype, cudaStream_t s, bool pdl) {
   if (p.B <= 0) return cudaSuccess;
   if (p.n_heads / p.kv.n_kv_heads > MAX_G || p.split <= 0 || (p.split % KVB) != 0) return cudaErrorInvalidValue;
-  if (kv_dtype == DT_F32)
-    return p.out_dtype == DT_F32 ? decode_t<float, float>(p, s, pdl) : decode_t<float, bf16>(p, s, pdl);
-  return p.out_dtype == DT_F32 ? decode_t<bf16, float>(p, s, pdl) : decode_t<bf16, bf16>(p, s, pdl);
+  if (kv_dtype == DT_F32 && p.out_dtype == DT_F32) return decode_t<float, float>(p, s, pdl);
+  if (kv_dtype == DT_F32 && p.out_dtype == DT_SPLIT) return decode_t<float, Split>(p, s, pdl);
+  if (kv_dtype == DT_BF16 && p.out_dtype == DT_F32) return decode_t<bf16, float>(p, s, pdl);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_prefill(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl) {
   if (p.n_items <= 0) return cudaSuccess;
-  if (kv_dtype == DT_F32)
-    return p.out_dtype == DT_F32 ? prefill_t<float, float>(p, s, pdl) : prefill_t<float, bf16>(p, s, pdl);
-  return p.out_dtype == DT_F32 ? prefill_t<bf16, float>(p, s, pdl) : prefill_t<bf16, bf16>(p, s, pdl);
+  if (kv_dtype != DT_F32) return cudaErrorInvalidValue;
+  if (p.out_dtype == DT_F32) return prefill_t<float, float>(p, s, pdl);
+  if (p.out_dtype == DT_SPLIT) return prefill_t<float, Split>(p, s, pdl);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace llm

@@ -15,7 +15,7 @@ struct AttnDecodeParams {
   int max_splits;           // grid.y
   float* part_o;            // [B][H][max_splits][64]
   float* part_ml;           // [B][H][max_splits][2]  (running max, sum of exp)
-  void* out;                // [B][H*64] in the activation dtype
+  void* out;                // [B][H*64] activations (DT_F32, or DT_SPLIT: row stride 2*H*64 bf16)
   int out_dtype;
   unsigned* flags;
 };
@@ -29,7 +29,7 @@ struct AttnPrefillParams {
   const int4* items;        // {seq, q_pos0, row0, len}
   int n_items;
   int n_heads;
-  void* out;                // [rows][H*64] activation dtype
+  void* out;                // [rows][H*64] activations (DT_F32 or DT_SPLIT)
   int out_dtype;
   unsigned* flags;
 };

@@ -7,7 +7,8 @@
 
 namespace llm {
 
-enum : int { DT_F32 = 0, DT_BF16 = 1 };
+// DT_SPLIT: activation storage of bf16-weight models (see Split below).
+enum : int { DT_F32 = 0, DT_BF16 = 1, DT_SPLIT = 2 };
 enum : int { ARCH_GPT2 = 0, ARCH_LLAMA = 1 };
 constexpr int HD = 64;          // head_dim (the only supported value)
 constexpr int KVB = 16;         // tokens per KV block
@@ -26,6 +27,54 @@ __device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
 template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// Activations of bf16-weight models. A value v is kept as the bf16 pair hi = bf16(v),
+// lo = bf16(v - hi), which holds v to about 2^-17 relative (bf16 alone: 2^-9). A row of n
+// values is stored as its n hi values followed by its n lo values (row stride 2n bf16), so
+// a tensor-core kernel reads the operand as two plain bf16 matrices and sums two products,
+// and a CUDA-core kernel adds the halves. Only the weights are bf16; what the step
+// computes between projections stays at fp32 accuracy.
+struct Split {};
+template <typename WT> struct ActOf { using type = float; };
+template <> struct ActOf<bf16> { using type = Split; };
+
+// Element n of row `row` of an activation matrix whose rows are `ld` storage elements apart
+// (fp32: ld >= n_cols; Split: ld = 2 * n_cols, the lo half starting at ld / 2).
+template <typename AT> __device__ __forceinline__ void act_store(void* base, size_t row, int ld, int n, float v);
+template <> __device__ __forceinline__ void act_store<float>(void* base, size_t row, int ld, int n, float v) {
+  reinterpret_cast<float*>(base)[row * ld + n] = v;
+}
+template <> __device__ __forceinline__ void act_store<Split>(void* base, size_t row, int ld, int n, float v) {
+  bf16* r = reinterpret_cast<bf16*>(base) + row * ld;
+  const bf16 hi = __float2bfloat16_rn(v);
+  r[n] = hi;
+  r[(ld >> 1) + n] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+template <typename AT> __device__ __forceinline__ float act_load(const void* base, size_t row, int ld, int n);
+template <> __device__ __forceinline__ float act_load<float>(const void* base, size_t row, int ld, int n) {
+  return reinterpret_cast<const float*>(base)[row * ld + n];
+}
+template <> __device__ __forceinline__ float act_load<Split>(const void* base, size_t row, int ld, int n) {
+  const bf16* r = reinterpret_cast<const bf16*>(base) + row * ld;
+  return __bfloat162float(r[n]) + __bfloat162float(r[(ld >> 1) + n]);
+}
+// Four consecutive elements n..n+3 (n a multiple of 4, row start 16-byte aligned for fp32,
+// 8-byte aligned for Split).
+template <typename AT> __device__ __forceinline__ void act_store4(void* base, size_t row, int ld, int n, const float* v);
+template <> __device__ __forceinline__ void act_store4<float>(void* base, size_t row, int ld, int n, const float* v) {
+  *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + row * ld + n) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <> __device__ __forceinline__ void act_store4<Split>(void* base, size_t row, int ld, int n, const float* v) {
+  bf16* r = reinterpret_cast<bf16*>(base) + row * ld;
+  __nv_bfloat162 h[2], l[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    l[i] = __floats2bfloat162_rn(v[2 * i] - __low2float(h[i]), v[2 * i + 1] - __high2float(h[i]));
+  }
+  *reinterpret_cast<uint2*>(r + n) = *reinterpret_cast<const uint2*>(h);
+  *reinterpret_cast<uint2*>(r + (ld >> 1) + n) = *reinterpret_cast<const uint2*>(l);
+}
 
 __device__ __forceinline__ void set_flag(unsigned* flags, unsigned bit) {
   if (flags) atomicOr(flags, bit);
@@ -162,7 +211,8 @@ struct StepArgs {
   int B;
 };
 
-// Paged KV pool of one layer: [block][kv_head][16][64], element type = weight dtype.
+// Paged KV pool of one layer: [block][kv_head][16][64] fp32 (the library's cache; the
+// stand-alone decode-attention entry point also reads bf16 pools).
 struct KVLayer {
   void* k;
   void* v;
@@ -197,7 +247,7 @@ enum : int {
 
 struct Epilogue {
   int kind;
-  int act_dtype;        // DT_F32 / DT_BF16 for `out`
+  int act_dtype;        // DT_F32 / DT_SPLIT for `out`
   const void* bias;     // [N] in the weight dtype, or nullptr
   void* out;            // STORE / GELU / SWIGLU output
   int ld_out;

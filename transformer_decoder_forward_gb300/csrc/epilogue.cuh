@@ -8,7 +8,7 @@
 //   RESID   residual add after the output / down projection;
 //   GELU    GPT-2's GELU-tanh with the tanh argument clamped to +-15 ("batch_forge");
 //   SWIGLU  silu(gate) * up;
-//   QKV     bias, RoPE on q and k (Llama), kv_write of k and v into the paged cache;
+//   QKV     bias, RoPE on q and k (Llama), kv_write of k and v into the paged fp32 cache;
 //   HEAD    tied-LM-head logits and a per-tile greedy argmax partial.
 //
 // Latency: the per-tile bias and the per-row KV slot are staged in shared memory
@@ -24,11 +24,6 @@ constexpr int EPI_MAX_ROWS = 256;   // rows of one epilogue call (every projecti
 template <typename WT>
 __device__ __forceinline__ float bias_at(const void* b, int n) {
   return b ? to_f32(reinterpret_cast<const WT*>(b)[n]) : 0.0f;
-}
-
-template <typename AT>
-__device__ __forceinline__ void store_act(void* out, size_t i, float v) {
-  reinterpret_cast<AT*>(out)[i] = from_f32<AT>(v);
 }
 
 // RoPE angle pos * inv_freq[d] reduced to about [-pi, pi] in fp32 without losing the
@@ -51,9 +46,12 @@ __device__ __forceinline__ void rope_sincos(int pos, float2 f, float* s, float* 
 // EPI_MAX_ROWS), tile columns 0..ncols-1 (ncols <= 64) map to output column n0 + c (for
 // SWIGLU: gate row n0 + c for c < 32 and up row F + n0 + c - 32; output column n0 + c).
 // N = output width. Every thread of the block must call it (it synchronises the block).
-template <typename WT, typename AT>
+// WT: weight (and bias) type; activations are stored as ActOf<WT> (fp32 or a bf16 pair),
+// the KV cache in fp32.
+template <typename WT>
 __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int m0, int mrows, int n0, int ncols,
                              int N) {
+  using AT = typename ActOf<WT>::type;
   __shared__ float s_bias[64];
   __shared__ int s_pos[EPI_MAX_ROWS];
   __shared__ int s_blk[EPI_MAX_ROWS];
@@ -95,10 +93,8 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
         const int m = i / ncols, c = i - m * ncols, n = n0 + c;
         if (n >= N) continue;
         const float y = tile[m * ldt + c] + s_bias[c];
-        const size_t o = (size_t)(m0 + m) * e.ld_out + n;
-        if (e.kind == EPI_STORE_F32) reinterpret_cast<float*>(e.out)[o] = y;
-        else if (e.kind == EPI_STORE_ACT) store_act<AT>(e.out, o, y);
-        else store_act<AT>(e.out, o, gelu_tanh_clamped(y));
+        if (e.kind == EPI_STORE_F32) reinterpret_cast<float*>(e.out)[(size_t)(m0 + m) * e.ld_out + n] = y;
+        else act_store<AT>(e.out, m0 + m, e.ld_out, n, e.kind == EPI_STORE_ACT ? y : gelu_tanh_clamped(y));
       }
       break;
     }
@@ -134,7 +130,7 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
         if (j >= N) continue;
         const float g = tile[m * ldt + c] + s_bias[c];
         const float u = tile[m * ldt + 32 + c] + s_bias[32 + c];
-        store_act<AT>(e.out, (size_t)(m0 + m) * e.ld_out + j, silu_f(g) * u);
+        act_store<AT>(e.out, m0 + m, e.ld_out, j, silu_f(g) * u);
       }
       break;
     }
@@ -168,9 +164,9 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
         const int pb = s_blk[m];
         if (pb < 0) continue;
         const int g = is_k ? hh - H : hh - H - Hkv;
-        WT* dst = reinterpret_cast<WT*>(is_k ? e.kv.k : e.kv.v) + kv_offset(e.kv, pb, g, pos & (KVB - 1));
-        dst[d] = from_f32<WT>(v0);
-        if (e.rope && is_k) dst[d + HD / 2] = from_f32<WT>(v1);
+        float* dst = reinterpret_cast<float*>(is_k ? e.kv.k : e.kv.v) + kv_offset(e.kv, pb, g, pos & (KVB - 1));
+        dst[d] = v0;
+        if (e.rope && is_k) dst[d + HD / 2] = v1;
       }
       break;
     }

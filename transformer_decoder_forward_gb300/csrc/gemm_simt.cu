@@ -4,8 +4,8 @@
 // of x and W staged in threadgroup memory ("rvllm-metal", section "The matmul
 // pain story"). Here a 128 x 64 tile (64 = one head, so the shared epilogues
 // see whole heads), K in steps of 16, 256 threads each holding an 8 x 4 block.
-// This is the fp32 path and the reference path for bf16; bf16 prefill uses the
-// tcgen05 kernel.
+// This is the fp32 path and the reference path for bf16 weights (whose activations
+// arrive as bf16 pairs); bf16 prefill uses the tcgen05 kernel.
 #include "epilogue.cuh"
 #include "linear.cuh"
 
@@ -17,11 +17,9 @@ constexpr int BM = 128, BN = 64, BK = 16;
 constexpr int SIMT_THREADS = 256;
 constexpr int AS_LD = BM + 4, BS_LD = BN + 4, OT_LD = BN + 1;
 
-template <typename T>
-__device__ __forceinline__ float ld_elem(const T* p) { return to_f32(*p); }
-
-template <typename WT, typename XT, typename AT>
+template <typename WT>
 __global__ void __launch_bounds__(SIMT_THREADS) k_gemm_simt(const LinearParams p) {
+  using AT = typename ActOf<WT>::type;   // activation storage: fp32 or a bf16 pair
   __shared__ __align__(16) float smem[BM * OT_LD];   // reused: As/Bs during the loop, output tile after
   float* As = smem;                  // [BK][AS_LD]  (k-major, m contiguous)
   float* Bs = smem + BK * AS_LD;     // [BK][BS_LD]
@@ -29,7 +27,6 @@ __global__ void __launch_bounds__(SIMT_THREADS) k_gemm_simt(const LinearParams p
   const int tile = blockIdx.x, m0 = blockIdx.y * BM;
   const int F = p.N;
   const WT* W = reinterpret_cast<const WT*>(p.W);
-  const XT* X = reinterpret_cast<const XT*>(p.X);
   pdl_wait();
 
   // loader coordinates
@@ -45,7 +42,6 @@ __global__ void __launch_bounds__(SIMT_THREADS) k_gemm_simt(const LinearParams p
     b_valid = b_wrow < p.N;
   }
   const bool a_valid = m0 + a_row < p.M;
-  const XT* xa = X + (size_t)(m0 + a_row) * p.ldx;
   const WT* wb = W + (size_t)b_wrow * p.K;
 
   const int ty = tid >> 4, tx = tid & 15;   // rows ty*8.., cols tx*4..
@@ -59,12 +55,12 @@ __global__ void __launch_bounds__(SIMT_THREADS) k_gemm_simt(const LinearParams p
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int k = k0 + a_k + j;
-      As[(a_k + j) * AS_LD + a_row] = (a_valid && k < p.K) ? ld_elem(xa + k) : 0.0f;
+      As[(a_k + j) * AS_LD + a_row] = (a_valid && k < p.K) ? act_load<AT>(p.X, m0 + a_row, p.ldx, k) : 0.0f;
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int k = k0 + b_k + j;
-      Bs[(b_k + j) * BS_LD + b_col] = (b_valid && k < p.K) ? ld_elem(wb + k) : 0.0f;
+      Bs[(b_k + j) * BS_LD + b_col] = (b_valid && k < p.K) ? to_f32(wb[k]) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -89,10 +85,10 @@ __global__ void __launch_bounds__(SIMT_THREADS) k_gemm_simt(const LinearParams p
   __syncthreads();
   pdl_trigger();
   const int n0 = p.swiglu ? tile * 32 : tile * BN;
-  run_epilogue<WT, AT>(p.epi, ot, OT_LD, m0, min(BM, p.M - m0), n0, BN, p.N);
+  run_epilogue<WT>(p.epi, ot, OT_LD, m0, min(BM, p.M - m0), n0, BN, p.N);
 }
 
-template <typename WT, typename XT, typename AT>
+template <typename WT>
 cudaError_t launch_t(const LinearParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(linear_tiles(p), (p.M + BM - 1) / BM);
@@ -104,20 +100,16 @@ cudaError_t launch_t(const LinearParams& p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_gemm_simt<WT, XT, AT>, p);
+  return cudaLaunchKernelEx(&cfg, k_gemm_simt<WT>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_simt(const LinearParams& p, cudaStream_t s, bool pdl) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
-  if (p.wdt == DT_F32) {
-    if (p.xdt != DT_F32) return cudaErrorInvalidValue;
-    return p.adt == DT_F32 ? launch_t<float, float, float>(p, s, pdl) : launch_t<float, float, bf16>(p, s, pdl);
-  }
-  if (p.xdt == DT_BF16)
-    return p.adt == DT_BF16 ? launch_t<bf16, bf16, bf16>(p, s, pdl) : launch_t<bf16, bf16, float>(p, s, pdl);
-  return p.adt == DT_BF16 ? launch_t<bf16, float, bf16>(p, s, pdl) : launch_t<bf16, float, float>(p, s, pdl);
+  if (p.wdt == DT_F32 && p.xdt == DT_F32 && p.adt == DT_F32) return launch_t<float>(p, s, pdl);
+  if (p.wdt == DT_BF16 && p.xdt == DT_SPLIT && p.adt == DT_SPLIT) return launch_t<bf16>(p, s, pdl);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace llm

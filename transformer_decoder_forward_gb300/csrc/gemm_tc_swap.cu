@@ -10,6 +10,8 @@
 //     (programmatic dependent launch) it already issues the weight tiles of the
 //     first stages: weights never depend on earlier kernels.
 //   - warp 1, one lane: issues tcgen05.mma into a 128 x N fp32 TMEM accumulator.
+//   - bf16 weights: activations arrive as bf16 (hi, lo) pairs; a stage holds the
+//     weight slice and both activation halves and the MMA sums W.X_hi + W.X_lo.
 //   - warps 2-5: for fp32 models they split each staged operand tile into tf32
 //     high and low parts in a separate buffer and release the TMA stage at once,
 //     so the weight stream runs ahead of the conversion; the MMA sums
@@ -42,8 +44,8 @@ constexpr int SW_MAX_KS = 8;                 // cluster size limit (portable)
 
 template <int NT, bool TF32>
 struct SwapCfg {
-  static constexpr int B_BYTES = NT * 128;
-  static constexpr int RAW = SW_A_BYTES + B_BYTES;      // one TMA stage: [W slice][X slice]
+  static constexpr int B_BYTES = NT * 128;                // one 128-byte K slice of NT activation rows
+  static constexpr int RAW = SW_A_BYTES + (TF32 ? 1 : 2) * B_BYTES;   // TMA stage: [W][X] or [W][X_hi][X_lo]
   static constexpr int CONVB = 2 * RAW;                 // tf32: [W hi][X hi][W lo][X lo]
   // TMA stages: bf16 keeps up to 4 within ~100 KB (a second CTA fits on the SM); tf32 keeps
   // 4 raw stages plus 2 converted buffers (2 + 1 for the widest tiles).
@@ -70,12 +72,13 @@ __device__ __forceinline__ float4 tf32_hi(const float4& x) {
   return make_float4(hi13(x.x), hi13(x.y), hi13(x.z), hi13(x.w));
 }
 
-template <typename AT, int NT, bool TF32>
+template <int NT, bool TF32>
 __global__ void __launch_bounds__(SW_THREADS, 1)
     k_gemm_tc_swap(const LinearParams p, const __grid_constant__ CUtensorMap tmW,
-                   const __grid_constant__ CUtensorMap tmX, int kcta, int ks_total) {
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo, int kcta,
+                   int ks_total) {
   using C = SwapCfg<NT, TF32>;
-  using WT = typename std::conditional<TF32, float, bf16>::type;   // weight / activation / KV type
+  using WT = typename std::conditional<TF32, float, bf16>::type;   // weight type
   constexpr int NR = C::NRAW, NC = C::NCONV > 0 ? C::NCONV : 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base =
@@ -138,14 +141,18 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
       mbar_arrive_expect_tx(&full[i], C::RAW);
       load_w(i, k0 + i * C::KE);
     }
+    auto load_x = [&](int r, int kc) {
+      tma_load_2d(raw_b(r), &tmX, kc, 0, &full[r]);
+      if constexpr (!TF32) tma_load_2d(raw_b(r) + C::B_BYTES, &tmXlo, kc, 0, &full[r]);
+    };
     pdl_wait();
-    for (int i = 0; i < pre; ++i) tma_load_2d(raw_b(i), &tmX, k0 + i * C::KE, 0, &full[i]);
+    for (int i = 0; i < pre; ++i) load_x(i, k0 + i * C::KE);
     for (int i = pre; i < kiters; ++i) {
       const int r = i % NR;
       if (!mbar_wait(&rfree[r], ((i / NR) - 1) & 1, flags)) break;
       mbar_arrive_expect_tx(&full[r], C::RAW);
       load_w(r, k0 + i * C::KE);
-      tma_load_2d(raw_b(r), &tmX, k0 + i * C::KE, 0, &full[r]);
+      load_x(r, k0 + i * C::KE);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -172,10 +179,12 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
         if (!mbar_wait(&full[r], (i / NR) & 1, flags)) break;
         tc_fence_after();
         const uint64_t da = sw128_desc(raw_a(r)), db = sw128_desc(raw_b(r));
+        const uint64_t dbl = sw128_desc(raw_b(r) + C::B_BYTES);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t o = (uint64_t)(kk * 2);
           tc_mma(tmem, da + o, db + o, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma(tmem, da + o, dbl + o, idesc, 1u);
         }
         tc_commit(&rfree[r]);
       }
@@ -254,7 +263,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
     for (int sub = 0; sub < SW_ROWS / 64; ++sub) {
       const int n0 = p.swiglu ? (tile * 2 + sub) * 32 : tile * SW_ROWS + sub * 64;
       if (!p.swiglu && n0 >= p.N) break;
-      run_epilogue<WT, AT>(p.epi, tl + sub * 64, SW_OT_LD, r0, nrows, n0, 64, p.N);
+      run_epilogue<WT>(p.epi, tl + sub * 64, SW_OT_LD, r0, nrows, n0, 64, p.N);
     }
   };
   if (ks_total == 1) {
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
   if (r1 > r0) epilogue(red, r0, r1 - r0);
 }
 
-template <typename AT, int NT, bool TF32>
+template <int NT, bool TF32>
 cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
   using C = SwapCfg<NT, TF32>;
   const int tiles = p.swiglu ? (p.N + 63) / 64 : (p.N + SW_ROWS - 1) / SW_ROWS;
@@ -294,7 +303,7 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
   // K split from the weight shape only (never from M): the largest cluster size <= 8 whose
   // grid still runs as one wave (the cluster occupancy the driver reports for this kernel),
   // with at least two K stages per CTA.
-  auto kern = k_gemm_tc_swap<AT, NT, TF32>;
+  auto kern = k_gemm_tc_swap<NT, TF32>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
@@ -331,9 +340,14 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
   kcta = ((kcta + C::KE - 1) / C::KE) * C::KE;
   ks = (p.K + kcta - 1) / kcta;
   const int dt = TF32 ? DT_F32 : DT_BF16;
-  CUtensorMap mw, mx;
+  CUtensorMap mw, mx, mxl;
   if (!make_map(&mw, p.W, dt, wrows, p.K, p.K, p.swiglu ? 32 : SW_ROWS)) return cudaErrorInvalidValue;
   if (!make_map(&mx, p.X, dt, p.M, p.K, p.ldx, NT)) return cudaErrorInvalidValue;
+  if (TF32) {
+    mxl = mx;   // unused
+  } else if (!make_map(&mxl, reinterpret_cast<const bf16*>(p.X) + p.ldx / 2, dt, p.M, p.K, p.ldx, NT)) {
+    return cudaErrorInvalidValue;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles, ks);
   cfg.blockDim = dim3(SW_THREADS);
@@ -355,23 +369,29 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, p, mw, mx, kcta, ks);
+  return cudaLaunchKernelEx(&cfg, kern, p, mw, mx, mxl, kcta, ks);
 }
 
-template <typename AT, bool TF32>
+template <bool TF32>
 cudaError_t launch_at(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
-  if (p.M <= 16) return launch_nt<AT, 16, TF32>(p, num_sms, s, pdl);
-  if (p.M <= 32) return launch_nt<AT, 32, TF32>(p, num_sms, s, pdl);
-  if (p.M <= 64) return launch_nt<AT, 64, TF32>(p, num_sms, s, pdl);
-  if (p.M <= 128) return launch_nt<AT, 128, TF32>(p, num_sms, s, pdl);
-  return launch_nt<AT, 256, TF32>(p, num_sms, s, pdl);
+  if (p.M <= 16) return launch_nt<16, TF32>(p, num_sms, s, pdl);
+  if (p.M <= 32) return launch_nt<32, TF32>(p, num_sms, s, pdl);
+  if (p.M <= 64) return launch_nt<64, TF32>(p, num_sms, s, pdl);
+  if (p.M <= 128) return launch_nt<128, TF32>(p, num_sms, s, pdl);
+  return launch_nt<256, TF32>(p, num_sms, s, pdl);
 }
 
 }  // namespace
 
+// fp32 weights with fp32 activations (three tf32 products) or bf16 weights with bf16-pair
+// activations (two bf16 products).
 bool gemm_tc_swap_supported(const LinearParams& p) {
-  if (p.M <= 0 || p.M > 256 || p.wdt != p.xdt || p.xnorm) return false;
+  if (p.M <= 0 || p.M > 256 || p.xnorm) return false;
+  const bool f32 = p.wdt == DT_F32 && p.xdt == DT_F32 && p.adt == DT_F32;
+  const bool pair = p.wdt == DT_BF16 && p.xdt == DT_SPLIT && p.adt == DT_SPLIT;
+  if (!f32 && !pair) return false;
   if (p.K % 8 != 0 || p.ldx % 8 != 0) return false;
+  if (pair && (p.ldx % 16 != 0 || p.ldx < 2 * p.K)) return false;
   if ((reinterpret_cast<uintptr_t>(p.W) | reinterpret_cast<uintptr_t>(p.X)) & 15) return false;
   return encode_fn() != nullptr;
 }
@@ -379,10 +399,7 @@ bool gemm_tc_swap_supported(const LinearParams& p) {
 cudaError_t launch_gemm_tc_swap(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
   if (!gemm_tc_swap_supported(p)) return cudaErrorNotSupported;
-  const bool tf32 = p.wdt == DT_F32;
-  if (p.adt == DT_BF16)
-    return tf32 ? launch_at<bf16, true>(p, num_sms, s, pdl) : launch_at<bf16, false>(p, num_sms, s, pdl);
-  return tf32 ? launch_at<float, true>(p, num_sms, s, pdl) : launch_at<float, false>(p, num_sms, s, pdl);
+  return p.wdt == DT_F32 ? launch_at<true>(p, num_sms, s, pdl) : launch_at<false>(p, num_sms, s, pdl);
 }
 
 }  // namespace llm

@@ -26,6 +26,7 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "epilogue.cuh"
 #include "linear.cuh"
@@ -41,42 +42,32 @@ constexpr int TL_LD = TILE_N + 1;   // padded row stride of the output tiles in 
 constexpr int GEMV_MT = 16;         // rows per CTA (larger M: more CTAs along grid.x)
 constexpr int U = 2;                // weight vectors per row in flight per thread and stage
 
-template <typename XT, int VEC>
-__device__ __forceinline__ void lds_x(const XT* p, float* f);
-template <>
-__device__ __forceinline__ void lds_x<float, 4>(const float* p, float* f) {
-  const float4 v = *reinterpret_cast<const float4*>(p);
-  f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-}
-template <>
-__device__ __forceinline__ void lds_x<float, 8>(const float* p, float* f) {
-  lds_x<float, 4>(p, f);
-  lds_x<float, 4>(p + 4, f + 4);
-}
-template <>
-__device__ __forceinline__ void lds_x<bf16, 8>(const bf16* p, float* f) {
-  Vec16<bf16>::unpack(*reinterpret_cast<const uint4*>(p), f);
-}
-template <>
-__device__ __forceinline__ void lds_x<bf16, 4>(const bf16* p, float* f) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  f[0] = __uint_as_float(u.x << 16); f[1] = __uint_as_float(u.x & 0xffff0000u);
-  f[2] = __uint_as_float(u.y << 16); f[3] = __uint_as_float(u.y & 0xffff0000u);
+// 4 or 8 staged activations (fp32 in shared memory) into registers
+template <int VEC>
+__device__ __forceinline__ void lds_x(const float* p, float* f) {
+#pragma unroll
+  for (int i = 0; i < VEC; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p + i);
+    f[i] = v.x; f[i + 1] = v.y; f[i + 2] = v.z; f[i + 3] = v.w;
+  }
 }
 
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-template <typename XT>
+// Activations are staged in shared memory as fp32 (a bf16 pair is summed on the way in).
+typedef float XT;
+constexpr int XE = 4;   // staged x elements per 16 bytes
+
 __host__ __device__ constexpr size_t gemv_smem(int MT, int kcta) {
-  return align16((size_t)MT * (kcta + 16 / sizeof(XT)) * sizeof(XT)) + 2 * (size_t)MT * TL_LD * sizeof(float);
+  return align16((size_t)MT * (kcta + XE) * sizeof(XT)) + 2 * (size_t)MT * TL_LD * sizeof(float);
 }
 
-template <typename WT, typename XT, typename AT, int MT>
+template <typename WT, int MT>
 __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int kcta, int ks_total) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr bool SPLIT_X = std::is_same<WT, bf16>::value;   // bf16 weights: x is a bf16 pair
   constexpr int VEC = Vec16<WT>::N;
   constexpr int STRIDE = 8 * VEC;
-  constexpr int XE = 16 / sizeof(XT);      // x elements per 16 bytes
   // grid.x = row chunk (fastest, so the chunks sharing a weight slice run together), grid.y = K split,
   // grid.z = output tile
   const int tile = blockIdx.z, ks = blockIdx.y, mbase = blockIdx.x * MT;
@@ -131,21 +122,48 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
   pdl_trigger();
   pdl_wait();
 
-  // ---- stage this CTA's slice of X (rows mbase.., columns k0..k0+kcl)
-  const XT* X = reinterpret_cast<const XT*>(p.X);
-  const bool x_vec = ((p.ldx % XE) == 0) && ((k0 % XE) == 0) && ((kcl % XE) == 0);
-  if (x_vec) {
-    const int chunks = kcl / XE;
-    for (int i = threadIdx.x; i < mcount * chunks; i += GEMV_THREADS) {
-      const int m = i / chunks, c = i - m * chunks;
-      cp_async16(xs + (size_t)m * ldxs + c * XE, X + (size_t)(mbase + m) * p.ldx + k0 + c * XE);
+  // ---- stage this CTA's slice of X (rows mbase.., columns k0..k0+kcl) as fp32
+  if constexpr (SPLIT_X) {
+    // row m: hi at [m*ldx + k], lo at [m*ldx + ldx/2 + k]
+    const bf16* X = reinterpret_cast<const bf16*>(p.X);
+    const int lo = p.ldx >> 1;
+    const bool x_vec = ((lo % 4) == 0) && ((k0 % 4) == 0) && ((kcl % 4) == 0);
+    if (x_vec) {
+      const int chunks = kcl / 4;
+      for (int i = threadIdx.x; i < mcount * chunks; i += GEMV_THREADS) {
+        const int m = i / chunks, c = i - m * chunks;
+        const bf16* r = X + (size_t)(mbase + m) * p.ldx + k0 + c * 4;
+        const uint2 hi = *reinterpret_cast<const uint2*>(r);
+        const uint2 lw = *reinterpret_cast<const uint2*>(r + lo);
+        float4 v;
+        v.x = __uint_as_float(hi.x << 16) + __uint_as_float(lw.x << 16);
+        v.y = __uint_as_float(hi.x & 0xffff0000u) + __uint_as_float(lw.x & 0xffff0000u);
+        v.z = __uint_as_float(hi.y << 16) + __uint_as_float(lw.y << 16);
+        v.w = __uint_as_float(hi.y & 0xffff0000u) + __uint_as_float(lw.y & 0xffff0000u);
+        *reinterpret_cast<float4*>(xs + (size_t)m * ldxs + c * 4) = v;
+      }
+    } else {
+      for (int i = threadIdx.x; i < mcount * kcl; i += GEMV_THREADS) {
+        const int m = i / kcl, k = i - m * kcl;
+        xs[(size_t)m * ldxs + k] = act_load<Split>(X, mbase + m, p.ldx, k0 + k);
+      }
     }
-    cp_async_commit();
-    cp_async_wait_all();
   } else {
-    for (int i = threadIdx.x; i < mcount * kcl; i += GEMV_THREADS) {
-      const int m = i / kcl, k = i - m * kcl;
-      xs[(size_t)m * ldxs + k] = X[(size_t)(mbase + m) * p.ldx + k0 + k];
+    const float* X = reinterpret_cast<const float*>(p.X);
+    const bool x_vec = ((p.ldx % XE) == 0) && ((k0 % XE) == 0) && ((kcl % XE) == 0);
+    if (x_vec) {
+      const int chunks = kcl / XE;
+      for (int i = threadIdx.x; i < mcount * chunks; i += GEMV_THREADS) {
+        const int m = i / chunks, c = i - m * chunks;
+        cp_async16(xs + (size_t)m * ldxs + c * XE, X + (size_t)(mbase + m) * p.ldx + k0 + c * XE);
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+    } else {
+      for (int i = threadIdx.x; i < mcount * kcl; i += GEMV_THREADS) {
+        const int m = i / kcl, k = i - m * kcl;
+        xs[(size_t)m * ldxs + k] = X[(size_t)(mbase + m) * p.ldx + k0 + k];
+      }
     }
   }
   __syncthreads();
@@ -164,7 +182,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
     for (int m = 0; m < MT; ++m) {
       if (m < mcount) {
         float xv[VEC];
-        lds_x<XT, VEC>(xs + (size_t)m * ldxs + k, xv);
+        lds_x<VEC>(xs + (size_t)m * ldxs + k, xv);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
           acc[0][m] = fmaf(f0[j], xv[j], acc[0][m]);
@@ -192,7 +210,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (m < mcount) {
-        const float x = to_f32(xs[(size_t)m * ldxs + kk]);
+        const float x = xs[(size_t)m * ldxs + kk];
         acc[0][m] = fmaf(a0, x, acc[0][m]);
         acc[1][m] = fmaf(a1, x, acc[1][m]);
       }
@@ -215,7 +233,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
   const int n0 = p.swiglu ? tile * 32 : tile * TILE_N;
   if (ks_total == 1) {
     __syncthreads();
-    run_epilogue<WT, AT>(p.epi, tl, TL_LD, mbase, mcount, n0, TILE_N, p.N);
+    run_epilogue<WT>(p.epi, tl, TL_LD, mbase, mcount, n0, TILE_N, p.N);
     return;
   }
   // ---- split-K reduction across the cluster through distributed shared memory
@@ -232,12 +250,12 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
     red[(m - r0) * TL_LD + c] = s;
   }
   cluster.sync();   // every rank has finished reading the others' partials
-  if (r1 > r0) run_epilogue<WT, AT>(p.epi, red, TL_LD, mbase + r0, r1 - r0, n0, TILE_N, p.N);
+  if (r1 > r0) run_epilogue<WT>(p.epi, red, TL_LD, mbase + r0, r1 - r0, n0, TILE_N, p.N);
 }
 
 // K split (cluster size) from the weight shape only: enough CTAs to cover the SMs and an
 // activation slice of at most 64 KB for a full row chunk.
-template <typename WT, typename XT>
+template <typename WT>
 void gemv_split(int tiles, int K, int num_sms, int* ks_out, int* kcta_out) {
   constexpr int STRIDE = 8 * Vec16<WT>::N;
   const int kmax = (64 * 1024) / (GEMV_MT * (int)sizeof(XT));
@@ -249,15 +267,15 @@ void gemv_split(int tiles, int K, int num_sms, int* ks_out, int* kcta_out) {
   *kcta_out = kcta;
 }
 
-template <typename WT, typename XT, typename AT, int MT>
+template <typename WT, int MT>
 cudaError_t launch_t(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
   const int tiles = linear_tiles(p);
   const int zch = (p.M + MT - 1) / MT;
   int ks, kcta;
-  gemv_split<WT, XT>(tiles, p.K, num_sms, &ks, &kcta);
-  const size_t smem = gemv_smem<XT>(MT, kcta);
+  gemv_split<WT>(tiles, p.K, num_sms, &ks, &kcta);
+  const size_t smem = gemv_smem(MT, kcta);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  auto kern = k_gemv<WT, XT, AT, MT>;
+  auto kern = k_gemv<WT, MT>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -289,30 +307,22 @@ cudaError_t launch_t(const LinearParams& p, int num_sms, cudaStream_t s, bool pd
   return cudaLaunchKernelEx(&cfg, kern, p, kcta, ks);
 }
 
-template <typename WT, typename XT, typename AT>
+template <typename WT>
 cudaError_t launch_m(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
-  if (p.M <= 1) return launch_t<WT, XT, AT, 1>(p, num_sms, s, pdl);
-  if (p.M <= 2) return launch_t<WT, XT, AT, 2>(p, num_sms, s, pdl);
-  if (p.M <= 4) return launch_t<WT, XT, AT, 4>(p, num_sms, s, pdl);
-  if (p.M <= 8) return launch_t<WT, XT, AT, 8>(p, num_sms, s, pdl);
-  return launch_t<WT, XT, AT, GEMV_MT>(p, num_sms, s, pdl);
+  if (p.M <= 1) return launch_t<WT, 1>(p, num_sms, s, pdl);
+  if (p.M <= 2) return launch_t<WT, 2>(p, num_sms, s, pdl);
+  if (p.M <= 4) return launch_t<WT, 4>(p, num_sms, s, pdl);
+  if (p.M <= 8) return launch_t<WT, 8>(p, num_sms, s, pdl);
+  return launch_t<WT, GEMV_MT>(p, num_sms, s, pdl);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
-  if (p.wdt == DT_F32) {
-    if (p.xdt != DT_F32) return cudaErrorInvalidValue;
-    return p.adt == DT_F32 ? launch_m<float, float, float>(p, num_sms, s, pdl)
-                           : launch_m<float, float, bf16>(p, num_sms, s, pdl);
-  }
-  if (p.xdt == DT_BF16) {
-    return p.adt == DT_BF16 ? launch_m<bf16, bf16, bf16>(p, num_sms, s, pdl)
-                            : launch_m<bf16, bf16, float>(p, num_sms, s, pdl);
-  }
-  return p.adt == DT_BF16 ? launch_m<bf16, float, bf16>(p, num_sms, s, pdl)
-                          : launch_m<bf16, float, float>(p, num_sms, s, pdl);
+  if (p.wdt == DT_F32 && p.xdt == DT_F32 && p.adt == DT_F32) return launch_m<float>(p, num_sms, s, pdl);
+  if (p.wdt == DT_BF16 && p.xdt == DT_SPLIT && p.adt == DT_SPLIT) return launch_m<bf16>(p, num_sms, s, pdl);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace llm

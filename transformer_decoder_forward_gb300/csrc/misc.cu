@@ -1,4 +1,6 @@
 // Embedding gather, row norms, greedy-argmax reduction and the step-argument node.
+#include <type_traits>
+
 #include "misc.cuh"
 
 namespace llm {
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
   const float scale = 1.0f / sqrtf(warp_sum(q) / p.d + p.eps);
   const WT* gw = reinterpret_cast<const WT*>(p.g);
   const WT* bw = reinterpret_cast<const WT*>(p.b);
-  AT* out = reinterpret_cast<AT*>(p.out) + (size_t)r * p.d;
+  const int ld = std::is_same<AT, Split>::value ? 2 * p.d : p.d;
   // gains / biases of this lane's columns: all loads issued before any store
   float gv[NORM_NV][4], bv[NORM_NV][4];
 #pragma unroll
@@ -88,8 +90,10 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
     const int i = lane + 32 * j;
     if (i >= d4) continue;
     const float xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    float y[4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) out[4 * i + t] = from_f32<AT>((xv[t] - mean) * scale * gv[j][t] + bv[j][t]);
+    for (int t = 0; t < 4; ++t) y[t] = (xv[t] - mean) * scale * gv[j][t] + bv[j][t];
+    act_store4<AT>(p.out, r, ld, 4 * i, y);
   }
 }
 
@@ -165,8 +169,9 @@ cudaError_t launch_embed(const EmbedParams& p, int wdt, cudaStream_t s, bool pdl
 cudaError_t launch_norm(const NormParams& p, int wdt, int adt, cudaStream_t s, bool pdl) {
   if (p.rows <= 0) return cudaSuccess;
   if (p.d % 8 != 0 || p.d > NORM_NV * 128) return cudaErrorInvalidValue;
-  if (wdt == DT_F32) return adt == DT_F32 ? norm_t<float, float>(p, s, pdl) : norm_t<float, bf16>(p, s, pdl);
-  return adt == DT_F32 ? norm_t<bf16, float>(p, s, pdl) : norm_t<bf16, bf16>(p, s, pdl);
+  if (wdt == DT_F32 && adt == DT_F32) return norm_t<float, float>(p, s, pdl);
+  if (wdt == DT_BF16 && adt == DT_SPLIT) return norm_t<bf16, Split>(p, s, pdl);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_argmax(const ArgmaxParams& p, int B, cudaStream_t s, bool pdl) {
