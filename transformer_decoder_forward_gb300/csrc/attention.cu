@@ -22,32 +22,76 @@ namespace llm {
 
 namespace {
 
-constexpr int AD_THREADS = 128;
+constexpr int AD_WARPS = 4;
+constexpr int AD_THREADS = AD_WARPS * 32;
 constexpr int MAX_G = 8;
-constexpr float SM_SCALE = 0.125f;   // 1/sqrt(64)
+constexpr int AD_MAX_BLOCKS_PER_WARP = 32;   // a split spans at most 4 * 32 blocks = 2048 tokens
+constexpr float SM_SCALE = 0.125f;          // 1/sqrt(64)
+constexpr float LOG2E = 1.4426950408889634f;
+
+// Shared-memory ring of one warp: NST stages, each one 16-token block of one KV head,
+// K then V (4 KB each in fp32, 2 KB in bf16), filled by 1-D TMA bulk copies.
+template <typename KT>
+struct AttnRing {
+  static constexpr int BLK = KVB * HD * (int)sizeof(KT);
+  static constexpr int NST = sizeof(KT) == 4 ? 3 : 4;
+  static constexpr int WARP_BYTES = NST * 2 * BLK;
+  static constexpr size_t SMEM = (size_t)AD_WARPS * WARP_BYTES + (size_t)AD_WARPS * NST * 8;
+};
+
+// Eight elements of one K or V row that lane dg (0..7) of a token row handles, as
+// fp32: for fp32 rows dims 4dg..4dg+3 and 32+4dg..32+4dg+3 (two 16-byte reads that
+// eight lanes take from distinct banks), for bf16 rows dims 8dg..8dg+7.
+__device__ __forceinline__ int lane_dim(int dg, int e, bool f32) {
+  return f32 ? (e < 4 ? 4 * dg + e : 32 + 4 * dg + (e - 4)) : 8 * dg + e;
+}
+template <typename KT> __device__ __forceinline__ void lds_row8(const KT* row, int dg, float* f);
+template <> __device__ __forceinline__ void lds_row8<float>(const float* row, int dg, float* f) {
+  const float4 a = *reinterpret_cast<const float4*>(row + 4 * dg);
+  const float4 c = *reinterpret_cast<const float4*>(row + 32 + 4 * dg);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
+}
+template <> __device__ __forceinline__ void lds_row8<bf16>(const bf16* row, int dg, float* f) {
+  Vec16<bf16>::unpack(*reinterpret_cast<const uint4*>(row + 8 * dg), f);
+}
 
 // Decode attention, one CTA per (sequence b, KV head g, chunk of `split` tokens).
-// The chunk's 16-token KV blocks are dealt to the 4 warps in turn; each warp streams
-// its blocks with 16-byte loads (two blocks in flight) and keeps an online softmax
-// (running max, sum of exp, unnormalised output) for every query head of the group
-// in registers. A token row is LPT lanes wide (8 for bf16, 16 for fp32); the lanes
-// that score a token are the lanes that weight its value row, so no probability has
-// to be broadcast. At the end the 4 warps' states are merged in shared memory and the
-// chunk's (max, sum, output) goes to the split-K partial buffer.
+// The chunk's 16-token KV blocks are dealt to the 4 warps in turn. Each warp runs its
+// own pipeline: lane 0 streams the warp's blocks into a ring of shared-memory stages
+// with 1-D TMA bulk copies (one mbarrier per stage), so several blocks per warp are
+// in flight without holding them in registers, while the warp computes on the oldest
+// stage and keeps an online softmax (running max, sum of exp, unnormalised output)
+// for every query head of the group in registers. A token row is 8 lanes wide (8
+// values a lane), four token rows per warp step; the lanes that score a token weight
+// its value row, so no probability is broadcast. Scores are kept in log2 units (q is
+// pre-scaled by log2(e)/sqrt(64)) so every exponential is one exp2. The 4 warps'
+// states are merged in shared memory and the chunk's (max, sum, output) goes to the
+// split-K partial buffer.
 template <typename KT, int GMAX>
 __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDecodeParams p) {
-  constexpr int EPL = 16 / sizeof(KT);    // elements per 16-byte load
-  constexpr int LPT = HD / EPL;           // lanes per token row: 8 (bf16) or 16 (fp32)
-  constexpr int TG = 32 / LPT;            // token groups per warp: 4 or 2
-  constexpr int IT = KVB / TG;            // loads per lane per 16-token block: 4 or 8
-  constexpr int NW = AD_THREADS / 32;
+  using R = AttnRing<KT>;
+  constexpr int NW = AD_WARPS, NST = R::NST;
+  constexpr int TG = 4, IT = KVB / TG;        // 4 token rows per step, 4 steps per block
+  constexpr bool F32 = sizeof(KT) == 4;
+  extern __shared__ __align__(128) unsigned char smem[];
   __shared__ float s_m[NW][GMAX], s_l[NW][GMAX];
   __shared__ __align__(16) float s_o[NW][GMAX][HD];
 
   const int Hkv = p.kv.n_kv_heads, H = p.n_heads, G = H / Hkv;
   const int b = blockIdx.x / Hkv, g = blockIdx.x - b * Hkv, sp = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int dg = lane % LPT, tg = lane / LPT;
+  const int dg = lane & 7, tg = lane >> 3;
+  unsigned char* ring = smem + (size_t)warp * R::WARP_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)NW * R::WARP_BYTES) + warp * NST;
+  auto kst = [&](int s) { return reinterpret_cast<const KT*>(ring + (size_t)s * 2 * R::BLK); };
+  auto vst = [&](int s) { return reinterpret_cast<const KT*>(ring + (size_t)s * 2 * R::BLK + R::BLK); };
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+
   pdl_wait();   // the new token's K/V is written by the projection that precedes this kernel
   const StepArgs* a = p.args;
   const int ctx = a->positions[b] + 1;
@@ -55,128 +99,149 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
   if (t0 >= ctx) return;
   const int nt = min(p.split, ctx - t0);
   const int nblk = (nt + KVB - 1) / KVB;
+  const int nj = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;   // this warp's blocks: warp + NW*j
+  // physical block of this warp's j-th block, held by lane j
+  int my_pb = -1;
+  if (lane < nj) my_pb = kv_block(p.kv, a->block_tables, b, t0 + (warp + NW * lane) * KVB, p.flags);
 
-  float qf[GMAX][EPL], o[GMAX][EPL], m[GMAX], l[GMAX];
+  const KT* kbase = reinterpret_cast<const KT*>(p.kv.k);
+  const KT* vbase = reinterpret_cast<const KT*>(p.kv.v);
+  auto issue = [&](int j) {   // every lane calls; lane 0 fills stage j % NST with block j
+    const int pb = __shfl_sync(0xffffffffu, my_pb, j);
+    if (lane == 0) {
+      uint64_t* bar = &bars[j % NST];
+      if (pb >= 0) {
+        const size_t off = kv_offset(p.kv, pb, g, 0);
+        mbar_arrive_expect_tx(bar, 2 * R::BLK);
+        bulk_g2s(const_cast<KT*>(kst(j % NST)), kbase + off, R::BLK, bar);
+        bulk_g2s(const_cast<KT*>(vst(j % NST)), vbase + off, R::BLK, bar);
+      } else {
+        mbar_arrive(bar);   // bad block (flagged): complete the phase without data
+      }
+    }
+  };
+  const int pre = min(NST, nj);
+  for (int j = 0; j < pre; ++j) issue(j);
+
+  float qf[GMAX][8], o[GMAX][8], m[GMAX], l[GMAX];
 #pragma unroll
   for (int j = 0; j < GMAX; ++j) {
     m[j] = -INFINITY;
     l[j] = 0.0f;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
+    for (int e = 0; e < 8; ++e) {
       o[j][e] = 0.0f;
-      qf[j][e] = j < G ? p.q[(size_t)b * H * HD + (size_t)(g * G + j) * HD + dg * EPL + e] * SM_SCALE : 0.0f;
+      qf[j][e] = j < G ? p.q[(size_t)b * H * HD + (size_t)(g * G + j) * HD + lane_dim(dg, e, F32)] * (SM_SCALE * LOG2E)
+                       : 0.0f;
     }
   }
-  const KT* kbase = reinterpret_cast<const KT*>(p.kv.k);
-  const KT* vbase = reinterpret_cast<const KT*>(p.kv.v);
 
-  auto load_block = [&](int bi, uint4* kq, uint4* vq, bool& ok) {
-    const int pb = kv_block(p.kv, a->block_tables, b, t0 + bi * KVB, p.flags);
-    ok = pb >= 0;
-    const size_t off = kv_offset(p.kv, ok ? pb : 0, g, 0) + dg * EPL;
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const int t = it * TG + tg;
-      kq[it] = ok ? ldg16(kbase + off + (size_t)t * HD) : make_uint4(0, 0, 0, 0);
-      vq[it] = ok ? ldg16(vbase + off + (size_t)t * HD) : make_uint4(0, 0, 0, 0);
-    }
-  };
-  auto consume = [&](int bi, const uint4* kq, const uint4* vq, bool ok) {
-    if (!ok) return;
-    float sc[GMAX][IT];
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      float kf[EPL];
-      Vec16<KT>::unpack(kq[it], kf);
-      const bool valid = bi * KVB + it * TG + tg < nt;
-#pragma unroll
-      for (int j = 0; j < GMAX; ++j) {
-        float d = 0.0f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) d = fmaf(kf[e], qf[j][e], d);
-#pragma unroll
-        for (int x = LPT / 2; x > 0; x >>= 1) d += __shfl_xor_sync(0xffffffffu, d, x);
-        sc[j][it] = valid ? d : -INFINITY;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < GMAX; ++j) {
-      if (j >= G) continue;
-      float mb = sc[j][0];
-#pragma unroll
-      for (int it = 1; it < IT; ++it) mb = fmaxf(mb, sc[j][it]);
-#pragma unroll
-      for (int x = LPT; x < 32; x <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, x));
-      const float mn = fmaxf(m[j], mb);
-      const float alpha = m[j] == -INFINITY ? 0.0f : expf(m[j] - mn);
-      m[j] = mn;
-      l[j] *= alpha;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) o[j][e] *= alpha;
+  bool ok = true;
+  int j = 0;
+  for (; j < nj; ++j) {
+    const int s = j % NST;
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars[s], (j / NST) & 1, p.flags)) != 0;
+    if (!ok) break;
+    const int pb = __shfl_sync(0xffffffffu, my_pb, j);
+    if (pb >= 0) {
+      const KT* K = kst(s);
+      const KT* V = vst(s);
+      const int tok0 = (warp + NW * j) * KVB;   // first token of the block inside the chunk
+      float sc[GMAX][IT];
 #pragma unroll
       for (int it = 0; it < IT; ++it) {
-        const float pr = sc[j][it] == -INFINITY ? 0.0f : expf(sc[j][it] - mn);
-        l[j] += pr;
-        float vf[EPL];
-        Vec16<KT>::unpack(vq[it], vf);
+        const int t = it * TG + tg;
+        float kf[8];
+        lds_row8<KT>(K + t * HD, dg, kf);
+        const bool valid = tok0 + t < nt;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(pr, vf[e], o[j][e]);
+        for (int jj = 0; jj < GMAX; ++jj) {
+          float d = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d = fmaf(kf[e], qf[jj][e], d);
+          d += __shfl_xor_sync(0xffffffffu, d, 4);
+          d += __shfl_xor_sync(0xffffffffu, d, 2);
+          d += __shfl_xor_sync(0xffffffffu, d, 1);
+          sc[jj][it] = valid ? d : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < GMAX; ++jj) {
+        if (jj >= G) continue;
+        float mb = sc[jj][0];
+#pragma unroll
+        for (int it = 1; it < IT; ++it) mb = fmaxf(mb, sc[jj][it]);
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+        const float mn = fmaxf(m[jj], mb);   // finite: token 0 of every block is valid
+        const float alpha = exp2f(m[jj] - mn);   // m = -inf gives 0
+        m[jj] = mn;
+        l[jj] *= alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[jj][e] *= alpha;
+      }
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        float vf[8];
+        lds_row8<KT>(V + (it * TG + tg) * HD, dg, vf);
+#pragma unroll
+        for (int jj = 0; jj < GMAX; ++jj) {
+          if (jj >= G) continue;
+          const float pr = exp2f(sc[jj][it] - m[jj]);   // masked: exp2(-inf) = 0
+          l[jj] += pr;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[jj][e] = fmaf(pr, vf[e], o[jj][e]);
+        }
       }
     }
-  };
-
-  // two blocks in flight per warp
-  uint4 ka[IT], va[IT], kb[IT], vb[IT];
-  bool oka = false, okb = false;
-  int bi = warp;
-  if (bi < nblk) load_block(bi, ka, va, oka);
-  for (; bi < nblk; bi += 2 * NW) {
-    const int bn = bi + NW;
-    if (bn < nblk) load_block(bn, kb, vb, okb);
-    consume(bi, ka, va, oka);
-    if (bn >= nblk) break;
-    const int bn2 = bn + NW;
-    if (bn2 < nblk) load_block(bn2, ka, va, oka);
-    consume(bn, kb, vb, okb);
+    __syncwarp();   // every lane is done with stage s
+    if (j + NST < nj) {
+      fence_async_smem();   // order the reads above before the bulk copy overwrites the stage
+      issue(j + NST);
+    }
+  }
+  if (!ok) {
+    // a copy never arrived (flag set): wait, bounded, for this warp's copies still in flight
+    for (int jj = j; jj < min(nj, j + NST); ++jj) mbar_wait(&bars[jj % NST], (jj / NST) & 1, p.flags);
   }
 
-  // warp: sum l and o over the token groups (m is warp-uniform)
+  // warp: sum l and o over the 4 token rows (m is warp-uniform)
 #pragma unroll
-  for (int j = 0; j < GMAX; ++j) {
+  for (int jj = 0; jj < GMAX; ++jj) {
 #pragma unroll
-    for (int x = LPT; x < 32; x <<= 1) {
-      l[j] += __shfl_xor_sync(0xffffffffu, l[j], x);
+    for (int x = 8; x < 32; x <<= 1) {
+      l[jj] += __shfl_xor_sync(0xffffffffu, l[jj], x);
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) o[j][e] += __shfl_xor_sync(0xffffffffu, o[j][e], x);
+      for (int e = 0; e < 8; ++e) o[jj][e] += __shfl_xor_sync(0xffffffffu, o[jj][e], x);
     }
   }
   if (tg == 0) {
 #pragma unroll
-    for (int j = 0; j < GMAX; ++j) {
-      if (j >= G) continue;
+    for (int jj = 0; jj < GMAX; ++jj) {
+      if (jj >= G) continue;
       if (dg == 0) {
-        s_m[warp][j] = m[j];
-        s_l[warp][j] = l[j];
+        s_m[warp][jj] = ok ? m[jj] : -INFINITY;
+        s_l[warp][jj] = ok ? l[jj] : 0.0f;
       }
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) s_o[warp][j][dg * EPL + e] = o[j][e];
+      for (int e = 0; e < 8; ++e) s_o[warp][jj][lane_dim(dg, e, F32)] = ok ? o[jj][e] : 0.0f;
     }
   }
   __syncthreads();
   pdl_trigger();
   for (int i = tid; i < G * HD; i += AD_THREADS) {
-    const int j = i / HD, d = i - j * HD;
+    const int jj = i / HD, d = i - jj * HD;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w][j]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w][jj]);
     float L = 0.0f, O = 0.0f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float c = s_m[w][j] == -INFINITY ? 0.0f : expf(s_m[w][j] - M);
-      L = fmaf(c, s_l[w][j], L);
-      O = fmaf(c, s_o[w][j][d], O);
+      const float c = s_m[w][jj] == -INFINITY ? 0.0f : exp2f(s_m[w][jj] - M);   // a warp without tokens: 0
+      L = fmaf(c, s_l[w][jj], L);
+      O = fmaf(c, s_o[w][jj][d], O);
     }
-    const size_t hs = ((size_t)b * H + g * G + j) * p.max_splits + sp;
+    const size_t hs = ((size_t)b * H + g * G + jj) * p.max_splits + sp;
     p.part_o[hs * HD + d] = O;
     if (d == 0) {
       p.part_ml[hs * 2] = M;
@@ -197,7 +262,7 @@ __global__ void __launch_bounds__(HD) k_attn_decode_merge(const AttnDecodeParams
   for (int s = 0; s < ns; ++s) m = fmaxf(m, ml[2 * s]);
   float l = 0.0f, o = 0.0f;
   for (int s = 0; s < ns; ++s) {
-    const float w = m == -INFINITY ? 0.0f : expf(ml[2 * s] - m);
+    const float w = m == -INFINITY ? 0.0f : exp2f(ml[2 * s] - m);   // maxima are in log2 units
     l = fmaf(w, ml[2 * s + 1], l);
     o = fmaf(w, po[s * HD + d], o);
   }
@@ -363,10 +428,12 @@ int attn_decode_split_for(int B, int n_kv_heads, int max_ctx, int num_sms) {
     const int v = atoi(env);
     if (v >= KVB && v % KVB == 0) return v;
   }
-  // as long as possible (fewer partials to merge, longer streams per warp) while the grid
-  // of (sequence, KV head, chunk) CTAs is still several waves deep
-  int split = 1024;
-  while (split > 64 && (long long)B * n_kv_heads * ((max_ctx + split - 1) / split) < 8LL * num_sms) split /= 2;
+  // 512 tokens (1024 when the (sequence, KV head) pairs alone fill the GPU several times):
+  // long streams per warp and few partials to merge, short enough that uneven context
+  // lengths still balance; shorter while the grid would not give every SM two CTAs.
+  const long long pairs = (long long)B * n_kv_heads;
+  int split = pairs >= 8LL * num_sms ? 1024 : 512;
+  while (split > 64 && pairs * ((max_ctx + split - 1) / split) < 2LL * num_sms) split /= 2;
   return split;
 }
 
@@ -375,11 +442,21 @@ namespace {
 template <typename KT, typename AT>
 cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
   const int G = p.n_heads / p.kv.n_kv_heads;
+  auto kern = G == 1 ? k_attn_decode_split<KT, 1>
+              : G == 2 ? k_attn_decode_split<KT, 2>
+              : G == 3 ? k_attn_decode_split<KT, 3>
+              : G == 4 ? k_attn_decode_split<KT, 4>
+                       : k_attn_decode_split<KT, 8>;
+  static bool attr_set[9] = {};
+  if (!attr_set[G]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AttnRing<KT>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[G] = true;
+  }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t c1 = make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(AD_THREADS), 0, s, attr, pdl);
-  cudaError_t e = G == 1 ? cudaLaunchKernelEx(&c1, k_attn_decode_split<KT, 1>, p)
-                  : G <= 4 ? cudaLaunchKernelEx(&c1, k_attn_decode_split<KT, 4>, p)
-                           : cudaLaunchKernelEx(&c1, k_attn_decode_split<KT, 8>, p);
+  cudaLaunchConfig_t c1 =
+      make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(AD_THREADS), AttnRing<KT>::SMEM, s, attr, pdl);
+  cudaError_t e = cudaLaunchKernelEx(&c1, kern, p);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t c2 = make_cfg(dim3(p.B * p.n_heads), dim3(HD), 0, s, attr2, pdl);
@@ -405,7 +482,9 @@ cudaError_t prefill_t(const AttnPrefillParams& p, cudaStream_t s, bool pdl) {
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int kv_dtype, cudaStream_t s, bool pdl) {
   if (p.B <= 0) return cudaSuccess;
-  if (p.n_heads / p.kv.n_kv_heads > MAX_G || p.split <= 0 || (p.split % KVB) != 0) return cudaErrorInvalidValue;
+  if (p.n_heads / p.kv.n_kv_heads > MAX_G || p.split <= 0 || (p.split % KVB) != 0 ||
+      p.split > AD_WARPS * AD_MAX_BLOCKS_PER_WARP * KVB)
+    return cudaErrorInvalidValue;
   if (kv_dtype == DT_F32 && p.out_dtype == DT_F32) return decode_t<float, float>(p, s, pdl);
   if (kv_dtype == DT_F32 && p.out_dtype == DT_SPLIT) return decode_t<float, Split>(p, s, pdl);
   if (kv_dtype == DT_BF16 && p.out_dtype == DT_F32) return decode_t<bf16, float>(p, s, pdl);

@@ -177,6 +177,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
   set_flag(flags, FLAG_WAIT_TIMEOUT);
   return false;
 }
+// Order this thread's earlier generic-proxy shared-memory accesses before later async-proxy
+// (TMA / tensor-core) accesses of the same shared memory.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // 1-D bulk copy global -> shared (TMA engine); completes `bytes` on the mbarrier.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {

@@ -85,7 +85,6 @@ __device__ __forceinline__ float to_tf32(float x) {
   return __uint_as_float(r);
 }
 // Make this thread's generic-proxy shared-memory writes visible to the tensor core (async proxy).
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
