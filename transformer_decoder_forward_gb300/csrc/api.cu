@@ -193,6 +193,7 @@ llm_status run(llm_handle* h, const char* name, F&& f) {
 
 int pick_variant(const llm_handle* h, const LinearParams& p) {
   if (h->lin_variant != LIN_AUTO) return h->lin_variant;
+  if (p.M <= 8) return LIN_GEMV;   // a few rows: the CUDA-core weight stream has the shortest path
   if (p.M <= 256 && gemm_tc_swap_supported(p)) return LIN_TC_SWAP;
   if (p.M <= 64) return LIN_GEMV;
   if (gemm_tc_supported(p)) return LIN_TC;
@@ -283,7 +284,6 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
       ap.split = h->split; ap.max_splits = h->max_splits; ap.part_o = h->attn_po; ap.part_ml = h->attn_ml;
       ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
       RUN("attn_decode", launch_attn_decode(ap, DT_F32, h->stream, h->pdl));
-      h->launch_counter++;   // split + merge
     } else {
       AttnPrefillParams ap;
       memset(&ap, 0, sizeof(ap));

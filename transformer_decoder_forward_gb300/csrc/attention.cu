@@ -10,7 +10,8 @@
 // Decode is split-K ("flash-decoding"): CTA (sequence b, KV head g, split s)
 // scores the split's tokens for all query heads that share KV head g
 // (grouped-query attention), keeps (max, sum of exp, unnormalised output), and a
-// merge kernel rescales the splits to the common maximum. Prefill is a tiled
+// merge kernel rescales the splits to the common maximum (no merge when every
+// sequence fits one split). Prefill is a tiled
 // online softmax: CTA (64 query rows, head) walks the causal key tiles.
 //
 // Scores are q.k / sqrt(64); masked keys get -inf so exp gives exactly 0.
@@ -66,9 +67,8 @@ template <> __device__ __forceinline__ void lds_row8<bf16>(const bf16* row, int 
 // values a lane), four token rows per warp step; the lanes that score a token weight
 // its value row, so no probability is broadcast. Scores are kept in log2 units (q is
 // pre-scaled by log2(e)/sqrt(64)) so every exponential is one exp2. The 4 warps'
-// states are merged in shared memory and the chunk's (max, sum, output) goes to the
-// split-K partial buffer.
-template <typename KT, int GMAX>
+// states are merged in shared memory at the end.
+template <typename KT, typename AT, int GMAX>
 __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDecodeParams p) {
   using R = AttnRing<KT>;
   constexpr int NW = AD_WARPS, NST = R::NST;
@@ -229,6 +229,10 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
   }
   __syncthreads();
   pdl_trigger();
+  // Combine the warps. With a single chunk per sequence (max_splits == 1) the result is
+  // final; otherwise the chunk's (max, sum, output) goes to the partial buffer for the
+  // merge kernel.
+  const int ldo = (std::is_same<AT, Split>::value ? 2 : 1) * H * HD;
   for (int i = tid; i < G * HD; i += AD_THREADS) {
     const int jj = i / HD, d = i - jj * HD;
     float M = -INFINITY;
@@ -241,6 +245,10 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
       L = fmaf(c, s_l[w][jj], L);
       O = fmaf(c, s_o[w][jj][d], O);
     }
+    if (p.max_splits == 1) {
+      act_store<AT>(p.out, b, ldo, (g * G + jj) * HD + d, L > 0.0f ? O / L : 0.0f);
+      continue;
+    }
     const size_t hs = ((size_t)b * H + g * G + jj) * p.max_splits + sp;
     p.part_o[hs * HD + d] = O;
     if (d == 0) {
@@ -250,6 +258,8 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
   }
 }
 
+// Merge of a sequence's chunks (max_splits > 1): CTA = (sequence, query head), thread = dim.
+// Rescales every chunk to the common maximum (log2 units) in chunk order.
 template <typename AT>
 __global__ void __launch_bounds__(HD) k_attn_decode_merge(const AttnDecodeParams p) {
   const int bh = blockIdx.x, b = bh / p.n_heads, d = threadIdx.x;
@@ -258,18 +268,34 @@ __global__ void __launch_bounds__(HD) k_attn_decode_merge(const AttnDecodeParams
   const int ns = ctx <= 0 ? 0 : min(p.max_splits, (ctx + p.split - 1) / p.split);
   const float* ml = p.part_ml + (size_t)bh * p.max_splits * 2;
   const float* po = p.part_o + (size_t)bh * p.max_splits * HD;
-  float m = -INFINITY;
-  for (int s = 0; s < ns; ++s) m = fmaxf(m, ml[2 * s]);
-  float l = 0.0f, o = 0.0f;
-  for (int s = 0; s < ns; ++s) {
-    const float w = m == -INFINITY ? 0.0f : exp2f(ml[2 * s] - m);   // maxima are in log2 units
-    l = fmaf(w, ml[2 * s + 1], l);
-    o = fmaf(w, po[s * HD + d], o);
+  constexpr int MS = 8;   // chunks per pass, all loads of a pass issued together
+  float M = -INFINITY, L = 0.0f, O = 0.0f;
+  for (int c0 = 0; c0 < ns; c0 += MS) {
+    float mv[MS], lv[MS], ov[MS];
+#pragma unroll
+    for (int c = 0; c < MS; ++c) {
+      const bool in = c0 + c < ns;
+      mv[c] = in ? ml[2 * (c0 + c)] : -INFINITY;
+      lv[c] = in ? ml[2 * (c0 + c) + 1] : 0.0f;
+      ov[c] = in ? po[(size_t)(c0 + c) * HD + d] : 0.0f;
+    }
+    float Mn = M;
+#pragma unroll
+    for (int c = 0; c < MS; ++c) Mn = fmaxf(Mn, mv[c]);
+    const float r = M == -INFINITY ? 0.0f : exp2f(M - Mn);
+    L *= r;
+    O *= r;
+#pragma unroll
+    for (int c = 0; c < MS; ++c) {
+      const float w = mv[c] == -INFINITY ? 0.0f : exp2f(mv[c] - Mn);
+      L = fmaf(w, lv[c], L);
+      O = fmaf(w, ov[c], O);
+    }
+    M = Mn;
   }
   pdl_trigger();
-  const float r = l > 0.0f ? o / l : 0.0f;
-  const int ld = (std::is_same<AT, Split>::value ? 2 : 1) * p.n_heads * HD;
-  act_store<AT>(p.out, b, ld, (bh - b * p.n_heads) * HD + d, r);
+  const int ldo = (std::is_same<AT, Split>::value ? 2 : 1) * p.n_heads * HD;
+  act_store<AT>(p.out, b, ldo, (bh - b * p.n_heads) * HD + d, L > 0.0f ? O / L : 0.0f);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -442,11 +468,11 @@ namespace {
 template <typename KT, typename AT>
 cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
   const int G = p.n_heads / p.kv.n_kv_heads;
-  auto kern = G == 1 ? k_attn_decode_split<KT, 1>
-              : G == 2 ? k_attn_decode_split<KT, 2>
-              : G == 3 ? k_attn_decode_split<KT, 3>
-              : G == 4 ? k_attn_decode_split<KT, 4>
-                       : k_attn_decode_split<KT, 8>;
+  auto kern = G == 1 ? k_attn_decode_split<KT, AT, 1>
+              : G == 2 ? k_attn_decode_split<KT, AT, 2>
+              : G == 3 ? k_attn_decode_split<KT, AT, 3>
+              : G == 4 ? k_attn_decode_split<KT, AT, 4>
+                       : k_attn_decode_split<KT, AT, 8>;
   static bool attr_set[9] = {};
   if (!attr_set[G]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AttnRing<KT>::SMEM);
@@ -457,7 +483,7 @@ cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t c1 =
       make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(AD_THREADS), AttnRing<KT>::SMEM, s, attr, pdl);
   cudaError_t e = cudaLaunchKernelEx(&c1, kern, p);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || p.max_splits == 1) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t c2 = make_cfg(dim3(p.B * p.n_heads), dim3(HD), 0, s, attr2, pdl);
   return cudaLaunchKernelEx(&c2, k_attn_decode_merge<AT>, p);

@@ -12,9 +12,9 @@ struct AttnDecodeParams {
   int B;
   int n_heads;
   int split;                // tokens per split (multiple of 16)
-  int max_splits;           // grid.y
+  int max_splits;           // grid.y; 1: the split kernel writes `out` itself, no merge launch
   float* part_o;            // [B][H][max_splits][64]
-  float* part_ml;           // [B][H][max_splits][2]  (running max, sum of exp)
+  float* part_ml;           // [B][H][max_splits][2]  (running max in log2 units, sum of exp)
   void* out;                // [B][H*64] activations (DT_F32, or DT_SPLIT: row stride 2*H*64 bf16)
   int out_dtype;
   unsigned* flags;
