@@ -177,6 +177,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
   set_flag(flags, FLAG_WAIT_TIMEOUT);
   return false;
 }
+// Split cluster barrier (every thread of every CTA of the cluster): arrive (release) now,
+// wait (acquire) later, so work in between overlaps the other CTAs' arrival.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Order this thread's earlier generic-proxy shared-memory accesses before later async-proxy
 // (TMA / tensor-core) accesses of the same shared memory.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

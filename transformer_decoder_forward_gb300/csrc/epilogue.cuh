@@ -20,6 +20,7 @@
 namespace llm {
 
 constexpr int EPI_MAX_ROWS = 256;   // rows of one epilogue call (every projection tile fits)
+constexpr int EPI_MAX_COLS = 128;   // tile columns of one epilogue call (two 64-column sub-tiles)
 
 template <typename WT>
 __device__ __forceinline__ float bias_at(const void* b, int n) {
@@ -43,31 +44,47 @@ __device__ __forceinline__ void rope_sincos(int pos, float2 f, float* s, float* 
 }
 
 // tile: fp32 [.., ldt] in shared memory. Rows m0 .. m0+mrows-1 of the launch (mrows <=
-// EPI_MAX_ROWS), tile columns 0..ncols-1 (ncols <= 64) map to output column n0 + c (for
-// SWIGLU: gate row n0 + c for c < 32 and up row F + n0 + c - 32; output column n0 + c).
-// N = output width. Every thread of the block must call it (it synchronises the block).
+// EPI_MAX_ROWS), tile columns 0..ncols-1 (ncols = 64 or 128, n0 a multiple of 64) map to
+// output column n0 + c. SWIGLU: each 64-column sub-tile s holds 32 gate rows then the 32
+// matching up rows, output columns n0 + 32 s .. n0 + 32 s + 31. HEAD: one argmax partial
+// per 64-column sub-tile. N = output width. Every thread of the block must call it (it
+// synchronises the block).
 // WT: weight (and bias) type; activations are stored as ActOf<WT> (fp32 or a bf16 pair),
 // the KV cache in fp32.
+//
+// run_epilogue = stage + apply. A kernel whose tile rows and columns are known before its
+// accumulator is ready can call epi_stage early (with its own thread subset) and epi_apply
+// once the tile is in shared memory, so the bias, position and KV-block loads overlap the
+// contraction; a block-wide barrier must separate the two.
+
+struct EpiStaging {
+  float bias[EPI_MAX_COLS];
+  int pos[EPI_MAX_ROWS];
+  int blk[EPI_MAX_ROWS];
+};
+__device__ __forceinline__ EpiStaging& epi_staging() {
+  __shared__ EpiStaging st;   // one per CTA
+  return st;
+}
+
+// Stage the call's bias columns and (QKV) row positions / KV blocks; threads tid of nth.
 template <typename WT>
-__device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int m0, int mrows, int n0, int ncols,
-                             int N) {
-  using AT = typename ActOf<WT>::type;
-  __shared__ float s_bias[64];
-  __shared__ int s_pos[EPI_MAX_ROWS];
-  __shared__ int s_blk[EPI_MAX_ROWS];
-  const int tid = threadIdx.x, nth = blockDim.x;
-  __syncthreads();   // a previous call's readers are done with the staging arrays
-  if (tid < ncols) {
+__device__ void epi_stage(const Epilogue& e, int m0, int mrows, int n0, int ncols, int N, int tid, int nth) {
+  EpiStaging& st = epi_staging();
+  float* s_bias = st.bias;
+  int* s_pos = st.pos;
+  int* s_blk = st.blk;
+  for (int t = tid; t < ncols; t += nth) {
     float b = 0.0f;
     if (e.bias) {
       if (e.kind == EPI_SWIGLU) {
-        const int j = n0 + (tid & 31);
-        if (j < N) b = bias_at<WT>(e.bias, tid < 32 ? j : N + j);
-      } else if (n0 + tid < N) {
-        b = bias_at<WT>(e.bias, n0 + tid);
+        const int j = n0 + (t >> 6) * 32 + (t & 31);
+        if (j < N) b = bias_at<WT>(e.bias, (t & 63) < 32 ? j : N + j);
+      } else if (n0 + t < N) {
+        b = bias_at<WT>(e.bias, n0 + t);
       }
     }
-    s_bias[tid] = b;
+    s_bias[t] = b;
   }
   if (e.kind == EPI_QKV) {
     const StepArgs* a = e.args;
@@ -83,8 +100,17 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
       }
     }
   }
-  __syncthreads();
+}
 
+// The tile's outputs, from the staged values; threads tid of nth.
+template <typename WT>
+__device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0, int mrows, int n0, int ncols, int N,
+                          int tid, int nth) {
+  using AT = typename ActOf<WT>::type;
+  EpiStaging& st = epi_staging();
+  const float* s_bias = st.bias;
+  const int* s_pos = st.pos;
+  const int* s_blk = st.blk;
   switch (e.kind) {
     case EPI_STORE_F32:
     case EPI_STORE_ACT:
@@ -124,12 +150,13 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
       break;
     }
     case EPI_SWIGLU: {
-      // output column j = n0 + c (c < 32); N = d_ff
-      for (int i = tid; i < mrows * 32; i += nth) {
-        const int m = i >> 5, c = i & 31, j = n0 + c;
+      // sub-tile s, gate column c < 32: output column j = n0 + 32 s + c; N = d_ff
+      const int nout = ncols / 2;
+      for (int i = tid; i < mrows * nout; i += nth) {
+        const int m = i / nout, o = i - m * nout, c = (o >> 5) * 64 + (o & 31), j = n0 + o;
         if (j >= N) continue;
         const float g = tile[m * ldt + c] + s_bias[c];
-        const float u = tile[m * ldt + 32 + c] + s_bias[32 + c];
+        const float u = tile[m * ldt + c + 32] + s_bias[c + 32];
         act_store<AT>(e.out, m0 + m, e.ld_out, j, silu_f(g) * u);
       }
       break;
@@ -179,14 +206,16 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
           if (n < N) logits[(size_t)(m0 + m) * e.vocab + n] = tile[m * ldt + c];
         }
       }
-      // per-row argmax over this tile's columns: one warp per row
+      // per-row argmax over each 64-column sub-tile: one warp per (row, sub-tile)
       const int warp = tid >> 5, lane = tid & 31, nwarps = nth >> 5;
-      const int tile_n = n0 / ncols;
+      const int nsub = ncols / 64;
       const int B = a->B;
-      for (int m = warp; m < mrows; m += nwarps) {
+      for (int ms = warp; ms < mrows * nsub; ms += nwarps) {
+        const int m = ms / nsub, sub = ms - m * nsub;
+        const int tile_n = n0 / 64 + sub;
         float best = -INFINITY;
         int bi = 0x7fffffff;
-        for (int c = lane; c < ncols; c += 32) {
+        for (int c = sub * 64 + lane; c < sub * 64 + 64; c += 32) {
           const int n = n0 + c;
           if (n >= N) break;
           const float v = tile[m * ldt + c];
@@ -207,6 +236,16 @@ __device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int 
       break;
     }
   }
+}
+
+// Every thread of the block: stage, then apply.
+template <typename WT>
+__device__ void run_epilogue(const Epilogue& e, const float* tile, int ldt, int m0, int mrows, int n0, int ncols,
+                             int N) {
+  __syncthreads();   // a previous call's readers are done with the staging arrays
+  epi_stage<WT>(e, m0, mrows, n0, ncols, N, threadIdx.x, blockDim.x);
+  __syncthreads();
+  epi_apply<WT>(e, tile, ldt, m0, mrows, n0, ncols, N, threadIdx.x, blockDim.x);
 }
 
 }  // namespace llm

@@ -136,12 +136,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   pdl_trigger();
   if (!ok) return;
   const int mrows = min(TC_BM, p.M - m0);
-#pragma unroll 1
-  for (int sub = 0; sub < TC_BN / 64; ++sub) {
-    const int n0 = p.swiglu ? (tile_n * 2 + sub) * 32 : tile_n * TC_BN + sub * 64;
-    if (!p.swiglu && n0 >= p.N) break;
-    run_epilogue<bf16>(p.epi, ot + sub * 64, OT_LD, m0, mrows, n0, 64, p.N);
-  }
+  run_epilogue<bf16>(p.epi, ot, OT_LD, m0, mrows, p.swiglu ? tile_n * 64 : tile_n * TC_BN, TC_BN, p.N);
 }
 
 }  // namespace

@@ -39,7 +39,7 @@ namespace {
 constexpr int SW_THREADS = 192;
 constexpr int SW_ROWS = 128;                 // weight rows per tile (MMA M)
 constexpr int SW_A_BYTES = SW_ROWS * 128;    // one 128-byte K slice of 128 weight rows
-constexpr int SW_OT_LD = SW_ROWS + 1;
+constexpr int SW_OT_LD = SW_ROWS + 4;        // output-tile row stride (floats): 16-byte rows
 constexpr int SW_MAX_KS = 8;                 // cluster size limit (portable)
 
 template <int NT, bool TF32>
@@ -220,10 +220,21 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
   }
 
   pdl_wait();   // every thread writes outputs in the epilogue: all of them pass the dependency wait
+  // rows whose epilogue this CTA runs: all of them, or its rank's slice of the split-K sum
+  int r0 = 0, r1 = M;
+  if (ks_total > 1) {
+    const int rank = (int)cg::this_cluster().block_rank();
+    const int rp = (M + ks_total - 1) / ks_total;
+    r0 = min(M, rank * rp);
+    r1 = min(M, r0 + rp);
+  }
+  const int n0 = p.swiglu ? tile * 64 : tile * SW_ROWS;
   // ---- accumulator -> shared memory, transposed to [token][weight row]
   bool ok = true;
   float* ot = reinterpret_cast<float*>(base);
   if (warp >= 2) {
+    // stage the epilogue's bias / positions / KV blocks while the MMAs run
+    epi_stage<WT>(p.epi, r0, r1 - r0, n0, SW_ROWS, p.N, threadIdx.x - 64, SW_THREADS - 64);
     ok = mbar_wait(done, 0, flags);
     if (!ok) ok = mbar_wait(done, 0, flags);
     tc_fence_after();
@@ -231,14 +242,20 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;          // weight row inside the tile
     if (ok) {
+      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < NT; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+      for (int c0 = 0; c0 < NT; c0 += 64) {   // two 32-column loads in flight per wait
+        uint32_t r[32], r2[32];
+        tmem_ld32(ta + (uint32_t)c0, r);
+        if (c0 + 32 < NT) tmem_ld32(ta + (uint32_t)(c0 + 32), r2);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (c0 + j < NT) ot[(c0 + j) * SW_OT_LD + row] = __uint_as_float(r[j]);
+        if (c0 + 32 < NT) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ot[(c0 + 32 + j) * SW_OT_LD + row] = __uint_as_float(r2[j]);
+        }
       }
     }
   }
@@ -258,41 +275,51 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
     return;
   }
 
-  auto epilogue = [&](const float* tl, int r0, int nrows) {
-#pragma unroll 1
-    for (int sub = 0; sub < SW_ROWS / 64; ++sub) {
-      const int n0 = p.swiglu ? (tile * 2 + sub) * 32 : tile * SW_ROWS + sub * 64;
-      if (!p.swiglu && n0 >= p.N) break;
-      run_epilogue<WT>(p.epi, tl + sub * 64, SW_OT_LD, r0, nrows, n0, 64, p.N);
-    }
-  };
+  // one epilogue over the tile's 128 columns (two 64-column sub-tiles), staged above
   if (ks_total == 1) {
-    epilogue(ot, 0, M);
+    epi_apply<WT>(p.epi, ot, SW_OT_LD, 0, M, n0, SW_ROWS, p.N, threadIdx.x, SW_THREADS);
     return;
   }
   // ---- split-K: rank r sums rows [r*rp, (r+1)*rp) of all ranks' partial tiles, in rank order
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  const int rank = (int)cluster.block_rank();
-  const int rp = (M + ks_total - 1) / ks_total;
-  const int r0 = min(M, rank * rp), r1 = min(M, r0 + rp);
   float* red = ot + (size_t)NT * SW_OT_LD;
   const float* src[SW_MAX_KS];
 #pragma unroll
   for (int j = 0; j < SW_MAX_KS; ++j) src[j] = cluster.map_shared_rank(ot, j < ks_total ? j : 0);
-  for (int i = threadIdx.x; i < (r1 - r0) * SW_ROWS; i += SW_THREADS) {
-    const int m = r0 + i / SW_ROWS, c = i % SW_ROWS;
-    float v[SW_MAX_KS];
+  constexpr int C4 = SW_ROWS / 4;   // 16-byte reads of the peers' tiles
+  constexpr int RU = 2;              // row groups per thread per round: 2 x ks reads in flight
+  const int nwork = (r1 - r0) * C4;
+  for (int i0 = threadIdx.x; i0 < nwork; i0 += RU * SW_THREADS) {
+    float4 v[RU][SW_MAX_KS];
 #pragma unroll
-    for (int j = 0; j < SW_MAX_KS; ++j) v[j] = j < ks_total ? src[j][m * SW_OT_LD + c] : 0.0f;
-    float s = 0.0f;
+    for (int u = 0; u < RU; ++u) {
+      const int i = i0 + u * SW_THREADS;
+      const int m = r0 + i / C4, c = (i % C4) * 4;
 #pragma unroll
-    for (int j = 0; j < SW_MAX_KS; ++j) s += v[j];
-    red[(m - r0) * SW_OT_LD + c] = s;
+      for (int j = 0; j < SW_MAX_KS; ++j)
+        v[u][j] = (i < nwork && j < ks_total) ? *reinterpret_cast<const float4*>(src[j] + m * SW_OT_LD + c)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      const int i = i0 + u * SW_THREADS;
+      if (i >= nwork) break;
+      const int m = r0 + i / C4, c = (i % C4) * 4;
+      float4 sum = v[u][0];
+#pragma unroll
+      for (int j = 1; j < SW_MAX_KS; ++j) {
+        sum.x += v[u][j].x; sum.y += v[u][j].y; sum.z += v[u][j].z; sum.w += v[u][j].w;
+      }
+      *reinterpret_cast<float4*>(red + (m - r0) * SW_OT_LD + c) = sum;
+    }
   }
-  cluster.sync();
+  // the peers may still read this CTA's tile: signal that this CTA is done reading theirs,
+  // run the epilogue, and only wait for the peers before exiting
+  cluster_arrive();
   __syncthreads();
-  if (r1 > r0) epilogue(red, r0, r1 - r0);
+  if (r1 > r0) epi_apply<WT>(p.epi, red, SW_OT_LD, r0, r1 - r0, n0, SW_ROWS, p.N, threadIdx.x, SW_THREADS);
+  cluster_wait();
 }
 
 template <int NT, bool TF32>
