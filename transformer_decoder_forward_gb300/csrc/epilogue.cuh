@@ -111,10 +111,31 @@ __device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0,
   const float* s_bias = st.bias;
   const int* s_pos = st.pos;
   const int* s_blk = st.blk;
+  // 4-wide path: 4 consecutive columns per thread step (vector loads and stores)
+  const bool vec = (N % 4) == 0;
   switch (e.kind) {
     case EPI_STORE_F32:
     case EPI_STORE_ACT:
     case EPI_GELU: {
+      const bool v4 = vec && (e.kind == EPI_STORE_F32 ? (e.ld_out % 4) == 0 : (e.ld_out % 8) == 0);
+      if (v4) {
+        const int c4n = ncols / 4;
+        for (int i = tid; i < mrows * c4n; i += nth) {
+          const int m = i / c4n, c = (i - m * c4n) * 4, n = n0 + c;
+          if (n >= N) continue;
+          float y[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            y[j] = tile[m * ldt + c + j] + s_bias[c + j];
+            if (e.kind == EPI_GELU) y[j] = gelu_tanh_clamped(y[j]);
+          }
+          if (e.kind == EPI_STORE_F32)
+            act_store4<float>(e.out, m0 + m, e.ld_out, n, y);
+          else
+            act_store4<AT>(e.out, m0 + m, e.ld_out, n, y);
+        }
+        break;
+      }
       for (int i = tid; i < mrows * ncols; i += nth) {
         const int m = i / ncols, c = i - m * ncols, n = n0 + c;
         if (n >= N) continue;
@@ -125,6 +146,34 @@ __device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0,
       break;
     }
     case EPI_RESID: {
+      if (vec && (e.ld_resid % 4) == 0) {
+        // residual read-modify-write, 16 bytes a step: a batch of loads, then the stores
+        constexpr int RB = 4;
+        const int c4n = ncols / 4, total = mrows * c4n;
+        for (int i0 = 0; i0 < total; i0 += RB * nth) {
+          float4 hv[RB];
+          float4* ad[RB];
+          bool ok[RB];
+#pragma unroll
+          for (int j = 0; j < RB; ++j) {
+            const int i = i0 + j * nth + tid;
+            const int m = i / c4n, c = (i - m * c4n) * 4;
+            ok[j] = i < total && n0 + c < N;
+            ad[j] = reinterpret_cast<float4*>(e.resid + (size_t)(m0 + m) * e.ld_resid + n0 + c);
+            hv[j] = ok[j] ? *ad[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < RB; ++j) {
+            const int i = i0 + j * nth + tid;
+            const int m = i / c4n, c = (i - m * c4n) * 4;
+            if (!ok[j]) continue;
+            const float* t = tile + m * ldt + c;
+            *ad[j] = make_float4(hv[j].x + t[0] + s_bias[c], hv[j].y + t[1] + s_bias[c + 1],
+                                 hv[j].z + t[2] + s_bias[c + 2], hv[j].w + t[3] + s_bias[c + 3]);
+          }
+        }
+        break;
+      }
       // residual read-modify-write: issue a batch of loads, then the stores
       constexpr int RB = 8;
       const int total = mrows * ncols;
@@ -152,6 +201,22 @@ __device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0,
     case EPI_SWIGLU: {
       // sub-tile s, gate column c < 32: output column j = n0 + 32 s + c; N = d_ff
       const int nout = ncols / 2;
+      if (vec && (e.ld_out % 8) == 0) {
+        const int o4n = nout / 4;
+        for (int i = tid; i < mrows * o4n; i += nth) {
+          const int m = i / o4n, o = (i - m * o4n) * 4, c = (o >> 5) * 64 + (o & 31), j = n0 + o;
+          if (j >= N) continue;
+          float y[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float g = tile[m * ldt + c + t] + s_bias[c + t];
+            const float u = tile[m * ldt + c + 32 + t] + s_bias[c + 32 + t];
+            y[t] = silu_f(g) * u;
+          }
+          act_store4<AT>(e.out, m0 + m, e.ld_out, j, y);
+        }
+        break;
+      }
       for (int i = tid; i < mrows * nout; i += nth) {
         const int m = i / nout, o = i - m * nout, c = (o >> 5) * 64 + (o & 31), j = n0 + o;
         if (j >= N) continue;
@@ -162,38 +227,47 @@ __device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0,
       break;
     }
     case EPI_QKV: {
+      // unit = (row, head of the tile, g): dims 4g..4g+3 and 32+4g..32+4g+3 of the head, so a
+      // RoPE pair (d, d + 32) stays in one thread; N is a multiple of 64 (whole heads)
       const int H = e.n_heads, Hkv = e.kv.n_kv_heads;
-      for (int i = tid; i < mrows * ncols; i += nth) {
-        const int m = i / ncols, c = i - m * ncols, n = n0 + c;
+      const int units_row = (ncols / HD) * 8;
+      for (int i = tid; i < mrows * units_row; i += nth) {
+        const int m = i / units_row, u = i - m * units_row;
+        const int c = (u >> 3) * HD + (u & 7) * 4;   // tile column of dim d = 4g
+        const int n = n0 + c;
         if (n >= N) continue;
         const int hh = n / HD, d = n - hh * HD;
         const int row = m0 + m;
         const int pos = s_pos[m];
         const bool is_q = hh < H, is_k = !is_q && hh < H + Hkv;
-        float v0 = tile[m * ldt + c] + s_bias[c];
-        float v1 = 0.0f;
+        float v0[4], v1[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          v0[t] = tile[m * ldt + c + t] + s_bias[c + t];
+          v1[t] = tile[m * ldt + c + HD / 2 + t] + s_bias[c + HD / 2 + t];
+        }
         if (e.rope && (is_q || is_k)) {
-          if (d >= HD / 2) continue;                  // the partner thread writes this element
-          v1 = tile[m * ldt + c + HD / 2] + s_bias[c + HD / 2];
-          float s, co;
-          rope_sincos(pos, e.rope_tab[d], &s, &co);
-          const float r0 = v0 * co - v1 * s;
-          const float r1 = v1 * co + v0 * s;
-          v0 = r0;
-          v1 = r1;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            float sn, co;
+            rope_sincos(pos, e.rope_tab[d + t], &sn, &co);
+            const float r0 = v0[t] * co - v1[t] * sn;
+            const float r1 = v1[t] * co + v0[t] * sn;
+            v0[t] = r0;
+            v1[t] = r1;
+          }
         }
+        float* dst;
         if (is_q) {
-          float* q = e.q_out + (size_t)row * H * HD + hh * HD;
-          q[d] = v0;
-          if (e.rope) q[d + HD / 2] = v1;
-          continue;
+          dst = e.q_out + (size_t)row * H * HD + hh * HD;
+        } else {
+          const int pb = s_blk[m];
+          if (pb < 0) continue;
+          const int g = is_k ? hh - H : hh - H - Hkv;
+          dst = reinterpret_cast<float*>(is_k ? e.kv.k : e.kv.v) + kv_offset(e.kv, pb, g, pos & (KVB - 1));
         }
-        const int pb = s_blk[m];
-        if (pb < 0) continue;
-        const int g = is_k ? hh - H : hh - H - Hkv;
-        float* dst = reinterpret_cast<float*>(is_k ? e.kv.k : e.kv.v) + kv_offset(e.kv, pb, g, pos & (KVB - 1));
-        dst[d] = v0;
-        if (e.rope && is_k) dst[d + HD / 2] = v1;
+        *reinterpret_cast<float4*>(dst + d) = make_float4(v0[0], v0[1], v0[2], v0[3]);
+        *reinterpret_cast<float4*>(dst + d + HD / 2) = make_float4(v1[0], v1[1], v1[2], v1[3]);
       }
       break;
     }

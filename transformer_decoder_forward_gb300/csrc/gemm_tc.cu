@@ -14,8 +14,8 @@
 //     accumulators in tensor memory, so the product carries the activations'
 //     full pair accuracy; tcgen05.commit releases each stage once the MMAs that
 //     read it finish, and marks the accumulator full after the tile's last one.
-//   - warps 2-5: read a full accumulator with tcgen05.ld (warp w owns TMEM lanes
-//     32(w%4).. = tile rows), hand it back to the MMA warp at once, stage it as
+//   - warps 2-9: read a full accumulator with tcgen05.ld (warp w owns TMEM lanes
+//     32(w%4).. = tile rows, half of the columns), hand it back to the MMA warp at once, stage it as
 //     an fp32 tile in shared memory and run the shared epilogue (bias, GELU /
 //     SwiGLU, RoPE + kv_write, residual add) while the MMA warp already fills the
 //     other accumulator with the next tile.
@@ -31,8 +31,9 @@ namespace llm {
 namespace {
 
 constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 3;
-constexpr int TC_THREADS = 192;                 // producer warp, MMA warp, 4 epilogue warps
-constexpr int TC_EPI_THREADS = 128;
+constexpr int TC_THREADS = 320;                 // producer warp, MMA warp, 8 epilogue warps
+constexpr int TC_EPI_THREADS = 256;
+constexpr int TC_EPI_WARPS = TC_EPI_THREADS / 32;
 constexpr int A_STAGE = TC_BM * TC_BK * 2;      // bytes
 constexpr int B_STAGE = TC_BN * TC_BK * 2;
 constexpr int STAGE = 2 * A_STAGE + B_STAGE;    // [x_hi][x_lo][W]
@@ -42,8 +43,8 @@ constexpr int TC_ACC = 2;                       // accumulators in TMEM
 constexpr uint32_t TC_TMEM_COLS = TC_ACC * TC_BN;
 constexpr size_t TC_SMEM = 1024 + (size_t)TC_STAGES * STAGE + OT_BYTES + 256;
 
-// Barrier among the four epilogue warps only (named barrier 1), plain or with an AND of a
-// predicate so that all four warps take the same branch after it.
+// Barrier among the epilogue warps only (named barrier 1), plain or with an AND of a
+// predicate so that all of them take the same branch after it.
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI_THREADS) : "memory"); }
 __device__ __forceinline__ bool epi_bar_all(bool v) {
   int r;
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int a = 0; a < TC_ACC; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);   // lane 0 of each epilogue warp
+      mbar_init(&acc_empty[a], TC_EPI_WARPS);   // lane 0 of each epilogue warp
     }
     mbar_init(drain, 1);
     mbar_fence_init();
@@ -169,9 +170,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ---- epilogue warps
-    const int et = threadIdx.x - 64;   // 0..127
+    // ---- epilogue warps: two per TMEM lane quadrant, each reading half of the columns
+    const int et = threadIdx.x - 64;   // 0..255
     const int q = warp & 3;            // TMEM lane quadrant = tile rows 32q..32q+31
+    const int half = (warp - 2) >> 2;  // columns 64 half .. 64 half + 63
     const int row = q * 32 + lane;
     pdl_wait();
     int lt = 0;
@@ -183,11 +185,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int a = lt % TC_ACC;
       epi_stage<bf16>(p.epi, m0, mrows, n0, TC_BN, p.N, et, TC_EPI_THREADS);
       const bool ok = mbar_wait(&acc_full[a], (lt / TC_ACC) & 1, flags);
-      if (!epi_bar_all(ok)) break;   // the four warps leave together
+      if (!epi_bar_all(ok)) break;   // the epilogue warps leave together
       tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * TC_BN);
-#pragma unroll 1
-      for (int c0 = 0; c0 < TC_BN; c0 += 64) {   // two 32-column loads in flight per wait
+      {
+        const int c0 = half * 64;   // two 32-column loads in flight
         uint32_t r[32], r2[32];
         tmem_ld32(ta + (uint32_t)c0, r);
         tmem_ld32(ta + (uint32_t)(c0 + 32), r2);
