@@ -289,7 +289,10 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
       memset(&ap, 0, sizeof(ap));
       ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.items = h->d_items; ap.n_items = n_items;
       ap.n_heads = H; ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
-      RUN("attn_prefill", launch_attn_prefill(ap, DT_F32, h->stream, h->pdl));
+      // bf16-weight models: tensor cores on bf16 (hi, lo) splits (about 16 bits of every
+      // operand); fp32-weight models keep fp32 FMA so their attention stays at fp32 accuracy
+      if (h->wdt == DT_BF16) RUN("attn_prefill", launch_attn_prefill_tc(ap, DT_F32, h->stream, h->pdl));
+      else RUN("attn_prefill", launch_attn_prefill(ap, DT_F32, h->stream, h->pdl));
     }
 
     // out projection + residual
@@ -573,6 +576,7 @@ llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* leng
     if ((L + KVB - 1) / KVB > c.max_blocks_per_seq) return fail(LLM_ERR_OUT_OF_RANGE, "prompt needs more blocks than max_blocks_per_seq");
   }
   begin_call(h);
+  const int item_rows = h->wdt == DT_BF16 ? 128 : 64;   // query rows per prefill-attention CTA
   size_t tok_off = 0;
   int s0 = 0;
   while (s0 < B) {
@@ -585,7 +589,7 @@ llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* leng
     for (int b = s0; b < s1; ++b) {
       const int L = lengths[b];
       for (int t = 0; t < L; ++t) { row_pos[r + t] = t; row_seq[r + t] = b; }
-      for (int q0 = 0; q0 < L; q0 += 64) items.push_back(make_int4(b, q0, r + q0, L));
+      for (int q0 = 0; q0 < L; q0 += item_rows) items.push_back(make_int4(b, q0, r + q0, L));
       r += L;
       last_row[b - s0] = r - 1;
     }

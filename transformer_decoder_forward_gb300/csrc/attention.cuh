@@ -40,5 +40,7 @@ int attn_decode_split_for(int B, int n_kv_heads, int max_ctx, int num_sms);
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int kv_dtype, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_prefill(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl);
+// Tensor-core prefill attention: items of up to 128 query rows, fp32 KV pool.
+cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl);
 
 }  // namespace llm
