@@ -4,18 +4,18 @@
 // place ("rvllm-metal", sections "What the kernels do" and "What's basic about it":
 // scores, -inf mask, softmax, probs @ V, without gathering the context into a
 // contiguous copy). CTA = (128 query rows of one sequence, query head h); one thread
-// per query row. For each block of 128 keys:
+// per query row; two CTAs per SM overlap each other's loads. For each block of 64 keys:
 //   1. the threads load the keys' K and V rows (fp32) from their paged blocks and
 //      split every value v into bf16 hi = bf16(v), lo = bf16(v - hi), written straight
 //      into the 128-byte-swizzled K-major layout the MMA reads (V transposed to
 //      dims x keys);
 //   2. one thread issues S = Q.K^T as hi.hi + hi.lo + lo.hi (tcgen05.mma, M = 128
-//      queries, N = 128 keys, fp32 accumulate in TMEM), so the scores carry about
+//      queries, N = 64 keys, fp32 accumulate in TMEM), so the scores carry about
 //      16 bits of the operands instead of bf16's 8;
 //   3. each thread reads its score row from TMEM, applies the scale and the causal
 //      mask, and updates an online softmax (running max and sum, log2 units); the
 //      probabilities are split the same way into the A operand of P.V;
-//   4. P.V (M = 128, N = 64, K = 128) goes to a second TMEM accumulator and each
+//   4. P.V (M = 128, N = 64, K = 64) goes to a second TMEM accumulator and each
 //      thread folds it into its output row: o = o * exp2(m_old - m_new) + P.V.
 // The output row is o / sum, stored as the activation dtype of the model.
 // Every wait is bounded (FLAG_WAIT_TIMEOUT) and the tensor memory is always freed.
@@ -29,17 +29,19 @@ namespace llm {
 namespace {
 
 constexpr int PT_Q = 128;          // query rows per CTA (MMA M)
-constexpr int PT_K = 128;          // keys per step
+constexpr int PT_K = 64;           // keys per step
 constexpr int PT_THREADS = 128;
 constexpr int PT_TILE = 128 * 128;   // bytes of a 128-row x 64-bf16 swizzled tile
-// shared-memory layout (bytes from a 1024-aligned base)
+constexpr int PT_HALF = 64 * 128;    // bytes of a 64-row x 64-bf16 swizzled tile
+// shared-memory layout (bytes from a 1024-aligned base): Q (128 queries x 64 dims),
+// K (64 keys x 64 dims), V transposed (64 dims x 64 keys), P (128 queries x 64 keys)
 constexpr int OFF_QHI = 0, OFF_QLO = OFF_QHI + PT_TILE;
-constexpr int OFF_KHI = OFF_QLO + PT_TILE, OFF_KLO = OFF_KHI + PT_TILE;
-constexpr int OFF_VHI = OFF_KLO + PT_TILE, OFF_VLO = OFF_VHI + PT_TILE;   // 2 atoms of 64 dims x 64 keys
-constexpr int OFF_PHI = OFF_VLO + PT_TILE, OFF_PLO = OFF_PHI + 2 * PT_TILE;   // 2 atoms of 128 rows x 64 keys
-constexpr int OFF_BAR = OFF_PLO + 2 * PT_TILE;
+constexpr int OFF_KHI = OFF_QLO + PT_TILE, OFF_KLO = OFF_KHI + PT_HALF;
+constexpr int OFF_VHI = OFF_KLO + PT_HALF, OFF_VLO = OFF_VHI + PT_HALF;
+constexpr int OFF_PHI = OFF_VLO + PT_HALF, OFF_PLO = OFF_PHI + PT_TILE;
+constexpr int OFF_BAR = OFF_PLO + PT_TILE;
 constexpr size_t PT_SMEM = 1024 + OFF_BAR + 64;
-constexpr uint32_t PT_TMEM_COLS = 256;   // S: columns 0..127, P.V: 128..191
+constexpr uint32_t PT_TMEM_COLS = 128;   // S: columns 0..63, P.V: 64..127
 constexpr float SCALE_LOG2 = 0.125f * 1.4426950408889634f;   // log2(e) / sqrt(64)
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a K-major tile with 128-byte rows and
@@ -69,7 +71,7 @@ __device__ __forceinline__ void load_row64(const float* src, float* v) {
 }
 
 template <typename AT>
-__global__ void __launch_bounds__(PT_THREADS, 1) k_attn_prefill_tc(const AttnPrefillParams p) {
+__global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPrefillParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* barS = reinterpret_cast<uint64_t*>(base + OFF_BAR);
@@ -132,43 +134,40 @@ __global__ void __launch_bounds__(PT_THREADS, 1) k_attn_prefill_tc(const AttnPre
   bool ok = true;
 
   for (int kb = 0; kb < nkb && ok; ++kb) {
-    // ---- K and V of keys kb*128 + r
+    // ---- K and V of key kb*64 + (r mod 64): this thread converts dims 32h .. 32h + 31, h = r / 64
     {
-      const int t = kb * PT_K + r;
-      float v[64];
+      const int kr = r & 63, hf = r >> 6;
+      const int t = kb * PT_K + kr;
+      float v[32];
       int pb = -1;
       if (t < kend) pb = kv_block(p.kv, a->block_tables, seq, t, flags);
-      const size_t off = pb >= 0 ? kv_offset(p.kv, pb, g, t & (KVB - 1)) : 0;
-      if (pb >= 0) {
-        load_row64(kpool + off, v);
-      } else {
+      const size_t off = (pb >= 0 ? kv_offset(p.kv, pb, g, t & (KVB - 1)) : 0) + hf * 32;
+      auto load32 = [&](const float* src) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = 0.0f;
-      }
+        for (int i = 0; i < 8; ++i) {
+          const float4 x = pb >= 0 ? *reinterpret_cast<const float4*>(src + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+        }
+      };
+      load32(kpool + off);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint4 hi, lo;
         split8(v + 8 * c, hi, lo);
-        *reinterpret_cast<uint4*>(base + OFF_KHI + sw_off(r, c)) = hi;
-        *reinterpret_cast<uint4*>(base + OFF_KLO + sw_off(r, c)) = lo;
+        *reinterpret_cast<uint4*>(base + OFF_KHI + sw_off(kr, 4 * hf + c)) = hi;
+        *reinterpret_cast<uint4*>(base + OFF_KLO + sw_off(kr, 4 * hf + c)) = lo;
       }
-      if (pb >= 0) {
-        load_row64(vpool + off, v);
-      } else {
+      load32(vpool + off);
+      // V transposed: B operand of P.V is dims (rows) x keys (K)
+      const int ck = kr >> 3, bk = (kr & 7) * 2;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = 0.0f;
-      }
-      // V transposed: B operand of P.V is dims (rows) x keys (K); key r sits in atom r / 64
-      unsigned char* vhi = base + OFF_VHI + (r >> 6) * (64 * 128);
-      unsigned char* vlo = base + OFF_VLO + (r >> 6) * (64 * 128);
-      const int kk = r & 63, ck = kk >> 3, bk = (kk & 7) * 2;
-#pragma unroll
-      for (int d = 0; d < HD; ++d) {
-        const bf16 hi = __float2bfloat16_rn(v[d]);
-        const bf16 lo = __float2bfloat16_rn(v[d] - __bfloat162float(hi));
+      for (int i = 0; i < 32; ++i) {
+        const int d = hf * 32 + i;
+        const bf16 hi = __float2bfloat16_rn(v[i]);
+        const bf16 lo = __float2bfloat16_rn(v[i] - __bfloat162float(hi));
         const uint32_t o2 = sw_off(d, ck) + bk;
-        *reinterpret_cast<bf16*>(vhi + o2) = hi;
-        *reinterpret_cast<bf16*>(vlo + o2) = lo;
+        *reinterpret_cast<bf16*>(base + OFF_VHI + o2) = hi;
+        *reinterpret_cast<bf16*>(base + OFF_VLO + o2) = lo;
       }
     }
     fence_async_smem();
@@ -221,14 +220,14 @@ __global__ void __launch_bounds__(PT_THREADS, 1) k_attn_prefill_tc(const AttnPre
         pr[j] = (t <= qpos && t < kend) ? exp2f(__uint_as_float(s[j]) * SCALE_LOG2 - m_new) : 0.0f;
         lsum += pr[j];
       }
-      // P row r, keys c0..c0+31: atom (c0 / 64), chunks ((c0 % 64) / 8) ..
-      unsigned char* phi = base + OFF_PHI + (c0 >> 6) * PT_TILE;
-      unsigned char* plo = base + OFF_PLO + (c0 >> 6) * PT_TILE;
+      // P row r, keys c0..c0+31: chunks c0 / 8 ..
+      unsigned char* phi = base + OFF_PHI;
+      unsigned char* plo = base + OFF_PLO;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint4 hi, lo;
         split8(pr + 8 * cc, hi, lo);
-        const int c = ((c0 & 63) >> 3) + cc;
+        const int c = (c0 >> 3) + cc;
         *reinterpret_cast<uint4*>(phi + sw_off(r, c)) = hi;
         *reinterpret_cast<uint4*>(plo + sw_off(r, c)) = lo;
       }
@@ -242,12 +241,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1) k_attn_prefill_tc(const AttnPre
       const uint32_t dO = tmem + (uint32_t)PT_K;
 #pragma unroll
       for (int ks = 0; ks < PT_K / 16; ++ks) {
-        const int atom = ks >> 2;
-        const uint64_t o2 = (uint64_t)((ks & 3) * 2);
-        const uint64_t dp = sw128_desc(base + OFF_PHI + atom * PT_TILE) + o2;
-        const uint64_t dpl = sw128_desc(base + OFF_PLO + atom * PT_TILE) + o2;
-        const uint64_t dv = sw128_desc(base + OFF_VHI + atom * (64 * 128)) + o2;
-        const uint64_t dvl = sw128_desc(base + OFF_VLO + atom * (64 * 128)) + o2;
+        const uint64_t o2 = (uint64_t)(ks * 2);
+        const uint64_t dp = sw128_desc(base + OFF_PHI) + o2;
+        const uint64_t dpl = sw128_desc(base + OFF_PLO) + o2;
+        const uint64_t dv = sw128_desc(base + OFF_VHI) + o2;
+        const uint64_t dvl = sw128_desc(base + OFF_VLO) + o2;
         tc_mma(dO, dp, dv, idO, ks > 0 ? 1u : 0u);
         tc_mma(dO, dp, dvl, idO, 1u);
         tc_mma(dO, dpl, dv, idO, 1u);
