@@ -200,16 +200,20 @@ int pick_variant(const llm_handle* h, const LinearParams& p) {
   return LIN_SIMT;
 }
 
-llm_status linear(llm_handle* h, const char* tag, LinearParams p) {
-  int v = pick_variant(h, p);
-  if (v == LIN_TC_SWAP && !gemm_tc_swap_supported(p)) v = gemm_tc_supported(p) ? LIN_TC : LIN_SIMT;
-  if (v == LIN_TC && !gemm_tc_supported(p)) v = LIN_SIMT;
+llm_status linear_v(llm_handle* h, const char* tag, const LinearParams& p, int v) {
   std::string name = std::string(v == LIN_GEMV ? "gemv_" : v == LIN_TC ? "gemm_tc_" : v == LIN_TC_SWAP ? "gemm_tcs_" : "gemm_simt_") + tag;
   if (v == LIN_GEMV) RUN(name.c_str(), launch_gemv(p, h->num_sms, h->stream, h->pdl));
   else if (v == LIN_TC) RUN(name.c_str(), launch_gemm_tc(p, h->num_sms, h->stream, h->pdl));
   else if (v == LIN_TC_SWAP) RUN(name.c_str(), launch_gemm_tc_swap(p, h->num_sms, h->stream, h->pdl));
   else RUN(name.c_str(), launch_gemm_simt(p, h->stream, h->pdl));
   return LLM_OK;
+}
+
+llm_status linear(llm_handle* h, const char* tag, LinearParams p) {
+  int v = pick_variant(h, p);
+  if (v == LIN_TC_SWAP && !gemm_tc_swap_supported(p)) v = gemm_tc_supported(p) ? LIN_TC : LIN_SIMT;
+  if (v == LIN_TC && !gemm_tc_supported(p)) v = LIN_SIMT;
+  return linear_v(h, tag, p, v);
 }
 
 KVLayer kv_layer(const llm_handle* h, int l) {
@@ -232,11 +236,28 @@ Epilogue base_epi(const llm_handle* h) {
   return e;
 }
 
-// y = Norm(h) . W^T: the norm kernel writes xn (activation storage), then the projection.
+// y = Norm(h) . W^T. Where the chosen projection is the GEMV, it normalises its own input from
+// the residual stream; otherwise the norm kernel writes xn (activation storage) first.
 llm_status norm_linear(llm_handle* h, const char* tag, LinearParams p, const void* g, const void* b,
                        bool last_row) {
   const llm_config& c = h->cfg;
   const bool gpt2 = c.arch == LLM_ARCH_GPT2;
+  if (!last_row) {
+    LinearParams f = p;
+    f.xnorm = 1;
+    f.X = h->h;
+    f.ldx = c.d_model;
+    f.xdt = DT_F32;
+    f.norm_g = g;
+    f.norm_b = gpt2 ? b : nullptr;
+    f.norm_eps = c.norm_eps;
+    f.norm_ln = gpt2 ? 1 : 0;
+    LinearParams plain = p;
+    plain.X = h->xn;
+    plain.ldx = h->act_mul * c.d_model;
+    const int v = pick_variant(h, plain);
+    if (v == LIN_GEMV && gemv_norm_supported(f)) return linear_v(h, tag, f, v);
+  }
   NormParams np{h->h, g, gpt2 ? b : nullptr, h->xn, h->d_args, p.M, c.d_model, gpt2 ? 1 : 0, last_row ? 1 : 0,
                 c.norm_eps};
   RUN("norm", launch_norm(np, h->wdt, h->adt, h->stream, h->pdl));

@@ -125,6 +125,47 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Row statistics of a LayerNorm / RMSNorm over one fp32 row x[0..d) by one warp (d a
+// multiple of 4, d <= 2048): mean (0 for RMSNorm) and rstd = 1 / sqrt(var + eps), var the
+// biased variance about the mean (RMSNorm: mean of squares). Every projection that
+// normalises its own input and the stand-alone norm kernel use this one routine, so both
+// give bit-identical normalised rows. The row is left in v (16 float4 a lane).
+constexpr int ROW_NV = 16;
+__device__ __forceinline__ void warp_row_stats(const float* x, int d, bool layer_norm, float eps, float4 (&v)[ROW_NV],
+                                               float& mean, float& rstd) {
+  const int lane = threadIdx.x & 31;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  const int d4 = d >> 2;
+  float s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < ROW_NV; ++j) {
+    const int i = lane + 32 * j;
+    v[j] = i < d4 ? x4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+  }
+  mean = layer_norm ? warp_sum(s) / d : 0.0f;
+  float q = 0.0f;
+#pragma unroll
+  for (int j = 0; j < ROW_NV; ++j) {
+    if (lane + 32 * j < d4) {
+      const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, e = v[j].w - mean;
+      q += (a * a + b * b) + (c * c + e * e);
+    }
+  }
+  rstd = 1.0f / sqrtf(warp_sum(q) / d + eps);
+}
+
+// One normalised element, with the arithmetic pinned (every kernel that normalises uses it,
+// so fused and stand-alone norms agree bit for bit).
+__device__ __forceinline__ float norm_apply(float x, float mean, float rstd, float g, float b) {
+  return fmaf((x - mean) * rstd, g, b);
+}
+// v as a bf16 pair reads it back: bf16(v) + bf16(v - bf16(v)).
+__device__ __forceinline__ float pair_round(float v) {
+  const float hi = __bfloat162float(__float2bfloat16_rn(v));
+  return hi + __bfloat162float(__float2bfloat16_rn(v - hi));
+}
+
 // Greedy-argmax order: NaN ranks above every number (lowest index among NaNs),
 // otherwise larger value wins and ties go to the lower index.
 __device__ __forceinline__ bool argmax_better(float a, int ia, float b, int ib) {

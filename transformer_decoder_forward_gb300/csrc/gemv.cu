@@ -123,7 +123,25 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
   pdl_wait();
 
   // ---- stage this CTA's slice of X (rows mbase.., columns k0..k0+kcl) as fp32
-  if constexpr (SPLIT_X) {
+  if (p.xnorm) {
+    // X = Norm(h): each warp computes its rows' statistics over the whole row, then writes the
+    // CTA's K slice of the normalised row (h is fp32, K % 4 == 0, K <= 2048)
+    const float* hx = reinterpret_cast<const float*>(p.X);
+    const WT* gw = reinterpret_cast<const WT*>(p.norm_g);
+    const WT* bw = reinterpret_cast<const WT*>(p.norm_b);
+    for (int m = warp; m < mcount; m += GEMV_THREADS / 32) {
+      float4 v[ROW_NV];
+      float mean, rstd;
+      warp_row_stats(hx + (size_t)(mbase + m) * p.ldx, p.K, p.norm_ln != 0, p.norm_eps, v, mean, rstd);
+      for (int k = lane; k < kcl; k += 32) {
+        const float x = hx[(size_t)(mbase + m) * p.ldx + k0 + k];
+        const float b = bw ? to_f32(bw[k0 + k]) : 0.0f;
+        const float y = norm_apply(x, mean, rstd, to_f32(gw[k0 + k]), b);
+        // bf16 weights: the value a stored activation pair would give back
+        xs[(size_t)m * ldxs + k] = SPLIT_X ? pair_round(y) : y;
+      }
+    }
+  } else if constexpr (SPLIT_X) {
     // row m: hi at [m*ldx + k], lo at [m*ldx + ldx/2 + k]
     const bf16* X = reinterpret_cast<const bf16*>(p.X);
     const int lo = p.ldx >> 1;
@@ -318,8 +336,18 @@ cudaError_t launch_m(const LinearParams& p, int num_sms, cudaStream_t s, bool pd
 
 }  // namespace
 
+bool gemv_norm_supported(const LinearParams& p) {
+  return p.M <= GEMV_MT && p.K % 4 == 0 && p.K <= ROW_NV * 128 && p.ldx % 4 == 0;
+}
+
 cudaError_t launch_gemv(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
+  if (p.xnorm) {
+    if (!gemv_norm_supported(p) || p.xdt != DT_F32) return cudaErrorInvalidValue;
+    if (p.wdt == DT_F32 && p.adt == DT_F32) return launch_m<float>(p, num_sms, s, pdl);
+    if (p.wdt == DT_BF16 && p.adt == DT_SPLIT) return launch_m<bf16>(p, num_sms, s, pdl);
+    return cudaErrorInvalidValue;
+  }
   if (p.wdt == DT_F32 && p.xdt == DT_F32 && p.adt == DT_F32) return launch_m<float>(p, num_sms, s, pdl);
   if (p.wdt == DT_BF16 && p.xdt == DT_SPLIT && p.adt == DT_SPLIT) return launch_m<bf16>(p, num_sms, s, pdl);
   return cudaErrorInvalidValue;

@@ -14,7 +14,15 @@ struct LinearParams {
   int wdt, xdt, adt;    // weight / input / activation-output dtypes
   int swiglu;           // 1: tile t reads gate rows t*32.. and up rows F + t*32..
   Epilogue epi;
-  int xnorm;            // reserved: 0 (X is read as is)
+  // Fused row norm (xnorm = 1): X is the fp32 residual stream h ([M][ldx], ldx = K) and the
+  // kernel uses row m as Norm(h[m]) = (h[m] - mean) * rstd * g + b (LayerNorm), or
+  // h[m] * rstd * g (RMSNorm), the statistics from warp_row_stats. Supported by the GEMV; the
+  // others take the norm kernel's output instead.
+  int xnorm;
+  const void* norm_g;   // [K] gains, weight dtype
+  const void* norm_b;   // [K] biases (LayerNorm) or nullptr
+  float norm_eps;
+  int norm_ln;          // 1: LayerNorm, 0: RMSNorm
 };
 
 inline int linear_tiles(const LinearParams& p) {
@@ -30,6 +38,7 @@ enum : int { LIN_AUTO = 0, LIN_GEMV = 1, LIN_SIMT = 2, LIN_TC = 3, LIN_TC_SWAP =
 
 // Each returns cudaSuccess or the launch error; `name` receives the kernel family name.
 cudaError_t launch_gemv(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
+bool gemv_norm_supported(const LinearParams& p);
 cudaError_t launch_gemm_simt(const LinearParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_gemm_tc(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
 bool gemm_tc_supported(const LinearParams& p);

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
 // threadgroup round trip is needed when one simdgroup owns the row). The row is
 // read with 16-byte loads; the variance pass re-reads it from L1.
 constexpr int NORM_ROWS = 8;   // rows (warps) per CTA
-constexpr int NORM_NV = 16;    // float4 per lane held in registers: d <= 16 * 128 = 2048
+constexpr int NORM_NV = ROW_NV;   // float4 per lane held in registers: d <= 16 * 128 = 2048
 
 template <typename WT, typename AT>
 __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
@@ -51,26 +51,10 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
   if (r >= p.rows) return;
   int src = r;
   if (p.use_last_row && p.args->last_row) src = p.args->last_row[r];
-  const float4* x4 = reinterpret_cast<const float4*>(p.h + (size_t)src * p.d);
-  const int d4 = p.d >> 2;   // d is a multiple of 8
-  float4 v[NORM_NV];
-  float s = 0.0f;
-#pragma unroll
-  for (int j = 0; j < NORM_NV; ++j) {
-    const int i = lane + 32 * j;
-    v[j] = i < d4 ? x4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
-  }
-  const float mean = p.layer_norm ? warp_sum(s) / p.d : 0.0f;
-  float q = 0.0f;
-#pragma unroll
-  for (int j = 0; j < NORM_NV; ++j) {
-    if (lane + 32 * j < d4) {
-      const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, e = v[j].w - mean;
-      q += (a * a + b * b) + (c * c + e * e);
-    }
-  }
-  const float scale = 1.0f / sqrtf(warp_sum(q) / p.d + p.eps);
+  float4 v[ROW_NV];
+  float mean, scale;
+  warp_row_stats(p.h + (size_t)src * p.d, p.d, p.layer_norm != 0, p.eps, v, mean, scale);
+  const int d4 = p.d >> 2;
   const WT* gw = reinterpret_cast<const WT*>(p.g);
   const WT* bw = reinterpret_cast<const WT*>(p.b);
   const int ld = std::is_same<AT, Split>::value ? 2 * p.d : p.d;
@@ -92,7 +76,7 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
     const float xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
     float y[4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) y[t] = (xv[t] - mean) * scale * gv[j][t] + bv[j][t];
+    for (int t = 0; t < 4; ++t) y[t] = norm_apply(xv[t], mean, scale, gv[j][t], bv[j][t]);
     act_store4<AT>(p.out, r, ld, 4 * i, y);
   }
 }
