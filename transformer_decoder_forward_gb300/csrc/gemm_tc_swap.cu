@@ -44,6 +44,7 @@ constexpr int SW_MAX_KS = 8;                 // cluster size limit (portable)
 
 template <int NT, bool TF32>
 struct SwapCfg {
+  static_assert((SW_A_BYTES + NT * 128) % 2048 == 0, "a tf32 stage splits evenly over 128 threads");
   static constexpr int B_BYTES = NT * 128;                // one 128-byte K slice of NT activation rows
   static constexpr int RAW = SW_A_BYTES + (TF32 ? 1 : 2) * B_BYTES;   // TMA stage: [W][X] or [W][X_hi][X_lo]
   static constexpr int CONVB = 2 * RAW;                 // tf32: [W hi][X hi][W lo][X lo]
@@ -202,12 +203,16 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
         const float4* src = reinterpret_cast<const float4*>(raw_a(r));   // [W][X] contiguous
         float4* hi = reinterpret_cast<float4*>(cv(c));
         float4* lo = reinterpret_cast<float4*>(cv(c) + C::RAW);
-#pragma unroll 4
-        for (int j = t; j < C::RAW / 16; j += 128) {
-          const float4 x = src[j];
-          const float4 h = tf32_hi(x);
-          hi[j] = h;
-          lo[j] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+        // every load of the stage first (one shared-memory latency), then the split and stores
+        constexpr int PER = C::RAW / 16 / 128;   // float4 per thread (the stage is a multiple of 2 KB)
+        float4 xv[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) xv[u] = src[t + 128 * u];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const float4 h = tf32_hi(xv[u]);
+          hi[t + 128 * u] = h;
+          lo[t + 128 * u] = make_float4(xv[u].x - h.x, xv[u].y - h.y, xv[u].z - h.z, xv[u].w - h.w);
         }
         fence_async_smem();
         __syncwarp();
