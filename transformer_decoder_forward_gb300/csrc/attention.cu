@@ -35,7 +35,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 template <typename KT>
 struct AttnRing {
   static constexpr int BLK = KVB * HD * (int)sizeof(KT);
-  static constexpr int NST = sizeof(KT) == 4 ? 3 : 4;
+  static constexpr int NST = sizeof(KT) == 4 ? 2 : 3;   // 64 KB (fp32) / 48 KB per CTA: three CTAs an SM
   static constexpr int WARP_BYTES = NST * 2 * BLK;
   static constexpr size_t SMEM = (size_t)AD_WARPS * WARP_BYTES + (size_t)AD_WARPS * NST * 8;
 };
@@ -95,9 +95,13 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
   pdl_wait();   // the new token's K/V is written by the projection that precedes this kernel
   const StepArgs* a = p.args;
   const int ctx = a->positions[b] + 1;
-  const int t0 = sp * p.split;
+  if (ctx <= 0) return;
+  // the sequence's ns = ceil(ctx / split) chunks share its context evenly (16-token multiples)
+  const int ns = min(p.max_splits, (ctx + p.split - 1) / p.split);
+  const int chunk = min(p.split, ((ctx + ns - 1) / ns + KVB - 1) / KVB * KVB);
+  const int t0 = sp * chunk;
   if (t0 >= ctx) return;
-  const int nt = min(p.split, ctx - t0);
+  const int nt = min(chunk, ctx - t0);
   const int nblk = (nt + KVB - 1) / KVB;
   const int nj = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;   // this warp's blocks: warp + NW*j
   // physical block of this warp's j-th block, held by lane j
