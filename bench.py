@@ -50,6 +50,24 @@ def peaks():
 # algorithmic work per unit (decode step)
 # ------------------------------------------------------------------------------------------------
 
+# DRAM traffic per launch of each workload's dominant kernel family, from one single-pass ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum summed over one decode step's or one
+# prefill's launches of that family, divided by the launch count). It holds for the kernel
+# build the capture was taken on; the bench reports it when its dominant family matches. The
+# commands and per-launch figures: profiles/dram_traffic_dominant_kernels.md.
+TRAFFIC = {
+    "gpt2-124m-fp32-b32-teacher": ("proj (gemm_tcs)", 10.386e6),
+    "gpt2-124m-fp32-b1-greedy": ("proj (gemv)", 10.184e6),
+    "smollm2-360m-bf16-b64-ctx64to2048": ("proj (gemm_tcs)", 6.156e6),
+    "gpt2-xl-bf16-b256-ctx1024": ("attn_decode", 3205.1e6),
+}
+
+
+def traffic_for(workload: str, kernel: str):
+    t = TRAFFIC.get(workload)
+    return t[1] if t and t[0] == kernel else None
+
+
 def weight_bytes(s: wl.ModelShape) -> int:
     """Projection weights read once per step, including the tied head (vocab x d)."""
     return (s.n_layers * s.layer_params() + s.vocab * s.d_model) * s.elt_bytes
@@ -334,6 +352,7 @@ def run_decode_bench(args, W):
             "peak_source": f"hbm_gbs of {pk_kind}",
             "alg_bytes_per_launch": (alg / fam[dom][0]) if alg else None,
             "avg_launch_us": 1000.0 * dom_ms / fam[dom][0]}
+    roof["traffic"] = traffic_for(W.name, roof["kernel"])
     step_alg = float(np.mean([step_bytes(s, c) for c in ctx_steps]))
     step_gbs = step_alg / (ms / args.steps / 1000.0) / 1e9
     kernel_share = {k: round(v[1] / sum(x[1] for x in fam.values()), 4) for k, v in sorted(fam.items())}
