@@ -60,6 +60,7 @@ TRAFFIC = {
     "gpt2-124m-fp32-b1-greedy": ("proj (gemv)", 10.184e6),
     "smollm2-360m-bf16-b64-ctx64to2048": ("proj (gemm_tcs)", 6.156e6),
     "gpt2-xl-bf16-b256-ctx1024": ("attn_decode", 3205.1e6),
+    "gpt2-124m-bf16-prefill-16x1024": ("gemm_tc (tcgen05 projections)", 182.1e6),
 }
 
 
@@ -466,7 +467,7 @@ def run_prefill_bench(args, W):
     achieved = gflops / (gem[1] / 1000.0) / 1e12 if gem[1] > 0 else None
     roof = {"bound": "tensor", "kernel": "gemm_tc (tcgen05 projections)", "launches": gem[0], "achieved": achieved,
             "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": (achieved / pk["bf16_tflops"]) if achieved else None,
-            "traffic": None, "peak_source": f"bf16_tflops (burst) of {pk_kind}",
+            "traffic": traffic_for(W.name, "gemm_tc (tcgen05 projections)"), "peak_source": f"bf16_tflops (burst) of {pk_kind}",
             "alg_flops_per_launch": gflops / gem[0] if gem[0] else None,
             "avg_launch_us": 1000.0 * gem[1] / gem[0] if gem[0] else None}
     total = sum(v[1] for v in fam.values())
