@@ -130,15 +130,17 @@ __device__ __forceinline__ float warp_max(float v) {
 // biased variance about the mean (RMSNorm: mean of squares). Every projection that
 // normalises its own input and the stand-alone norm kernel use this one routine, so both
 // give bit-identical normalised rows. The row is left in v (16 float4 a lane).
+// NV: float4 per lane held (d <= 128 NV); any NV that covers d gives bit-identical results.
 constexpr int ROW_NV = 16;
-__device__ __forceinline__ void warp_row_stats(const float* x, int d, bool layer_norm, float eps, float4 (&v)[ROW_NV],
+template <int NV = ROW_NV>
+__device__ __forceinline__ void warp_row_stats(const float* x, int d, bool layer_norm, float eps, float4 (&v)[NV],
                                                float& mean, float& rstd) {
   const int lane = threadIdx.x & 31;
   const float4* x4 = reinterpret_cast<const float4*>(x);
   const int d4 = d >> 2;
   float s = 0.0f;
 #pragma unroll
-  for (int j = 0; j < ROW_NV; ++j) {
+  for (int j = 0; j < NV; ++j) {
     const int i = lane + 32 * j;
     v[j] = i < d4 ? x4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
@@ -146,7 +148,7 @@ __device__ __forceinline__ void warp_row_stats(const float* x, int d, bool layer
   mean = layer_norm ? warp_sum(s) / d : 0.0f;
   float q = 0.0f;
 #pragma unroll
-  for (int j = 0; j < ROW_NV; ++j) {
+  for (int j = 0; j < NV; ++j) {
     if (lane + 32 * j < d4) {
       const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, e = v[j].w - mean;
       q += (a * a + b * b) + (c * c + e * e);
@@ -322,11 +324,14 @@ __device__ __forceinline__ int swiglu_row(int n0_half, int c, int d_ff) {
   return c < 32 ? n0_half + c : d_ff + n0_half + (c - 32);
 }
 
+// GELU-tanh with the tanh argument u clamped to [-15, 15]. 0.5 (1 + tanh(u)) equals the
+// logistic function of 2u, so the value is x / (1 + e^(-2u)): one exponential and one
+// division, and with the clamp the exponential stays below e^30 (finite).
 __device__ __forceinline__ float gelu_tanh_clamped(float x) {
   const float kC = 0.7978845608028654f;   // sqrt(2/pi)
   float u = kC * (x + 0.044715f * x * x * x);
   u = fminf(15.0f, fmaxf(-15.0f, u));
-  return 0.5f * x * (1.0f + tanhf(u));
+  return __fdividef(x, 1.0f + __expf(-2.0f * u));
 }
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 

@@ -14,8 +14,8 @@
 //     accumulators in tensor memory, so the product carries the activations'
 //     full pair accuracy; tcgen05.commit releases each stage once the MMAs that
 //     read it finish, and marks the accumulator full after the tile's last one.
-//   - warps 2-9: read a full accumulator with tcgen05.ld (warp w owns TMEM lanes
-//     32(w%4).. = tile rows, half of the columns), hand it back to the MMA warp at once, stage it as
+//   - warps 2-17: read a full accumulator with tcgen05.ld (warp w owns TMEM lanes
+//     32(w%4).. = tile rows, a quarter of the columns), hand it back to the MMA warp at once, stage it as
 //     an fp32 tile in shared memory and run the shared epilogue (bias, GELU /
 //     SwiGLU, RoPE + kv_write, residual add) while the MMA warp already fills the
 //     other accumulator with the next tile.
@@ -31,8 +31,8 @@ namespace llm {
 namespace {
 
 constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 3;
-constexpr int TC_THREADS = 320;                 // producer warp, MMA warp, 8 epilogue warps
-constexpr int TC_EPI_THREADS = 256;
+constexpr int TC_THREADS = 576;                 // producer warp, MMA warp, 16 epilogue warps
+constexpr int TC_EPI_THREADS = 512;
 constexpr int TC_EPI_WARPS = TC_EPI_THREADS / 32;
 constexpr int A_STAGE = TC_BM * TC_BK * 2;      // bytes
 constexpr int B_STAGE = TC_BN * TC_BK * 2;
@@ -170,10 +170,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ---- epilogue warps: two per TMEM lane quadrant, each reading half of the columns
-    const int et = threadIdx.x - 64;   // 0..255
+    // ---- epilogue warps: four per TMEM lane quadrant, each reading a quarter of the columns
+    const int et = threadIdx.x - 64;   // 0..511
     const int q = warp & 3;            // TMEM lane quadrant = tile rows 32q..32q+31
-    const int half = (warp - 2) >> 2;  // columns 64 half .. 64 half + 63
+    const int quarter = (warp - 2) >> 2;   // columns 32 quarter .. 32 quarter + 31
     const int row = q * 32 + lane;
     pdl_wait();
     int lt = 0;
@@ -189,16 +189,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * TC_BN);
       {
-        const int c0 = half * 64;   // two 32-column loads in flight
-        uint32_t r[32], r2[32];
+        const int c0 = quarter * 32;
+        uint32_t r[32];
         tmem_ld32(ta + (uint32_t)c0, r);
-        tmem_ld32(ta + (uint32_t)(c0 + 32), r2);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          ot[row * OT_LD + c0 + j] = __uint_as_float(r[j]);
-          ot[row * OT_LD + c0 + 32 + j] = __uint_as_float(r2[j]);
-        }
+        for (int j = 0; j < 32; ++j) ot[row * OT_LD + c0 + j] = __uint_as_float(r[j]);
       }
       tc_fence_before();
       __syncwarp();

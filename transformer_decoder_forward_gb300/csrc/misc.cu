@@ -40,9 +40,9 @@ __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
 // threadgroup round trip is needed when one simdgroup owns the row). The row is
 // read with 16-byte loads; the variance pass re-reads it from L1.
 constexpr int NORM_ROWS = 8;   // rows (warps) per CTA
-constexpr int NORM_NV = ROW_NV;   // float4 per lane held in registers: d <= 16 * 128 = 2048
 
-template <typename WT, typename AT>
+// NORM_NV float4 per lane are held in registers: d <= 128 NORM_NV.
+template <typename WT, typename AT, int NORM_NV>
 __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * NORM_ROWS + warp;
@@ -51,9 +51,9 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
   if (r >= p.rows) return;
   int src = r;
   if (p.use_last_row && p.args->last_row) src = p.args->last_row[r];
-  float4 v[ROW_NV];
+  float4 v[NORM_NV];
   float mean, scale;
-  warp_row_stats(p.h + (size_t)src * p.d, p.d, p.layer_norm != 0, p.eps, v, mean, scale);
+  warp_row_stats<NORM_NV>(p.h + (size_t)src * p.d, p.d, p.layer_norm != 0, p.eps, v, mean, scale);
   const int d4 = p.d >> 2;
   const WT* gw = reinterpret_cast<const WT*>(p.g);
   const WT* bw = reinterpret_cast<const WT*>(p.b);
@@ -126,7 +126,12 @@ cudaError_t norm_t(const NormParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t c = make_launch_cfg(dim3((p.rows + NORM_ROWS - 1) / NORM_ROWS), dim3(NORM_ROWS * 32), 0, s,
                                          attr, pdl);
-  return cudaLaunchKernelEx(&c, k_norm<WT, AT>, p);
+  const int nv = (p.d + 127) / 128;   // registers sized for the row width
+  if (nv <= 2) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 2>, p);
+  if (nv <= 4) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 4>, p);
+  if (nv <= 8) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 8>, p);
+  if (nv <= 13) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 13>, p);
+  return cudaLaunchKernelEx(&c, k_norm<WT, AT, ROW_NV>, p);
 }
 
 }  // namespace
@@ -152,7 +157,7 @@ cudaError_t launch_embed(const EmbedParams& p, int wdt, cudaStream_t s, bool pdl
 
 cudaError_t launch_norm(const NormParams& p, int wdt, int adt, cudaStream_t s, bool pdl) {
   if (p.rows <= 0) return cudaSuccess;
-  if (p.d % 8 != 0 || p.d > NORM_NV * 128) return cudaErrorInvalidValue;
+  if (p.d % 8 != 0 || p.d > ROW_NV * 128) return cudaErrorInvalidValue;
   if (wdt == DT_F32 && adt == DT_F32) return norm_t<float, float>(p, s, pdl);
   if (wdt == DT_BF16 && adt == DT_SPLIT) return norm_t<bf16, Split>(p, s, pdl);
   return cudaErrorInvalidValue;
