@@ -158,16 +158,21 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
         *reinterpret_cast<uint4*>(base + OFF_KLO + sw_off(kr, 4 * hf + c)) = lo;
       }
       load32(vpool + off);
-      // V transposed: B operand of P.V is dims (rows) x keys (K)
-      const int ck = kr >> 3, bk = (kr & 7) * 2;
+      // V transposed: B operand of P.V is dims (rows) x keys (K). Neighbouring keys 2j, 2j+1
+      // (lanes kr, kr ^ 1) pair up so every store is one 32-bit word of two keys: the even
+      // lane writes dims 0..15 of its half, the odd lane dims 16..31.
+      const int odd = kr & 1, ck = kr >> 3, bk = (kr & 6) * 2;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int d = hf * 32 + i;
-        const bf16 hi = __float2bfloat16_rn(v[i]);
-        const bf16 lo = __float2bfloat16_rn(v[i] - __bfloat162float(hi));
+      for (int j = 0; j < 16; ++j) {
+        const float mine = odd ? v[16 + j] : v[j];
+        const float other = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[16 + j], 1);
+        const float ke = odd ? other : mine, ko = odd ? mine : other;   // keys 2j, 2j + 1
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(ke, ko);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(ke - __low2float(hi), ko - __high2float(hi));
+        const int d = hf * 32 + odd * 16 + j;
         const uint32_t o2 = sw_off(d, ck) + bk;
-        *reinterpret_cast<bf16*>(base + OFF_VHI + o2) = hi;
-        *reinterpret_cast<bf16*>(base + OFF_VLO + o2) = lo;
+        *reinterpret_cast<__nv_bfloat162*>(base + OFF_VHI + o2) = hi;
+        *reinterpret_cast<__nv_bfloat162*>(base + OFF_VLO + o2) = lo;
       }
     }
     fence_async_smem();
