@@ -334,7 +334,7 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
   const int wrows = p.swiglu ? 2 * p.N : p.N;
   // K split from the weight shape only (never from M): the largest cluster size <= 8 whose
   // grid still runs as one wave (the cluster occupancy the driver reports for this kernel),
-  // with at least two K stages per CTA.
+  // with at least two K stages per CTA. Sizes need not be powers of two.
   auto kern = k_gemm_tc_swap<NT, TF32>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -367,7 +367,8 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
     return capacity[c];
   };
   int ks = 1;
-  while (ks < SW_MAX_KS && tiles * ks * 2 <= wave(ks * 2) && p.K / (ks * 2) >= 2 * C::KE) ks *= 2;
+  for (int c = 2; c <= SW_MAX_KS; ++c)   // any cluster size: 6 ranks pack a GPC better than 8
+    if (tiles * c <= wave(c) && p.K / c >= 2 * C::KE) ks = c;
   int kcta = (p.K + ks - 1) / ks;
   kcta = ((kcta + C::KE - 1) / C::KE) * C::KE;
   ks = (p.K + kcta - 1) / kcta;

@@ -46,19 +46,11 @@ template <typename WT, typename AT, int NORM_NV>
 __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * NORM_ROWS + warp;
-  pdl_wait();
-  pdl_trigger();
-  if (r >= p.rows) return;
-  int src = r;
-  if (p.use_last_row && p.args->last_row) src = p.args->last_row[r];
-  float4 v[NORM_NV];
-  float mean, scale;
-  warp_row_stats<NORM_NV>(p.h + (size_t)src * p.d, p.d, p.layer_norm != 0, p.eps, v, mean, scale);
   const int d4 = p.d >> 2;
   const WT* gw = reinterpret_cast<const WT*>(p.g);
   const WT* bw = reinterpret_cast<const WT*>(p.b);
   const int ld = std::is_same<AT, Split>::value ? 2 * p.d : p.d;
-  // gains / biases of this lane's columns: all loads issued before any store
+  // gains / biases of this lane's columns: weights, so loaded before waiting on the producer
   float gv[NORM_NV][4], bv[NORM_NV][4];
 #pragma unroll
   for (int j = 0; j < NORM_NV; ++j) {
@@ -69,6 +61,14 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
       bv[j][t] = (i < d4 && bw) ? to_f32(bw[4 * i + t]) : 0.0f;
     }
   }
+  pdl_wait();
+  pdl_trigger();
+  if (r >= p.rows) return;
+  int src = r;
+  if (p.use_last_row && p.args->last_row) src = p.args->last_row[r];
+  float4 v[NORM_NV];
+  float mean, scale;
+  warp_row_stats<NORM_NV>(p.h + (size_t)src * p.d, p.d, p.layer_norm != 0, p.eps, v, mean, scale);
 #pragma unroll
   for (int j = 0; j < NORM_NV; ++j) {
     const int i = lane + 32 * j;
