@@ -69,6 +69,21 @@ def traffic_for(workload: str, kernel: str):
     return t[1] if t and t[0] == kernel else None
 
 
+def job_rate(ms_local: float, units_per_rank: float, world: int, device: str = "cuda"):
+    """Whole-job rate of N replicas: the job takes as long as its slowest rank (max over ranks of
+    the timed milliseconds) and processes every rank's units. Returns (ms, units, units per s).
+    Call on every rank (it is a collective when world > 1)."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    units = units_per_rank * world
+    return ms, units, units / (ms / 1000.0)
+
+
 def weight_bytes(s: wl.ModelShape) -> int:
     """Projection weights read once per step, including the tied head (vocab x d)."""
     return (s.n_layers * s.layer_params() + s.vocab * s.d_model) * s.elt_bytes
@@ -309,13 +324,7 @@ def run_decode_bench(args, W):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = B * args.steps * world
-    value = tokens / (ms / 1000.0)
+    ms, tokens, value = job_rate(ev0.elapsed_time(ev1), B * args.steps, world)
     assert run.dec.error_flags() == 0, "device error flags set during the bench"
 
     # ---- per-kernel durations (CUDA events around every launch, one pass of the workload)
@@ -442,12 +451,7 @@ def run_prefill_bench(args, W):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = tokens_total * args.steps * world / (ms / 1000.0)
+    ms, _, value = job_rate(ev0.elapsed_time(ev1), tokens_total * args.steps, world)
     assert run.dec.error_flags() == 0, "device error flags set during the bench"
     # per-kernel durations over one more prefill
     run.dec.set_profiling(True)
