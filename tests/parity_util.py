@@ -44,8 +44,10 @@ def oracle_teacher(model: oracle.OracleModel, prompt, stream) -> np.ndarray:
     return oracle.teacher_forced(model, prompt, stream)
 
 
-def run_gpu_teacher(run, stream_tokens: np.ndarray, rows=None, variant: int = 0, graphs: bool = True):
-    """Prefill then teacher-forced decode on the GPU.
+def run_gpu_teacher(run, stream_tokens: np.ndarray, rows=None, variant: int = 0, graphs: bool = True,
+                    profiling: bool = False):
+    """Prefill then teacher-forced decode on the GPU (decode steps with per-launch timing if
+    `profiling`).
 
     stream_tokens [S, B] int32. Returns (ids [1+S, B], logits [1+S, len(rows), V]) on the host.
     """
@@ -62,9 +64,11 @@ def run_gpu_teacher(run, stream_tokens: np.ndarray, rows=None, variant: int = 0,
     ids.append(run.next_ids.cpu().numpy().copy())
     zs.append(logits[rows].cpu().numpy())
     toks = torch.from_numpy(np.ascontiguousarray(stream_tokens, dtype=np.int32)).cuda()
+    run.dec.set_profiling(profiling)
     for s in range(stream_tokens.shape[0]):
         run.decode(toks[s], s, logits)
         torch.cuda.synchronize()
         ids.append(run.next_ids.cpu().numpy().copy())
         zs.append(logits[rows].cpu().numpy())
+    run.dec.set_profiling(False)
     return np.stack(ids), np.stack(zs)

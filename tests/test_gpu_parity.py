@@ -67,6 +67,26 @@ def test_graph_replay_equals_eager_bitwise(gpu_lib, small_models):
     np.testing.assert_array_equal(outs[0][1], outs[1][1])
 
 
+def test_profiled_step_equals_graph_step_bitwise(gpu_lib, small_models):
+    """Per-launch timing (the step captured with an event node around every launch, replayed
+    without programmatic launch) changes no result and times every kernel launch of the step."""
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, _ = small_models[SMALL_GPT2.name]
+    stream = wl.draw_stream(len(LENGTHS), STEPS, SMALL_GPT2.vocab)
+    outs = []
+    for prof in (False, True):
+        run = WorkloadRun(small_workload(SMALL_GPT2), host_weights=w, lengths=LENGTHS)
+        run.dec.kernel_stats(reset=True)
+        outs.append(run_gpu_teacher(run, stream, profiling=prof))
+        stats = run.dec.kernel_stats(reset=True)
+        per_step = run.dec.last_launch_count() - 1   # every launch but the step-arguments node
+        run.close()
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+    assert sum(n for n, _ in stats.values()) == STEPS * per_step
+    assert all(t > 0.0 for _, t in stats.values()), stats
+
+
 def test_programmatic_launch_does_not_change_results(gpu_lib, small_models):
     """Kernels launched with programmatic dependent launch (the default) and without it agree bitwise."""
     import subprocess

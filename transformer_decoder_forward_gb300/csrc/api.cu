@@ -116,6 +116,7 @@ struct llm_handle {
   std::map<int, GraphEntry> graphs;
   // profiling
   bool profiling = false;
+  bool prof_capture = false;   // a profiled decode step is being captured
   std::vector<ProfRec> prof;
   std::vector<cudaEvent_t> event_pool;
   size_t event_next = 0;
@@ -167,10 +168,12 @@ cudaEvent_t next_event(llm_handle* h) {
 template <typename F>
 llm_status run(llm_handle* h, const char* name, F&& f) {
   cudaEvent_t a = nullptr, b = nullptr;
+  // inside a capture the records become event nodes of the graph
+  const unsigned rec = h->prof_capture ? cudaEventRecordExternal : cudaEventRecordDefault;
   if (h->profiling) {
     a = next_event(h);
     b = next_event(h);
-    cudaEventRecord(a, h->stream);
+    cudaEventRecordWithFlags(a, h->stream, rec);
   }
   cudaError_t e = f();
   if (e != cudaSuccess) {
@@ -178,7 +181,7 @@ llm_status run(llm_handle* h, const char* name, F&& f) {
     return fail(LLM_ERR_CUDA, std::string(name) + ": " + cudaGetErrorString(e));
   }
   if (h->profiling) {
-    cudaEventRecord(b, h->stream);
+    cudaEventRecordWithFlags(b, h->stream, rec);
     h->prof.push_back({name, a, b});
   }
   h->launch_counter++;
@@ -535,6 +538,42 @@ llm_status llm_decode_step(llm_handle* h, const int32_t* tokens, const int32_t* 
   if (!tables && !h->cfg.contiguous_kv) return fail(LLM_ERR_INVALID_ARG, "NULL block_tables");
   StepArgs a{tokens, positions, nullptr, tables, next_ids, logits, nullptr, B, B};
   begin_call(h);
+  if (h->profiling && stream_capturable(h->stream)) {
+    // Per-launch timing. Launched one by one, a decode step's kernels are shorter than the
+    // host's launch calls, so events around eager launches would time the host. The step is
+    // captured with an event record node around every launch instead, and replayed once:
+    // the events then time the kernels back to back on the device. Programmatic launch is
+    // off in this mode, so each interval holds one kernel alone.
+    const bool pdl = h->pdl;
+    h->pdl = false;
+    h->prof_capture = true;
+    const size_t nprof = h->prof.size();
+    cudaError_t e = cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal);
+    llm_status fs = LLM_ERR_CUDA;
+    cudaGraph_t g = nullptr;
+    if (e == cudaSuccess) {
+      e = launch_set_args(h->d_args, a, h->stream);
+      h->launch_counter++;
+      fs = e == cudaSuccess ? enqueue_forward(h, B, B, false, 0) : LLM_ERR_CUDA;
+      const cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
+      if (e == cudaSuccess) e = ee;
+    }
+    h->pdl = pdl;
+    h->prof_capture = false;
+    cudaGraphExec_t x = nullptr;
+    if (e == cudaSuccess && fs == LLM_OK) e = cudaGraphInstantiate(&x, g, 0);
+    if (g) cudaGraphDestroy(g);
+    if (e == cudaSuccess && fs == LLM_OK) e = cudaGraphLaunch(x, h->stream);
+    if (x) cudaGraphExecDestroy(x);   // released once the replay completes
+    end_call(h);
+    if (fs != LLM_OK || e != cudaSuccess) {
+      h->prof.resize(nprof);   // no records of a step that did not run
+      if (fs != LLM_OK) return fs;
+      cudaGetLastError();
+      return fail(LLM_ERR_CUDA, std::string("profiled step: ") + cudaGetErrorString(e));
+    }
+    return LLM_OK;
+  }
   if (!h->use_graphs || h->profiling) {
     CUDA_TRY(launch_set_args(h->d_args, a, h->stream));
     h->launch_counter++;

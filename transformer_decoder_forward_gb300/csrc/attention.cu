@@ -92,15 +92,20 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
   }
   __syncwarp();
 
-  pdl_wait();   // the new token's K/V is written by the projection that precedes this kernel
+  // Before the dependency wait this CTA reads only what no kernel of the step writes: the
+  // step's positions and block tables, and every KV block except the one holding the new
+  // token, which the projection that precedes this kernel writes. So the table lookups and
+  // the first copies of older blocks overlap the end of that projection.
   const StepArgs* a = p.args;
   const int ctx = a->positions[b] + 1;
-  if (ctx <= 0) return;
   // the sequence's ns = ceil(ctx / split) chunks share its context evenly (16-token multiples)
-  const int ns = min(p.max_splits, (ctx + p.split - 1) / p.split);
-  const int chunk = min(p.split, ((ctx + ns - 1) / ns + KVB - 1) / KVB * KVB);
+  const int ns = ctx > 0 ? min(p.max_splits, (ctx + p.split - 1) / p.split) : 0;
+  const int chunk = ns > 0 ? min(p.split, ((ctx + ns - 1) / ns + KVB - 1) / KVB * KVB) : 0;
   const int t0 = sp * chunk;
-  if (t0 >= ctx) return;
+  if (ns <= 0 || t0 >= ctx) {
+    pdl_wait();
+    return;
+  }
   const int nt = min(chunk, ctx - t0);
   const int nblk = (nt + KVB - 1) / KVB;
   const int nj = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;   // this warp's blocks: warp + NW*j
@@ -125,7 +130,12 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
     }
   };
   const int pre = min(NST, nj);
-  for (int j = 0; j < pre; ++j) issue(j);
+  const int new_blk = (ctx - 1) / KVB - t0 / KVB;   // chunk-relative block of the new token
+  int early = 0;                                     // this warp's leading blocks older than it
+  while (early < pre && warp + NW * early < new_blk) ++early;
+  for (int j = 0; j < early; ++j) issue(j);
+  pdl_wait();   // q and the new token's K/V come from the preceding projection
+  for (int j = early; j < pre; ++j) issue(j);
 
   float qf[GMAX][8], o[GMAX][8], m[GMAX], l[GMAX];
 #pragma unroll
@@ -177,12 +187,15 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
         for (int it = 1; it < IT; ++it) mb = fmaxf(mb, sc[jj][it]);
         mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
         mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-        const float mn = fmaxf(m[jj], mb);   // finite: token 0 of every block is valid
-        const float alpha = exp2f(m[jj] - mn);   // m = -inf gives 0
-        m[jj] = mn;
-        l[jj] *= alpha;
+        // mb is finite (token 0 of every block is valid) and the same in every lane; the
+        // running state only needs rescaling when the maximum grows (alpha = 1 otherwise)
+        if (mb > m[jj]) {
+          const float alpha = exp2f(m[jj] - mb);   // m = -inf gives 0
+          m[jj] = mb;
+          l[jj] *= alpha;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[jj][e] *= alpha;
+          for (int e = 0; e < 8; ++e) o[jj][e] *= alpha;
+        }
       }
 #pragma unroll
       for (int it = 0; it < IT; ++it) {

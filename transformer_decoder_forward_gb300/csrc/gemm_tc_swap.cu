@@ -12,10 +12,13 @@
 //   - warp 1, one lane: issues tcgen05.mma into a 128 x N fp32 TMEM accumulator.
 //   - bf16 weights: activations arrive as bf16 (hi, lo) pairs; a stage holds the
 //     weight slice and both activation halves and the MMA sums W.X_hi + W.X_lo.
-//   - warps 2-5: for fp32 models they split each staged operand tile into tf32
-//     high and low parts in a separate buffer and release the TMA stage at once,
-//     so the weight stream runs ahead of the conversion; the MMA sums
-//     W_hi.X_hi + W_hi.X_lo + W_lo.X_hi (three tf32 products, fp32-level accuracy).
+//   - warps 2-5: for fp32 models they split each staged tile into tf32 high and low
+//     parts and release the TMA stage at once, so the weight stream runs ahead of the
+//     conversion; the MMA sums W_hi.X_hi + W_hi.X_lo + W_lo.X_hi (three tf32
+//     products, fp32-level accuracy). The weight parts go to tensor memory (each
+//     thread owns one weight row, its TMEM lane) and the MMAs read A from there: read
+//     three times from shared memory instead, the weight tile made the stage shared-
+//     memory bound (about 140 KB of shared-memory traffic for 16 KB of weights).
 //     After the last MMA they read the accumulator with tcgen05.ld and stage it
 //     transposed (tokens x weight rows) for the shared epilogue.
 // Small matrices split K across a thread-block cluster; partial tiles are summed in
@@ -44,22 +47,28 @@ constexpr int SW_MAX_KS = 8;                 // cluster size limit (portable)
 
 template <int NT, bool TF32>
 struct SwapCfg {
-  static_assert((SW_A_BYTES + NT * 128) % 2048 == 0, "a tf32 stage splits evenly over 128 threads");
   static constexpr int B_BYTES = NT * 128;                // one 128-byte K slice of NT activation rows
   static constexpr int RAW = SW_A_BYTES + (TF32 ? 1 : 2) * B_BYTES;   // TMA stage: [W][X] or [W][X_hi][X_lo]
-  static constexpr int CONVB = 2 * RAW;                 // tf32: [W hi][X hi][W lo][X lo]
+  static constexpr int CONVB = 2 * B_BYTES;             // tf32: [X hi][X lo] (the weight parts sit in TMEM)
   // TMA stages: bf16 keeps up to 4 within ~100 KB (a second CTA fits on the SM); tf32 keeps
-  // 4 raw stages plus 2 converted buffers (2 + 1 for the widest tiles).
-  static constexpr int NRAW = TF32 ? (NT <= 64 ? 4 : 2)
+  // up to 6 raw stages (one CTA an SM) plus 2 converted buffers (1 for the widest tiles).
+  static constexpr int NRAW = TF32 ? (NT <= 64 ? 6 : (NT <= 128 ? 4 : 2))
                                    : (4 * RAW <= 100 * 1024 ? 4 : (3 * RAW <= 100 * 1024 ? 3 : 2));
-  static constexpr int NCONV = TF32 ? (NT <= 64 ? 2 : 1) : 0;
+  static constexpr int NCONV = TF32 ? (NT <= 128 ? 2 : 1) : 0;
   static constexpr size_t PIPE = (size_t)NRAW * RAW + (size_t)NCONV * CONVB;
   static constexpr size_t OT = (size_t)NT * SW_OT_LD * 4;
   static constexpr size_t RED = (size_t)((NT + 1) / 2) * SW_OT_LD * 4;   // ks >= 2: a rank reduces <= NT/2 rows
   static constexpr size_t BODY = PIPE > OT + RED ? PIPE : OT + RED;
   static constexpr size_t SMEM = 1024 + BODY + 256;
   static constexpr int KE = TF32 ? 32 : 64;            // K elements per stage (128 bytes)
-  static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
+  // TMEM: the accumulator (NT columns), then for tf32 one A buffer per converted stage
+  // (32 columns of W_hi, 32 of W_lo); allocations are powers of two
+  static constexpr int A_COL0 = NT < 32 ? 32 : NT;
+  static constexpr int COLS_USED = A_COL0 + (TF32 ? NCONV * 64 : 0);
+  static constexpr int TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128
+                                 : COLS_USED <= 256 ? 256 : 512;
+  static_assert(COLS_USED <= 512, "TMEM holds 512 columns");
+  static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
 
 // tf32 high part: the fp32 value rounded to 10 mantissa bits (to nearest, ties away, by an
@@ -92,7 +101,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   auto raw_a = [&](int r) { return base + (size_t)r * C::RAW; };
   auto raw_b = [&](int r) { return base + (size_t)r * C::RAW + SW_A_BYTES; };
-  auto cv = [&](int c) { return base + (size_t)NR * C::RAW + (size_t)c * C::CONVB; };   // [A hi][B hi][A lo][B lo]
+  auto cv = [&](int c) { return base + (size_t)NR * C::RAW + (size_t)c * C::CONVB; };   // [X hi][X lo]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, ks = blockIdx.y;
@@ -164,15 +173,15 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
         const int c = i % NC;
         if (!mbar_wait(&conv[c], (i / NC) & 1, flags)) break;
         tc_fence_after();
-        unsigned char* b = cv(c);
-        const uint64_t da = sw128_desc(b), db = sw128_desc(b + SW_A_BYTES);
-        const uint64_t dal = sw128_desc(b + C::RAW), dbl = sw128_desc(b + C::RAW + SW_A_BYTES);
+        const uint32_t ahi = tmem + (uint32_t)(C::A_COL0 + c * 64), alo = ahi + 32;
+        const uint64_t db = sw128_desc(cv(c)), dbl = sw128_desc(cv(c) + C::B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {   // 32 bytes of K per MMA
+        for (int kk = 0; kk < 4; ++kk) {   // 8 K elements per MMA: 8 TMEM columns of A, 32 bytes of B
           const uint64_t o = (uint64_t)(kk * 2);
-          tc_mma_tf32(tmem, da + o, db + o, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-          tc_mma_tf32(tmem, da + o, dbl + o, idesc, 1u);
-          tc_mma_tf32(tmem, dal + o, db + o, idesc, 1u);
+          const uint32_t ak = (uint32_t)(kk * 8);
+          tc_mma_tf32_ts(tmem, ahi + ak, db + o, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_tf32_ts(tmem, ahi + ak, dbl + o, idesc, 1u);
+          tc_mma_tf32_ts(tmem, alo + ak, db + o, idesc, 1u);
         }
         tc_commit(&cfree[c]);
       } else {
@@ -194,26 +203,58 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
   } else if (warp >= 2) {
     pdl_wait();
     if constexpr (TF32) {
-      // ---- tf32 split: raw stage r -> converted buffer c, then release r to the producer
-      const int t = threadIdx.x - 64;   // 0..127
+      // ---- tf32 split of raw stage r into buffer c, then r goes back to the producer.
+      // Weights: thread = one row of the tile = its TMEM lane; the row's 32 values are read
+      // from the 128-byte-swizzled tile (16-byte chunk j of row m sits at chunk j ^ (m mod 8),
+      // so eight lanes cover all banks) and its high and low parts go to TMEM columns
+      // [0, 32) and [32, 64) of A buffer c. Activations: split elementwise in shared memory
+      // (the swizzled layout is kept), the MMA's B operand.
+      const int t = threadIdx.x - 64;                 // 0..127
+      const int row = (warp & 3) * 32 + lane;         // this warp's TMEM lane quadrant
+      const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      constexpr int XV = C::B_BYTES / 16;             // float4 of the activation tile
+      constexpr int XPER = (XV + 127) / 128;
       for (int i = 0; i < kiters; ++i) {
         const int r = i % NR, c = i % NC;
         if (!mbar_wait(&full[r], (i / NR) & 1, flags)) break;
-        if (i >= NC && !mbar_wait(&cfree[c], ((i / NC) - 1) & 1, flags)) break;
-        const float4* src = reinterpret_cast<const float4*>(raw_a(r));   // [W][X] contiguous
-        float4* hi = reinterpret_cast<float4*>(cv(c));
-        float4* lo = reinterpret_cast<float4*>(cv(c) + C::RAW);
-        // every load of the stage first (one shared-memory latency), then the split and stores
-        constexpr int PER = C::RAW / 16 / 128;   // float4 per thread (the stage is a multiple of 2 KB)
-        float4 xv[PER];
-#pragma unroll
-        for (int u = 0; u < PER; ++u) xv[u] = src[t + 128 * u];
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-          const float4 h = tf32_hi(xv[u]);
-          hi[t + 128 * u] = h;
-          lo[t + 128 * u] = make_float4(xv[u].x - h.x, xv[u].y - h.y, xv[u].z - h.z, xv[u].w - h.w);
+        if (i >= NC) {
+          if (!mbar_wait(&cfree[c], ((i / NC) - 1) & 1, flags)) break;
+          tc_fence_after();   // the MMAs that read A buffer c are complete
         }
+        const float4* wrow = reinterpret_cast<const float4*>(raw_a(r) + row * 128);
+        const float4* xs = reinterpret_cast<const float4*>(raw_b(r));
+        float4 wv[8], xv[XPER];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wv[j] = wrow[j ^ (row & 7)];
+#pragma unroll
+        for (int u = 0; u < XPER; ++u) xv[u] = (t + 128 * u < XV) ? xs[t + 128 * u] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t ta = tq + (uint32_t)(C::A_COL0 + c * 64);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {   // 16 columns a store
+          uint32_t whi[16], wlo[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 v = wv[hh * 4 + j];
+            const float4 h = tf32_hi(v);
+            whi[4 * j + 0] = __float_as_uint(h.x); wlo[4 * j + 0] = __float_as_uint(v.x - h.x);
+            whi[4 * j + 1] = __float_as_uint(h.y); wlo[4 * j + 1] = __float_as_uint(v.y - h.y);
+            whi[4 * j + 2] = __float_as_uint(h.z); wlo[4 * j + 2] = __float_as_uint(v.z - h.z);
+            whi[4 * j + 3] = __float_as_uint(h.w); wlo[4 * j + 3] = __float_as_uint(v.w - h.w);
+          }
+          tmem_st16(ta + (uint32_t)(hh * 16), whi);
+          tmem_st16(ta + (uint32_t)(32 + hh * 16), wlo);
+        }
+        float4* xh = reinterpret_cast<float4*>(cv(c));
+        float4* xl = reinterpret_cast<float4*>(cv(c) + C::B_BYTES);
+#pragma unroll
+        for (int u = 0; u < XPER; ++u) {
+          if (t + 128 * u >= XV) break;
+          const float4 h = tf32_hi(xv[u]);
+          xh[t + 128 * u] = h;
+          xl[t + 128 * u] = make_float4(xv[u].x - h.x, xv[u].y - h.y, xv[u].z - h.z, xv[u].w - h.w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {

@@ -78,6 +78,25 @@ __device__ __forceinline__ void tc_mma_tf32(uint32_t d, uint64_t a, uint64_t b, 
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// tcgen05.mma kind::tf32 with A read from tensor memory: row m of A in TMEM lane m, one
+// element a 32-bit column, K along the columns (8 columns an instruction).
+__device__ __forceinline__ void tc_mma_tf32_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Sixteen consecutive 32-bit columns of this thread's TMEM lane (warp w reaches lanes 32*(w%4)..+31).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // fp32 -> tf32 (round to nearest, ties away), returned as an fp32 bit pattern whose low 13 bits are 0.
 __device__ __forceinline__ float to_tf32(float x) {
   uint32_t r;
