@@ -3,20 +3,25 @@
 // Causal attention over the prompt, reading K and V from the paged fp32 cache in
 // place ("rvllm-metal", sections "What the kernels do" and "What's basic about it":
 // scores, -inf mask, softmax, probs @ V, without gathering the context into a
-// contiguous copy). CTA = (128 query rows of one sequence, query head h); one thread
-// per query row; two CTAs per SM overlap each other's loads. For each block of 64 keys:
-//   1. the threads load the keys' K and V rows (fp32) from their paged blocks and
-//      split every value v into bf16 hi = bf16(v), lo = bf16(v - hi), written straight
-//      into the 128-byte-swizzled K-major layout the MMA reads (V transposed to
-//      dims x keys);
+// contiguous copy). CTA = (128 query rows of one sequence, query head h); two threads
+// per query row, each owning 32 of a block's 64 key columns in the softmax and 32 of the
+// 64 output dims; two CTAs (16 warps) per SM. For each block of 64 keys:
+//   1. the threads split the keys' K and V rows (fp32, loaded from their paged blocks
+//      into registers during the previous block) into bf16 hi = bf16(v),
+//      lo = bf16(v - hi), written straight into the 128-byte-swizzled K-major layout
+//      the MMA reads (V transposed to dims x keys), then issue the loads of the next
+//      block's rows, which land while steps 2-4 run;
 //   2. one thread issues S = Q.K^T as hi.hi + hi.lo + lo.hi (tcgen05.mma, M = 128
 //      queries, N = 64 keys, fp32 accumulate in TMEM), so the scores carry about
 //      16 bits of the operands instead of bf16's 8;
-//   3. each thread reads its score row from TMEM, applies the scale and the causal
-//      mask, and updates an online softmax (running max and sum, log2 units); the
+//   3. each thread reads its half of the score row from TMEM, applies the scale and the
+//      causal mask, and the two threads of a row agree on the row maximum through shared
+//      memory; the online softmax (running max, partial sums, log2 units) proceeds and the
 //      probabilities are split the same way into the A operand of P.V;
 //   4. P.V (M = 128, N = 64, K = 64) goes to a second TMEM accumulator and each
-//      thread folds it into its output row: o = o * exp2(m_old - m_new) + P.V.
+//      thread folds its 32 dims into its output: o = o * exp2(m_old - m_new) + P.V.
+// One thread per query row ran about 1,200 dependent instructions per block with only 8
+// warps an SM to hide their latency; the kernel was issue-latency bound.
 // The output row is o / sum, stored as the activation dtype of the model.
 // Every wait is bounded (FLAG_WAIT_TIMEOUT) and the tensor memory is always freed.
 #include <type_traits>
@@ -30,18 +35,24 @@ namespace {
 
 constexpr int PT_Q = 128;          // query rows per CTA (MMA M)
 constexpr int PT_K = 64;           // keys per step
-constexpr int PT_THREADS = 128;
+constexpr int PT_THREADS = 256;    // two threads per query row
 constexpr int PT_TILE = 128 * 128;   // bytes of a 128-row x 64-bf16 swizzled tile
 constexpr int PT_HALF = 64 * 128;    // bytes of a 64-row x 64-bf16 swizzled tile
-// shared-memory layout (bytes from a 1024-aligned base): Q (128 queries x 64 dims),
-// K (64 keys x 64 dims), V transposed (64 dims x 64 keys), P (128 queries x 64 keys)
+// shared-memory layout (bytes from a 1024-aligned base): Q (128 queries x 64 dims), two
+// buffers of K (64 keys x 64 dims) and V transposed (64 dims x 64 keys), the halves' row
+// maxima / sums, and the CTA's physical KV blocks
 constexpr int OFF_QHI = 0, OFF_QLO = OFF_QHI + PT_TILE;
-constexpr int OFF_KHI = OFF_QLO + PT_TILE, OFF_KLO = OFF_KHI + PT_HALF;
-constexpr int OFF_VHI = OFF_KLO + PT_HALF, OFF_VLO = OFF_VHI + PT_HALF;
-constexpr int OFF_PHI = OFF_VLO + PT_HALF, OFF_PLO = OFF_PHI + PT_TILE;
-constexpr int OFF_BAR = OFF_PLO + PT_TILE;
+constexpr int OFF_KV = OFF_QLO + PT_TILE;
+constexpr int KV_BUF = 4 * PT_HALF;                          // [K hi][K lo][V hi][V lo]
+constexpr int KV_KHI = 0, KV_KLO = PT_HALF, KV_VHI = 2 * PT_HALF, KV_VLO = 3 * PT_HALF;
+constexpr int OFF_RED = OFF_KV + 2 * KV_BUF;                 // [2][128] floats
+constexpr int PT_MAX_LB = 256;                               // table entries staged (4096 keys)
+constexpr int OFF_PB = OFF_RED + 2 * PT_Q * 4;               // [PT_MAX_LB] ints
+constexpr int OFF_BAR = OFF_PB + PT_MAX_LB * 4;
 constexpr size_t PT_SMEM = 1024 + OFF_BAR + 64;
-constexpr uint32_t PT_TMEM_COLS = 128;   // S: columns 0..63, P.V: 64..127
+// TMEM: S in columns 0..63 (fp32), overwritten in place by P as bf16 pairs (P_hi in
+// columns 0..31, P_lo in 32..63, two keys a column) for the P.V MMA's A operand; P.V in 64..127
+constexpr uint32_t PT_TMEM_COLS = 128;
 constexpr float SCALE_LOG2 = 0.125f * 1.4426950408889634f;   // log2(e) / sqrt(64)
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a K-major tile with 128-byte rows and
@@ -62,14 +73,6 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-__device__ __forceinline__ void load_row64(const float* src, float* v) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 x = *reinterpret_cast<const float4*>(src + 4 * i);
-    v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-  }
-}
-
 template <typename AT>
 __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPrefillParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -77,8 +80,10 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   uint64_t* barS = reinterpret_cast<uint64_t*>(base + OFF_BAR);
   uint64_t* barO = barS + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(barO + 1);
+  float* s_red = reinterpret_cast<float*>(base + OFF_RED);
 
-  const int r = threadIdx.x, warp = r >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = tid & (PT_Q - 1), half = tid >> 7;   // query row; key columns and dims 32 half ..
   const int4 it = p.items[blockIdx.x];
   const int seq = it.x, qp0 = it.y, row0 = it.z, len = it.w;
   const int h = blockIdx.y, H = p.n_heads, Hkv = p.kv.n_kv_heads, g = h / (H / Hkv);
@@ -89,7 +94,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
     tmem_alloc(tmem_slot, PT_TMEM_COLS);
     tmem_relinquish();
   }
-  if (r == 32) {
+  if (tid == 32) {
     mbar_init(barS, 1);
     mbar_init(barO, 1);
     mbar_fence_init();
@@ -98,25 +103,30 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_lane = (uint32_t)(warp * 32) << 16;   // this warp's TMEM lanes = its query rows
+  const uint32_t t_lane = (uint32_t)((warp & 3) * 32) << 16;   // warp w reaches TMEM lanes 32(w%4).. = rows r
   pdl_wait();
   const StepArgs* a = p.args;
 
-  // Q rows (unscaled) -> Q_hi / Q_lo
+  // Q row r (unscaled), dims 32 half .. 32 half + 31 -> Q_hi / Q_lo chunks 4 half ..
   {
-    float v[64];
+    float v[32];
     if (r < nq) {
-      load_row64(p.q + (size_t)(row0 + r) * H * HD + h * HD, v);
+      const float* src = p.q + (size_t)(row0 + r) * H * HD + h * HD + half * 32;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(src + 4 * i);
+        v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+      }
     } else {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) v[i] = 0.0f;
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
     }
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       uint4 hi, lo;
       split8(v + 8 * c, hi, lo);
-      *reinterpret_cast<uint4*>(base + OFF_QHI + sw_off(r, c)) = hi;
-      *reinterpret_cast<uint4*>(base + OFF_QLO + sw_off(r, c)) = lo;
+      *reinterpret_cast<uint4*>(base + OFF_QHI + sw_off(r, 4 * half + c)) = hi;
+      *reinterpret_cast<uint4*>(base + OFF_QLO + sw_off(r, 4 * half + c)) = lo;
     }
   }
 
@@ -127,61 +137,86 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   const float* vpool = reinterpret_cast<const float*>(p.kv.v);
   constexpr uint32_t idS = idesc_bf16(PT_Q, PT_K);
   constexpr uint32_t idO = idesc_bf16(PT_Q, HD);
-  float o[HD];
+  float o[32];
 #pragma unroll
-  for (int d = 0; d < HD; ++d) o[d] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f;
+  for (int d = 0; d < 32; ++d) o[d] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;   // l_run: this thread's key columns only
   bool ok = true;
 
-  for (int kb = 0; kb < nkb && ok; ++kb) {
-    // ---- K and V of key kb*64 + (r mod 64): this thread converts dims 32h .. 32h + 31, h = r / 64
-    {
-      const int kr = r & 63, hf = r >> 6;
-      const int t = kb * PT_K + kr;
-      float v[32];
-      int pb = -1;
-      if (t < kend) pb = kv_block(p.kv, a->block_tables, seq, t, flags);
-      const size_t off = (pb >= 0 ? kv_offset(p.kv, pb, g, t & (KVB - 1)) : 0) + hf * 32;
-      auto load32 = [&](const float* src) {
+  // physical block of every 16-key block the CTA reads (-1: out of range, flagged), so the
+  // loads below wait on no table lookup
+  int* s_pb = reinterpret_cast<int*>(base + OFF_PB);
+  const int nlb = (kend + KVB - 1) / KVB;
+  for (int lb = tid; lb < min(nlb, PT_MAX_LB); lb += PT_THREADS)
+    s_pb[lb] = kv_block(p.kv, a->block_tables, seq, lb * KVB, flags);
+  __syncthreads();
+
+  // K and V of key kb*64 + kr, kr = tid mod 64: this thread converts dims 16 q4 .. 16 q4 + 15,
+  // q4 = tid / 64. kv holds a later block's values (K, then V), loaded ahead in registers.
+  const int kr = tid & 63, q4 = tid >> 6;
+  float kv[32];
+  auto prefetch = [&](int kb) {
+    const int t = kb * PT_K + kr;
+    int pb = -1;
+    if (t < kend) pb = (t >> 4) < PT_MAX_LB ? s_pb[t >> 4] : kv_block(p.kv, a->block_tables, seq, t, flags);
+    const size_t off = (pb >= 0 ? kv_offset(p.kv, pb, g, t & (KVB - 1)) : 0) + q4 * 16;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 x = pb >= 0 ? *reinterpret_cast<const float4*>(src + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-        }
-      };
-      load32(kpool + off);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint4 hi, lo;
-        split8(v + 8 * c, hi, lo);
-        *reinterpret_cast<uint4*>(base + OFF_KHI + sw_off(kr, 4 * hf + c)) = hi;
-        *reinterpret_cast<uint4*>(base + OFF_KLO + sw_off(kr, 4 * hf + c)) = lo;
-      }
-      load32(vpool + off);
-      // V transposed: B operand of P.V is dims (rows) x keys (K). Neighbouring keys 2j, 2j+1
-      // (lanes kr, kr ^ 1) pair up so every store is one 32-bit word of two keys: the even
-      // lane writes dims 0..15 of its half, the odd lane dims 16..31.
-      const int odd = kr & 1, ck = kr >> 3, bk = (kr & 6) * 2;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float mine = odd ? v[16 + j] : v[j];
-        const float other = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[16 + j], 1);
-        const float ke = odd ? other : mine, ko = odd ? mine : other;   // keys 2j, 2j + 1
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(ke, ko);
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(ke - __low2float(hi), ko - __high2float(hi));
-        const int d = hf * 32 + odd * 16 + j;
-        const uint32_t o2 = sw_off(d, ck) + bk;
-        *reinterpret_cast<__nv_bfloat162*>(base + OFF_VHI + o2) = hi;
-        *reinterpret_cast<__nv_bfloat162*>(base + OFF_VLO + o2) = lo;
-      }
+    for (int i = 0; i < 4; ++i) {
+      const float4 x = pb >= 0 ? *reinterpret_cast<const float4*>(kpool + off + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      kv[4 * i] = x.x; kv[4 * i + 1] = x.y; kv[4 * i + 2] = x.z; kv[4 * i + 3] = x.w;
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (r == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 x = pb >= 0 ? *reinterpret_cast<const float4*>(vpool + off + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      kv[16 + 4 * i] = x.x; kv[16 + 4 * i + 1] = x.y; kv[16 + 4 * i + 2] = x.z; kv[16 + 4 * i + 3] = x.w;
+    }
+  };
+  // split the values in kv into K / V-transposed buffer b
+  auto store_kv = [&](int b) {
+    unsigned char* kvb = base + OFF_KV + b * KV_BUF;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint4 hi, lo;
+      split8(kv + 8 * c, hi, lo);
+      *reinterpret_cast<uint4*>(kvb + KV_KHI + sw_off(kr, 2 * q4 + c)) = hi;
+      *reinterpret_cast<uint4*>(kvb + KV_KLO + sw_off(kr, 2 * q4 + c)) = lo;
+    }
+    // V transposed: B operand of P.V is dims (rows) x keys (K). Neighbouring keys 2j, 2j+1
+    // (lanes kr, kr ^ 1) pair up so every store is one 32-bit word of two keys: the even
+    // lane writes dims 0..7 of its 16, the odd lane dims 8..15.
+    const float* v = kv + 16;
+    const int odd = kr & 1, ck = kr >> 3, bk = (kr & 6) * 2;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float mine = odd ? v[8 + j] : v[j];
+      const float other = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[8 + j], 1);
+      const float ke = odd ? other : mine, ko = odd ? mine : other;   // keys 2j, 2j + 1
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(ke, ko);
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(ke - __low2float(hi), ko - __high2float(hi));
+      const int d = q4 * 16 + odd * 8 + j;
+      const uint32_t o2 = sw_off(d, ck) + bk;
+      *reinterpret_cast<__nv_bfloat162*>(kvb + KV_VHI + o2) = hi;
+      *reinterpret_cast<__nv_bfloat162*>(kvb + KV_VLO + o2) = lo;
+    }
+  };
+  if (nkb > 0) {
+    prefetch(0);
+    store_kv(0);
+    if (nkb > 1) prefetch(1);
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();   // Q and block 0 in shared memory
+  tc_fence_after();
+
+  // Per block kb: the S MMA runs while the threads store block kb + 1 into the other buffer
+  // and load block kb + 2; softmax; P to TMEM; the P.V MMA; fold into o.
+  for (int kb = 0; kb < nkb && ok; ++kb) {
+    const int b = kb & 1;
+    unsigned char* kvb = base + OFF_KV + b * KV_BUF;
+    if (tid == 0) {   // S = Q.K^T (three products), over S / P's columns: P.V of kb - 1 has completed
       const uint64_t dq = sw128_desc(base + OFF_QHI), dql = sw128_desc(base + OFF_QLO);
-      const uint64_t dk = sw128_desc(base + OFF_KHI), dkl = sw128_desc(base + OFF_KLO);
+      const uint64_t dk = sw128_desc(kvb + KV_KHI), dkl = sw128_desc(kvb + KV_KLO);
 #pragma unroll
       for (int ks = 0; ks < HD / 16; ++ks) {
         const uint64_t o2 = (uint64_t)(ks * 2);   // 32 bytes of K per MMA
@@ -191,69 +226,70 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
       }
       tc_commit(barS);
     }
+    if (kb + 1 < nkb) {
+      store_kv(b ^ 1);   // buffer b ^ 1 was last read by the P.V MMA of kb - 1, complete
+      if (kb + 2 < nkb) prefetch(kb + 2);
+      fence_async_smem();
+    }
     ok = mbar_wait(barS, kb & 1, flags);
-    ok = __syncthreads_and(ok) != 0;
+    ok = __syncthreads_and(ok) != 0;   // also: block kb + 1 is in shared memory
     if (!ok) break;
     tc_fence_after();
 
-    // ---- online softmax of this thread's score row (log2 units)
+    // ---- online softmax: this thread's 32 key columns of row r (log2 units)
+    float sc[32];
     float mb = -INFINITY;
-#pragma unroll 1
-    for (int c0 = 0; c0 < PT_K; c0 += 32) {
-      uint32_t s[32];
-      tmem_ld32(tmem + t_lane + (uint32_t)c0, s);
+    {
+      uint32_t sr[32];
+      tmem_ld32(tmem + t_lane + (uint32_t)(32 * half), sr);
       tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int t = kb * PT_K + c0 + j;
-        if (t <= qpos && t < kend) mb = fmaxf(mb, __uint_as_float(s[j]) * SCALE_LOG2);
+        const int t = kb * PT_K + 32 * half + j;
+        sc[j] = (t <= qpos && t < kend) ? __uint_as_float(sr[j]) * SCALE_LOG2 : -INFINITY;
+        mb = fmaxf(mb, sc[j]);
       }
     }
-    const float m_new = fmaxf(m_run, mb);   // finite: key 0 <= qpos is in block 0
+    s_red[half * PT_Q + r] = mb;
+    tc_fence_before();
+    __syncthreads();   // both halves' maxima are visible, and every S column has been read
+    tc_fence_after();
+    const float m_new = fmaxf(m_run, fmaxf(mb, s_red[(half ^ 1) * PT_Q + r]));   // finite: key 0 is in block 0
     const float alpha = exp2f(m_run - m_new);
     m_run = m_new;
     float lsum = 0.0f;
-#pragma unroll 1
-    for (int c0 = 0; c0 < PT_K; c0 += 32) {
-      uint32_t s[32];
-      tmem_ld32(tmem + t_lane + (uint32_t)c0, s);
-      tmem_ld_wait();
-      float pr[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int t = kb * PT_K + c0 + j;
-        pr[j] = (t <= qpos && t < kend) ? exp2f(__uint_as_float(s[j]) * SCALE_LOG2 - m_new) : 0.0f;
-        lsum += pr[j];
-      }
-      // P row r, keys c0..c0+31: chunks c0 / 8 ..
-      unsigned char* phi = base + OFF_PHI;
-      unsigned char* plo = base + OFF_PLO;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint4 hi, lo;
-        split8(pr + 8 * cc, hi, lo);
-        const int c = (c0 >> 3) + cc;
-        *reinterpret_cast<uint4*>(phi + sw_off(r, c)) = hi;
-        *reinterpret_cast<uint4*>(plo + sw_off(r, c)) = lo;
-      }
+    for (int j = 0; j < 32; ++j) {
+      sc[j] = exp2f(sc[j] - m_new);   // masked: exp2(-inf) = 0
+      lsum += sc[j];
     }
     l_run = l_run * alpha + lsum;
-    fence_async_smem();
+    {   // P row r, keys 32 half .. + 31 as bf16 pairs: P_hi columns 16 half .., P_lo 32 + 16 half ..
+      uint32_t ph[16], pl[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(sc[2 * i], sc[2 * i + 1]);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(sc[2 * i] - __low2float(hi), sc[2 * i + 1] - __high2float(hi));
+        ph[i] = *reinterpret_cast<const uint32_t*>(&hi);
+        pl[i] = *reinterpret_cast<const uint32_t*>(&lo);
+      }
+      tmem_st16(tmem + t_lane + (uint32_t)(16 * half), ph);
+      tmem_st16(tmem + t_lane + (uint32_t)(32 + 16 * half), pl);
+      tmem_st_wait();
+    }
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();   // P complete in TMEM
     tc_fence_after();
-    if (r == 0) {
+    if (tid == 0) {   // P.V: A = P from TMEM (8 columns per 16 keys), B = V transposed
       const uint32_t dO = tmem + (uint32_t)PT_K;
+      const uint64_t dv = sw128_desc(kvb + KV_VHI), dvl = sw128_desc(kvb + KV_VLO);
 #pragma unroll
       for (int ks = 0; ks < PT_K / 16; ++ks) {
         const uint64_t o2 = (uint64_t)(ks * 2);
-        const uint64_t dp = sw128_desc(base + OFF_PHI) + o2;
-        const uint64_t dpl = sw128_desc(base + OFF_PLO) + o2;
-        const uint64_t dv = sw128_desc(base + OFF_VHI) + o2;
-        const uint64_t dvl = sw128_desc(base + OFF_VLO) + o2;
-        tc_mma(dO, dp, dv, idO, ks > 0 ? 1u : 0u);
-        tc_mma(dO, dp, dvl, idO, 1u);
-        tc_mma(dO, dpl, dv, idO, 1u);
+        const uint32_t ph = tmem + (uint32_t)(ks * 8), pl = tmem + (uint32_t)(32 + ks * 8);
+        tc_mma_ts(dO, ph, dv + o2, idO, ks > 0 ? 1u : 0u);
+        tc_mma_ts(dO, ph, dvl + o2, idO, 1u);
+        tc_mma_ts(dO, pl, dv + o2, idO, 1u);
       }
       tc_commit(barO);
     }
@@ -262,28 +298,28 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
     if (!ok) break;
     tc_fence_after();
     {
-      uint32_t v0[32], v1[32];
-      tmem_ld32(tmem + t_lane + (uint32_t)PT_K, v0);
-      tmem_ld32(tmem + t_lane + (uint32_t)(PT_K + 32), v1);
+      uint32_t v0[32];
+      tmem_ld32(tmem + t_lane + (uint32_t)(PT_K + 32 * half), v0);   // dims 32 half ..
       tmem_ld_wait();
 #pragma unroll
-      for (int d = 0; d < 32; ++d) {
-        o[d] = fmaf(o[d], alpha, __uint_as_float(v0[d]));
-        o[32 + d] = fmaf(o[32 + d], alpha, __uint_as_float(v1[d]));
-      }
+      for (int d = 0; d < 32; ++d) o[d] = fmaf(o[d], alpha, __uint_as_float(v0[d]));
     }
+    // the next S MMA writes only S / P's columns, which every thread is done with; the next
+    // P.V MMA comes after two more barriers, so these P.V reads are complete by then
     tc_fence_before();
-    __syncthreads();   // every thread is done with this block's buffers and TMEM reads
-    tc_fence_after();
   }
   pdl_trigger();
+  // the row's sum of exponentials: this thread's key columns plus its partner's
+  __syncthreads();   // every thread is done with s_red
+  s_red[half * PT_Q + r] = l_run;
+  __syncthreads();
   if (ok && r < nq) {
-    const float inv = 1.0f / l_run;
+    const float inv = 1.0f / (l_run + s_red[(half ^ 1) * PT_Q + r]);
     const int ld = (std::is_same<AT, Split>::value ? 2 : 1) * H * HD;
 #pragma unroll
-    for (int d = 0; d < HD; d += 4) {
+    for (int d = 0; d < 32; d += 4) {
       float y[4] = {o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv};
-      act_store4<AT>(p.out, row0 + r, ld, h * HD + d, y);
+      act_store4<AT>(p.out, row0 + r, ld, h * HD + 32 * half + d, y);
     }
   }
   tc_fence_before();

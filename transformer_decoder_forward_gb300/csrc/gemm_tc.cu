@@ -9,16 +9,21 @@
 //   - warp 0, one lane: TMA producer. 128-byte-swizzled 128 x 64 slices of x_hi,
 //     x_lo and W go into a 3-stage shared-memory ring, each stage guarded by a
 //     "full" and an "empty" mbarrier; it runs ahead across tile boundaries.
-//   - warp 1, one lane: issues tcgen05.mma (M = 128, N = 128, K = 16, bf16 in,
-//     fp32 accumulate) for x_hi.W and x_lo.W into one of two 128 x 128 fp32
-//     accumulators in tensor memory, so the product carries the activations'
-//     full pair accuracy; tcgen05.commit releases each stage once the MMAs that
-//     read it finish, and marks the accumulator full after the tile's last one.
+//   - warp 1, one lane: issues tcgen05.mma with the weights on the M side and the
+//     tokens on N: M = 128 weight rows, N = 256 = the tile's 128 rows of x_hi then
+//     its 128 rows of x_lo (adjacent in the stage, so one B operand), K = 16, bf16
+//     in, fp32 accumulate, into one of two 128 x 256 accumulators in tensor memory.
+//     One MMA carries both halves of the activation pair, each operand byte is read
+//     from shared memory once per MMA, and the stage costs 24 KB of shared-memory
+//     traffic per 16 K rather than 28 KB with two 128 x 128 products: the kernel is
+//     bound by shared-memory bandwidth. tcgen05.commit releases each stage once the
+//     MMAs that read it finish, and marks the accumulator full after the tile's last.
 //   - warps 2-17: read a full accumulator with tcgen05.ld (warp w owns TMEM lanes
-//     32(w%4).. = tile rows, a quarter of the columns), hand it back to the MMA warp at once, stage it as
-//     an fp32 tile in shared memory and run the shared epilogue (bias, GELU /
-//     SwiGLU, RoPE + kv_write, residual add) while the MMA warp already fills the
-//     other accumulator with the next tile.
+//     32(w%4).. = weight rows, a quarter of the tokens), add the x_hi and x_lo
+//     columns, hand the accumulator back to the MMA warp, stage the tile transposed
+//     (tokens x weight rows, fp32) in shared memory and run the shared epilogue
+//     (bias, GELU / SwiGLU, RoPE + kv_write, residual add) while the MMA warp
+//     already fills the other accumulator with the next tile.
 // Every wait is bounded (FLAG_WAIT_TIMEOUT) and the tensor memory is always freed.
 #include <algorithm>
 
@@ -40,7 +45,8 @@ constexpr int STAGE = 2 * A_STAGE + B_STAGE;    // [x_hi][x_lo][W]
 constexpr int OT_LD = TC_BN + 1;                // epilogue tile row stride (floats): conflict-free row writes
 constexpr size_t OT_BYTES = (size_t)TC_BM * OT_LD * 4;
 constexpr int TC_ACC = 2;                       // accumulators in TMEM
-constexpr uint32_t TC_TMEM_COLS = TC_ACC * TC_BN;
+constexpr int TC_ACC_COLS = 2 * TC_BM;          // x_hi tokens, then x_lo tokens
+constexpr uint32_t TC_TMEM_COLS = TC_ACC * TC_ACC_COLS;   // all 512 columns
 constexpr size_t TC_SMEM = 1024 + (size_t)TC_STAGES * STAGE + OT_BYTES + 256;
 
 // Barrier among the epilogue warps only (named barrier 1), plain or with an AND of a
@@ -135,15 +141,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer: accumulator (local tile count) % 2
-      constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
+      // ---- MMA issuer: accumulator (local tile count) % 2; A = W tile, B = [x_hi; x_lo]
+      static_assert(TC_BN == 128 && 2 * TC_BM == 256, "M = 128 weight rows, N = 2 x 128 tokens");
+      constexpr uint32_t idesc = idesc_bf16(TC_BN, 2 * TC_BM);
       int it = 0, lt = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
         const int a = lt % TC_ACC;
         if (lt >= TC_ACC && !mbar_wait(&acc_empty[a], ((lt / TC_ACC) - 1) & 1, flags)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(a * TC_BN);
+        const uint32_t d = tmem + (uint32_t)(a * TC_ACC_COLS);
         for (int i = 0; i < kiters; ++i, ++it) {
           const int s = it % TC_STAGES;
           if (!mbar_wait(&full[s], (it / TC_STAGES) & 1, flags)) {
@@ -151,13 +158,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t da = sw128_desc(sA(s)), dal = sw128_desc(sAlo(s));
-          const uint64_t db = sw128_desc(sB(s));
+          const uint64_t dw = sw128_desc(sB(s));   // 128 weight rows
+          const uint64_t dx = sw128_desc(sA(s));   // 256 rows: x_hi, then x_lo at +A_STAGE
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk) {   // 16 bf16 = 32 bytes per MMA step
             const uint64_t o = (uint64_t)(kk * 2);
-            tc_mma(d, da + o, db + o, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-            tc_mma(d, dal + o, db + o, idesc, 1u);
+            tc_mma(d, dw + o, dx + o, idesc, (i > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&empty[s]);
         }
@@ -170,11 +176,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ---- epilogue warps: four per TMEM lane quadrant, each reading a quarter of the columns
+    // ---- epilogue warps: four per TMEM lane quadrant, each reading a quarter of the tokens
     const int et = threadIdx.x - 64;   // 0..511
-    const int q = warp & 3;            // TMEM lane quadrant = tile rows 32q..32q+31
-    const int quarter = (warp - 2) >> 2;   // columns 32 quarter .. 32 quarter + 31
-    const int row = q * 32 + lane;
+    const int q = warp & 3;            // TMEM lane quadrant = weight rows 32q..32q+31
+    const int quarter = (warp - 2) >> 2;   // tokens 32 quarter .. 32 quarter + 31
+    const int wrow = q * 32 + lane;
     pdl_wait();
     int lt = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
@@ -187,14 +193,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const bool ok = mbar_wait(&acc_full[a], (lt / TC_ACC) & 1, flags);
       if (!epi_bar_all(ok)) break;   // the epilogue warps leave together
       tc_fence_after();
-      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * TC_BN);
+      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * TC_ACC_COLS);
       {
         const int c0 = quarter * 32;
-        uint32_t r[32];
-        tmem_ld32(ta + (uint32_t)c0, r);
+        uint32_t rh[32], rl[32];
+        tmem_ld32(ta + (uint32_t)c0, rh);             // x_hi . W
+        tmem_ld32(ta + (uint32_t)(TC_BM + c0), rl);   // x_lo . W
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ot[row * OT_LD + c0 + j] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) ot[(c0 + j) * OT_LD + wrow] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
       }
       tc_fence_before();
       __syncwarp();

@@ -87,6 +87,15 @@ __device__ __forceinline__ void tc_mma_tf32_ts(uint32_t d, uint32_t a_tmem, uint
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// tcgen05.mma kind::f16 with A read from tensor memory: row m of A in TMEM lane m, two
+// 16-bit elements a 32-bit column (the lower K index in the low half), 8 columns per
+// 16-element K step.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Sixteen consecutive 32-bit columns of this thread's TMEM lane (warp w reaches lanes 32*(w%4)..+31).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
