@@ -43,7 +43,8 @@ constexpr int SW_THREADS = 192;
 constexpr int SW_ROWS = 128;                 // weight rows per tile (MMA M)
 constexpr int SW_A_BYTES = SW_ROWS * 128;    // one 128-byte K slice of 128 weight rows
 constexpr int SW_OT_LD = SW_ROWS + 4;        // output-tile row stride (floats): 16-byte rows
-constexpr int SW_MAX_KS = 8;                 // cluster size limit (portable)
+constexpr int SW_MAX_KS = 16;                // cluster size limit (non-portable; 8 is portable)
+constexpr int SW_RED_GROUP = 8;              // peers whose tiles one reduction round reads
 
 template <int NT, bool TF32>
 struct SwapCfg {
@@ -330,34 +331,46 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   float* red = ot + (size_t)NT * SW_OT_LD;
-  const float* src[SW_MAX_KS];
-#pragma unroll
-  for (int j = 0; j < SW_MAX_KS; ++j) src[j] = cluster.map_shared_rank(ot, j < ks_total ? j : 0);
   constexpr int C4 = SW_ROWS / 4;   // 16-byte reads of the peers' tiles
-  constexpr int RU = 2;              // row groups per thread per round: 2 x ks reads in flight
+  constexpr int RU = 2;              // row groups per thread per round: 2 x 8 reads in flight
   const int nwork = (r1 - r0) * C4;
   for (int i0 = threadIdx.x; i0 < nwork; i0 += RU * SW_THREADS) {
-    float4 v[RU][SW_MAX_KS];
+    float4 sum[RU];
 #pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      const int i = i0 + u * SW_THREADS;
-      const int m = r0 + i / C4, c = (i % C4) * 4;
+    for (int u = 0; u < RU; ++u) sum[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // peers in rank order, eight at a time; ranks past ks_total add exact zeros
+    for (int j0 = 0; j0 < ks_total; j0 += SW_RED_GROUP) {
+      float4 v[RU][SW_RED_GROUP];
 #pragma unroll
-      for (int j = 0; j < SW_MAX_KS; ++j)
-        v[u][j] = (i < nwork && j < ks_total) ? *reinterpret_cast<const float4*>(src[j] + m * SW_OT_LD + c)
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int jj = 0; jj < SW_RED_GROUP; ++jj) {
+        const int j = j0 + jj;
+        const float* src = cluster.map_shared_rank(ot, j < ks_total ? j : 0);
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+          const int i = i0 + u * SW_THREADS;
+          const int m = r0 + i / C4, c = (i % C4) * 4;
+          v[u][jj] = (i < nwork && j < ks_total) ? *reinterpret_cast<const float4*>(src + m * SW_OT_LD + c)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+#pragma unroll
+        for (int jj = 0; jj < SW_RED_GROUP; ++jj) {
+          if (j0 + jj == 0) {
+            sum[u] = v[u][jj];
+          } else {
+            sum[u].x += v[u][jj].x; sum[u].y += v[u][jj].y; sum[u].z += v[u][jj].z; sum[u].w += v[u][jj].w;
+          }
+        }
+      }
     }
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
       const int i = i0 + u * SW_THREADS;
       if (i >= nwork) break;
       const int m = r0 + i / C4, c = (i % C4) * 4;
-      float4 sum = v[u][0];
-#pragma unroll
-      for (int j = 1; j < SW_MAX_KS; ++j) {
-        sum.x += v[u][j].x; sum.y += v[u][j].y; sum.z += v[u][j].z; sum.w += v[u][j].w;
-      }
-      *reinterpret_cast<float4*>(red + (m - r0) * SW_OT_LD + c) = sum;
+      *reinterpret_cast<float4*>(red + (m - r0) * SW_OT_LD + c) = sum[u];
     }
   }
   // the peers may still read this CTA's tile: signal that this CTA is done reading theirs,
@@ -380,7 +393,7 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -401,14 +414,14 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
         cudaGetLastError();
-        n = num_sms / c;
+        n = c <= 8 ? num_sms / c : 0;   // a non-portable size the driver does not confirm is not used
       }
       capacity[c] = n * c;
     }
     return capacity[c];
   };
   int ks = 1;
-  for (int c = 2; c <= SW_MAX_KS; ++c)   // any cluster size: 6 ranks pack a GPC better than 8
+  for (int c = 2; c <= SW_MAX_KS; ++c)   // any cluster size: 6 ranks pack a GPC better than 8, 12 or 16 halve long K
     if (tiles * c <= wave(c) && p.K / c >= 2 * C::KE) ks = c;
   int kcta = (p.K + ks - 1) / ks;
   kcta = ((kcta + C::KE - 1) / C::KE) * C::KE;
