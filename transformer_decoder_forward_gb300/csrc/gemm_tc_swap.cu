@@ -52,8 +52,9 @@ struct SwapCfg {
   static constexpr int RAW = SW_A_BYTES + (TF32 ? 1 : 2) * B_BYTES;   // TMA stage: [W][X] or [W][X_hi][X_lo]
   static constexpr int CONVB = 2 * B_BYTES;             // tf32: [X hi][X lo] (the weight parts sit in TMEM)
   // TMA stages: bf16 keeps up to 4 within ~100 KB (a second CTA fits on the SM); tf32 keeps
-  // up to 6 raw stages (one CTA an SM) plus 2 converted buffers (1 for the widest tiles).
-  static constexpr int NRAW = TF32 ? (NT <= 64 ? 6 : (NT <= 128 ? 4 : 2))
+  // 4 raw stages for up to 32 tokens (about 97 KB, two CTAs an SM, so split-K clusters can
+  // be twice as large), 6 for 64 (one CTA an SM), plus 2 converted buffers (1 for the widest).
+  static constexpr int NRAW = TF32 ? (NT <= 32 ? 4 : (NT <= 64 ? 6 : (NT <= 128 ? 4 : 2)))
                                    : (4 * RAW <= 100 * 1024 ? 4 : (3 * RAW <= 100 * 1024 ? 3 : 2));
   static constexpr int NCONV = TF32 ? (NT <= 128 ? 2 : 1) : 0;
   static constexpr size_t PIPE = (size_t)NRAW * RAW + (size_t)NCONV * CONVB;
