@@ -179,8 +179,16 @@ llm_status llm_decode_step_host(llm_handle* h, const int32_t* tokens, const int3
  * Returns LLM_ERR_DEVICE_FLAG when any bit was set, LLM_OK otherwise. */
 llm_status llm_get_error_flags(llm_handle* h, uint32_t* flags);
 
-/* Per-kernel timing. While enabled, steps run without graph replay and every
- * launch is bracketed by CUDA events on the handle's stream. */
+/* Self-test of the device-side bounded wait: launches, on the handle's stream, one
+ * kernel that waits on a barrier nothing completes. The wait gives up after its limit
+ * (about 2^31 SM clocks, one second) and sets LLM_FLAG_WAIT_TIMEOUT, which the next
+ * llm_get_error_flags returns; the context stays usable. Asynchronous. */
+llm_status llm_selftest_wait_timeout(llm_handle* h);
+
+/* Per-kernel timing. While enabled, every launch is bracketed by CUDA events on the
+ * handle's stream. A decode step is captured as a graph with an event record node
+ * around each kernel and replayed once (programmatic launch off), so the events time
+ * the kernels back to back on the device; prefill launches run eagerly. */
 typedef struct {
   char name[48];
   int launches;

@@ -201,6 +201,31 @@ def test_device_error_flags_and_host_status(gpu_lib, small_models):
     run.close()
 
 
+def test_bounded_wait_gives_up_sets_flag_and_context_stays_usable(gpu_lib, small_models):
+    """A device wait on a barrier that nothing completes gives up after its limit (about one
+    second of SM clocks), sets the wait-timeout bit for the host, and later steps still run and
+    match a fresh run bit for bit."""
+    import time
+    import transformer_decoder_forward_gb300 as L
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, _ = small_models[SMALL_GPT2.name]
+    stream = wl.draw_stream(len(LENGTHS), STEPS, SMALL_GPT2.vocab)
+    ref = WorkloadRun(small_workload(SMALL_GPT2), host_weights=w, lengths=LENGTHS)
+    want = run_gpu_teacher(ref, stream)
+    ref.close()
+    run = WorkloadRun(small_workload(SMALL_GPT2), host_weights=w, lengths=LENGTHS)
+    assert run.dec.error_flags() == 0
+    t0 = time.monotonic()
+    run.dec.selftest_wait_timeout()
+    assert run.dec.error_flags() == L.FLAG_WAIT_TIMEOUT
+    assert 0.2 < time.monotonic() - t0 < 30.0
+    got = run_gpu_teacher(run, stream)
+    assert run.dec.error_flags() == 0
+    np.testing.assert_array_equal(got[0], want[0])
+    np.testing.assert_array_equal(got[1], want[1])
+    run.close()
+
+
 # ------------------------------------------------------------------------------------------------
 # the five workloads at their full sizes, in the launch configuration the bench uses
 # ------------------------------------------------------------------------------------------------

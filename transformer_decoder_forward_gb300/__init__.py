@@ -21,7 +21,7 @@ STATUS = {0: "LLM_OK", 1: "LLM_ERR_INVALID_ARG", 2: "LLM_ERR_OUT_OF_RANGE", 3: "
 FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8, 16
 
 EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_decode_step", "llm_decode_step_host",
-           "llm_get_error_flags", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
+           "llm_get_error_flags", "llm_selftest_wait_timeout", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
            "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode", "llm_op_attention_decode_noalloc",
            "llm_status_string", "llm_last_error"]
 
@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_decode_step_host.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp]
     lib.llm_get_error_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.llm_set_profiling.argtypes = [vp, ctypes.c_int]
+    lib.llm_selftest_wait_timeout.argtypes = [vp]
     lib.llm_get_kernel_stats.argtypes = [vp, ctypes.POINTER(KernelStat), ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                          ctypes.c_int]
     lib.llm_last_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -87,7 +88,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_last_error.argtypes = []
     lib.llm_last_error.restype = ctypes.c_char_p
     for name in ("llm_create", "llm_prefill", "llm_decode_step", "llm_decode_step_host", "llm_get_error_flags",
-                 "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
+                 "llm_set_profiling", "llm_selftest_wait_timeout", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
                  "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode",
                  "llm_op_attention_decode_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
@@ -225,6 +226,11 @@ class Decoder:
         if st not in (LLM_OK, 7):
             _check(st)
         return int(f.value)
+
+    def selftest_wait_timeout(self) -> None:
+        """Launch a kernel whose bounded wait runs out (about one second); the next
+        error_flags() returns LLM_FLAG_WAIT_TIMEOUT."""
+        _check(self.lib.llm_selftest_wait_timeout(self.handle))
 
     def set_profiling(self, on: bool) -> None:
         _check(self.lib.llm_set_profiling(self.handle, int(on)))

@@ -708,6 +708,13 @@ llm_status llm_get_error_flags(llm_handle* h, uint32_t* flags) {
   return v ? fail(LLM_ERR_DEVICE_FLAG, "device error flags 0x" + std::to_string(v)) : LLM_OK;
 }
 
+llm_status llm_selftest_wait_timeout(llm_handle* h) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  CUDA_TRY(launch_selftest_wait(h->flags, h->stream));
+  return LLM_OK;
+}
+
 llm_status llm_set_profiling(llm_handle* h, int enable) {
   llm_status st = check_handle(h);
   if (st != LLM_OK) return st;

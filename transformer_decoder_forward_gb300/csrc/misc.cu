@@ -177,4 +177,21 @@ cudaError_t launch_set_args(StepArgs* dst, const StepArgs& v, cudaStream_t s) {
 
 const void* set_args_kernel() { return reinterpret_cast<const void*>(&k_set_args); }
 
+// Self-test of the bounded wait every kernel uses: an mbarrier that nothing arrives at, so
+// the wait gives up after its limit (about one second) and sets FLAG_WAIT_TIMEOUT.
+__global__ void k_selftest_wait(unsigned* flags) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, flags);
+}
+
+cudaError_t launch_selftest_wait(unsigned* flags, cudaStream_t s) {
+  k_selftest_wait<<<1, 32, 0, s>>>(flags);
+  return cudaGetLastError();
+}
+
 }  // namespace llm

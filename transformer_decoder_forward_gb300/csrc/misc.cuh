@@ -40,5 +40,6 @@ cudaError_t launch_norm(const NormParams& p, int wdt, int adt, cudaStream_t s, b
 cudaError_t launch_argmax(const ArgmaxParams& p, int B, cudaStream_t s, bool pdl);
 cudaError_t launch_set_args(StepArgs* dst, const StepArgs& v, cudaStream_t s);
 const void* set_args_kernel();
+cudaError_t launch_selftest_wait(unsigned* flags, cudaStream_t s);
 
 }  // namespace llm
