@@ -421,12 +421,21 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
     }
     return capacity[c];
   };
-  int ks = 1;
-  for (int c = 2; c <= SW_MAX_KS; ++c)   // any cluster size: 6 ranks pack a GPC better than 8, 12 or 16 halve long K
-    if (tiles * c <= wave(c) && p.K / c >= 2 * C::KE) ks = c;
-  int kcta = (p.K + ks - 1) / ks;
-  kcta = ((kcta + C::KE - 1) / C::KE) * C::KE;
-  ks = (p.K + kcta - 1) / kcta;
+  // Candidate splits in whole K stages: r ranks of s = ceil(stages / r) stages each (the last
+  // rank may hold fewer), kept when every rank but the last streams at least two stages and
+  // the grid is one wave; the most ranks win. Any size is allowed: 6 ranks pack a 19-SM GPC
+  // better than 8, and 12 or 16 shorten long K.
+  const int stages = (p.K + C::KE - 1) / C::KE;
+  int ks = 1, kst = stages;   // ranks, stages per rank
+  for (int c = 2; c <= SW_MAX_KS; ++c) {
+    const int spr = (stages + c - 1) / c;
+    const int ranks = (stages + spr - 1) / spr;
+    if (spr >= 2 && ranks > ks && tiles * ranks <= wave(ranks)) {
+      ks = ranks;
+      kst = spr;
+    }
+  }
+  const int kcta = kst * C::KE;
   const int dt = TF32 ? DT_F32 : DT_BF16;
   CUtensorMap mw, mx, mxl;
   if (!make_map(&mw, p.W, dt, wrows, p.K, p.K, p.swiglu ? 32 : SW_ROWS)) return cudaErrorInvalidValue;
