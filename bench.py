@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
-BASELINE_METRIC = "decode tok/s at batch B and prefill tok/s; % of GB300 HBM BW / bf16 TC peak"
+METRIC = "decode tok/s at batch B and prefill tok/s; % of GB300 HBM BW / bf16 TC peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -255,7 +255,7 @@ def run_reference(args, W):
         dt = time.perf_counter() - t0
         rate = n * len(prompt) / dt
         desc = f"float64 NumPy oracle, stateless forward of 1 of {W.batch} prompts ({len(prompt)} tokens), {n} times"
-        line = {"impl": "reference", "metric": BASELINE_METRIC, "metric_detail": "prefill tok/s", "value": rate,
+        line = {"impl": "reference", "metric": METRIC, "metric_detail": "prefill tok/s", "value": rate,
                 "unit": "tok/s", "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": 1000.0 * dt / n,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": W.name, "batch": W.batch, "prompt_len": len(prompt)},
@@ -264,7 +264,7 @@ def run_reference(args, W):
         print(json.dumps(line), flush=True)
         return 0
     rate, dt, desc = oracle_decode_rate(W, args.steps, args.warmup, n_seq=1)
-    line = {"impl": "reference", "metric": BASELINE_METRIC, "metric_detail": f"decode tok/s at batch {W.batch}",
+    line = {"impl": "reference", "metric": METRIC, "metric_detail": f"decode tok/s at batch {W.batch}",
             "value": rate, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -383,7 +383,7 @@ def run_decode_bench(args, W):
     e2e = {"value": B * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * 4,
            "steps": n_e2e, "api": "llm_decode_step_host"}
 
-    line = {"metric": BASELINE_METRIC, "metric_detail": f"decode tok/s at batch {B}", "value": value,
+    line = {"metric": METRIC, "metric_detail": f"decode tok/s at batch {B}", "value": value,
             "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
@@ -491,7 +491,7 @@ def run_prefill_bench(args, W):
     e2e_s = time.perf_counter() - t0
     e2e = {"value": tokens_total * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": int(tok_h.numel() * 4),
            "d2h_bytes_per_step": B * 4, "steps": n_e2e, "api": "llm_prefill (pinned host ids in, ids out)"}
-    line = {"metric": BASELINE_METRIC, "metric_detail": f"prefill tok/s, {B} x {int(run.lengths[0])} tokens",
+    line = {"metric": METRIC, "metric_detail": f"prefill tok/s, {B} x {int(run.lengths[0])} tokens",
             "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
