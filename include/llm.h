@@ -54,7 +54,7 @@ typedef enum {
   LLM_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, inconsistent config */
   LLM_ERR_OUT_OF_RANGE = 2,  /* a size beyond what the handle was created for */
   LLM_ERR_NO_DEVICE = 3,     /* no CUDA device, or not a compute capability 10.3 device */
-  LLM_ERR_UNSUPPORTED = 4,   /* a config this build does not implement (e.g. head_dim != 64) */
+  LLM_ERR_UNSUPPORTED = 4,   /* a config the library does not implement (e.g. head_dim != 64) */
   LLM_ERR_OOM = 5,           /* device allocation failed in llm_create */
   LLM_ERR_CUDA = 6,          /* a CUDA runtime call failed */
   LLM_ERR_DEVICE_FLAG = 7    /* llm_get_error_flags found a device-side error bit set */

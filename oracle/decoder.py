@@ -24,7 +24,7 @@ cache remark in "batch_forge"):
 * ``forward_full`` recomputes the whole sequence (stateless, O(T^2) per step);
 * ``Sequence.prefill`` / ``Sequence.step`` keep per-layer K/V arrays.
 
-Readings where the pages leave the step open (each is listed in the design doc):
+Readings where the pages leave the step open:
 GELU is GPT-2's tanh form with the tanh argument clamped to [-15, 15]
 ("batch_forge", GELU-overflow paragraph); LayerNorm uses the biased variance
 with eps inside the square root; RMSNorm is x / sqrt(mean(x^2) + eps) * g; RoPE

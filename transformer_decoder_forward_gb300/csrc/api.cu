@@ -420,7 +420,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   cudaDeviceProp prop;
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return fail(LLM_ERR_NO_DEVICE, "cannot query device");
   if (!(prop.major == 10 && prop.minor == 3))
-    return fail(LLM_ERR_NO_DEVICE, "this build runs on compute capability 10.3 (GB300) only");
+    return fail(LLM_ERR_NO_DEVICE, "the library runs on compute capability 10.3 (GB300) only");
 
   llm_handle* h = new llm_handle();
   h->cfg = c;
