@@ -490,7 +490,8 @@ cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
               : G == 3 ? k_attn_decode_split<KT, AT, 3>
               : G == 4 ? k_attn_decode_split<KT, AT, 4>
                        : k_attn_decode_split<KT, AT, 8>;
-  static bool attr_set[9] = {};
+  static bool attr_set_dev[MAX_DEVICES][9] = {};
+  bool* attr_set = attr_set_dev[current_device()];
   if (!attr_set[G]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AttnRing<KT>::SMEM);
     if (e != cudaSuccess) return e;
@@ -509,7 +510,8 @@ cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
 template <typename KT, typename AT>
 cudaError_t prefill_t(const AttnPrefillParams& p, cudaStream_t s, bool pdl) {
   const size_t smem = (size_t)(2 * HD * AP_LD + 2 * AP_T * AP_LD) * sizeof(float);
-  static bool attr_set = false;
+  static bool attr_set_dev[MAX_DEVICES] = {};
+  bool& attr_set = attr_set_dev[current_device()];
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<KT, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);

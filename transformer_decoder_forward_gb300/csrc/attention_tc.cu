@@ -332,7 +332,8 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
 
 template <typename AT>
 cudaError_t prefill_tc_t(const AttnPrefillParams& p, cudaStream_t s, bool pdl) {
-  static bool attr_set = false;
+  static bool attr_set_dev[MAX_DEVICES] = {};
+  bool& attr_set = attr_set_dev[current_device()];
   if (!attr_set) {
     cudaError_t e =
         cudaFuncSetAttribute(k_attn_prefill_tc<AT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PT_SMEM);

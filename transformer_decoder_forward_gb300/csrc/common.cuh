@@ -13,6 +13,15 @@ enum : int { ARCH_GPT2 = 0, ARCH_LLAMA = 1 };
 constexpr int HD = 64;          // head_dim (the only supported value)
 constexpr int KVB = 16;         // tokens per KV block
 
+// Launch state that belongs to a device (function attributes, occupancy answers) is cached
+// per device, so one process may drive several GPUs.
+constexpr int MAX_DEVICES = 64;
+inline int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return 0;
+  return d % MAX_DEVICES;
+}
+
 // Device error word bits (mirrors LLM_FLAG_* in include/llm.h).
 constexpr unsigned FLAG_BAD_TOKEN = 0x01u;
 constexpr unsigned FLAG_BAD_POSITION = 0x02u;

@@ -239,7 +239,8 @@ cudaError_t launch_gemm_tc(const LinearParams& p, int num_sms, cudaStream_t s, b
   if (!make_map(&mb, p.W, DT_BF16, wrows, p.K, p.K, p.swiglu ? 32 : TC_BN)) return cudaErrorInvalidValue;
   const int tiles_n = p.swiglu ? (p.N + 63) / 64 : (p.N + TC_BN - 1) / TC_BN;
   const int tiles_m = (p.M + TC_BM - 1) / TC_BM;
-  static bool attr_set = false;
+  static bool attr_set_dev[MAX_DEVICES] = {};
+  bool& attr_set = attr_set_dev[current_device()];
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
     if (e != cudaSuccess) return e;

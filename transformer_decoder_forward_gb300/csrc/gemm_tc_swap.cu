@@ -391,14 +391,16 @@ cudaError_t launch_nt(const LinearParams& p, int num_sms, cudaStream_t s, bool p
   // grid still runs as one wave (the cluster occupancy the driver reports for this kernel),
   // with at least two K stages per CTA. Sizes need not be powers of two.
   auto kern = k_gemm_tc_swap<NT, TF32>;
-  static bool attr_set = false;
+  static bool attr_set_dev[MAX_DEVICES] = {};
+  bool& attr_set = attr_set_dev[current_device()];
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  static int capacity[SW_MAX_KS + 1] = {0};   // CTAs of one wave per cluster size
+  static int capacity_dev[MAX_DEVICES][SW_MAX_KS + 1] = {};   // CTAs of one wave per cluster size
+  int* capacity = capacity_dev[current_device()];
   auto wave = [&](int c) {
     if (!capacity[c]) {
       cudaLaunchConfig_t q = {};

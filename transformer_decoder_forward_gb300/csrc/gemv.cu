@@ -294,7 +294,8 @@ cudaError_t launch_t(const LinearParams& p, int num_sms, cudaStream_t s, bool pd
   const size_t smem = gemv_smem(MT, kcta);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   auto kern = k_gemv<WT, MT>;
-  static bool attr_set = false;
+  static bool attr_set_dev[MAX_DEVICES] = {};
+  bool& attr_set = attr_set_dev[current_device()];
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
