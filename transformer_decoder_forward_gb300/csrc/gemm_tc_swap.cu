@@ -17,13 +17,14 @@
 //     conversion; the MMA sums W_hi.X_hi + W_hi.X_lo + W_lo.X_hi (three tf32
 //     products, fp32-level accuracy). The weight parts go to tensor memory (each
 //     thread owns one weight row, its TMEM lane) and the MMAs read A from there: read
-//     three times from shared memory instead, the weight tile made the stage shared-
-//     memory bound (about 140 KB of shared-memory traffic for 16 KB of weights).
+//     three times from shared memory instead, the weight tile costs about 140 KB of
+//     shared-memory traffic per 16 KB of weights.
 //     After the last MMA they read the accumulator with tcgen05.ld and stage it
 //     transposed (tokens x weight rows) for the shared epilogue.
-// Small matrices split K across a thread-block cluster; partial tiles are summed in
-// rank order through distributed shared memory. The split and the stage count
-// depend on the weight shape only. Every wait is bounded and TMEM is always freed.
+// Small matrices split K across a thread-block cluster of up to 16 CTAs; partial tiles
+// are summed in rank order through distributed shared memory. The split depends on the
+// weight shape and the cluster occupancy of the kernel variant, never on the data. Every
+// wait is bounded and TMEM is always freed.
 #include <cooperative_groups.h>
 
 #include <algorithm>
