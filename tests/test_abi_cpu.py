@@ -98,3 +98,40 @@ def test_calls_on_a_null_handle_fail_cleanly(lib):
     lib.llm_destroy(None)
     assert lib.llm_status_string(0) == b"ok"
     assert lib.llm_status_string(7) == b"device error flag set"
+
+
+def test_control_calls_on_a_null_handle_fail_cleanly(lib):
+    n = ctypes.c_int(0)
+    assert lib.llm_selftest_wait_timeout(None) == 1
+    assert lib.llm_set_profiling(None, 1) == 1
+    assert lib.llm_set_graphs(None, 1) == 1
+    assert lib.llm_set_linear_variant(None, 1) == 1
+    assert lib.llm_last_launch_count(None, ctypes.byref(n)) == 1
+    assert lib.llm_get_kernel_stats(None, None, 0, ctypes.byref(n), 0) == 1
+
+
+def test_op_linear_checks_arguments_on_the_host(lib):
+    p = ctypes.c_void_p(256)   # never dereferenced: every call below fails its host checks
+    F32, BF16 = 0, 1
+    assert lib.llm_op_linear(F32, 0, 8, 8, p, p, None, p, 1, None) == 1       # size
+    assert lib.llm_op_linear(F32, 4, 8, 8, None, p, None, p, 1, None) == 1    # NULL x
+    assert lib.llm_op_linear(7, 4, 8, 8, p, p, None, p, 1, None) == 1         # dtype
+    assert lib.llm_op_linear(F32, 4, 8, 8, p, p, None, p, 0, None) == 1       # variant
+    assert lib.llm_op_linear(F32, 4, 8, 8, p, p, None, p, 3, None) == 4       # tcgen05 prefill GEMM is bf16 only
+    assert lib.llm_op_linear(BF16, 4, 8, 12, p, p, None, p, 4, None) == 1     # K % 8
+    assert lib.llm_op_linear(BF16, 300, 8, 16, p, p, None, p, 4, None) == 1   # weights-on-M path: M <= 256
+    assert b"256" in lib.llm_last_error()
+
+
+@pytest.mark.parametrize("entry", ["llm_op_attention_decode", "llm_op_attention_decode_noalloc"])
+def test_op_attention_decode_checks_arguments_on_the_host(lib, entry):
+    f = getattr(lib, entry)
+    p = ctypes.c_void_p(256)
+    #        kv_dtype, B, H, Hkv, q, k, v, blocks, pos, tables, mbps, out, stream
+    assert f(0, 0, 12, 12, p, p, p, 8, p, p, 4, p, None) == 1        # B
+    assert f(0, 2, 12, 12, None, p, p, 8, p, p, 4, p, None) == 1     # NULL q
+    assert f(5, 2, 12, 12, p, p, p, 8, p, p, 4, p, None) == 1        # kv dtype
+    assert f(0, 2, 12, 5, p, p, p, 8, p, p, 4, p, None) == 1         # H % Hkv
+    assert f(0, 2, 18, 2, p, p, p, 8, p, p, 4, p, None) == 1         # more than 8 query heads a KV head
+    if entry.endswith("noalloc"):                                    # scratch beyond the fixed array
+        assert f(0, 256, 64, 8, p, p, p, 8, p, p, 4096, p, None) == 2
