@@ -1,19 +1,22 @@
 #!/usr/bin/env python3
 """Benchmark of the GB300 KV-cached decoder step.
 
-Default workload: GPT-2-124M-shaped fp32 decoder, batch 32, 128-token prompts,
-decode positions 128..255 (the teacher-forced 128-step workload), contiguous
-KV cache. One bench step = one batched decode step (every row of the hot path:
-embed, norm+QKV+RoPE/kv_write, paged attention, O+residual, norm+FFN, final
-norm + tied head + argmax), replayed as one CUDA graph. Decode positions cycle
-through the workload's 128 steps, so every 128 bench steps are exactly one pass
-of the workload.
+Default workload: the GPT-2-XL-shaped bf16 decoder, batch 256, 960-token prompts in shuffled
+paged blocks, decode positions 960..1023 (its 64 teacher-forced steps, the last one attending
+over 1024 keys). One bench step = one batched decode step (every row of the hot path: embed,
+norm+QKV(+RoPE)/kv_write, paged attention, O+residual, norm+FFN, final norm + tied head +
+argmax), replayed as one CUDA graph. Decode positions cycle through the workload's steps, so
+every `decode_steps` bench steps are exactly one pass of the workload.
 
---impl reference times the float64 CPU oracle on the host cores on a bounded
-sample of the same workload (test infrastructure, never the product path).
+The same JSON line carries a "prefill" object: prefill tok/s of the GPT-2-124M-shaped bf16
+model on 16 x 1024-token prompts (one step = one llm_prefill of all 16 prompts), with its own
+tensor-core roofline, CPU baseline and end-to-end figure.
 
-Prints one JSON line (rank 0). Multi-GPU: launched by torchrun, one replica per
-rank (the decode batch shards by sequence; no data-path collective).
+--impl reference times the float64 CPU oracle on the host cores on a bounded sample of the same
+workloads (test infrastructure, never the product path).
+
+Prints one JSON line (rank 0). Multi-GPU: launched by torchrun, one replica per rank (the decode
+batch shards by sequence; no data-path collective).
 """
 from __future__ import annotations
 
@@ -27,6 +30,11 @@ import threading
 import time
 
 import numpy as np
+
+try:
+    import torch.distributed as dist
+except Exception:   # the reference arm runs without torch
+    dist = None
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -53,8 +61,8 @@ def peaks():
 # DRAM traffic per launch of each workload's dominant kernel family, from one single-pass ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum summed over one decode step's or one
 # prefill's launches of that family, divided by the launch count). It holds for the kernel
-# build the capture was taken on; the bench reports it when its dominant family matches. The
-# commands and per-launch figures: profiles/dram_traffic_dominant_kernels.md.
+# build the capture was taken on; the bench reports it when its dominant family matches, and
+# the commands and per-launch figures sit with the other profile summaries.
 TRAFFIC = {
     "gpt2-124m-fp32-b32-teacher": ("proj (gemm_tcs)", 10.392e6),
     "gpt2-124m-fp32-b1-greedy": ("proj (gemv)", 10.185e6),
@@ -239,28 +247,51 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def run_reference(args, W):
+# Bounded CPU sample of each decode workload for the oracle: (sequences, decode steps). The
+# prefill that fills each sampled sequence's cache is untimed.
+CPU_SAMPLE = {
+    wl.W_GPT2XL_B256.name: (2, 2),
+    wl.W_SMOLLM2_B64.name: (2, 1),
+    wl.W_GPT2_F32_B32.name: (1, 256),
+    wl.W_GPT2_F32_B32_X8.name: (1, 256),
+    wl.W_GPT2_F32_B1.name: (1, 16),
+}
+
+
+def oracle_prefill_rate(W: wl.Workload, n: int = 1, weights=None):
+    """Time the float64 oracle's stateless forward over one prompt of a prefill workload, n times.
+    Returns (tok/s, seconds, description)."""
+    import oracle
+    w = weights or wl.make_weights(W.model, scale=W.weight_scale)
+    model = oracle.OracleModel(w)
+    prompt = wl.draw_prompts(W.lengths(), W.model.vocab)[0]
+    t0 = time.perf_counter()
+    for _ in range(n):
+        oracle.forward_full(model, prompt, last_only=True)
+    dt = time.perf_counter() - t0
+    desc = (f"float64 NumPy oracle, stateless forward of 1 of {W.batch} prompts ({len(prompt)} tokens), "
+            f"{n} time(s)")
+    return n * len(prompt) / dt, dt, desc
+
+
+def reference_prefill_object(W: wl.Workload, n: int):
+    rate, dt, desc = oracle_prefill_rate(W, n)
+    return {"metric_detail": f"prefill tok/s, {W.batch} x {int(W.lengths()[0])} tokens", "value": rate,
+            "unit": "tok/s", "ms_per_step": 1000.0 * dt / n, "steps": n, "dtype": "f64",
+            "config": {"workload": W.name, "batch": W.batch, "prompt_len": int(W.lengths()[0])},
+            "cpu_baseline": {"value": rate, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": rate, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_reference(args, W, PW):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     if W.mode == "prefill" or W.decode_steps == 0:
-        import oracle
-        w = wl.make_weights(W.model, scale=W.weight_scale)
-        model = oracle.OracleModel(w)
-        prompt = wl.draw_prompts(W.lengths(), W.model.vocab)[0]
         n = max(1, min(args.steps, 3))
-        t0 = time.perf_counter()
-        for _ in range(n):
-            oracle.forward_full(model, prompt, last_only=True)
-        dt = time.perf_counter() - t0
-        rate = n * len(prompt) / dt
-        desc = f"float64 NumPy oracle, stateless forward of 1 of {W.batch} prompts ({len(prompt)} tokens), {n} times"
-        line = {"impl": "reference", "metric": METRIC, "metric_detail": "prefill tok/s", "value": rate,
-                "unit": "tok/s", "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": 1000.0 * dt / n,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": W.name, "batch": W.batch, "prompt_len": len(prompt)},
-                "cpu_baseline": {"value": rate, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc},
-                "e2e": {"value": rate, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        obj = reference_prefill_object(W, n)
+        line = {"impl": "reference", "metric": METRIC, "n_gpus": args.gpus, "warmup": 0,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic", **obj}
         print(json.dumps(line), flush=True)
         return 0
     rate, dt, desc = oracle_decode_rate(W, args.steps, args.warmup, n_seq=1)
@@ -272,6 +303,8 @@ def run_reference(args, W):
                        "decode_steps_cycled": W.decode_steps},
             "cpu_baseline": {"value": rate, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc},
             "e2e": {"value": rate, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    if PW is not None:
+        line["prefill"] = reference_prefill_object(PW, 1)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -280,17 +313,33 @@ def run_reference(args, W):
 # GPU arm
 # ------------------------------------------------------------------------------------------------
 
-def run_decode_bench(args, W):
-    import torch
-    import torch.distributed as dist
-    from transformer_decoder_forward_gb300.runner import WorkloadRun
+def family_roofline(fams: dict, dom: str, steps_profiled: int, ms_step: float, alg_total: float, unit: str,
+                    peak: float, peak_source: str, label: str, traffic):
+    launches, dom_ms = fams[dom]
+    total_ms = sum(v[1] for v in fams.values())
+    share = dom_ms / total_ms
+    per_step_events = dom_ms / steps_profiled
+    if per_step_events <= ms_step:
+        per_step, method = per_step_events, "CUDA events around every launch (profiled graph replay)"
+    else:
+        per_step, method = share * ms_step, "share of the event-timed launches x the timed step"
+    assert per_step <= ms_step * (1 + 1e-9), "dominant family's time per step exceeds the step"
+    avg_launch_s = per_step * steps_profiled / launches / 1000.0
+    per_launch = alg_total / launches
+    scale = 1e9 if unit == "GB/s" else 1e12
+    achieved = per_launch / avg_launch_s / scale
+    return {"bound": "hbm" if unit == "GB/s" else "tensor", "kernel": label, "launches": launches,
+            "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak, "traffic": traffic,
+            "peak_source": peak_source,
+            ("alg_bytes_per_launch" if unit == "GB/s" else "alg_flops_per_launch"): per_launch,
+            "avg_launch_us": avg_launch_s * 1e6, "duration_method": method,
+            "family_ms_per_step": per_step, "family_share": share,
+            "event_ms_per_step": per_step_events}
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
+
+def decode_part(args, W, world: int, rank: int, local: int) -> dict:
+    import torch
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
 
     s = W.model
     host_w = wl.make_weights(s, scale=W.weight_scale)
@@ -325,17 +374,18 @@ def run_decode_bench(args, W):
         if world > 1:
             dist.barrier()
     ms, tokens, value = job_rate(ev0.elapsed_time(ev1), B * args.steps, world)
+    ms_step = ms / args.steps
     assert run.dec.error_flags() == 0, "device error flags set during the bench"
 
-    # ---- per-kernel durations (CUDA events around every launch, one pass of the workload)
+    # ---- per-kernel durations: the timed steps' positions once more, CUDA events around every launch
+    n_prof = min(args.steps, period)
     run.dec.set_profiling(True)
     run.dec.kernel_stats(reset=True)
-    for i in range(period):
+    for i in range(n_prof):
         step(i)
     stats = run.dec.kernel_stats(reset=True)
     run.dec.set_profiling(False)
-    fam = {}
-    kinds = {}
+    fam, kinds = {}, {}
     for name, (n, t) in stats.items():
         # every projection kernel (CUDA-core GEMV or tcgen05) is one family: they share the
         # weight-stream roofline
@@ -347,24 +397,20 @@ def run_decode_bench(args, W):
         a[1] += t
     dom = max(fam, key=lambda k: fam[k][1])
     pk, pk_kind = peaks()
-    ctx_steps = np.stack([run.lengths + j + 1 for j in range(period)])          # keys read per step
+    ctx_of = lambda i: run.lengths + (i % period) + 1        # keys read by step i
     if dom == "proj":
-        alg = gemv_bytes(s, B) * period
+        alg = float(gemv_bytes(s, B)) * n_prof
     elif dom == "attn_decode":
-        alg = sum(attn_bytes(s, c) for c in ctx_steps)
+        alg = float(sum(attn_bytes(s, ctx_of(i)) for i in range(n_prof)))
     else:
         alg = None
-    dom_ms = fam[dom][1]
-    achieved = alg / (dom_ms / 1000.0) / 1e9 if alg else None
-    roof = {"bound": "hbm", "kernel": dom if dom != "proj" else "proj (" + "+".join(sorted(kinds)) + ")",
-            "launches": fam[dom][0], "achieved": achieved, "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "traffic": None,
-            "peak_source": f"hbm_gbs of {pk_kind}",
-            "alg_bytes_per_launch": (alg / fam[dom][0]) if alg else None,
-            "avg_launch_us": 1000.0 * dom_ms / fam[dom][0]}
-    roof["traffic"] = traffic_for(W.name, roof["kernel"])
-    step_alg = float(np.mean([step_bytes(s, c) for c in ctx_steps]))
-    step_gbs = step_alg / (ms / args.steps / 1000.0) / 1e9
+    label = dom if dom != "proj" else "proj (" + "+".join(sorted(kinds)) + ")"
+    roof = None
+    if alg is not None:
+        roof = family_roofline(fam, dom, n_prof, ms_step, alg, "GB/s", pk["hbm_gbs"], f"hbm_gbs of {pk_kind}",
+                               label, traffic_for(W.name, label))
+    step_alg = float(np.mean([step_bytes(s, ctx_of(i)) for i in range(args.steps)]))
+    step_gbs = step_alg / (ms_step / 1000.0) / 1e9
     kernel_share = {k: round(v[1] / sum(x[1] for x in fam.values()), 4) for k, v in sorted(fam.items())}
 
     # ---- end to end through the C ABI with host buffers (H2D inputs, D2H ids, every step)
@@ -380,61 +426,58 @@ def run_decode_bench(args, W):
         run.dec.decode_step_host(tok_h[j], pos_h[j], tables_h, ids_h)
     e2e_s = time.perf_counter() - t0
     h2d = B * 4 * 2 + (0 if tables_h is None else tables_h.nbytes)
-    e2e = {"value": B * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * 4,
+    e2e = {"value": B * n_e2e / e2e_s * world, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * 4,
            "steps": n_e2e, "api": "llm_decode_step_host"}
-
+    ctx_lo, ctx_hi = int(run.lengths.min()) + 1, int(run.lengths.max()) + min(args.steps, period)
     line = {"metric": METRIC, "metric_detail": f"decode tok/s at batch {B}", "value": value,
             "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
             "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]),
                        "decode_positions": f"{int(run.lengths.min())}..{int(run.lengths.max()) + period - 1} cycled",
-                       "kv": ("contiguous" if W.contiguous_kv else "paged16") + " fp32",
+                       "context_timed": f"{ctx_lo}..{ctx_hi} keys",
+                       "kv": ("contiguous" if W.contiguous_kv else "paged16, shuffled tables") + ", fp32",
                        "precision": ("fp32 weights" if s.dtype == wl.DTYPE_F32 else "bf16 weights")
                        + ", fp32 KV cache and residual, fp32 accumulation"
                        + ("" if s.dtype == wl.DTYPE_F32 else ", activations as bf16 (hi, lo) pairs"),
                        "l2": "inputs larger than L2: %.0f MB weights + %.0f MB KV per step" % (
-                           weight_bytes(s) / 1e6, attn_bytes(s, ctx_steps[-1]) / 1e6),
+                           weight_bytes(s) / 1e6, attn_bytes(s, ctx_of(0)) / 1e6),
                        "graph": "one CUDA graph per step"},
             "roofline": roof,
             "step_roofline": {"alg_bytes_per_step": step_alg, "achieved_gbs": step_gbs,
-                              "frac": step_gbs / pk["hbm_gbs"], "peak_source": f"hbm_gbs of {pk_kind}"},
+                              "frac": step_gbs / pk["hbm_gbs"], "peak_source": f"hbm_gbs of {pk_kind}",
+                              "positions": "the timed steps' positions"},
             "kernel_share": kernel_share,
             "gpu_launches": launches_per_step * args.steps,
             "launches_per_step": launches_per_step,
             "e2e": e2e,
             "clocks": clk.summary()}
+    run.close()
+    del run, toks
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        del run
-        rate, dt, desc = oracle_decode_rate(W, args.cpu_steps, 0, n_seq=1, weights=host_w)
+        n_seq, n_steps = CPU_SAMPLE.get(W.name, (1, 4))
+        if args.cpu_steps:
+            n_steps = args.cpu_steps
+        rate, dt, desc = oracle_decode_rate(W, n_steps, 0, n_seq=n_seq, weights=host_w)
         line["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
                                 "sample": desc, "seconds": dt}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
+    return line
 
 
-def run_prefill_bench(args, W):
+def prefill_part(args, W, world: int, rank: int, local: int, steps: int, warmup: int) -> dict:
     """One step = one prefill of the whole batch (every row of the hot path, attention over the
     full causal prompt, K/V written into the paged pool, last-position argmax)."""
     import torch
-    import torch.distributed as dist
     from transformer_decoder_forward_gb300.runner import WorkloadRun
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
     s = W.model
     host_w = wl.make_weights(s, scale=W.weight_scale)
     run = WorkloadRun(W, host_weights=host_w)
     B = run.B
     tokens_total = int(run.lengths.sum())
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         run.prefill()
     torch.cuda.synchronize()
     launches_per_step = run.dec.last_launch_count()
@@ -445,15 +488,16 @@ def run_prefill_bench(args, W):
             dist.barrier()
         torch.cuda.synchronize()
         ev0.record(st)
-        for _ in range(args.steps):
+        for _ in range(steps):
             run.prefill()
         ev1.record(st)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    ms, _, value = job_rate(ev0.elapsed_time(ev1), tokens_total * args.steps, world)
+    ms, _, value = job_rate(ev0.elapsed_time(ev1), tokens_total * steps, world)
+    ms_step = ms / steps
     assert run.dec.error_flags() == 0, "device error flags set during the bench"
-    # per-kernel durations over one more prefill
+    # per-kernel durations over one more prefill (eager launches, a CUDA event around each)
     run.dec.set_profiling(True)
     run.dec.kernel_stats(reset=True)
     run.prefill()
@@ -466,20 +510,23 @@ def run_prefill_bench(args, W):
         a[0] += n
         a[1] += t
     pk, pk_kind = peaks()
-    gem = fam.get("gemm_tc", [0, 0.0])
     gflops = prefill_gemm_flops(s, run.lengths)
-    achieved = gflops / (gem[1] / 1000.0) / 1e12 if gem[1] > 0 else None
-    roof = {"bound": "tensor", "kernel": "gemm_tc (tcgen05 projections)", "launches": gem[0], "achieved": achieved,
-            "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": (achieved / pk["bf16_tflops"]) if achieved else None,
-            "traffic": traffic_for(W.name, "gemm_tc (tcgen05 projections)"), "peak_source": f"bf16_tflops (burst) of {pk_kind}",
-            "alg_flops_per_launch": gflops / gem[0] if gem[0] else None,
-            "avg_launch_us": 1000.0 * gem[1] / gem[0] if gem[0] else None}
+    label = "gemm_tc (tcgen05 projections)"
+    roof = None
+    if "gemm_tc" in fam:
+        roof = family_roofline(fam, "gemm_tc", 1, ms_step, gflops, "TFLOP/s", pk["bf16_tflops"],
+                               f"bf16_tflops (burst) of {pk_kind}", label, traffic_for(W.name, label))
+    attn_roof = None
+    if "attn_prefill" in fam:
+        attn_roof = family_roofline(fam, "attn_prefill", 1, ms_step, prefill_attn_flops(s, run.lengths), "TFLOP/s",
+                                    pk["bf16_tflops"], f"bf16_tflops (burst) of {pk_kind}",
+                                    "attn_prefill (causal attention, algorithmic flops)", None)
     total = sum(v[1] for v in fam.values())
     kernel_share = {k: round(v[1] / total, 4) for k, v in sorted(fam.items())}
     # end to end: host token ids in, next ids out, through the C ABI
     tok_h = torch.from_numpy(np.concatenate(run.prompts).astype(np.int32)).pin_memory()
     ids_h = torch.zeros(B, dtype=torch.int32).pin_memory()
-    n_e2e = max(1, min(args.steps, 10))
+    n_e2e = max(1, min(steps, 10))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(n_e2e):
@@ -489,43 +536,43 @@ def run_prefill_bench(args, W):
             ids_h.copy_(run.next_ids, non_blocking=True)
         st.synchronize()
     e2e_s = time.perf_counter() - t0
-    e2e = {"value": tokens_total * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": int(tok_h.numel() * 4),
+    e2e = {"value": tokens_total * n_e2e / e2e_s * world, "unit": "tok/s", "h2d_bytes_per_step": int(tok_h.numel() * 4),
            "d2h_bytes_per_step": B * 4, "steps": n_e2e, "api": "llm_prefill (pinned host ids in, ids out)"}
     line = {"metric": METRIC, "metric_detail": f"prefill tok/s, {B} x {int(run.lengths[0])} tokens",
-            "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "value": value, "unit": "tok/s", "n_gpus": world, "steps": steps, "warmup": warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
-            "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]), "kv": "paged16",
+            "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]), "kv": "paged16, fp32",
                        "l2": "inputs larger than L2: %.0f MB activations per step" % (tokens_total * s.d_model * 4 / 1e6)},
             "roofline": roof,
+            "attention_roofline": attn_roof,
             "attention_flops_per_step": prefill_attn_flops(s, run.lengths),
             "gemm_flops_per_step": gflops,
-            "kernel_share": kernel_share, "gpu_launches": launches_per_step * args.steps,
+            "kernel_share": kernel_share, "gpu_launches": launches_per_step * steps,
             "launches_per_step": launches_per_step, "e2e": e2e, "clocks": clk.summary()}
+    run.close()
+    del run
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
-        model = oracle.OracleModel(host_w)
-        t0 = time.perf_counter()
-        oracle.forward_full(model, run.prompts[0], last_only=True)
-        dt = time.perf_counter() - t0
-        line["cpu_baseline"] = {"value": int(run.lengths[0]) / dt, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": f"float64 NumPy oracle, 1 of {B} prompts ({int(run.lengths[0])} tokens), "
-                                          "stateless forward", "seconds": dt}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
+        rate, dt, desc = oracle_prefill_rate(W, 1, weights=host_w)
+        line["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    return line
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1280)
-    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=wl.W_GPT2_F32_B32.name, choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--cpu-steps", type=int, default=1024)
+    ap.add_argument("--workload", default=wl.W_GPT2XL_B256.name, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--prefill-workload", default=wl.W_GPT2_BF16_PREFILL.name,
+                    choices=sorted(n for n, w in wl.WORKLOADS.items() if w.mode == "prefill") + ["none"],
+                    help="prefill workload reported in the decode line's 'prefill' object")
+    ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--cpu-steps", type=int, default=0, help="oracle decode steps of the CPU sample (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -533,11 +580,29 @@ def main():
         print(f"bench: --warmup {args.warmup} raised to 3", file=sys.stderr)
         args.warmup = 3
     W = wl.WORKLOADS[args.workload]
+    is_prefill = W.mode == "prefill" or W.decode_steps == 0
+    PW = None if (is_prefill or args.prefill_workload == "none") else wl.WORKLOADS[args.prefill_workload]
     if args.impl == "reference":
-        return run_reference(args, W)
-    if W.mode == "prefill" or W.decode_steps == 0:
-        return run_prefill_bench(args, W)
-    return run_decode_bench(args, W)
+        return run_reference(args, W, PW)
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if is_prefill:
+        line = prefill_part(args, W, world, rank, local, args.steps, args.warmup)
+    else:
+        line = decode_part(args, W, world, rank, local)
+        if PW is not None:
+            line["prefill"] = prefill_part(args, PW, world, rank, local, args.prefill_steps, max(3, args.warmup))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":

@@ -130,7 +130,16 @@ typedef struct {
 
 typedef struct llm_handle llm_handle;
 
-/* Validate the config, check the device (compute capability 10.3), copy the
+/* Set up one model on the current device: the session object of the pages' engines, which
+ * keep the weights resident on the GPU and allocate the KV cache once ("rvllm-metal",
+ * sections "What the kernels do": the paged cache that kv_write fills through a block
+ * table, and "You record work, then you submit it": buffers the GPU reads without copies).
+ * A device that cannot run the kernels is an error, never a silent fallback: "batch_forge"
+ * (usage paragraph: an explicitly requested backend that is unavailable returns an error)
+ * and "rvllm-metal", section "Things that were problematic" (a runtime that quietly gave up
+ * made the GPU tests pass without running; a kernel that does not load is a hard failure).
+ *
+ * Validate the config, check the device (compute capability 10.3), copy the
  * per-layer pointer arrays, allocate the KV pool
  * (2 * n_layers * num_kv_blocks * n_kv_heads * 16 * head_dim fp32 values,
  * laid out [layer][block][kv_head][16][head_dim], K and V in separate pools)
@@ -140,7 +149,9 @@ typedef struct llm_handle llm_handle;
 llm_status llm_create(const llm_config* config, const llm_weights* weights, void* cuda_stream,
                       llm_handle** out);
 
-/* Free the pool, workspace and cached graphs (synchronises the stream). NULL is a no-op. */
+/* The end of the lifetime llm_create starts (the pages describe set-up only; this is its
+ * inverse): free the pool, workspace and cached graphs (synchronises the stream). The
+ * caller's weights are untouched. NULL is a no-op. */
 void llm_destroy(llm_handle* h);
 
 /* Prompt prefill from position 0 ("rvllm-metal", sections "The matmul pain story"
@@ -175,7 +186,12 @@ llm_status llm_decode_step(llm_handle* h, const int32_t* tokens, const int32_t* 
 llm_status llm_decode_step_host(llm_handle* h, const int32_t* tokens, const int32_t* positions,
                                 const int32_t* block_tables, int B, int32_t* next_ids, float* logits);
 
-/* Synchronise the stream, return the device error word in *flags and clear it.
+/* Errors the device sees ("rvllm-metal", section "Things that were problematic": a failure
+ * that is swallowed instead of reported let every GPU test pass; "How I know it's correct":
+ * argmax with NaN is a tested case). Kernels never trap: a token, position or block id out
+ * of range, a NaN logit, or a bounded wait that gave up sets a bit of the handle's device
+ * error word and the offending access is skipped.
+ * Synchronise the stream, return the device error word in *flags and clear it.
  * Returns LLM_ERR_DEVICE_FLAG when any bit was set, LLM_OK otherwise. */
 llm_status llm_get_error_flags(llm_handle* h, uint32_t* flags);
 
@@ -253,14 +269,15 @@ llm_status llm_op_attention_decode(int kv_dtype, int B, int n_heads, int n_kv_he
  * pages have no counterpart of this entry point. Same arguments, layouts and result as
  * llm_op_attention_decode, but no cudaMalloc / cudaFree / allocating call of any
  * library: the scratch (a 256-byte argument block plus B * n_heads * ceil(max_blocks_per_seq
- * * 16 / 64) * 264 bytes of split partials) lives in one fixed 4 MiB __device__ array that
- * every GPU loading the library holds until the process exits.
+ * * 16 / split) * 264 bytes of split partials) lives in one fixed 4 MiB __device__ array that
+ * every GPU loading the library holds until the process exits. The split (tokens per chunk)
+ * starts at llm_op_attention_decode's choice and doubles, up to 2048, until the partials fit.
  *   - The first call on a device resolves the array's device address (cudaGetSymbolAddress)
  *     for that device; make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents: calls whose
  *     execution overlaps on the GPU (other streams, other threads) race on it.
- * Errors: as llm_op_attention_decode, plus OUT_OF_RANGE when the scratch needed exceeds
- * the array (nothing is launched), UNSUPPORTED for device ordinals above 63. */
+ * Errors: as llm_op_attention_decode, plus OUT_OF_RANGE when the scratch needed at a split
+ * of 2048 exceeds the array (nothing is launched), UNSUPPORTED for device ordinals above 63. */
 llm_status llm_op_attention_decode_noalloc(int kv_dtype, int B, int n_heads, int n_kv_heads, const float* q,
                                            const void* k_pool, const void* v_pool, int num_blocks,
                                            const int32_t* positions, const int32_t* block_tables,

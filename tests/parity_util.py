@@ -2,6 +2,9 @@
 same seeded inputs and compare them element by element."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 import oracle
@@ -12,28 +15,40 @@ import workloads as wl
 #
 # The magnitude-scaled GPT-2 copy (every weight x8) is the one exception: its logits are
 # 8x larger and the model amplifies rounding, so the same definition evaluated in plain
-# float32 (NumPy/BLAS, no GPU) already misses the float64 oracle by up to ~5e-3 on its
-# prompt rows. Its bound (and the id margin) is the fp32 bound scaled by the weight scale:
-# the same relative accuracy as the x1 model.
+# float32 (NumPy/BLAS, no GPU) already misses the float64 oracle by 3e-3 to 8e-3 on its
+# rows. Its test measures that float32 floor on the rows it checks and bounds the GPU by
+# FLOOR_MULT times it (and by no less than the fp32 bound); the id margin is half the bound,
+# the same ratio as 1e-3 to 2e-3.
 LOGIT_TOL = {wl.DTYPE_F32: 2e-3, wl.DTYPE_BF16: 3e-2}
 MARGIN = 1e-3
+FLOOR_MULT = 2.0
 
 
-def check_logits(z_gpu: np.ndarray, z_ref: np.ndarray, dtype: int, what: str = "", scale: float = 1.0) -> float:
+def record(what: str, err: float, tol: float, n_ids: int, **extra) -> None:
+    """Print one parity result; also append it as a JSON line to $LLM_PARITY_LOG when set."""
+    d = dict(what=what, max_abs_err=err, tol=tol, ids_checked=n_ids, **extra)
+    print("PARITY " + json.dumps(d))
+    path = os.environ.get("LLM_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(d) + "\n")
+
+
+def check_logits(z_gpu: np.ndarray, z_ref: np.ndarray, dtype: int, what: str = "", tol: float = None) -> float:
     z_gpu = np.asarray(z_gpu, dtype=np.float64)
     assert z_gpu.shape == z_ref.shape, (z_gpu.shape, z_ref.shape)
     assert np.all(np.isfinite(z_gpu)), f"{what}: non-finite logits"
     err = float(np.abs(z_gpu - z_ref).max())
-    tol = LOGIT_TOL[dtype] * scale
+    tol = LOGIT_TOL[dtype] if tol is None else tol
     assert err <= tol, f"{what}: max-abs logit error {err:.3e} > {tol:.1e}"
     return err
 
 
-def check_ids(ids_gpu, z_ref_rows, what: str = "", scale: float = 1.0) -> int:
+def check_ids(ids_gpu, z_ref_rows, what: str = "", margin: float = MARGIN) -> int:
     """Greedy ids must match where the oracle has a clear winner; returns the number checked."""
     n = 0
     for i, (g, z) in enumerate(zip(np.asarray(ids_gpu).reshape(-1), z_ref_rows)):
-        if oracle.top2_margin(z) > MARGIN * scale:
+        if oracle.top2_margin(z) > margin:
             assert int(g) == oracle.argmax_rule(z), f"{what}: id mismatch at row {i}: {g} vs {oracle.argmax_rule(z)}"
             n += 1
     return n

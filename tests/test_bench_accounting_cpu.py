@@ -64,3 +64,21 @@ def test_traffic_table_matches_only_its_own_kernel_family():
         assert name in wl.WORKLOADS
         assert bench.traffic_for(name, family) == value > 0
         assert bench.traffic_for(name, family + " (other)") is None
+
+
+def test_family_roofline_never_charges_more_than_the_step():
+    import bench
+    # long kernels: the event-timed duration fits in the step and is used as measured
+    fams = {"attn_decode": [48, 10.0], "proj": [196, 4.0]}
+    r = bench.family_roofline(fams, "attn_decode", 1, 15.0, 48 * 1e9, "GB/s", 6000.0, "x", "attn", None)
+    assert r["duration_method"].startswith("CUDA events")
+    assert abs(r["avg_launch_us"] - 10.0e3 / 48) < 1e-9
+    assert abs(r["achieved"] - 1e9 / (10.0e-3 / 48) / 1e9) < 1e-6
+    # short kernels whose event intervals add launch latency: the family's event time per step
+    # (0.7 ms) exceeds the timed step (0.55 ms), so it is charged its share of the step
+    fams = {"proj": [49, 0.70], "norm": [25, 0.20], "attn_decode": [12, 0.10]}
+    r = bench.family_roofline(fams, "proj", 1, 0.55, 49 * 10e6, "GB/s", 6000.0, "x", "proj", None)
+    assert r["duration_method"].startswith("share")
+    assert abs(r["family_ms_per_step"] - 0.55 * 0.7) < 1e-12
+    assert r["family_ms_per_step"] <= 0.55
+    assert abs(r["frac"] - r["achieved"] / 6000.0) < 1e-12

@@ -67,4 +67,4 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     import bench
     import workloads as wl
     monkeypatch.setenv("RANK", "1")
-    assert bench.run_reference(None, wl.W_GPT2_F32_B32) == 0   # returns before any work
+    assert bench.run_reference(None, wl.W_GPT2XL_B256, wl.W_GPT2_BF16_PREFILL) == 0   # returns before any work

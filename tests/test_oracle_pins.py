@@ -334,3 +334,64 @@ def test_weight_draws_are_reproducible_and_scaled():
     np.testing.assert_array_equal(a.w_qkv[1] * np.float32(8), b.w_qkv[1])
     assert abs(a.tok_emb.std() - 0.02) < 1e-3
     assert np.all(a.ln1_w[0] == 1) and np.all(a.b_o[0] == 0)
+
+
+# ------------------------------------------------------------------------------------------------
+# greedy generation ("bare-metal-llm", "What got built": prefill, then one token at a time, each
+# new token the argmax of the previous step's logits)
+# ------------------------------------------------------------------------------------------------
+
+GREEDY = [
+    (TINY[0], [3, 10, 0], 6),
+    (TINY[1], [2, 8], 6),
+    (SMALL[0], [2, 96, 17], 8),
+    (SMALL[1], [2, 96, 17], 8),
+]
+
+
+@pytest.mark.parametrize("shape,prompt,steps", GREEDY, ids=["tiny-gpt2", "tiny-llama", "small-gpt2", "small-llama"])
+def test_greedy_generate_is_the_argmax_chain_of_stateless_recomputes(shape, prompt, steps):
+    """ids[i] is the argmax of the stateless recompute over prompt + ids[:i], and the logits the
+    generator returns are that recompute's last row. Feeding back a wrong token (an older id, or
+    the argmax of another row) changes the chain and fails here."""
+    w = wl.make_weights(shape, scale=20.0 if shape.d_model <= 8 else 8.0, perturb=True)
+    m = oracle.OracleModel(w)
+    ids, zs = oracle.greedy_generate(m, prompt, steps)
+    assert ids.shape == (steps + 1,) and zs.shape == (steps + 1, shape.vocab)
+    assert len(set(ids.tolist())) > 1, "a constant stream would not tell which id was fed back"
+    for i in range(steps + 1):
+        ctx = list(prompt) + [int(t) for t in ids[:i]]
+        z = oracle.forward_full(m, ctx, last_only=True)[0]
+        np.testing.assert_allclose(zs[i], z, rtol=RTOL, atol=1e-12)
+        assert int(ids[i]) == oracle.argmax_rule(z)
+    if shape.d_model <= 8:
+        # the scalar-loop model, fed the same chain, agrees row by row
+        brute = np.array(oracle.BruteModel(w).run(list(prompt) + [int(t) for t in ids[:-1]]))
+        np.testing.assert_allclose(zs, brute[len(prompt) - 1:], rtol=RTOL, atol=1e-12)
+        assert [oracle.argmax_rule(z) for z in brute[len(prompt) - 1:]] == ids.tolist()
+
+
+# ------------------------------------------------------------------------------------------------
+# the float32 floor of the GPT-2 workloads (why the magnitude-scaled copy has a wider logit bound)
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("W", [wl.W_GPT2_F32_B32, wl.W_GPT2_F32_B32_X8], ids=["x1", "x8"])
+def test_float32_floor_of_gpt2_workloads(W):
+    """A plain float32 evaluation of the same definition (NumPy/BLAS, no GPU) against the float64
+    oracle on one sequence of the batch-32 workload (its 128 prompt rows and 64 teacher-forced
+    rows). On the x1 model it agrees to ~3e-6, far inside the 2e-3 bound. On the x8 copy (every
+    weight x8) the logits are 8x larger and the model amplifies rounding: float32 itself misses
+    float64 by more than 2e-3, so no float32 program can meet the literal fp32 bound there and
+    the GPU test measures this floor and bounds the GPU by a small multiple of it."""
+    from fp32_eval import gpt2_forward_f32
+    w = wl.make_weights(W.model, scale=W.weight_scale)
+    m = oracle.OracleModel(w)
+    prompt = wl.draw_prompts(W.lengths(), W.model.vocab)[0]
+    stream = wl.draw_stream(W.batch, W.decode_steps, W.model.vocab)[:64, 0]
+    toks = np.concatenate([prompt, stream])
+    gap = float(np.abs(gpt2_forward_f32(w, toks) - oracle.forward_full(m, toks)).max())
+    if W.weight_scale == 1.0:
+        assert gap < 2e-4, gap
+    else:
+        assert gap > 2e-3, gap
+        assert gap < 2e-2, gap

@@ -29,8 +29,10 @@ __device__ __forceinline__ float bias_at(const void* b, int n) {
 
 // RoPE angle pos * inv_freq[d] reduced to about [-pi, pi] in fp32 without losing the
 // position's precision. inv_freq is split on the host into hi (11 significant bits, so
-// pos * hi is exact for pos < 2^13) + lo; 2*pi is split Cody-Waite style into three
-// floats so that k * 2*pi is subtracted exactly for the quotients that occur.
+// pos * hi is exact for pos < 2^13) + lo. The reduction is the Cody-Waite method (W. J. Cody
+// and W. Waite, "Software Manual for the Elementary Functions", 1980): 2*pi is written as
+// the sum of three floats whose leading parts have few significant bits, so each product
+// k * part is exact for the quotients k that occur and the subtractions lose nothing.
 __device__ __forceinline__ void rope_sincos(int pos, float2 f, float* s, float* c) {
   const float p = (float)pos;
   const float a_hi = p * f.x;                         // exact

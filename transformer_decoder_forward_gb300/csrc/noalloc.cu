@@ -10,6 +10,7 @@
 // call. Every GPU that loads the library holds this array until the process exits.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -22,10 +23,16 @@ using namespace llm;
 namespace {
 
 // 4 MiB: a 256-byte argument block, then B * n_heads * splits * (64 + 2) floats of partials
-// (splits = ceil(max_blocks_per_seq * 16 / 64)).
+// (splits = ceil(max_blocks_per_seq * 16 / split)). The split starts where the allocating entry
+// point's does and doubles, up to the kernel's 2048-token limit, until the partials fit.
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(4) << 20;
 constexpr size_t NOALLOC_ARGS_BYTES = 256;
-constexpr int NOALLOC_SPLIT = 64;
+constexpr int NOALLOC_MAX_SPLIT = 2048;   // a decode-attention chunk spans at most 2048 tokens
+
+size_t noalloc_need(int B, int n_heads, int max_ctx, int split) {
+  const size_t splits = (size_t)(max_ctx + split - 1) / split;
+  return NOALLOC_ARGS_BYTES + (size_t)B * n_heads * splits * (HD + 2) * sizeof(float);
+}
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 // Device address of g_noalloc_scratch, per device ordinal. In host code the symbol's name
@@ -64,18 +71,25 @@ extern "C" llm_status llm_op_attention_decode_noalloc(int kv_dtype, int B, int n
     return llm_internal_fail(LLM_ERR_INVALID_ARG, "bad kv_dtype");
   if (n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > 8)
     return llm_internal_fail(LLM_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads, at most 8 per KV head");
-  const int max_splits = (max_blocks_per_seq * KVB + NOALLOC_SPLIT - 1) / NOALLOC_SPLIT;
-  const size_t part_o = (size_t)B * n_heads * max_splits * HD;
-  const size_t part_ml = (size_t)B * n_heads * max_splits * 2;
-  const size_t need = NOALLOC_ARGS_BYTES + (part_o + part_ml) * sizeof(float);
-  if (need > NOALLOC_SCRATCH_BYTES)
+  const int max_ctx = max_blocks_per_seq * KVB;
+  const size_t need_min = noalloc_need(B, n_heads, max_ctx, NOALLOC_MAX_SPLIT);
+  if (need_min > NOALLOC_SCRATCH_BYTES)
     return llm_internal_fail(LLM_ERR_OUT_OF_RANGE,
-                             "llm_op_attention_decode_noalloc: needs " + std::to_string(need) +
-                                 " bytes of scratch, the fixed array holds " + std::to_string(NOALLOC_SCRATCH_BYTES) +
-                                 " (B * n_heads * ceil(max_blocks_per_seq * 16 / 64) * 264 + 256)");
-  int dev = 0;
+                             "llm_op_attention_decode_noalloc: needs " + std::to_string(need_min) +
+                                 " bytes of scratch at the largest split (2048 tokens), the fixed array holds " +
+                                 std::to_string(NOALLOC_SCRATCH_BYTES) +
+                                 " (B * n_heads * ceil(max_blocks_per_seq * 16 / 2048) * 264 + 256)");
+  int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return llm_internal_fail(LLM_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return llm_internal_fail(LLM_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+  // the allocating entry point's split, doubled until the partials fit the array
+  int split = attn_decode_split_for(B, n_kv_heads, max_ctx, sms);
+  while (noalloc_need(B, n_heads, max_ctx, split) > NOALLOC_SCRATCH_BYTES && split < NOALLOC_MAX_SPLIT)
+    split = std::min(NOALLOC_MAX_SPLIT, split * 2);
+  const int max_splits = (max_ctx + split - 1) / split;
+  const size_t part_o = (size_t)B * n_heads * max_splits * HD;
   if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return llm_internal_fail(LLM_ERR_UNSUPPORTED, "device ordinal above 63");
   unsigned char* scratch = nullptr;
   llm_status st = noalloc_scratch(dev, &scratch);
@@ -95,7 +109,7 @@ extern "C" llm_status llm_op_attention_decode_noalloc(int kv_dtype, int B, int n
   p.args = args;
   p.B = B;
   p.n_heads = n_heads;
-  p.split = NOALLOC_SPLIT;
+  p.split = split;
   p.max_splits = max_splits;
   p.part_o = reinterpret_cast<float*>(scratch + NOALLOC_ARGS_BYTES);
   p.part_ml = p.part_o + part_o;
