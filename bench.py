@@ -109,15 +109,16 @@ def gemv_bytes(s: wl.ModelShape, B: int) -> int:
     return weight_bytes(s) + s.n_layers * per_layer + B * d * a
 
 
-def attn_bytes(s: wl.ModelShape, ctx: np.ndarray) -> int:
-    """Decode attention: K and V of every cached position (incl. the new one) once per layer."""
-    kv = int(ctx.sum()) * s.n_kv_heads * s.head_dim * 4 * 2 * s.n_layers   # fp32 cache
+def attn_bytes(s: wl.ModelShape, ctx: np.ndarray, kv_elt: int = 4) -> int:
+    """Decode attention: K and V of every cached position (incl. the new one) once per layer
+    (kv_elt bytes an element: 4 for the fp32 cache, 2 for bf16)."""
+    kv = int(ctx.sum()) * s.n_kv_heads * s.head_dim * kv_elt * 2 * s.n_layers
     qo = len(ctx) * s.n_heads * s.head_dim * (4 + 4) * s.n_layers
     return kv + qo
 
 
-def step_bytes(s: wl.ModelShape, ctx: np.ndarray) -> int:
-    return gemv_bytes(s, len(ctx)) + attn_bytes(s, ctx)
+def step_bytes(s: wl.ModelShape, ctx: np.ndarray, kv_elt: int = 4) -> int:
+    return gemv_bytes(s, len(ctx)) + attn_bytes(s, ctx, kv_elt)
 
 
 def prefill_gemm_flops(s: wl.ModelShape, lengths: np.ndarray) -> float:
@@ -203,7 +204,7 @@ def oracle_decode_rate(W: wl.Workload, steps: int, warmup: int = 0, n_seq: int =
     """
     import oracle
     w = weights or wl.make_weights(W.model, scale=W.weight_scale)
-    model = oracle.OracleModel(w)
+    model = oracle.OracleModel(w, kv_dtype=W.kv_dtype)
     prompts = wl.draw_prompts(W.lengths(), W.model.vocab)
     stream = wl.draw_stream(W.batch, max(W.decode_steps, 1), W.model.vocab)
     period = max(W.decode_steps, 1)
@@ -342,6 +343,7 @@ def decode_part(args, W, world: int, rank: int, local: int) -> dict:
     from transformer_decoder_forward_gb300.runner import WorkloadRun
 
     s = W.model
+    kv_elt = 2 if W.kv_dtype == wl.DTYPE_BF16 else 4
     host_w = wl.make_weights(s, scale=W.weight_scale)
     period = W.decode_steps
     run = WorkloadRun(W, host_weights=host_w)
@@ -401,7 +403,7 @@ def decode_part(args, W, world: int, rank: int, local: int) -> dict:
     if dom == "proj":
         alg = float(gemv_bytes(s, B)) * n_prof
     elif dom == "attn_decode":
-        alg = float(sum(attn_bytes(s, ctx_of(i)) for i in range(n_prof)))
+        alg = float(sum(attn_bytes(s, ctx_of(i), kv_elt) for i in range(n_prof)))
     else:
         alg = None
     label = dom if dom != "proj" else "proj (" + "+".join(sorted(kinds)) + ")"
@@ -409,7 +411,7 @@ def decode_part(args, W, world: int, rank: int, local: int) -> dict:
     if alg is not None:
         roof = family_roofline(fam, dom, n_prof, ms_step, alg, "GB/s", pk["hbm_gbs"], f"hbm_gbs of {pk_kind}",
                                label, traffic_for(W.name, label))
-    step_alg = float(np.mean([step_bytes(s, ctx_of(i)) for i in range(args.steps)]))
+    step_alg = float(np.mean([step_bytes(s, ctx_of(i), kv_elt) for i in range(args.steps)]))
     step_gbs = step_alg / (ms_step / 1000.0) / 1e9
     kernel_share = {k: round(v[1] / sum(x[1] for x in fam.values()), 4) for k, v in sorted(fam.items())}
 
@@ -436,12 +438,14 @@ def decode_part(args, W, world: int, rank: int, local: int) -> dict:
             "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]),
                        "decode_positions": f"{int(run.lengths.min())}..{int(run.lengths.max()) + period - 1} cycled",
                        "context_timed": f"{ctx_lo}..{ctx_hi} keys",
-                       "kv": ("contiguous" if W.contiguous_kv else "paged16, shuffled tables") + ", fp32",
+                       "kv": ("contiguous" if W.contiguous_kv else "paged16, shuffled tables")
+                       + (", bf16" if kv_elt == 2 else ", fp32"),
                        "precision": ("fp32 weights" if s.dtype == wl.DTYPE_F32 else "bf16 weights")
-                       + ", fp32 KV cache and residual, fp32 accumulation"
+                       + (", bf16 KV cache" if kv_elt == 2 else ", fp32 KV cache")
+                       + ", fp32 residual, fp32 accumulation"
                        + ("" if s.dtype == wl.DTYPE_F32 else ", activations as bf16 (hi, lo) pairs"),
                        "l2": "inputs larger than L2: %.0f MB weights + %.0f MB KV per step" % (
-                           weight_bytes(s) / 1e6, attn_bytes(s, ctx_of(0)) / 1e6),
+                           weight_bytes(s) / 1e6, attn_bytes(s, ctx_of(0), kv_elt) / 1e6),
                        "graph": "one CUDA graph per step"},
             "roofline": roof,
             "step_roofline": {"alg_bytes_per_step": step_alg, "achieved_gbs": step_gbs,
@@ -574,12 +578,16 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--cpu-steps", type=int, default=0, help="oracle decode steps of the CPU sample (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-dtype", default="f32", choices=["f32", "bf16"], help="element type of the KV cache")
     args = ap.parse_args()
     if args.warmup < 3:
         # the timing rules' minimum; the JSON line reports the count actually run
         print(f"bench: --warmup {args.warmup} raised to 3", file=sys.stderr)
         args.warmup = 3
     W = wl.WORKLOADS[args.workload]
+    if args.kv_dtype == "bf16":
+        from dataclasses import replace
+        W = replace(W, kv_dtype=wl.DTYPE_BF16)
     is_prefill = W.mode == "prefill" or W.decode_steps == 0
     PW = None if (is_prefill or args.prefill_workload == "none") else wl.WORKLOADS[args.prefill_workload]
     if args.impl == "reference":

@@ -16,7 +16,7 @@
  * kv_write into the paged cache, division and modulo of the position).
  *
  * Precision: only the weights take config.dtype. The residual stream, the KV cache
- * and the logits are fp32 (the weights alone are half precision in "rvllm-metal",
+ * (unless config.kv_dtype asks for bf16) and the logits are fp32 (the weights alone are half precision in "rvllm-metal",
  * section "The matmul pain story"; its KV cache is F32, section "What's basic about
  * it"); with bf16 weights the activations fed to a projection are kept as bf16
  * (hi, lo) pairs, about 2^-17 relative, so the tensor cores take two bf16 products
@@ -89,6 +89,10 @@ typedef struct {
   int max_blocks_per_seq; /* row length of a block table */
   int max_prefill_tokens; /* rows of one prefill chunk (workspace size); >= the longest prompt */
   int contiguous_kv;      /* 1: sequence b owns slots [b*max_blocks_per_seq*16, ...), tables ignored */
+  int kv_dtype;           /* element type of the KV cache: LLM_DTYPE_F32 (0, the default) or
+                             LLM_DTYPE_BF16, K and V rounded to nearest bf16 (ties to even) when
+                             written; half the cache bytes ("rvllm-metal", section "What's basic
+                             about it", names the F32 cache as a weakness) */
 } llm_config;
 
 /*
@@ -141,7 +145,7 @@ typedef struct llm_handle llm_handle;
  *
  * Validate the config, check the device (compute capability 10.3), copy the
  * per-layer pointer arrays, allocate the KV pool
- * (2 * n_layers * num_kv_blocks * n_kv_heads * 16 * head_dim fp32 values,
+ * (2 * n_layers * num_kv_blocks * n_kv_heads * 16 * head_dim values of kv_dtype,
  * laid out [layer][block][kv_head][16][head_dim], K and V in separate pools)
  * and the workspace. cuda_stream is a cudaStream_t (NULL = the legacy default
  * stream, which disables CUDA-graph replay). Errors: INVALID_ARG, UNSUPPORTED,
@@ -166,6 +170,26 @@ void llm_destroy(llm_handle* h);
  * chunks of at most max_prefill_tokens rows. Errors: INVALID_ARG, OUT_OF_RANGE. */
 llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* lengths, const int32_t* block_tables,
                        int B, int32_t* next_ids, float* logits);
+
+/* One pass over sequences that each feed any number of new tokens: prefill and decode rows
+ * mixed in one batch ("rvllm-metal", section "What's next": batched requests through one
+ * forward pass; "What the kernels do": attention of the new tokens over the cached blocks).
+ * Sequence b feeds lengths[b] tokens at positions starts[b] .. starts[b] + lengths[b] - 1,
+ * writes their K/V into its blocks, attends over positions 0 .. starts[b] + lengths[b] - 1
+ * (the earlier ones already in the cache), and gets the argmax after its last token. A decode
+ * row is lengths[b] = 1 with starts[b] = its context length; a prompt is starts[b] = 0; a
+ * prompt continued in chunks has starts[b] > 0.
+ *   tokens        device int32 [sum(lengths)], packed by sequence in order
+ *   lengths       HOST int32 [B], each in [1, max_prefill_tokens]
+ *   starts        HOST int32 [B], each >= 0 (NULL: all 0), starts[b] + lengths[b] <= n_ctx
+ *   block_tables  device int32 [B][max_blocks_per_seq] (row b for sequence b; ignored when
+ *                 contiguous_kv); the first ceil((starts[b] + lengths[b]) / 16) entries valid
+ *   next_ids      device int32 [B];  logits  device float [B][vocab] or NULL
+ * Sequences are processed in chunks of at most max_prefill_tokens rows. When the batch opens
+ * with one-token sequences, those rows take the split-K decode attention and the others the
+ * tiled prefill attention, in the same pass. Errors: INVALID_ARG, OUT_OF_RANGE. */
+llm_status llm_step(llm_handle* h, const int32_t* tokens, const int32_t* lengths, const int32_t* starts,
+                    const int32_t* block_tables, int B, int32_t* next_ids, float* logits);
 
 /* One batched decode step ("rvllm-metal", section "What the kernels do").
  *   tokens        device int32 [B], the token fed to each sequence

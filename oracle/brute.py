@@ -13,9 +13,10 @@ Intended sizes: 1 layer, d = 8, 2 heads x 4, vocab 11, at most ~6 tokens.
 from __future__ import annotations
 
 import math
+import struct
 from typing import List
 
-from workloads import ARCH_GPT2, Weights
+from workloads import ARCH_GPT2, DTYPE_BF16, DTYPE_F32, Weights
 
 
 def _f(a) -> List:
@@ -23,10 +24,19 @@ def _f(a) -> List:
     return None if a is None else a.tolist()
 
 
+def _bf16(v: float) -> float:
+    """Nearest bfloat16 (ties to even) of v: float32 first, then the low 16 bits rounded away."""
+    bits = struct.unpack("<I", struct.pack("<f", v))[0]
+    lsb = (bits >> 16) & 1
+    bits = ((bits + 0x7FFF + lsb) >> 16) << 16
+    return struct.unpack("<f", struct.pack("<I", bits & 0xFFFFFFFF))[0]
+
+
 class BruteModel:
-    def __init__(self, w: Weights):
+    def __init__(self, w: Weights, kv_dtype: int = DTYPE_F32):
         s = w.shape
         self.s = s
+        self.kv_bf16 = kv_dtype == DTYPE_BF16
         self.tok = _f(w.as_f64(w.tok_emb))
         self.pos = _f(w.as_f64(w.pos_emb))
         self.L = []
@@ -111,6 +121,9 @@ class BruteModel:
                 if s.arch != ARCH_GPT2:
                     q = [self._rope(x, t) for x in q]
                     k = [self._rope(x, t) for x in k]
+                if self.kv_bf16:   # a bf16 KV cache stores rounded values
+                    k = [[_bf16(x) for x in kk] for kk in k]
+                    v = [[_bf16(x) for x in vv] for vv in v]
                 kc[l].append(k)
                 vc[l].append(v)
                 o = []

@@ -39,7 +39,7 @@ from typing import Dict, List, Optional
 
 import numpy as np
 
-from workloads import ARCH_GPT2, ARCH_LLAMA, ModelShape, Weights
+from workloads import ARCH_GPT2, ARCH_LLAMA, DTYPE_BF16, DTYPE_F32, ModelShape, Weights
 
 GELU_C = np.sqrt(2.0 / np.pi)
 GELU_CUBIC = 0.044715
@@ -133,6 +133,19 @@ def causal_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.ndar
     return out.reshape(tq, hq * hd)
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value, ties to even (returned widened to float64).
+
+    A bf16 KV cache stores each K and V element with the float32 exponent and the top 7
+    explicit mantissa bits; the value is first taken to float32 (nearest), then its 16 low bits
+    are rounded away to nearest, ties to the even result.
+    """
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)) << np.uint64(16)
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def argmax_rule(z: np.ndarray) -> int:
     """Greedy id: NaN ranks above every number (first NaN wins); ties go to the lowest index."""
     z = np.asarray(z)
@@ -153,10 +166,17 @@ def top2_margin(z: np.ndarray) -> float:
 # ----------------------------------------------------------------------------------------------
 
 class OracleModel:
-    """A model's parameters widened to float64, plus the per-layer forward."""
+    """A model's parameters widened to float64, plus the per-layer forward.
 
-    def __init__(self, w: Weights):
+    ``kv_dtype`` is the element type of the KV cache the method stores: DTYPE_F32 keeps K and V
+    as computed (float32 holds them to about 2^-24, below what the float64 oracle models);
+    DTYPE_BF16 stores them rounded to bfloat16, which is part of what that mode computes, so
+    the oracle rounds them the same way before any attention reads them.
+    """
+
+    def __init__(self, w: Weights, kv_dtype: int = DTYPE_F32):
         self.shape: ModelShape = w.shape
+        self.kv_dtype = kv_dtype
         f = w.as_f64
         self.tok_emb = f(w.tok_emb)
         self.pos_emb = f(w.pos_emb)
@@ -204,6 +224,8 @@ class OracleModel:
         if s.arch == ARCH_LLAMA:
             q = rope(q, positions, s.rope_theta)
             k = rope(k, positions, s.rope_theta)
+        if self.kv_dtype == DTYPE_BF16:
+            k, v = round_bf16(k), round_bf16(v)
         k_all = k if k_cache is None else np.concatenate([k_cache, k], axis=0)
         v_all = v if v_cache is None else np.concatenate([v_cache, v], axis=0)
         o = causal_attention(q, k_all, v_all, positions)

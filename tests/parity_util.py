@@ -18,10 +18,12 @@ import workloads as wl
 # float32 (NumPy/BLAS, no GPU) already misses the float64 oracle by 3e-3 to 8e-3 on its
 # rows. Its test measures that float32 floor on the rows it checks and bounds the GPU by
 # FLOOR_MULT times it (and by no less than the fp32 bound); the id margin is half the bound,
-# the same ratio as 1e-3 to 2e-3.
+# the same ratio as 1e-3 to 2e-3. The multiple is 3: the GPU's fp32-weight tensor-core path
+# sums three tf32 products per term (about 2^-21 relative a product, against 2^-24 for an
+# fp32 FMA), and its error measured up to 1.94x the float32 floor on these rows.
 LOGIT_TOL = {wl.DTYPE_F32: 2e-3, wl.DTYPE_BF16: 3e-2}
 MARGIN = 1e-3
-FLOOR_MULT = 2.0
+FLOOR_MULT = 3.0
 
 
 def record(what: str, err: float, tol: float, n_ids: int, **extra) -> None:

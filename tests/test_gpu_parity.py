@@ -54,6 +54,25 @@ def test_small_model_matches_oracle(gpu_lib, small_models, shape, variant):
     run.close()
 
 
+@pytest.mark.parametrize("variant", [0, 2], ids=["auto", "simt"])
+@pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
+def test_small_model_bf16_kv_matches_oracle(gpu_lib, small_models, shape, variant):
+    """A bf16 KV cache: every attention kernel (decode split-K, fp32-weight prefill tiles, tcgen05
+    prefill) reads bf16 K/V, against the oracle that stores K and V rounded to bf16."""
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, _ = small_models[shape.name]
+    model = oracle.OracleModel(w, kv_dtype=wl.DTYPE_BF16)
+    run = WorkloadRun(replace(small_workload(shape), kv_dtype=wl.DTYPE_BF16), host_weights=w, lengths=LENGTHS)
+    stream = wl.draw_stream(run.B, STEPS, shape.vocab)
+    ids, z = run_gpu_teacher(run, stream, variant=variant)
+    assert run.dec.error_flags() == 0
+    run.close()
+    for b in range(run.B):
+        ref = oracle_teacher(model, run.prompts[b], stream[:, b])
+        check_logits(z[:, b], ref, shape.dtype, f"{shape.name} bf16 KV seq {b}")
+        check_ids(ids[:, b], ref, f"{shape.name} bf16 KV seq {b}")
+
+
 def test_graph_replay_equals_eager_bitwise(gpu_lib, small_models):
     from transformer_decoder_forward_gb300.runner import WorkloadRun
     w, _ = small_models[SMALL_LLAMA.name]

@@ -395,3 +395,30 @@ def test_float32_floor_of_gpt2_workloads(W):
     else:
         assert gap > 2e-3, gap
         assert gap < 2e-2, gap
+
+
+# ------------------------------------------------------------------------------------------------
+# bf16 KV cache ("rvllm-metal", section "What's basic about it": the F32 cache as a weakness)
+# ------------------------------------------------------------------------------------------------
+
+def test_round_bf16_matches_torch_and_bounds():
+    x = np.concatenate([rng(21).normal(size=200000).astype(np.float32) * 3,
+                        np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 0.0, -0.0, 1e-30], np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = od.round_bf16(x.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+    np.testing.assert_array_equal(od.round_bf16(got), got)                 # idempotent
+    assert np.all(np.abs(got - x) <= 2.0 ** -8 * np.abs(x))                # half an ulp of 8 significant bits
+
+
+@pytest.mark.parametrize("shape", TINY[:2], ids=["gpt2", "llama-gqa"])
+def test_bf16_kv_brute_force_equals_vectorised_oracle(shape):
+    w = wl.make_weights(shape, scale=20.0, perturb=True)
+    tokens = [3, 10, 0, 7, 7, 1]
+    brute = np.array(oracle.BruteModel(w, kv_dtype=wl.DTYPE_BF16).run(tokens))
+    m = oracle.OracleModel(w, kv_dtype=wl.DTYPE_BF16)
+    np.testing.assert_allclose(oracle.forward_full(m, tokens), brute, rtol=RTOL, atol=1e-12)
+    seq = oracle.Sequence(m)
+    np.testing.assert_allclose(np.stack([seq.step(t) for t in tokens]), brute, rtol=RTOL, atol=1e-12)
+    # the rounding is there: the fp32-cache model differs
+    assert np.abs(np.array(oracle.BruteModel(w).run(tokens)) - brute).max() > 1e-6

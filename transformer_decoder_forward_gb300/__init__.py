@@ -20,7 +20,7 @@ STATUS = {0: "LLM_OK", 1: "LLM_ERR_INVALID_ARG", 2: "LLM_ERR_OUT_OF_RANGE", 3: "
           4: "LLM_ERR_UNSUPPORTED", 5: "LLM_ERR_OOM", 6: "LLM_ERR_CUDA", 7: "LLM_ERR_DEVICE_FLAG"}
 FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8, 16
 
-EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_decode_step", "llm_decode_step_host",
+EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_host",
            "llm_get_error_flags", "llm_selftest_wait_timeout", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
            "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode", "llm_op_attention_decode_noalloc",
            "llm_status_string", "llm_last_error"]
@@ -37,7 +37,7 @@ class LLMConfig(ctypes.Structure):
                                              "head_dim", "d_ff", "vocab", "n_ctx")] + \
                [("norm_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
                [(n, ctypes.c_int) for n in ("kv_block_size", "num_kv_blocks", "max_batch", "max_blocks_per_seq",
-                                             "max_prefill_tokens", "contiguous_kv")]
+                                             "max_prefill_tokens", "contiguous_kv", "kv_dtype")]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -70,6 +70,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_destroy.argtypes = [vp]
     lib.llm_destroy.restype = None
     lib.llm_prefill.argtypes = [vp, i32p, ctypes.POINTER(ctypes.c_int32), i32p, ctypes.c_int, i32p, vp]
+    lib.llm_step.argtypes = [vp, i32p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), i32p,
+                             ctypes.c_int, i32p, vp]
     lib.llm_decode_step.argtypes = [vp, i32p, i32p, i32p, ctypes.c_int, i32p, vp]
     lib.llm_decode_step_host.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp]
     lib.llm_get_error_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -87,7 +89,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_status_string.restype = ctypes.c_char_p
     lib.llm_last_error.argtypes = []
     lib.llm_last_error.restype = ctypes.c_char_p
-    for name in ("llm_create", "llm_prefill", "llm_decode_step", "llm_decode_step_host", "llm_get_error_flags",
+    for name in ("llm_create", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_host", "llm_get_error_flags",
                  "llm_set_profiling", "llm_selftest_wait_timeout", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
                  "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode",
                  "llm_op_attention_decode_noalloc"):
@@ -166,7 +168,7 @@ class Decoder:
     """
 
     def __init__(self, shape, dev_w, *, max_batch: int, max_blocks_per_seq: int, num_kv_blocks: int = 0,
-                 max_prefill_tokens: int = 4096, contiguous_kv: bool = False, stream=None):
+                 max_prefill_tokens: int = 4096, contiguous_kv: bool = False, kv_dtype: int = 0, stream=None):
         import torch
         self.lib = load()
         self.shape = shape
@@ -177,7 +179,8 @@ class Decoder:
                       d_ff=shape.d_ff, vocab=shape.vocab, n_ctx=shape.n_ctx, norm_eps=shape.norm_eps,
                       rope_theta=shape.rope_theta, kv_block_size=16, num_kv_blocks=num_kv_blocks,
                       max_batch=max_batch, max_blocks_per_seq=max_blocks_per_seq,
-                      max_prefill_tokens=max_prefill_tokens, contiguous_kv=int(contiguous_kv))
+                      max_prefill_tokens=max_prefill_tokens, contiguous_kv=int(contiguous_kv),
+                      kv_dtype=int(kv_dtype))
         self.config = c
         L = shape.n_layers
         self._arrays = []
@@ -206,6 +209,13 @@ class Decoder:
         lens = (ctypes.c_int32 * len(lengths))(*[int(x) for x in lengths])
         _check(self.lib.llm_prefill(self.handle, _ptr(tokens), lens, _ptr(block_tables), len(lengths),
                                     _ptr(next_ids), _ptr(logits)))
+
+    def step(self, tokens, lengths: Sequence[int], starts: Sequence[int], block_tables, next_ids, logits=None) -> None:
+        """Mixed pass: sequence b feeds lengths[b] tokens from position starts[b] (host lists)."""
+        lens = (ctypes.c_int32 * len(lengths))(*[int(x) for x in lengths])
+        sts = (ctypes.c_int32 * len(starts))(*[int(x) for x in starts])
+        _check(self.lib.llm_step(self.handle, _ptr(tokens), lens, sts, _ptr(block_tables), len(lengths),
+                                 _ptr(next_ids), _ptr(logits)))
 
     def decode_step(self, tokens, positions, block_tables, next_ids, logits=None) -> None:
         _check(self.lib.llm_decode_step(self.handle, _ptr(tokens), _ptr(positions), _ptr(block_tables),

@@ -77,7 +77,9 @@ struct llm_handle {
   int act_mul = 1;    // row stride of an activation matrix in storage elements = act_mul * width
   const void *tok_emb = nullptr, *pos_emb = nullptr, *lnf_w = nullptr, *lnf_b = nullptr;
   std::vector<LayerW> layers;
-  // KV pool (fp32)
+  // KV pool (fp32, or bf16 when cfg.kv_dtype asks for it)
+  int kvdt = DT_F32;
+  size_t kv_elt = 4;
   void* k_pool = nullptr;
   void* v_pool = nullptr;
   size_t layer_kv_elems = 0;
@@ -221,8 +223,9 @@ llm_status linear(llm_handle* h, const char* tag, LinearParams p) {
 
 KVLayer kv_layer(const llm_handle* h, int l) {
   KVLayer kv;
-  kv.k = static_cast<float*>(h->k_pool) + (size_t)l * h->layer_kv_elems;
-  kv.v = static_cast<float*>(h->v_pool) + (size_t)l * h->layer_kv_elems;
+  kv.k = static_cast<char*>(h->k_pool) + (size_t)l * h->layer_kv_elems * h->kv_elt;
+  kv.v = static_cast<char*>(h->v_pool) + (size_t)l * h->layer_kv_elems * h->kv_elt;
+  kv.dtype = h->kvdt;
   kv.num_blocks = h->num_blocks;
   kv.n_kv_heads = h->cfg.n_kv_heads;
   kv.mbps = h->cfg.max_blocks_per_seq;
@@ -272,7 +275,9 @@ llm_status norm_linear(llm_handle* h, const char* tag, LinearParams p, const voi
 // The kernels of one forward pass over M rows (decode: M = B, one row per
 // sequence; prefill chunk: the packed prompt rows), reading d_args.
 // items != 0 selects prefill attention over `n_items` work items.
-llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_items) {
+// In a prefill pass, the first n_dec sequences (n_dec rows, one token each, rows 0..n_dec-1,
+// block-table rows 0..n_dec-1) take the split-K decode attention and the items the rest.
+llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_items, int n_dec = 0) {
   const llm_config& c = h->cfg;
   const int d = c.d_model, H = c.n_heads, Hkv = c.n_kv_heads, F = c.d_ff;
   const bool gpt2 = c.arch == LLM_ARCH_GPT2;
@@ -301,22 +306,23 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
     { llm_status s_ = norm_linear(h, "qkv", lp, w.ln1_w, w.ln1_b, false); if (s_ != LLM_OK) return s_; }
 
     // attention
-    if (!prefill) {
+    if (!prefill || n_dec > 0) {
       AttnDecodeParams ap;
       memset(&ap, 0, sizeof(ap));
-      ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.B = B; ap.n_heads = H;
+      ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.B = prefill ? n_dec : B; ap.n_heads = H;
       ap.split = h->split; ap.max_splits = h->max_splits; ap.part_o = h->attn_po; ap.part_ml = h->attn_ml;
       ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
-      RUN("attn_decode", launch_attn_decode(ap, DT_F32, h->stream, h->pdl));
-    } else {
+      RUN("attn_decode", launch_attn_decode(ap, h->kvdt, h->stream, h->pdl));
+    }
+    if (prefill && n_items > 0) {
       AttnPrefillParams ap;
       memset(&ap, 0, sizeof(ap));
       ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.items = h->d_items; ap.n_items = n_items;
       ap.n_heads = H; ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
       // bf16-weight models: tensor cores on bf16 (hi, lo) splits (about 16 bits of every
       // operand); fp32-weight models keep fp32 FMA so their attention stays at fp32 accuracy
-      if (h->wdt == DT_BF16) RUN("attn_prefill", launch_attn_prefill_tc(ap, DT_F32, h->stream, h->pdl));
-      else RUN("attn_prefill", launch_attn_prefill(ap, DT_F32, h->stream, h->pdl));
+      if (h->wdt == DT_BF16) RUN("attn_prefill", launch_attn_prefill_tc(ap, h->kvdt, h->stream, h->pdl));
+      else RUN("attn_prefill", launch_attn_prefill(ap, h->kvdt, h->stream, h->pdl));
     }
 
     // out projection + residual
@@ -402,6 +408,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   if (c.d_model % 8 != 0 || c.d_ff % 8 != 0) return fail(LLM_ERR_UNSUPPORTED, "d_model and d_ff must be multiples of 8");
   if (c.arch == LLM_ARCH_LLAMA && !(c.rope_theta > 0.0f)) return fail(LLM_ERR_INVALID_ARG, "rope_theta must be > 0");
   if (!c.contiguous_kv && c.num_kv_blocks <= 0) return fail(LLM_ERR_INVALID_ARG, "num_kv_blocks must be positive");
+  if (c.kv_dtype != LLM_DTYPE_F32 && c.kv_dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_INVALID_ARG, "bad kv_dtype");
   const bool gpt2 = c.arch == LLM_ARCH_GPT2;
   if (!wp->tok_emb || (gpt2 && !wp->pos_emb) || !wp->lnf_w || (gpt2 && !wp->lnf_b))
     return fail(LLM_ERR_INVALID_ARG, "missing embedding or final-norm weights");
@@ -432,6 +439,8 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   h->wdt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
   h->adt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : DT_SPLIT;
   h->act_mul = h->adt == DT_SPLIT ? 2 : 1;
+  h->kvdt = c.kv_dtype == LLM_DTYPE_BF16 ? DT_BF16 : DT_F32;
+  h->kv_elt = h->kvdt == DT_BF16 ? 2 : 4;
   h->tok_emb = wp->tok_emb;
   h->pos_emb = gpt2 ? wp->pos_emb : nullptr;
   h->lnf_w = wp->lnf_w;
@@ -470,8 +479,8 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
     st = dev_alloc(h, reinterpret_cast<T**>(&(ptr)), (size_t)(n));               \
     if (st != LLM_OK) { free_all(h); delete h; return st; }                      \
   } while (0)
-  ALLOC(h->k_pool, float, (size_t)c.n_layers * h->layer_kv_elems);
-  ALLOC(h->v_pool, float, (size_t)c.n_layers * h->layer_kv_elems);
+  ALLOC(h->k_pool, char, (size_t)c.n_layers * h->layer_kv_elems * h->kv_elt);
+  ALLOC(h->v_pool, char, (size_t)c.n_layers * h->layer_kv_elems * h->kv_elt);
   ALLOC(h->h, float, R * d);
   ALLOC(h->xn, char, R * d * act);
   ALLOC(h->q, float, R * H * HD);
@@ -619,8 +628,8 @@ llm_status llm_decode_step(llm_handle* h, const int32_t* tokens, const int32_t* 
   return LLM_OK;
 }
 
-llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* lengths, const int32_t* tables, int B,
-                       int32_t* next_ids, float* logits) {
+llm_status llm_step(llm_handle* h, const int32_t* tokens, const int32_t* lengths, const int32_t* starts,
+                    const int32_t* tables, int B, int32_t* next_ids, float* logits) {
   llm_status st = check_handle(h);
   if (st != LLM_OK) return st;
   const llm_config& c = h->cfg;
@@ -629,11 +638,13 @@ llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* leng
   if (!tokens || !lengths || !next_ids) return fail(LLM_ERR_INVALID_ARG, "NULL tokens/lengths/next_ids");
   if (!tables && !c.contiguous_kv) return fail(LLM_ERR_INVALID_ARG, "NULL block_tables");
   for (int b = 0; b < B; ++b) {
-    const int L = lengths[b];
-    if (L <= 0) return fail(LLM_ERR_INVALID_ARG, "prompt length must be positive");
-    if (L > c.max_prefill_tokens) return fail(LLM_ERR_OUT_OF_RANGE, "prompt longer than max_prefill_tokens");
-    if (L > c.n_ctx) return fail(LLM_ERR_OUT_OF_RANGE, "prompt longer than n_ctx");
-    if ((L + KVB - 1) / KVB > c.max_blocks_per_seq) return fail(LLM_ERR_OUT_OF_RANGE, "prompt needs more blocks than max_blocks_per_seq");
+    const int L = lengths[b], P = starts ? starts[b] : 0;
+    if (L <= 0) return fail(LLM_ERR_INVALID_ARG, "length must be positive");
+    if (P < 0) return fail(LLM_ERR_INVALID_ARG, "start position must be >= 0");
+    if (L > c.max_prefill_tokens) return fail(LLM_ERR_OUT_OF_RANGE, "more tokens than max_prefill_tokens");
+    if ((long long)P + L > c.n_ctx) return fail(LLM_ERR_OUT_OF_RANGE, "start + length beyond n_ctx");
+    if ((P + L + KVB - 1) / KVB > c.max_blocks_per_seq)
+      return fail(LLM_ERR_OUT_OF_RANGE, "sequence needs more blocks than max_blocks_per_seq");
   }
   begin_call(h);
   const int item_rows = h->wdt == DT_BF16 ? 128 : 64;   // query rows per prefill-attention CTA
@@ -643,13 +654,19 @@ llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* leng
     int s1 = s0, rows = 0;
     while (s1 < B && rows + lengths[s1] <= c.max_prefill_tokens) rows += lengths[s1++];
     const int nb = s1 - s0;
+    // a leading run of one-token sequences in the first chunk (decode rows: row b is sequence b)
+    // takes the split-K decode attention; every other sequence is cut into query tiles
+    int n_dec = 0;
+    if (s0 == 0)
+      while (n_dec < nb && lengths[n_dec] == 1) ++n_dec;
     std::vector<int> row_pos(rows), row_seq(rows), last_row(nb);
     std::vector<int4> items;
     int r = 0;
     for (int b = s0; b < s1; ++b) {
-      const int L = lengths[b];
-      for (int t = 0; t < L; ++t) { row_pos[r + t] = t; row_seq[r + t] = b; }
-      for (int q0 = 0; q0 < L; q0 += item_rows) items.push_back(make_int4(b, q0, r + q0, L));
+      const int L = lengths[b], P = starts ? starts[b] : 0;
+      for (int t = 0; t < L; ++t) { row_pos[r + t] = P + t; row_seq[r + t] = b; }
+      if (b - s0 >= n_dec)
+        for (int q0 = 0; q0 < L; q0 += item_rows) items.push_back(make_int4(b, P + q0, r + q0, P + L));
       r += L;
       last_row[b - s0] = r - 1;
     }
@@ -657,18 +674,24 @@ llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* leng
     CUDA_TRY(cudaMemcpyAsync(h->d_row_pos, row_pos.data(), rows * sizeof(int), cudaMemcpyHostToDevice, h->stream));
     CUDA_TRY(cudaMemcpyAsync(h->d_row_seq, row_seq.data(), rows * sizeof(int), cudaMemcpyHostToDevice, h->stream));
     CUDA_TRY(cudaMemcpyAsync(h->d_last_row, last_row.data(), nb * sizeof(int), cudaMemcpyHostToDevice, h->stream));
-    CUDA_TRY(cudaMemcpyAsync(h->d_items, items.data(), items.size() * sizeof(int4), cudaMemcpyHostToDevice, h->stream));
+    if (!items.empty())
+      CUDA_TRY(cudaMemcpyAsync(h->d_items, items.data(), items.size() * sizeof(int4), cudaMemcpyHostToDevice, h->stream));
     StepArgs a{tokens + tok_off, h->d_row_pos, h->d_row_seq, tables, next_ids + s0,
                logits ? logits + (size_t)s0 * c.vocab : nullptr, h->d_last_row, rows, nb};
     CUDA_TRY(launch_set_args(h->d_args, a, h->stream));
     h->launch_counter++;
-    st = enqueue_forward(h, rows, nb, true, (int)items.size());
+    st = enqueue_forward(h, rows, nb, true, (int)items.size(), n_dec);
     if (st != LLM_OK) { end_call(h); return st; }
     tok_off += rows;
     s0 = s1;
   }
   end_call(h);
   return LLM_OK;
+}
+
+llm_status llm_prefill(llm_handle* h, const int32_t* tokens, const int32_t* lengths, const int32_t* tables, int B,
+                       int32_t* next_ids, float* logits) {
+  return llm_step(h, tokens, lengths, nullptr, tables, B, next_ids, logits);
 }
 
 llm_status llm_decode_step_host(llm_handle* h, const int32_t* tokens, const int32_t* positions,
@@ -830,6 +853,7 @@ llm_status llm_op_attention_decode(int kv_dtype, int B, int n_heads, int n_kv_he
   p.kv.n_kv_heads = n_kv_heads;
   p.kv.mbps = max_blocks_per_seq;
   p.kv.contiguous = 0;
+  p.kv.dtype = kv_dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
   p.args = args;
   p.B = B;
   p.n_heads = n_heads;

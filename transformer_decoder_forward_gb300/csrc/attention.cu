@@ -533,14 +533,16 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, int kv_dtype, cudaStre
   if (kv_dtype == DT_F32 && p.out_dtype == DT_F32) return decode_t<float, float>(p, s, pdl);
   if (kv_dtype == DT_F32 && p.out_dtype == DT_SPLIT) return decode_t<float, Split>(p, s, pdl);
   if (kv_dtype == DT_BF16 && p.out_dtype == DT_F32) return decode_t<bf16, float>(p, s, pdl);
+  if (kv_dtype == DT_BF16 && p.out_dtype == DT_SPLIT) return decode_t<bf16, Split>(p, s, pdl);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_prefill(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl) {
   if (p.n_items <= 0) return cudaSuccess;
-  if (kv_dtype != DT_F32) return cudaErrorInvalidValue;
-  if (p.out_dtype == DT_F32) return prefill_t<float, float>(p, s, pdl);
-  if (p.out_dtype == DT_SPLIT) return prefill_t<float, Split>(p, s, pdl);
+  if (kv_dtype == DT_F32 && p.out_dtype == DT_F32) return prefill_t<float, float>(p, s, pdl);
+  if (kv_dtype == DT_F32 && p.out_dtype == DT_SPLIT) return prefill_t<float, Split>(p, s, pdl);
+  if (kv_dtype == DT_BF16 && p.out_dtype == DT_F32) return prefill_t<bf16, float>(p, s, pdl);
+  if (kv_dtype == DT_BF16 && p.out_dtype == DT_SPLIT) return prefill_t<bf16, Split>(p, s, pdl);
   return cudaErrorInvalidValue;
 }
 

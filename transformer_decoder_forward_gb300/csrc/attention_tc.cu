@@ -1,6 +1,6 @@
 // Prefill attention on the tensor cores (tcgen05 / TMEM).
 //
-// Causal attention over the prompt, reading K and V from the paged fp32 cache in
+// Causal attention over the prompt, reading K and V from the paged cache (fp32 or bf16) in
 // place ("rvllm-metal", sections "What the kernels do" and "What's basic about it":
 // scores, -inf mask, softmax, probs @ V, without gathering the context into a
 // contiguous copy). CTA = (128 query rows of one sequence, query head h); two threads
@@ -73,8 +73,11 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-template <typename AT>
+// KT: element type of the KV pool. A bf16 pool holds exactly its bf16 values, so K and V need
+// no lo half and S and P.V take two products each (Q_hi.K + Q_lo.K, P_hi.V + P_lo.V).
+template <typename KT, typename AT>
 __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPrefillParams p) {
+  constexpr bool KV16 = std::is_same<KT, bf16>::value;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* barS = reinterpret_cast<uint64_t*>(base + OFF_BAR);
@@ -133,8 +136,8 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   const int qpos = qp0 + min(r, nq - 1);        // rows beyond the item repeat the last query
   const int kend = min(len, qp0 + nq);          // keys 0..kend-1 are visible to some row
   const int nkb = (kend + PT_K - 1) / PT_K;
-  const float* kpool = reinterpret_cast<const float*>(p.kv.k);
-  const float* vpool = reinterpret_cast<const float*>(p.kv.v);
+  const KT* kpool = reinterpret_cast<const KT*>(p.kv.k);
+  const KT* vpool = reinterpret_cast<const KT*>(p.kv.v);
   constexpr uint32_t idS = idesc_bf16(PT_Q, PT_K);
   constexpr uint32_t idO = idesc_bf16(PT_Q, HD);
   float o[32];
@@ -152,23 +155,34 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   __syncthreads();
 
   // K and V of key kb*64 + kr, kr = tid mod 64: this thread converts dims 16 q4 .. 16 q4 + 15,
-  // q4 = tid / 64. kv holds a later block's values (K, then V), loaded ahead in registers.
+  // q4 = tid / 64. kv holds a later block's values (K, then V), loaded ahead in registers
+  // (fp32 pool: 32 floats; bf16 pool: K in kraw, V unpacked to floats for the transpose).
   const int kr = tid & 63, q4 = tid >> 6;
   float kv[32];
+  uint4 kraw[2];
   auto prefetch = [&](int kb) {
     const int t = kb * PT_K + kr;
     int pb = -1;
     if (t < kend) pb = (t >> 4) < PT_MAX_LB ? s_pb[t >> 4] : kv_block(p.kv, a->block_tables, seq, t, flags);
     const size_t off = (pb >= 0 ? kv_offset(p.kv, pb, g, t & (KVB - 1)) : 0) + q4 * 16;
+    if constexpr (KV16) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 x = pb >= 0 ? *reinterpret_cast<const float4*>(kpool + off + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-      kv[4 * i] = x.x; kv[4 * i + 1] = x.y; kv[4 * i + 2] = x.z; kv[4 * i + 3] = x.w;
-    }
+      for (int i = 0; i < 2; ++i) {
+        kraw[i] = pb >= 0 ? *reinterpret_cast<const uint4*>(kpool + off + 8 * i) : make_uint4(0, 0, 0, 0);
+        const uint4 x = pb >= 0 ? *reinterpret_cast<const uint4*>(vpool + off + 8 * i) : make_uint4(0, 0, 0, 0);
+        Vec16<bf16>::unpack(x, kv + 16 + 8 * i);
+      }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 x = pb >= 0 ? *reinterpret_cast<const float4*>(vpool + off + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-      kv[16 + 4 * i] = x.x; kv[16 + 4 * i + 1] = x.y; kv[16 + 4 * i + 2] = x.z; kv[16 + 4 * i + 3] = x.w;
+      for (int i = 0; i < 4; ++i) {
+        const float4 x = pb >= 0 ? *reinterpret_cast<const float4*>(kpool + off + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        kv[4 * i] = x.x; kv[4 * i + 1] = x.y; kv[4 * i + 2] = x.z; kv[4 * i + 3] = x.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 x = pb >= 0 ? *reinterpret_cast<const float4*>(vpool + off + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        kv[16 + 4 * i] = x.x; kv[16 + 4 * i + 1] = x.y; kv[16 + 4 * i + 2] = x.z; kv[16 + 4 * i + 3] = x.w;
+      }
     }
   };
   // split the values in kv into K / V-transposed buffer b
@@ -176,10 +190,14 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
     unsigned char* kvb = base + OFF_KV + b * KV_BUF;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      uint4 hi, lo;
-      split8(kv + 8 * c, hi, lo);
-      *reinterpret_cast<uint4*>(kvb + KV_KHI + sw_off(kr, 2 * q4 + c)) = hi;
-      *reinterpret_cast<uint4*>(kvb + KV_KLO + sw_off(kr, 2 * q4 + c)) = lo;
+      if constexpr (KV16) {
+        *reinterpret_cast<uint4*>(kvb + KV_KHI + sw_off(kr, 2 * q4 + c)) = kraw[c];
+      } else {
+        uint4 hi, lo;
+        split8(kv + 8 * c, hi, lo);
+        *reinterpret_cast<uint4*>(kvb + KV_KHI + sw_off(kr, 2 * q4 + c)) = hi;
+        *reinterpret_cast<uint4*>(kvb + KV_KLO + sw_off(kr, 2 * q4 + c)) = lo;
+      }
     }
     // V transposed: B operand of P.V is dims (rows) x keys (K). Neighbouring keys 2j, 2j+1
     // (lanes kr, kr ^ 1) pair up so every store is one 32-bit word of two keys: the even
@@ -191,12 +209,14 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
       const float mine = odd ? v[8 + j] : v[j];
       const float other = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[8 + j], 1);
       const float ke = odd ? other : mine, ko = odd ? mine : other;   // keys 2j, 2j + 1
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(ke, ko);
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(ke - __low2float(hi), ko - __high2float(hi));
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(ke, ko);   // exact for a bf16 pool
       const int d = q4 * 16 + odd * 8 + j;
       const uint32_t o2 = sw_off(d, ck) + bk;
       *reinterpret_cast<__nv_bfloat162*>(kvb + KV_VHI + o2) = hi;
-      *reinterpret_cast<__nv_bfloat162*>(kvb + KV_VLO + o2) = lo;
+      if constexpr (!KV16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(ke - __low2float(hi), ko - __high2float(hi));
+        *reinterpret_cast<__nv_bfloat162*>(kvb + KV_VLO + o2) = lo;
+      }
     }
   };
   if (nkb > 0) {
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
       for (int ks = 0; ks < HD / 16; ++ks) {
         const uint64_t o2 = (uint64_t)(ks * 2);   // 32 bytes of K per MMA
         tc_mma(tmem, dq + o2, dk + o2, idS, ks > 0 ? 1u : 0u);
-        tc_mma(tmem, dq + o2, dkl + o2, idS, 1u);
+        if constexpr (!KV16) tc_mma(tmem, dq + o2, dkl + o2, idS, 1u);
         tc_mma(tmem, dql + o2, dk + o2, idS, 1u);
       }
       tc_commit(barS);
@@ -288,7 +308,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
         const uint64_t o2 = (uint64_t)(ks * 2);
         const uint32_t ph = tmem + (uint32_t)(ks * 8), pl = tmem + (uint32_t)(32 + ks * 8);
         tc_mma_ts(dO, ph, dv + o2, idO, ks > 0 ? 1u : 0u);
-        tc_mma_ts(dO, ph, dvl + o2, idO, 1u);
+        if constexpr (!KV16) tc_mma_ts(dO, ph, dvl + o2, idO, 1u);
         tc_mma_ts(dO, pl, dv + o2, idO, 1u);
       }
       tc_commit(barO);
@@ -330,13 +350,13 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   }
 }
 
-template <typename AT>
+template <typename KT, typename AT>
 cudaError_t prefill_tc_t(const AttnPrefillParams& p, cudaStream_t s, bool pdl) {
   static bool attr_set_dev[MAX_DEVICES] = {};
   bool& attr_set = attr_set_dev[current_device()];
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(k_attn_prefill_tc<AT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PT_SMEM);
+        cudaFuncSetAttribute(k_attn_prefill_tc<KT, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PT_SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -350,16 +370,18 @@ cudaError_t prefill_tc_t(const AttnPrefillParams& p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_attn_prefill_tc<AT>, p);
+  return cudaLaunchKernelEx(&cfg, k_attn_prefill_tc<KT, AT>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl) {
   if (p.n_items <= 0) return cudaSuccess;
-  if (kv_dtype != DT_F32 || p.n_heads % p.kv.n_kv_heads != 0) return cudaErrorInvalidValue;
-  if (p.out_dtype == DT_F32) return prefill_tc_t<float>(p, s, pdl);
-  if (p.out_dtype == DT_SPLIT) return prefill_tc_t<Split>(p, s, pdl);
+  if (p.n_heads % p.kv.n_kv_heads != 0) return cudaErrorInvalidValue;
+  if (kv_dtype == DT_F32 && p.out_dtype == DT_F32) return prefill_tc_t<float, float>(p, s, pdl);
+  if (kv_dtype == DT_F32 && p.out_dtype == DT_SPLIT) return prefill_tc_t<float, Split>(p, s, pdl);
+  if (kv_dtype == DT_BF16 && p.out_dtype == DT_F32) return prefill_tc_t<bf16, float>(p, s, pdl);
+  if (kv_dtype == DT_BF16 && p.out_dtype == DT_SPLIT) return prefill_tc_t<bf16, Split>(p, s, pdl);
   return cudaErrorInvalidValue;
 }
 

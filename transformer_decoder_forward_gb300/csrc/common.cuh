@@ -270,8 +270,7 @@ struct StepArgs {
   int B;
 };
 
-// Paged KV pool of one layer: [block][kv_head][16][64] fp32 (the library's cache; the
-// stand-alone decode-attention entry point also reads bf16 pools).
+// Paged KV pool of one layer: [block][kv_head][16][64], fp32 (the default) or bf16.
 struct KVLayer {
   void* k;
   void* v;
@@ -279,6 +278,7 @@ struct KVLayer {
   int n_kv_heads;
   int mbps;        // max blocks per sequence (block-table row length)
   int contiguous;  // sequence s owns blocks [s*mbps, (s+1)*mbps)
+  int dtype;       // DT_F32 or DT_BF16: element type of k and v
 };
 
 // Physical block holding logical position `pos` of sequence `seq`, or -1 (and a flag).

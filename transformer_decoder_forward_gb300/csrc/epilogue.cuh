@@ -8,7 +8,7 @@
 //   RESID   residual add after the output / down projection;
 //   GELU    GPT-2's GELU-tanh with the tanh argument clamped to +-15 ("batch_forge");
 //   SWIGLU  silu(gate) * up;
-//   QKV     bias, RoPE on q and k (Llama), kv_write of k and v into the paged fp32 cache;
+//   QKV     bias, RoPE on q and k (Llama), kv_write of k and v into the paged cache (fp32 or bf16);
 //   HEAD    tied-LM-head logits and a per-tile greedy argmax partial.
 //
 // Latency: the per-tile bias and the per-row KV slot are staged in shared memory
@@ -266,7 +266,19 @@ __device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0,
           const int pb = s_blk[m];
           if (pb < 0) continue;
           const int g = is_k ? hh - H : hh - H - Hkv;
-          dst = reinterpret_cast<float*>(is_k ? e.kv.k : e.kv.v) + kv_offset(e.kv, pb, g, pos & (KVB - 1));
+          const size_t off = kv_offset(e.kv, pb, g, pos & (KVB - 1));
+          if (e.kv.dtype == DT_BF16) {
+            // a bf16 cache stores k and v rounded to nearest (ties to even)
+            bf16* kd = reinterpret_cast<bf16*>(is_k ? e.kv.k : e.kv.v) + off;
+            const __nv_bfloat162 a0 = __floats2bfloat162_rn(v0[0], v0[1]), a1 = __floats2bfloat162_rn(v0[2], v0[3]);
+            const __nv_bfloat162 b0 = __floats2bfloat162_rn(v1[0], v1[1]), b1 = __floats2bfloat162_rn(v1[2], v1[3]);
+            *reinterpret_cast<uint2*>(kd + d) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&a0), *reinterpret_cast<const uint32_t*>(&a1));
+            *reinterpret_cast<uint2*>(kd + d + HD / 2) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+            continue;
+          }
+          dst = reinterpret_cast<float*>(is_k ? e.kv.k : e.kv.v) + off;
         }
         *reinterpret_cast<float4*>(dst + d) = make_float4(v0[0], v0[1], v0[2], v0[3]);
         *reinterpret_cast<float4*>(dst + d + HD / 2) = make_float4(v1[0], v1[1], v1[2], v1[3]);

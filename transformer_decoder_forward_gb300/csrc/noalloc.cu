@@ -106,6 +106,7 @@ extern "C" llm_status llm_op_attention_decode_noalloc(int kv_dtype, int B, int n
   p.kv.n_kv_heads = n_kv_heads;
   p.kv.mbps = max_blocks_per_seq;
   p.kv.contiguous = 0;
+  p.kv.dtype = kv_dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
   p.args = args;
   p.B = B;
   p.n_heads = n_heads;

@@ -41,7 +41,7 @@ class WorkloadRun:
         self.dev_w = dev_w
         mpt = max_prefill_tokens or max(int(self.lengths.max()), min(int(self.lengths.sum()), 16384))
         self.dec = Decoder(s, dev_w, max_batch=self.B, max_blocks_per_seq=self.mbps, num_kv_blocks=self.n_blocks,
-                           max_prefill_tokens=mpt, contiguous_kv=w.contiguous_kv)
+                           max_prefill_tokens=mpt, contiguous_kv=w.contiguous_kv, kv_dtype=w.kv_dtype)
         dev = "cuda"
         self.tables = torch.from_numpy(self.tables_np).to(dev)
         self.tokens = torch.from_numpy(np.concatenate(self.prompts).astype(np.int32)).to(dev)

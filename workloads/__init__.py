@@ -95,6 +95,7 @@ class Workload:
     contiguous_kv: bool = False
     shuffle_tables: bool = True
     weight_scale: float = 1.0  # 8.0 for the magnitude-scaled GPT-2 copy
+    kv_dtype: int = DTYPE_F32  # element type of the KV cache (DTYPE_BF16: rounded when written)
 
     def lengths(self) -> np.ndarray:
         if self.prompt_len:
