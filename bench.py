@@ -410,7 +410,7 @@ def decode_part(args, W, world: int, rank: int, local: int) -> dict:
     roof = None
     if alg is not None:
         roof = family_roofline(fam, dom, n_prof, ms_step, alg, "GB/s", pk["hbm_gbs"], f"hbm_gbs of {pk_kind}",
-                               label, traffic_for(W.name, label))
+                               label, traffic_for(W.name, label) if kv_elt == 4 else None)
     step_alg = float(np.mean([step_bytes(s, ctx_of(i), kv_elt) for i in range(args.steps)]))
     step_gbs = step_alg / (ms_step / 1000.0) / 1e9
     kernel_share = {k: round(v[1] / sum(x[1] for x in fam.values()), 4) for k, v in sorted(fam.items())}

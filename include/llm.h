@@ -203,6 +203,23 @@ llm_status llm_step(llm_handle* h, const int32_t* tokens, const int32_t* lengths
 llm_status llm_decode_step(llm_handle* h, const int32_t* tokens, const int32_t* positions,
                            const int32_t* block_tables, int B, int32_t* next_ids, float* logits);
 
+/* llm_decode_step that samples the next token instead of taking the argmax ("batch_forge",
+ * component table: sampling greedy, temperature, top-k). Per sequence b the candidates are
+ * the top_k largest logits (ties at the cut keep the lower index), ordered by value then
+ * index; p_i = exp((z_i - z_top) / temperature); the token is the first candidate whose
+ * running sum of p exceeds uniforms[b] * sum(p).
+ *   temperature   >= 0; 0 is greedy
+ *   top_k         1..64; 1 is greedy
+ *   uniforms      device float [B], the caller's draws in [0, 1) (values outside are clamped),
+ *                 or NULL for u = 0 (the most likely token); no random numbers are drawn here
+ *   logits        device float [B][vocab] or NULL (the handle keeps its own copy then)
+ * A NaN logit returns the first NaN index and sets LLM_FLAG_NAN_LOGIT, as the argmax does.
+ * Other arguments, graph capture and errors as llm_decode_step (INVALID_ARG also for
+ * temperature or top_k out of range). */
+llm_status llm_decode_step_sample(llm_handle* h, const int32_t* tokens, const int32_t* positions,
+                                  const int32_t* block_tables, int B, float temperature, int top_k,
+                                  const float* uniforms, int32_t* next_ids, float* logits);
+
 /* The same step from HOST buffers: copies tokens, positions and (unless NULL or
  * contiguous_kv) block_tables to the device, runs llm_decode_step, copies
  * next_ids (and logits when not NULL) back, and synchronises the stream before

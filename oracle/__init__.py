@@ -6,9 +6,9 @@ and never calls it.
 """
 from .decoder import (OracleModel, Sequence, argmax_rule, causal_attention, forward_full,
                       gelu_tanh, gelu_tanh_arg, greedy_generate, layer_norm, rms_norm, rope,
-                      round_bf16, silu, softmax, teacher_forced, top2_margin)
+                      round_bf16, sample_top_k, silu, softmax, teacher_forced, top2_margin)
 from .brute import BruteModel
 
 __all__ = ["OracleModel", "Sequence", "argmax_rule", "causal_attention", "forward_full", "gelu_tanh",
-           "gelu_tanh_arg", "greedy_generate", "layer_norm", "rms_norm", "rope", "round_bf16", "silu", "softmax",
+           "gelu_tanh_arg", "greedy_generate", "layer_norm", "rms_norm", "rope", "round_bf16", "sample_top_k", "silu", "softmax",
            "teacher_forced", "top2_margin", "BruteModel"]

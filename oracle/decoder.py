@@ -155,6 +155,26 @@ def argmax_rule(z: np.ndarray) -> int:
     return int(np.flatnonzero(z == z.max())[0])
 
 
+def sample_top_k(z: np.ndarray, temperature: float, top_k: int, u: float) -> int:
+    """Temperature / top-k sampling of one next token ("batch_forge", component table:
+    sampling greedy, temperature, top-k), with the uniform draw u in [0, 1) given.
+
+    The k largest logits are the candidates, ordered by value (ties: the lower index first,
+    so a tie at the k-th place keeps the lower index); p_i = exp((z_i - z_top) / T) over them;
+    the token is the first candidate whose running sum of p exceeds u * sum(p). top_k <= 1 or
+    T <= 0 is greedy (the argmax rule). A NaN logit gives the argmax rule's first NaN.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    if np.isnan(z).any() or top_k <= 1 or temperature <= 0.0:
+        return argmax_rule(z)
+    k = min(int(top_k), z.size)
+    order = np.lexsort((np.arange(z.size), -z))[:k]          # value descending, then index ascending
+    p = np.exp((z[order] - z[order[0]]) / float(temperature))
+    c = np.cumsum(p)
+    i = int(np.searchsorted(c, float(u) * c[-1], side="right"))
+    return int(order[min(i, k - 1)])
+
+
 def top2_margin(z: np.ndarray) -> float:
     """top-1 minus top-2 logit (the near-tie test of "rvllm-metal", section "How I know it's correct")."""
     part = np.partition(np.asarray(z, dtype=np.float64), -2)

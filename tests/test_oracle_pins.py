@@ -422,3 +422,46 @@ def test_bf16_kv_brute_force_equals_vectorised_oracle(shape):
     np.testing.assert_allclose(np.stack([seq.step(t) for t in tokens]), brute, rtol=RTOL, atol=1e-12)
     # the rounding is there: the fp32-cache model differs
     assert np.abs(np.array(oracle.BruteModel(w).run(tokens)) - brute).max() > 1e-6
+
+
+# ------------------------------------------------------------------------------------------------
+# temperature / top-k sampling ("batch_forge", component table: greedy, temperature, top-k)
+# ------------------------------------------------------------------------------------------------
+
+def test_sample_top_k_reduces_to_greedy():
+    z = rng(31).normal(size=500)
+    for u in (0.0, 0.3, 0.999):
+        assert od.sample_top_k(z, 0.7, 1, u) == od.argmax_rule(z)      # k = 1
+        assert od.sample_top_k(z, 0.0, 40, u) == od.argmax_rule(z)     # T = 0
+        assert od.sample_top_k(z, 1e-6, 40, u) == od.argmax_rule(z)    # T -> 0
+    assert od.sample_top_k(z, 0.9, 40, 0.0) == od.argmax_rule(z)       # u = 0: the top candidate
+    zn = z.copy()
+    zn[[7, 300]] = np.nan
+    assert od.sample_top_k(zn, 0.9, 40, 0.5) == 7                      # NaN: the argmax rule
+
+
+def test_sample_top_k_frequencies_are_the_truncated_softmax():
+    """Over a uniform grid of u the chosen tokens' frequencies equal the temperature softmax
+    restricted to the k largest logits (closed form, to 1/N)."""
+    z = rng(32).normal(size=300) * 2
+    T, k, N = 0.8, 12, 20000
+    top = np.argsort(-z, kind="stable")[:k]
+    p = np.exp((z[top] - z[top].max()) / T)
+    p /= p.sum()
+    counts = np.zeros(z.size)
+    for u in (np.arange(N) + 0.5) / N:
+        counts[od.sample_top_k(z, T, k, u)] += 1
+    assert set(np.flatnonzero(counts)) <= set(top.tolist())
+    np.testing.assert_allclose(counts[top] / N, p, atol=1.5 / N)
+    # adding a constant to every logit changes nothing
+    assert all(od.sample_top_k(z + 3.25, T, k, u) == od.sample_top_k(z, T, k, u) for u in (0.1, 0.5, 0.93))
+
+
+def test_sample_top_k_tie_at_the_cut_keeps_the_lower_index():
+    z = np.array([5.0, 1.0, 3.0, 3.0, 0.5, 3.0])
+    # k = 2: candidates 0 and the lowest-index 3.0 (index 2); a u past token 0's share picks 2
+    p0 = 1.0 / (1.0 + np.exp(-2.0))
+    assert od.sample_top_k(z, 1.0, 2, p0 + 1e-6) == 2
+    assert od.sample_top_k(z, 1.0, 2, p0 - 1e-6) == 0
+    # k = 3: candidates 0, 2, 3; the last share belongs to index 3
+    assert od.sample_top_k(z, 1.0, 3, 0.999999) == 3

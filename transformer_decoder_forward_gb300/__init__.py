@@ -20,7 +20,7 @@ STATUS = {0: "LLM_OK", 1: "LLM_ERR_INVALID_ARG", 2: "LLM_ERR_OUT_OF_RANGE", 3: "
           4: "LLM_ERR_UNSUPPORTED", 5: "LLM_ERR_OOM", 6: "LLM_ERR_CUDA", 7: "LLM_ERR_DEVICE_FLAG"}
 FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8, 16
 
-EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_host",
+EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_sample", "llm_decode_step_host",
            "llm_get_error_flags", "llm_selftest_wait_timeout", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
            "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode", "llm_op_attention_decode_noalloc",
            "llm_status_string", "llm_last_error"]
@@ -73,6 +73,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_step.argtypes = [vp, i32p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), i32p,
                              ctypes.c_int, i32p, vp]
     lib.llm_decode_step.argtypes = [vp, i32p, i32p, i32p, ctypes.c_int, i32p, vp]
+    lib.llm_decode_step_sample.argtypes = [vp, i32p, i32p, i32p, ctypes.c_int, ctypes.c_float, ctypes.c_int, vp,
+                                           i32p, vp]
     lib.llm_decode_step_host.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp]
     lib.llm_get_error_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.llm_set_profiling.argtypes = [vp, ctypes.c_int]
@@ -89,7 +91,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_status_string.restype = ctypes.c_char_p
     lib.llm_last_error.argtypes = []
     lib.llm_last_error.restype = ctypes.c_char_p
-    for name in ("llm_create", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_host", "llm_get_error_flags",
+    for name in ("llm_create", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_sample", "llm_decode_step_host", "llm_get_error_flags",
                  "llm_set_profiling", "llm_selftest_wait_timeout", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
                  "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode",
                  "llm_op_attention_decode_noalloc"):
@@ -220,6 +222,13 @@ class Decoder:
     def decode_step(self, tokens, positions, block_tables, next_ids, logits=None) -> None:
         _check(self.lib.llm_decode_step(self.handle, _ptr(tokens), _ptr(positions), _ptr(block_tables),
                                         int(tokens.numel()), _ptr(next_ids), _ptr(logits)))
+
+    def decode_step_sample(self, tokens, positions, block_tables, temperature: float, top_k: int, uniforms,
+                           next_ids, logits=None) -> None:
+        """A decode step that samples (temperature, top-k) with the caller's uniforms [B] (device)."""
+        _check(self.lib.llm_decode_step_sample(self.handle, _ptr(tokens), _ptr(positions), _ptr(block_tables),
+                                               int(tokens.numel()), float(temperature), int(top_k),
+                                               _ptr(uniforms), _ptr(next_ids), _ptr(logits)))
 
     def decode_step_host(self, tokens: np.ndarray, positions: np.ndarray, block_tables: Optional[np.ndarray],
                          next_ids: np.ndarray, logits: Optional[np.ndarray] = None) -> None:

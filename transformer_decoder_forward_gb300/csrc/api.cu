@@ -111,6 +111,7 @@ struct llm_handle {
   int* d_host_tables = nullptr;
   int* d_host_ids = nullptr;
   float* d_host_logits = nullptr;
+  float* d_samp_logits = nullptr;   // logits of a sampled step when the caller asks for none
   // execution options
   bool use_graphs = true;
   bool pdl = true;   // programmatic dependent launch between the step's kernels
@@ -277,7 +278,9 @@ llm_status norm_linear(llm_handle* h, const char* tag, LinearParams p, const voi
 // items != 0 selects prefill attention over `n_items` work items.
 // In a prefill pass, the first n_dec sequences (n_dec rows, one token each, rows 0..n_dec-1,
 // block-table rows 0..n_dec-1) take the split-K decode attention and the items the rest.
-llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_items, int n_dec = 0) {
+// sample: the step ends in temperature / top-k sampling (StepArgs) instead of the argmax.
+llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_items, int n_dec = 0,
+                           bool sample = false) {
   const llm_config& c = h->cfg;
   const int d = c.d_model, H = c.n_heads, Hkv = c.n_kv_heads, F = c.d_ff;
   const bool gpt2 = c.arch == LLM_ARCH_GPT2;
@@ -353,6 +356,11 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
   hp.epi = base_epi(h);
   hp.epi.kind = EPI_HEAD; hp.epi.part_val = h->head_val; hp.epi.part_idx = h->head_idx; hp.epi.vocab = c.vocab;
   { llm_status s_ = norm_linear(h, "head", hp, h->lnf_w, h->lnf_b, prefill); if (s_ != LLM_OK) return s_; }
+  if (sample) {
+    SampleParams sp{h->d_args, c.vocab, h->flags};
+    RUN("sample", launch_sample(sp, B, h->stream, h->pdl));
+    return LLM_OK;
+  }
   ArgmaxParams amp{h->head_val, h->head_idx, h->head_tiles, h->d_args, h->flags};
   RUN("argmax", launch_argmax(amp, B, h->stream, h->pdl));
   return LLM_OK;
@@ -369,6 +377,95 @@ void begin_call(llm_handle* h) { h->launch_counter = 0; }
 void end_call(llm_handle* h) { h->last_launches = h->launch_counter; }
 
 bool stream_capturable(cudaStream_t s) { return s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread; }
+
+// A decode step (greedy or sampled): eager, profiled or replayed from the graph cached for
+// (B, sampled).
+llm_status decode_step_impl(llm_handle* h, const StepArgs& a, bool sample) {
+  const int B = a.B;
+  llm_status st = LLM_OK;
+  begin_call(h);
+  if (h->profiling && stream_capturable(h->stream)) {
+    // Per-launch timing. Launched one by one, a decode step's kernels are shorter than the
+    // host's launch calls, so events around eager launches would time the host. The step is
+    // captured with an event record node around every launch instead, and replayed once:
+    // the events then time the kernels back to back on the device. Programmatic launch is
+    // off in this mode, so each interval holds one kernel alone.
+    const bool pdl = h->pdl;
+    h->pdl = false;
+    h->prof_capture = true;
+    const size_t nprof = h->prof.size();
+    cudaError_t e = cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal);
+    llm_status fs = LLM_ERR_CUDA;
+    cudaGraph_t g = nullptr;
+    if (e == cudaSuccess) {
+      e = launch_set_args(h->d_args, a, h->stream);
+      h->launch_counter++;
+      fs = e == cudaSuccess ? enqueue_forward(h, B, B, false, 0, 0, sample) : LLM_ERR_CUDA;
+      const cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
+      if (e == cudaSuccess) e = ee;
+    }
+    h->pdl = pdl;
+    h->prof_capture = false;
+    cudaGraphExec_t x = nullptr;
+    if (e == cudaSuccess && fs == LLM_OK) e = cudaGraphInstantiate(&x, g, 0);
+    if (g) cudaGraphDestroy(g);
+    if (e == cudaSuccess && fs == LLM_OK) e = cudaGraphLaunch(x, h->stream);
+    if (x) cudaGraphExecDestroy(x);   // released once the replay completes
+    end_call(h);
+    if (fs != LLM_OK || e != cudaSuccess) {
+      h->prof.resize(nprof);   // no records of a step that did not run
+      if (fs != LLM_OK) return fs;
+      cudaGetLastError();
+      return fail(LLM_ERR_CUDA, std::string("profiled step: ") + cudaGetErrorString(e));
+    }
+    return LLM_OK;
+  }
+  if (!h->use_graphs || h->profiling) {
+    CUDA_TRY(launch_set_args(h->d_args, a, h->stream));
+    h->launch_counter++;
+    st = enqueue_forward(h, B, B, false, 0, 0, sample);
+    end_call(h);
+    return st;
+  }
+  const int key = B | (sample ? (1 << 24) : 0);
+  auto it = h->graphs.find(key);
+  if (it == h->graphs.end()) {
+    GraphEntry ge;
+    CUDA_TRY(cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = launch_set_args(h->d_args, a, h->stream);
+    h->launch_counter++;
+    llm_status fs = e == cudaSuccess ? enqueue_forward(h, B, B, false, 0, 0, sample) : LLM_ERR_CUDA;
+    cudaGraph_t g = nullptr;
+    cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
+    if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("set_args: ") + cudaGetErrorString(e));
+    if (fs != LLM_OK) { if (g) cudaGraphDestroy(g); return fs; }
+    if (ee != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("end capture: ") + cudaGetErrorString(ee));
+    size_t nroots = 0;
+    CUDA_TRY(cudaGraphGetRootNodes(g, nullptr, &nroots));
+    std::vector<cudaGraphNode_t> roots(nroots);
+    CUDA_TRY(cudaGraphGetRootNodes(g, roots.data(), &nroots));
+    if (nroots != 1) { cudaGraphDestroy(g); return fail(LLM_ERR_CUDA, "captured step has more than one root"); }
+    ge.graph = g;
+    ge.args_node = roots[0];
+    CUDA_TRY(cudaGraphInstantiate(&ge.exec, g, 0));
+    ge.launches = h->launch_counter;
+    it = h->graphs.emplace(key, ge).first;
+  }
+  cudaKernelNodeParams kp;
+  memset(&kp, 0, sizeof(kp));
+  StepArgs* dst = h->d_args;
+  StepArgs av = a;
+  void* params[2] = {&dst, &av};
+  kp.func = const_cast<void*>(set_args_kernel());
+  kp.gridDim = dim3(1);
+  kp.blockDim = dim3(1);
+  kp.kernelParams = params;
+  CUDA_TRY(cudaGraphExecKernelNodeSetParams(it->second.exec, it->second.args_node, &kp));
+  CUDA_TRY(cudaGraphLaunch(it->second.exec, h->stream));
+  h->launch_counter = it->second.launches;
+  end_call(h);
+  return LLM_OK;
+}
 
 }  // namespace
 
@@ -501,6 +598,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   ALLOC(h->d_host_tables, int, (size_t)c.max_batch * c.max_blocks_per_seq);
   ALLOC(h->d_host_ids, int, c.max_batch);
   ALLOC(h->d_host_logits, float, (size_t)c.max_batch * c.vocab);
+  ALLOC(h->d_samp_logits, float, (size_t)c.max_batch * c.vocab);
   ALLOC(h->d_rope, float2, HD / 2);
 #undef ALLOC
   {
@@ -537,6 +635,7 @@ void llm_destroy(llm_handle* h) {
   delete h;
 }
 
+
 llm_status llm_decode_step(llm_handle* h, const int32_t* tokens, const int32_t* positions, const int32_t* tables,
                            int B, int32_t* next_ids, float* logits) {
   llm_status st = check_handle(h);
@@ -545,87 +644,24 @@ llm_status llm_decode_step(llm_handle* h, const int32_t* tokens, const int32_t* 
   if (B > h->cfg.max_batch) return fail(LLM_ERR_OUT_OF_RANGE, "B exceeds max_batch");
   if (!tokens || !positions || !next_ids) return fail(LLM_ERR_INVALID_ARG, "NULL tokens/positions/next_ids");
   if (!tables && !h->cfg.contiguous_kv) return fail(LLM_ERR_INVALID_ARG, "NULL block_tables");
-  StepArgs a{tokens, positions, nullptr, tables, next_ids, logits, nullptr, B, B};
-  begin_call(h);
-  if (h->profiling && stream_capturable(h->stream)) {
-    // Per-launch timing. Launched one by one, a decode step's kernels are shorter than the
-    // host's launch calls, so events around eager launches would time the host. The step is
-    // captured with an event record node around every launch instead, and replayed once:
-    // the events then time the kernels back to back on the device. Programmatic launch is
-    // off in this mode, so each interval holds one kernel alone.
-    const bool pdl = h->pdl;
-    h->pdl = false;
-    h->prof_capture = true;
-    const size_t nprof = h->prof.size();
-    cudaError_t e = cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal);
-    llm_status fs = LLM_ERR_CUDA;
-    cudaGraph_t g = nullptr;
-    if (e == cudaSuccess) {
-      e = launch_set_args(h->d_args, a, h->stream);
-      h->launch_counter++;
-      fs = e == cudaSuccess ? enqueue_forward(h, B, B, false, 0) : LLM_ERR_CUDA;
-      const cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
-      if (e == cudaSuccess) e = ee;
-    }
-    h->pdl = pdl;
-    h->prof_capture = false;
-    cudaGraphExec_t x = nullptr;
-    if (e == cudaSuccess && fs == LLM_OK) e = cudaGraphInstantiate(&x, g, 0);
-    if (g) cudaGraphDestroy(g);
-    if (e == cudaSuccess && fs == LLM_OK) e = cudaGraphLaunch(x, h->stream);
-    if (x) cudaGraphExecDestroy(x);   // released once the replay completes
-    end_call(h);
-    if (fs != LLM_OK || e != cudaSuccess) {
-      h->prof.resize(nprof);   // no records of a step that did not run
-      if (fs != LLM_OK) return fs;
-      cudaGetLastError();
-      return fail(LLM_ERR_CUDA, std::string("profiled step: ") + cudaGetErrorString(e));
-    }
-    return LLM_OK;
-  }
-  if (!h->use_graphs || h->profiling) {
-    CUDA_TRY(launch_set_args(h->d_args, a, h->stream));
-    h->launch_counter++;
-    st = enqueue_forward(h, B, B, false, 0);
-    end_call(h);
-    return st;
-  }
-  auto it = h->graphs.find(B);
-  if (it == h->graphs.end()) {
-    GraphEntry ge;
-    CUDA_TRY(cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
-    cudaError_t e = launch_set_args(h->d_args, a, h->stream);
-    h->launch_counter++;
-    llm_status fs = e == cudaSuccess ? enqueue_forward(h, B, B, false, 0) : LLM_ERR_CUDA;
-    cudaGraph_t g = nullptr;
-    cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
-    if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("set_args: ") + cudaGetErrorString(e));
-    if (fs != LLM_OK) { if (g) cudaGraphDestroy(g); return fs; }
-    if (ee != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("end capture: ") + cudaGetErrorString(ee));
-    size_t nroots = 0;
-    CUDA_TRY(cudaGraphGetRootNodes(g, nullptr, &nroots));
-    std::vector<cudaGraphNode_t> roots(nroots);
-    CUDA_TRY(cudaGraphGetRootNodes(g, roots.data(), &nroots));
-    if (nroots != 1) { cudaGraphDestroy(g); return fail(LLM_ERR_CUDA, "captured step has more than one root"); }
-    ge.graph = g;
-    ge.args_node = roots[0];
-    CUDA_TRY(cudaGraphInstantiate(&ge.exec, g, 0));
-    ge.launches = h->launch_counter;
-    it = h->graphs.emplace(B, ge).first;
-  }
-  cudaKernelNodeParams kp;
-  memset(&kp, 0, sizeof(kp));
-  StepArgs* dst = h->d_args;
-  void* params[2] = {&dst, &a};
-  kp.func = const_cast<void*>(set_args_kernel());
-  kp.gridDim = dim3(1);
-  kp.blockDim = dim3(1);
-  kp.kernelParams = params;
-  CUDA_TRY(cudaGraphExecKernelNodeSetParams(it->second.exec, it->second.args_node, &kp));
-  CUDA_TRY(cudaGraphLaunch(it->second.exec, h->stream));
-  h->launch_counter = it->second.launches;
-  end_call(h);
-  return LLM_OK;
+  StepArgs a{tokens, positions, nullptr, tables, next_ids, logits, nullptr, B, B, nullptr, 0.0f, 1};
+  return decode_step_impl(h, a, false);
+}
+
+llm_status llm_decode_step_sample(llm_handle* h, const int32_t* tokens, const int32_t* positions,
+                                  const int32_t* tables, int B, float temperature, int top_k, const float* uniforms,
+                                  int32_t* next_ids, float* logits) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  if (B <= 0) return fail(LLM_ERR_INVALID_ARG, "B must be positive");
+  if (B > h->cfg.max_batch) return fail(LLM_ERR_OUT_OF_RANGE, "B exceeds max_batch");
+  if (!tokens || !positions || !next_ids) return fail(LLM_ERR_INVALID_ARG, "NULL tokens/positions/next_ids");
+  if (!tables && !h->cfg.contiguous_kv) return fail(LLM_ERR_INVALID_ARG, "NULL block_tables");
+  if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return fail(LLM_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+  if (top_k < 1 || top_k > SAMPLE_MAX_K) return fail(LLM_ERR_INVALID_ARG, "top_k must be in 1..64");
+  StepArgs a{tokens, positions, nullptr, tables, next_ids, logits ? logits : h->d_samp_logits, nullptr, B, B,
+             uniforms, temperature, top_k};
+  return decode_step_impl(h, a, true);
 }
 
 llm_status llm_step(llm_handle* h, const int32_t* tokens, const int32_t* lengths, const int32_t* starts,

@@ -268,6 +268,10 @@ struct StepArgs {
   const int* last_row;      // [B] row of each sequence's last token, or nullptr (row b)
   int M;
   int B;
+  // sampled decode steps: one uniform draw in [0, 1) per sequence, temperature and top-k
+  const float* uniforms;    // [B] or nullptr
+  float temperature;
+  int top_k;
 };
 
 // Paged KV pool of one layer: [block][kv_head][16][64], fp32 (the default) or bf16.

@@ -33,11 +33,21 @@ struct ArgmaxParams {
   unsigned* flags;
 };
 
+// Temperature / top-k sampling of the next token (reads logits, uniforms, temperature and
+// top_k from the step arguments).
+constexpr int SAMPLE_MAX_K = 64;
+struct SampleParams {
+  const StepArgs* args;
+  int vocab;
+  unsigned* flags;
+};
+
 cudaLaunchConfig_t make_launch_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr,
                                    bool pdl);
 cudaError_t launch_embed(const EmbedParams& p, int wdt, cudaStream_t s, bool pdl);
 cudaError_t launch_norm(const NormParams& p, int wdt, int adt, cudaStream_t s, bool pdl);
 cudaError_t launch_argmax(const ArgmaxParams& p, int B, cudaStream_t s, bool pdl);
+cudaError_t launch_sample(const SampleParams& p, int B, cudaStream_t s, bool pdl);
 cudaError_t launch_set_args(StepArgs* dst, const StepArgs& v, cudaStream_t s);
 const void* set_args_kernel();
 cudaError_t launch_selftest_wait(unsigned* flags, cudaStream_t s);

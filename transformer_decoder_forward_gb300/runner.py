@@ -69,5 +69,13 @@ class WorkloadRun:
             self.dec.decode_step(tokens_dev, self.step_positions[step], self.tables, next_ids if next_ids is not None else self.next_ids,
                                  logits)
 
+    def decode_sample(self, tokens_dev, step: int, temperature: float, top_k: int, uniforms, logits=None,
+                      next_ids=None):
+        """Decode step `step` that samples the next token (temperature, top-k, the caller's uniforms)."""
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.dec.decode_step_sample(tokens_dev, self.step_positions[step], self.tables, temperature, top_k, uniforms,
+                                        next_ids if next_ids is not None else self.next_ids, logits)
+
     def close(self):
         self.dec.close()
