@@ -93,6 +93,21 @@ typedef struct {
                              LLM_DTYPE_BF16, K and V rounded to nearest bf16 (ties to even) when
                              written; half the cache bytes ("rvllm-metal", section "What's basic
                              about it", names the F32 cache as a weakness) */
+  /* Model-feature variants ("rvllm-metal", section "What the kernels do", last paragraph:
+   * Llama 3 RoPE scaling, Qwen2 attention biases, Qwen3 Q/K norm, Gemma's sliding window).
+   * All zero: none of them. Attention biases need no field: the Llama variant uses b_qkv
+   * when the weights give it. */
+  int sliding_window;         /* W > 0: a query at position p attends to p-W+1 .. p only */
+  int sliding_window_pattern; /* 0: every layer windowed; P > 0: layers l with (l+1) % P == 0
+                                 attend globally (Gemma's interleaving) */
+  int qk_norm;                /* 1: RMSNorm (eps = norm_eps, gains q_norm_w / k_norm_w [head_dim]
+                                 per layer) of every q and k head before RoPE (Llama variant) */
+  float rope_scale_factor;    /* Llama 3 RoPE scaling when > 1: a pair with wavelength 2 pi / f
+                                 above original / low_freq_factor turns at f / factor, below
+                                 original / high_freq_factor at f, linearly mixed in between */
+  float rope_low_freq_factor;
+  float rope_high_freq_factor;
+  int rope_original_max_pos;
 } llm_config;
 
 /*
@@ -112,6 +127,8 @@ typedef struct {
  *   b_up  [F] (GPT-2)
  *   w_down [d][F], b_down [d]
  *   lnf_w/lnf_b [d]               final norm
+ *   q_norm_w/k_norm_w [head_dim]  Q/K-norm gains per layer (config.qk_norm), else NULL
+ * The Llama variant has no biases except an optional b_qkv (attention biases).
  */
 typedef struct {
   const void* tok_emb;
@@ -130,6 +147,8 @@ typedef struct {
   const void* const* b_down;
   const void* lnf_w;
   const void* lnf_b;
+  const void* const* q_norm_w;
+  const void* const* k_norm_w;
 } llm_weights;
 
 typedef struct llm_handle llm_handle;

@@ -5,10 +5,10 @@ reference arm may import this package. The CUDA library shares no code with it
 and never calls it.
 """
 from .decoder import (OracleModel, Sequence, argmax_rule, causal_attention, forward_full,
-                      gelu_tanh, gelu_tanh_arg, greedy_generate, layer_norm, rms_norm, rope,
+                      gelu_tanh, gelu_tanh_arg, greedy_generate, layer_norm, llama3_scaled_inv_freq, rms_norm, rope,
                       round_bf16, sample_top_k, silu, softmax, teacher_forced, top2_margin)
 from .brute import BruteModel
 
 __all__ = ["OracleModel", "Sequence", "argmax_rule", "causal_attention", "forward_full", "gelu_tanh",
-           "gelu_tanh_arg", "greedy_generate", "layer_norm", "rms_norm", "rope", "round_bf16", "sample_top_k", "silu", "softmax",
+           "gelu_tanh_arg", "greedy_generate", "layer_norm", "llama3_scaled_inv_freq", "rms_norm", "rope", "round_bf16", "sample_top_k", "silu", "softmax",
            "teacher_forced", "top2_margin", "BruteModel"]

@@ -46,6 +46,10 @@ class BruteModel:
                 "w_up", "b_up", "w_down", "b_down")})
         self.lnf_w = _f(w.as_f64(w.lnf_w))
         self.lnf_b = _f(w.as_f64(w.lnf_b))
+        if s.qk_norm:
+            for l in range(s.n_layers):
+                self.L[l]["q_norm_w"] = _f(w.as_f64(w.q_norm_w[l]))
+                self.L[l]["k_norm_w"] = _f(w.as_f64(w.k_norm_w[l]))
 
     # ---- scalar helpers ------------------------------------------------------------------
     def _norm(self, x, g, b):
@@ -87,12 +91,39 @@ class BruteModel:
         u = min(15.0, max(-15.0, u))
         return 0.5 * x * (1.0 + math.tanh(u))
 
+    def _freq(self, i, hd):
+        """Frequency of RoPE pair i, with Llama 3 scaling when the shape asks for it."""
+        f = self.s.rope_theta ** (-2.0 * i / hd)
+        if self.s.rope_scaling is None:
+            return f
+        factor, lo, hi, orig = self.s.rope_scaling
+        wl = 2.0 * math.pi / f
+        if wl < orig / hi:
+            return f
+        if wl > orig / lo:
+            return f / factor
+        sm = (orig / wl - lo) / (hi - lo)
+        return (1.0 - sm) * f / factor + sm * f
+
+    def _window(self, l):
+        s = self.s
+        if s.sliding_window <= 0 or (s.sliding_window_pattern > 0 and (l + 1) % s.sliding_window_pattern == 0):
+            return 0
+        return s.sliding_window
+
+    def _head_rms(self, vec, g):
+        ss = 0.0
+        for x in vec:
+            ss += x * x
+        r = 1.0 / math.sqrt(ss / len(vec) + self.s.norm_eps)
+        return [vec[i] * r * g[i] for i in range(len(vec))]
+
     def _rope(self, vec, pos):
         hd = len(vec)
         half = hd // 2
         out = list(vec)
         for i in range(half):
-            ang = pos * self.s.rope_theta ** (-2.0 * i / hd)
+            ang = pos * self._freq(i, hd)
             c, sn = math.cos(ang), math.sin(ang)
             a, b = vec[i], vec[i + half]
             out[i] = a * c - b * sn
@@ -118,6 +149,9 @@ class BruteModel:
                 q = [qkv[hh * hd:(hh + 1) * hd] for hh in range(hq)]
                 k = [qkv[(hq + g) * hd:(hq + g + 1) * hd] for g in range(hkv)]
                 v = [qkv[(hq + hkv + g) * hd:(hq + hkv + g + 1) * hd] for g in range(hkv)]
+                if s.qk_norm:
+                    q = [self._head_rms(x, p["q_norm_w"]) for x in q]
+                    k = [self._head_rms(x, p["k_norm_w"]) for x in k]
                 if s.arch != ARCH_GPT2:
                     q = [self._rope(x, t) for x in q]
                     k = [self._rope(x, t) for x in k]
@@ -127,10 +161,12 @@ class BruteModel:
                 kc[l].append(k)
                 vc[l].append(v)
                 o = []
+                W = self._window(l)
+                j0 = max(0, t - W + 1) if W > 0 else 0
                 for hh in range(hq):
                     g = hh * hkv // hq
                     scores = []
-                    for j in range(t + 1):
+                    for j in range(j0, t + 1):
                         dot = 0.0
                         for e in range(hd):
                             dot += q[hh][e] * kc[l][j][g][e]
@@ -140,8 +176,8 @@ class BruteModel:
                     den = sum(ex)
                     for e in range(hd):
                         acc = 0.0
-                        for j in range(t + 1):
-                            acc += ex[j] / den * vc[l][j][g][e]
+                        for j in range(j0, t + 1):
+                            acc += ex[j - j0] / den * vc[l][j][g][e]
                         o.append(acc)
                 proj = self._matvec(p["w_o"], o, p["b_o"])
                 h = [h[i] + proj[i] for i in range(s.d_model)]

@@ -89,15 +89,37 @@ def silu(x: np.ndarray) -> np.ndarray:
         return x / (1.0 + np.exp(-x))
 
 
-def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
+def llama3_scaled_inv_freq(inv_freq: np.ndarray, factor: float, low_freq_factor: float, high_freq_factor: float,
+                           original_max_position: int) -> np.ndarray:
+    """Llama 3 RoPE scaling ("rvllm-metal", section "What the kernels do", last paragraph, names
+    it; the rule is the one the Llama 3.1 release defines). A pair whose wavelength 2 pi / f is
+    shorter than original_max_position / high_freq_factor keeps its frequency; one longer than
+    original_max_position / low_freq_factor is slowed by `factor`; in between the two are
+    mixed linearly in s = (original_max_position / wavelength - low_freq_factor) /
+    (high_freq_factor - low_freq_factor): f' = (1 - s) f / factor + s f.
+    """
+    f = np.asarray(inv_freq, dtype=np.float64)
+    wavelen = 2.0 * np.pi / f
+    low_wl = original_max_position / low_freq_factor
+    high_wl = original_max_position / high_freq_factor
+    s = (original_max_position / wavelen - low_freq_factor) / (high_freq_factor - low_freq_factor)
+    mid = (1.0 - s) * f / factor + s * f
+    return np.where(wavelen < high_wl, f, np.where(wavelen > low_wl, f / factor, mid))
+
+
+def rope(x: np.ndarray, pos: np.ndarray, theta: float, scaling=None) -> np.ndarray:
     """Rotate [T, H, hd] by position ("rvllm-metal", "What the kernels do": RoPE per pair).
 
     Element i of a head is paired with element i + hd/2 (half-split pairing);
-    pair i turns by the angle pos * theta^(-2i/hd).
+    pair i turns by the angle pos * theta^(-2i/hd) (with Llama 3 scaling of those
+    frequencies when ``scaling`` = (factor, low_freq_factor, high_freq_factor,
+    original_max_position) is given).
     """
     hd = x.shape[-1]
     half = hd // 2
     inv_freq = theta ** (-(2.0 * np.arange(half, dtype=np.float64)) / hd)
+    if scaling is not None:
+        inv_freq = llama3_scaled_inv_freq(inv_freq, *scaling)
     ang = np.asarray(pos, dtype=np.float64)[:, None] * inv_freq[None, :]      # [T, half]
     c = np.cos(ang)[:, None, :]
     s = np.sin(ang)[:, None, :]
@@ -112,18 +134,23 @@ def softmax(s: np.ndarray, axis: int = -1) -> np.ndarray:
     return e / e.sum(axis=axis, keepdims=True)
 
 
-def causal_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.ndarray) -> np.ndarray:
+def causal_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.ndarray, window: int = 0) -> np.ndarray:
     """Causal (grouped-query) attention.
 
     q [Tq, Hq, hd] at positions q_pos; k, v [Tk, Hkv, hd] hold positions 0..Tk-1.
-    Query i of head h reads KV head h // (Hq/Hkv) over keys j <= q_pos[i]:
+    Query i of head h reads KV head h // (Hq/Hkv) over keys j <= q_pos[i] (and, with a
+    sliding window W > 0, j > q_pos[i] - W: the W most recent positions, its own included;
+    "rvllm-metal", section "What the kernels do", names Gemma's sliding window):
     softmax_j(q.k_j / sqrt(hd)) weighted sum of v_j. Returns [Tq, Hq * hd].
     """
     tq, hq, hd = q.shape
     tk, hkv, _ = k.shape
     group = hq // hkv
     scale = 1.0 / np.sqrt(hd)
-    mask = np.arange(tk)[None, :] > np.asarray(q_pos)[:, None]                 # [Tq, Tk]
+    qp = np.asarray(q_pos)[:, None]
+    mask = np.arange(tk)[None, :] > qp                                          # [Tq, Tk]
+    if window > 0:
+        mask = mask | (np.arange(tk)[None, :] <= qp - window)
     out = np.empty((tq, hq, hd), dtype=np.float64)
     for h in range(hq):
         g = h // group
@@ -207,7 +234,21 @@ class OracleModel:
                 "w_up", "b_up", "w_down", "b_down")})
         self.lnf_w = f(w.lnf_w)
         self.lnf_b = f(w.lnf_b)
+        if self.shape.qk_norm:
+            for l in range(self.shape.n_layers):
+                self.layers[l]["q_norm_w"] = f(w.q_norm_w[l])
+                self.layers[l]["k_norm_w"] = f(w.k_norm_w[l])
         self.stats: Dict[str, float] = {}
+
+    def window(self, l: int) -> int:
+        """Sliding window of layer l (0: full causal). With a pattern P > 0 every P-th layer
+        (l + 1 a multiple of P) attends globally, as Gemma interleaves local and global layers."""
+        s = self.shape
+        if s.sliding_window <= 0:
+            return 0
+        if s.sliding_window_pattern > 0 and (l + 1) % s.sliding_window_pattern == 0:
+            return 0
+        return s.sliding_window
 
     # -- pieces ------------------------------------------------------------------------------
     def norm(self, x, g, b):
@@ -241,14 +282,19 @@ class OracleModel:
         q = qkv[:, : hq * hd].reshape(t, hq, hd)
         k = qkv[:, hq * hd: (hq + hkv) * hd].reshape(t, hkv, hd)
         v = qkv[:, (hq + hkv) * hd:].reshape(t, hkv, hd)
+        if s.qk_norm:
+            # Q/K norm ("rvllm-metal", "What the kernels do", names Qwen3's): RMSNorm of every
+            # q and k head over its head_dim values, before RoPE
+            q = rms_norm(q, p["q_norm_w"], s.norm_eps)
+            k = rms_norm(k, p["k_norm_w"], s.norm_eps)
         if s.arch == ARCH_LLAMA:
-            q = rope(q, positions, s.rope_theta)
-            k = rope(k, positions, s.rope_theta)
+            q = rope(q, positions, s.rope_theta, s.rope_scaling)
+            k = rope(k, positions, s.rope_theta, s.rope_scaling)
         if self.kv_dtype == DTYPE_BF16:
             k, v = round_bf16(k), round_bf16(v)
         k_all = k if k_cache is None else np.concatenate([k_cache, k], axis=0)
         v_all = v if v_cache is None else np.concatenate([v_cache, v], axis=0)
-        o = causal_attention(q, k_all, v_all, positions)
+        o = causal_attention(q, k_all, v_all, positions, self.window(l))
         h = h + self.linear(o, p["w_o"], p["b_o"])
         m = self.norm(h, p["ln2_w"], p["ln2_b"])
         up = self.linear(m, p["w_up"], p["b_up"])

@@ -22,8 +22,12 @@ CALLS = [
 ]
 
 
+WINDOWED = [replace(SMALL[2], name="small-llama-window", sliding_window=24, qk_norm=True),
+            replace(SMALL[0], name="small-gpt2-window", sliding_window=20)]
+
+
 @pytest.mark.parametrize("kv", [wl.DTYPE_F32, wl.DTYPE_BF16], ids=["kv-f32", "kv-bf16"])
-@pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
+@pytest.mark.parametrize("shape", SMALL + WINDOWED, ids=[s.name for s in SMALL + WINDOWED])
 def test_mixed_step_matches_oracle(gpu_lib, shape, kv):
     import torch
     from transformer_decoder_forward_gb300.runner import WorkloadRun

@@ -465,3 +465,85 @@ def test_sample_top_k_tie_at_the_cut_keeps_the_lower_index():
     assert od.sample_top_k(z, 1.0, 2, p0 - 1e-6) == 0
     # k = 3: candidates 0, 2, 3; the last share belongs to index 3
     assert od.sample_top_k(z, 1.0, 3, 0.999999) == 3
+
+
+# ------------------------------------------------------------------------------------------------
+# model-feature variants ("rvllm-metal", section "What the kernels do", last paragraph: Llama 3
+# RoPE scaling, Qwen2 attention biases, Qwen3 Q/K norm, Gemma's sliding window)
+# ------------------------------------------------------------------------------------------------
+
+LLAMA3_SCALING = (8.0, 1.0, 4.0, 8192)
+
+
+def test_llama3_rope_scaling_regions():
+    hd, theta = 128, 5e5
+    f = theta ** (-(2.0 * np.arange(hd // 2)) / hd)
+    g = od.llama3_scaled_inv_freq(f, *LLAMA3_SCALING)
+    wl_ = 2 * np.pi / f
+    hi_wl, lo_wl = 8192 / 4.0, 8192 / 1.0
+    np.testing.assert_array_equal(g[wl_ < hi_wl], f[wl_ < hi_wl])                  # fast pairs kept
+    np.testing.assert_allclose(g[wl_ > lo_wl], f[wl_ > lo_wl] / 8.0, rtol=1e-15)   # slow pairs / factor
+    mid = (wl_ >= hi_wl) & (wl_ <= lo_wl)
+    assert mid.any() and np.all(g[mid] <= f[mid]) and np.all(g[mid] >= f[mid] / 8.0)
+    assert np.all(np.diff(g) < 0)                                                  # still ordered
+    # the blend is continuous at both ends of the middle band
+    for w_edge, want in ((hi_wl, 1.0), (lo_wl, 1.0 / 8.0)):
+        fe = 2 * np.pi / w_edge
+        got = od.llama3_scaled_inv_freq(np.array([fe * (1 - 1e-12), fe * (1 + 1e-12)]), *LLAMA3_SCALING)
+        np.testing.assert_allclose(got / fe, want, rtol=1e-9)
+
+
+def test_sliding_window_attention_special_cases_and_torch():
+    r = rng(41)
+    T, hq, hkv, hd = 11, 4, 2, 8
+    q, k, v = r.normal(size=(T, hq, hd)), r.normal(size=(T, hkv, hd)), r.normal(size=(T, hkv, hd))
+    pos = np.arange(T)
+    full = od.causal_attention(q, k, v, pos)
+    np.testing.assert_array_equal(od.causal_attention(q, k, v, pos, window=T), full)    # W >= T: plain causal
+    one = od.causal_attention(q, k, v, pos, window=1).reshape(T, hq, hd)               # W = 1: itself only
+    np.testing.assert_allclose(one, np.repeat(v, hq // hkv, axis=1), rtol=1e-15)
+    W = 4
+    i, j = np.arange(T)[:, None], np.arange(T)[None, :]
+    allowed = torch.from_numpy((j <= i) & (j > i - W))
+    tq = torch.from_numpy(q).permute(1, 0, 2)
+    tk = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)
+    tv = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)
+    ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=allowed).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(od.causal_attention(q, k, v, pos, window=W).reshape(T, hq, hd), ref,
+                               rtol=1e-12, atol=1e-13)
+
+
+VARIANTS = [
+    wl.tiny_shape(wl.ARCH_LLAMA, n_heads=4, n_kv_heads=2, rope_theta=1e4, qk_norm=True, attn_bias=True,
+                  rope_scaling=(4.0, 1.0, 4.0, 8), sliding_window=3),
+    wl.tiny_shape(wl.ARCH_LLAMA, n_layers=2, n_heads=2, n_kv_heads=1, sliding_window=2, sliding_window_pattern=2,
+                  dtype=wl.DTYPE_BF16),
+    wl.tiny_shape(wl.ARCH_GPT2, sliding_window=3),
+]
+
+
+@pytest.mark.parametrize("shape", VARIANTS, ids=["llama-all-features", "llama-window-pattern", "gpt2-window"])
+def test_feature_variants_brute_force_equals_vectorised_oracle(shape):
+    w = wl.make_weights(shape, scale=20.0, perturb=True)
+    tokens = [3, 10, 0, 7, 7, 1]
+    brute = np.array(oracle.BruteModel(w).run(tokens))
+    m = oracle.OracleModel(w)
+    np.testing.assert_allclose(oracle.forward_full(m, tokens), brute, rtol=RTOL, atol=1e-12)
+    seq = oracle.Sequence(m)
+    np.testing.assert_allclose(np.stack([seq.step(t) for t in tokens]), brute, rtol=RTOL, atol=1e-12)
+    # every feature changes the result (none is silently dropped)
+    from dataclasses import replace
+    for off in (dict(sliding_window=0), dict(qk_norm=False), dict(rope_scaling=None), dict(attn_bias=False)):
+        key, val = next(iter(off.items()))
+        if getattr(shape, key) == val:
+            continue
+        w2 = wl.make_weights(replace(shape, **off), scale=20.0, perturb=True)
+        assert np.abs(oracle.forward_full(oracle.OracleModel(w2), tokens) - brute).max() > 1e-6, key
+
+
+def test_qk_norm_gives_unit_rms_heads():
+    r = rng(43)
+    q = r.normal(size=(5, 3, 64)) * 0.1
+    y = od.rms_norm(q, np.ones(64), 1e-5)
+    ms = (q * q).mean(-1)
+    np.testing.assert_allclose(np.sqrt((y * y).mean(-1)), np.sqrt(ms / (ms + 1e-5)), rtol=1e-12)

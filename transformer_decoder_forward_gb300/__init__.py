@@ -37,7 +37,10 @@ class LLMConfig(ctypes.Structure):
                                              "head_dim", "d_ff", "vocab", "n_ctx")] + \
                [("norm_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
                [(n, ctypes.c_int) for n in ("kv_block_size", "num_kv_blocks", "max_batch", "max_blocks_per_seq",
-                                             "max_prefill_tokens", "contiguous_kv", "kv_dtype")]
+                                             "max_prefill_tokens", "contiguous_kv", "kv_dtype", "sliding_window",
+                                             "sliding_window_pattern", "qk_norm")] + \
+               [(n, ctypes.c_float) for n in ("rope_scale_factor", "rope_low_freq_factor", "rope_high_freq_factor")] + \
+               [("rope_original_max_pos", ctypes.c_int)]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -47,7 +50,7 @@ class LLMWeights(ctypes.Structure):
     _fields_ = [("tok_emb", ctypes.c_void_p), ("pos_emb", ctypes.c_void_p)] + \
                [(n, _PP) for n in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b",
                                    "w_up", "b_up", "w_down", "b_down")] + \
-               [("lnf_w", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p)]
+               [("lnf_w", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p), ("q_norm_w", _PP), ("k_norm_w", _PP)]
 
 
 class KernelStat(ctypes.Structure):
@@ -158,6 +161,8 @@ def upload_weights(w, device: str = "cuda"):
     out = {"tok_emb": dev(w.tok_emb), "pos_emb": dev(w.pos_emb), "lnf_w": dev(w.lnf_w), "lnf_b": dev(w.lnf_b)}
     for k in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b", "w_up", "b_up", "w_down", "b_down"):
         out[k] = [dev(a) for a in getattr(w, k)]
+    for k in ("q_norm_w", "k_norm_w"):
+        out[k] = None if getattr(w, k) is None else [dev(a) for a in getattr(w, k)]
     return out
 
 
@@ -182,7 +187,11 @@ class Decoder:
                       rope_theta=shape.rope_theta, kv_block_size=16, num_kv_blocks=num_kv_blocks,
                       max_batch=max_batch, max_blocks_per_seq=max_blocks_per_seq,
                       max_prefill_tokens=max_prefill_tokens, contiguous_kv=int(contiguous_kv),
-                      kv_dtype=int(kv_dtype))
+                      kv_dtype=int(kv_dtype), sliding_window=int(shape.sliding_window),
+                      sliding_window_pattern=int(shape.sliding_window_pattern), qk_norm=int(shape.qk_norm))
+        if shape.rope_scaling is not None:
+            c.rope_scale_factor, c.rope_low_freq_factor, c.rope_high_freq_factor = (float(x) for x in shape.rope_scaling[:3])
+            c.rope_original_max_pos = int(shape.rope_scaling[3])
         self.config = c
         L = shape.n_layers
         self._arrays = []
@@ -198,7 +207,7 @@ class Decoder:
         w = LLMWeights(tok_emb=_ptr(dev_w["tok_emb"]), pos_emb=_ptr(dev_w["pos_emb"]),
                        lnf_w=_ptr(dev_w["lnf_w"]), lnf_b=_ptr(dev_w["lnf_b"]))
         for k in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b", "w_up", "b_up", "w_down",
-                  "b_down"):
+                  "b_down", "q_norm_w", "k_norm_w"):
             setattr(w, k, arr(k))
         handle = ctypes.c_void_p()
         torch.cuda.synchronize()

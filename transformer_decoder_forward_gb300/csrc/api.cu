@@ -45,6 +45,7 @@ llm_status fail(llm_status s, const std::string& msg) {
 
 struct LayerW {
   const void *ln1_w, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o, *ln2_w, *ln2_b, *w_up, *b_up, *w_down, *b_down;
+  const void *q_norm_w, *k_norm_w;   // Q/K-norm gains, or nullptr
 };
 
 struct GraphEntry {
@@ -234,6 +235,14 @@ KVLayer kv_layer(const llm_handle* h, int l) {
   return kv;
 }
 
+// Sliding window of layer l (0: full causal attention).
+int layer_window(const llm_handle* h, int l) {
+  const llm_config& c = h->cfg;
+  if (c.sliding_window <= 0) return 0;
+  if (c.sliding_window_pattern > 0 && (l + 1) % c.sliding_window_pattern == 0) return 0;
+  return c.sliding_window;
+}
+
 Epilogue base_epi(const llm_handle* h) {
   Epilogue e;
   memset(&e, 0, sizeof(e));
@@ -306,6 +315,9 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
     lp.epi.rope = gpt2 ? 0 : 1;
     lp.epi.rope_theta = c.rope_theta;
     lp.epi.rope_tab = h->d_rope;
+    lp.epi.qn_g = w.q_norm_w;
+    lp.epi.kn_g = w.k_norm_w;
+    lp.epi.qk_eps = c.norm_eps;
     { llm_status s_ = norm_linear(h, "qkv", lp, w.ln1_w, w.ln1_b, false); if (s_ != LLM_OK) return s_; }
 
     // attention
@@ -314,14 +326,14 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
       memset(&ap, 0, sizeof(ap));
       ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.B = prefill ? n_dec : B; ap.n_heads = H;
       ap.split = h->split; ap.max_splits = h->max_splits; ap.part_o = h->attn_po; ap.part_ml = h->attn_ml;
-      ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
+      ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags; ap.window = layer_window(h, l);
       RUN("attn_decode", launch_attn_decode(ap, h->kvdt, h->stream, h->pdl));
     }
     if (prefill && n_items > 0) {
       AttnPrefillParams ap;
       memset(&ap, 0, sizeof(ap));
       ap.q = h->q; ap.kv = kv_layer(h, l); ap.args = h->d_args; ap.items = h->d_items; ap.n_items = n_items;
-      ap.n_heads = H; ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags;
+      ap.n_heads = H; ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags; ap.window = layer_window(h, l);
       // bf16-weight models: tensor cores on bf16 (hi, lo) splits (about 16 bits of every
       // operand); fp32-weight models keep fp32 FMA so their attention stays at fp32 accuracy
       if (h->wdt == DT_BF16) RUN("attn_prefill", launch_attn_prefill_tc(ap, h->kvdt, h->stream, h->pdl));
@@ -506,6 +518,11 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   if (c.arch == LLM_ARCH_LLAMA && !(c.rope_theta > 0.0f)) return fail(LLM_ERR_INVALID_ARG, "rope_theta must be > 0");
   if (!c.contiguous_kv && c.num_kv_blocks <= 0) return fail(LLM_ERR_INVALID_ARG, "num_kv_blocks must be positive");
   if (c.kv_dtype != LLM_DTYPE_F32 && c.kv_dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_INVALID_ARG, "bad kv_dtype");
+  if (c.sliding_window < 0 || c.sliding_window_pattern < 0) return fail(LLM_ERR_INVALID_ARG, "negative sliding window");
+  if (c.qk_norm && (!wp->q_norm_w || !wp->k_norm_w)) return fail(LLM_ERR_INVALID_ARG, "qk_norm needs q_norm_w and k_norm_w");
+  if (c.rope_scale_factor > 1.0f &&
+      !(c.rope_original_max_pos > 0 && c.rope_high_freq_factor > c.rope_low_freq_factor && c.rope_low_freq_factor > 0.0f))
+    return fail(LLM_ERR_INVALID_ARG, "RoPE scaling needs original_max_pos > 0 and high_freq_factor > low_freq_factor > 0");
   const bool gpt2 = c.arch == LLM_ARCH_GPT2;
   if (!wp->tok_emb || (gpt2 && !wp->pos_emb) || !wp->lnf_w || (gpt2 && !wp->lnf_b))
     return fail(LLM_ERR_INVALID_ARG, "missing embedding or final-norm weights");
@@ -551,7 +568,14 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
     w.ln2_w = wp->ln2_w[l]; w.ln2_b = wp->ln2_b ? wp->ln2_b[l] : nullptr;
     w.w_up = wp->w_up[l]; w.b_up = wp->b_up ? wp->b_up[l] : nullptr;
     w.w_down = wp->w_down[l]; w.b_down = wp->b_down ? wp->b_down[l] : nullptr;
-    if (!gpt2) { w.ln1_b = w.b_qkv = w.b_o = w.ln2_b = w.b_up = w.b_down = nullptr; }
+    w.q_norm_w = c.qk_norm ? wp->q_norm_w[l] : nullptr;
+    w.k_norm_w = c.qk_norm ? wp->k_norm_w[l] : nullptr;
+    // the Llama variant has no biases but the optional attention (q, k, v) biases
+    if (!gpt2) { w.ln1_b = w.b_o = w.ln2_b = w.b_up = w.b_down = nullptr; }
+    if (c.qk_norm && (!w.q_norm_w || !w.k_norm_w)) {
+      delete h;
+      return fail(LLM_ERR_INVALID_ARG, "NULL Q/K-norm gain in layer " + std::to_string(l));
+    }
     if (!w.ln1_w || !w.w_qkv || !w.w_o || !w.ln2_w || !w.w_up || !w.w_down ||
         (gpt2 && (!w.ln1_b || !w.b_qkv || !w.b_o || !w.ln2_b || !w.b_up || !w.b_down))) {
       delete h;
@@ -606,7 +630,19 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
     // pos * hi is exact in fp32 for pos < 2^13) + lo, computed once here in double
     float2 tab[HD / 2];
     for (int d = 0; d < HD / 2; ++d) {
-      const double f = gpt2 ? 0.0 : pow((double)c.rope_theta, -2.0 * d / HD);
+      double f = gpt2 ? 0.0 : pow((double)c.rope_theta, -2.0 * d / HD);
+      if (!gpt2 && c.rope_scale_factor > 1.0f) {
+        // Llama 3 frequency scaling: long wavelengths slowed by the factor, short ones kept,
+        // a linear blend between the two bands
+        const double pi = 3.14159265358979323846, orig = c.rope_original_max_pos;
+        const double lo = c.rope_low_freq_factor, hi = c.rope_high_freq_factor, wl = 2.0 * pi / f;
+        if (wl > orig / lo) {
+          f = f / c.rope_scale_factor;
+        } else if (wl >= orig / hi) {
+          const double sm = (orig / wl - lo) / (hi - lo);
+          f = (1.0 - sm) * f / c.rope_scale_factor + sm * f;
+        }
+      }
       float hi = (float)f;
       uint32_t bits;
       memcpy(&bits, &hi, 4);

@@ -98,10 +98,15 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
   // the first copies of older blocks overlap the end of that projection.
   const StepArgs* a = p.args;
   const int ctx = a->positions[b] + 1;
-  // the sequence's ns = ceil(ctx / split) chunks share its context evenly (16-token multiples)
-  const int ns = ctx > 0 ? min(p.max_splits, (ctx + p.split - 1) / p.split) : 0;
-  const int chunk = ns > 0 ? min(p.split, ((ctx + ns - 1) / ns + KVB - 1) / KVB * KVB) : 0;
-  const int t0 = sp * chunk;
+  // visible keys lo..ctx-1 (a sliding window starts at ctx - W); the span from the block that
+  // holds lo is cut into ns = ceil(span / split) even chunks (16-token multiples). Every block
+  // a warp reads then holds at least one visible key, so its score maximum is finite.
+  const int lo = p.window > 0 ? max(0, ctx - p.window) : 0;
+  const int tb = lo & ~(KVB - 1);
+  const int span = ctx - tb;
+  const int ns = ctx > 0 ? min(p.max_splits, (span + p.split - 1) / p.split) : 0;
+  const int chunk = ns > 0 ? min(p.split, ((span + ns - 1) / ns + KVB - 1) / KVB * KVB) : 0;
+  const int t0 = tb + sp * chunk;
   if (ns <= 0 || t0 >= ctx) {
     pdl_wait();
     return;
@@ -167,7 +172,7 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
         const int t = it * TG + tg;
         float kf[8];
         lds_row8<KT>(K + t * HD, dg, kf);
-        const bool valid = tok0 + t < nt;
+        const bool valid = tok0 + t < nt && t0 + tok0 + t >= lo;
 #pragma unroll
         for (int jj = 0; jj < GMAX; ++jj) {
           float d = 0.0f;
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
         for (int it = 1; it < IT; ++it) mb = fmaxf(mb, sc[jj][it]);
         mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
         mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-        // mb is finite (token 0 of every block is valid) and the same in every lane; the
+        // mb is finite (every block holds a visible key) and the same in every lane; the
         // running state only needs rescaling when the maximum grows (alpha = 1 otherwise)
         if (mb > m[jj]) {
           const float alpha = exp2f(m[jj] - mb);   // m = -inf gives 0
@@ -282,7 +287,8 @@ __global__ void __launch_bounds__(HD) k_attn_decode_merge(const AttnDecodeParams
   const int bh = blockIdx.x, b = bh / p.n_heads, d = threadIdx.x;
   pdl_wait();
   const int ctx = p.args->positions[b] + 1;
-  const int ns = ctx <= 0 ? 0 : min(p.max_splits, (ctx + p.split - 1) / p.split);
+  const int tb = (p.window > 0 ? max(0, ctx - p.window) : 0) & ~(KVB - 1);   // as the split kernel
+  const int ns = ctx <= 0 ? 0 : min(p.max_splits, (ctx - tb + p.split - 1) / p.split);
   const float* ml = p.part_ml + (size_t)bh * p.max_splits * 2;
   const float* po = p.part_o + (size_t)bh * p.max_splits * HD;
   constexpr int MS = 8;   // chunks per pass, all loads of a pass issued together
@@ -353,7 +359,9 @@ __global__ void __launch_bounds__(AP_THREADS) k_attn_prefill(const AttnPrefillPa
   const KT* vbase = reinterpret_cast<const KT*>(p.kv.v);
   const int last_q = qp0 + nq - 1;
   const int n_kt = last_q / AP_T + 1;
-  for (int kt = 0; kt < n_kt; ++kt) {
+  const int W = p.window;
+  const int kt0 = W > 0 ? max(0, qp0 - W + 1) / AP_T : 0;   // first tile any row's window reaches
+  for (int kt = kt0; kt < n_kt; ++kt) {
     __syncthreads();
     // load K (transposed) and V for keys kt*64 .. kt*64+63
     constexpr int EPL = 16 / sizeof(KT);
@@ -401,17 +409,20 @@ __global__ void __launch_bounds__(AP_THREADS) k_attn_prefill(const AttnPrefillPa
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int kp = kt * AP_T + tx * 4 + j;
-        if (kp > qpos) s[i][j] = -INFINITY;
+        if (kp > qpos || (W > 0 && kp <= qpos - W)) s[i][j] = -INFINITY;
         tmax = fmaxf(tmax, s[i][j]);
       }
 #pragma unroll
       for (int off = 1; off < 16; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
       const float mnew = fmaxf(mrow[i], tmax);
-      const float alpha = expf(mrow[i] - mnew);   // mrow = -inf on the first tile -> 0
+      // a row that has seen no visible key yet (its window starts later) keeps m = -inf; the
+      // reference 0 then gives alpha = 0 and exp(-inf) = 0 instead of exp(-inf - -inf)
+      const float mref = mnew == -INFINITY ? 0.0f : mnew;
+      const float alpha = expf(mrow[i] - mref);   // mrow = -inf on the first tile -> 0
       float psum = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float e = expf(s[i][j] - mnew);
+        const float e = expf(s[i][j] - mref);
         s[i][j] = e;
         psum += e;
       }

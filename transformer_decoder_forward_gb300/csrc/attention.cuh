@@ -18,6 +18,7 @@ struct AttnDecodeParams {
   void* out;                // [B][H*64] activations (DT_F32, or DT_SPLIT: row stride 2*H*64 bf16)
   int out_dtype;
   unsigned* flags;
+  int window;               // sliding window W > 0: keys positions[b]-W+1 .. positions[b]; 0: all
 };
 
 // Prefill: packed rows; a work item is (sequence, first query position, row of that
@@ -32,6 +33,7 @@ struct AttnPrefillParams {
   void* out;                // [rows][H*64] activations (DT_F32 or DT_SPLIT)
   int out_dtype;
   unsigned* flags;
+  int window;               // sliding window W > 0: a query at p sees keys p-W+1 .. p; 0: all
 };
 
 // Tokens per decode split for a batch of B sequences of up to max_ctx keys (a multiple of

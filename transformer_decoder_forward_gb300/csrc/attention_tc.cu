@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   const int qpos = qp0 + min(r, nq - 1);        // rows beyond the item repeat the last query
   const int kend = min(len, qp0 + nq);          // keys 0..kend-1 are visible to some row
   const int nkb = (kend + PT_K - 1) / PT_K;
+  const int W = p.window;                       // sliding window: keys qpos-W+1 .. qpos
+  const int kb0 = W > 0 ? max(0, qp0 - W + 1) / PT_K : 0;   // first 64-key block any row sees
+  const int lb0 = kb0 * (PT_K / KVB);
   const KT* kpool = reinterpret_cast<const KT*>(p.kv.k);
   const KT* vpool = reinterpret_cast<const KT*>(p.kv.v);
   constexpr uint32_t idS = idesc_bf16(PT_Q, PT_K);
@@ -150,8 +153,8 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   // loads below wait on no table lookup
   int* s_pb = reinterpret_cast<int*>(base + OFF_PB);
   const int nlb = (kend + KVB - 1) / KVB;
-  for (int lb = tid; lb < min(nlb, PT_MAX_LB); lb += PT_THREADS)
-    s_pb[lb] = kv_block(p.kv, a->block_tables, seq, lb * KVB, flags);
+  for (int lb = lb0 + tid; lb < min(nlb, lb0 + PT_MAX_LB); lb += PT_THREADS)
+    s_pb[lb - lb0] = kv_block(p.kv, a->block_tables, seq, lb * KVB, flags);
   __syncthreads();
 
   // K and V of key kb*64 + kr, kr = tid mod 64: this thread converts dims 16 q4 .. 16 q4 + 15,
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
   auto prefetch = [&](int kb) {
     const int t = kb * PT_K + kr;
     int pb = -1;
-    if (t < kend) pb = (t >> 4) < PT_MAX_LB ? s_pb[t >> 4] : kv_block(p.kv, a->block_tables, seq, t, flags);
+    if (t < kend) pb = (t >> 4) - lb0 < PT_MAX_LB ? s_pb[(t >> 4) - lb0] : kv_block(p.kv, a->block_tables, seq, t, flags);
     const size_t off = (pb >= 0 ? kv_offset(p.kv, pb, g, t & (KVB - 1)) : 0) + q4 * 16;
     if constexpr (KV16) {
 #pragma unroll
@@ -219,10 +222,10 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
       }
     }
   };
-  if (nkb > 0) {
-    prefetch(0);
+  if (nkb > kb0) {
+    prefetch(kb0);
     store_kv(0);
-    if (nkb > 1) prefetch(1);
+    if (nkb > kb0 + 1) prefetch(kb0 + 1);
   }
   fence_async_smem();
   tc_fence_before();
@@ -231,8 +234,8 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
 
   // Per block kb: the S MMA runs while the threads store block kb + 1 into the other buffer
   // and load block kb + 2; softmax; P to TMEM; the P.V MMA; fold into o.
-  for (int kb = 0; kb < nkb && ok; ++kb) {
-    const int b = kb & 1;
+  for (int kb = kb0; kb < nkb && ok; ++kb) {
+    const int b = (kb - kb0) & 1;
     unsigned char* kvb = base + OFF_KV + b * KV_BUF;
     if (tid == 0) {   // S = Q.K^T (three products), over S / P's columns: P.V of kb - 1 has completed
       const uint64_t dq = sw128_desc(base + OFF_QHI), dql = sw128_desc(base + OFF_QLO);
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
       if (kb + 2 < nkb) prefetch(kb + 2);
       fence_async_smem();
     }
-    ok = mbar_wait(barS, kb & 1, flags);
+    ok = mbar_wait(barS, (kb - kb0) & 1, flags);
     ok = __syncthreads_and(ok) != 0;   // also: block kb + 1 is in shared memory
     if (!ok) break;
     tc_fence_after();
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int t = kb * PT_K + 32 * half + j;
-        sc[j] = (t <= qpos && t < kend) ? __uint_as_float(sr[j]) * SCALE_LOG2 : -INFINITY;
+        sc[j] = (t <= qpos && t < kend && (W <= 0 || t > qpos - W)) ? __uint_as_float(sr[j]) * SCALE_LOG2 : -INFINITY;
         mb = fmaxf(mb, sc[j]);
       }
     }
@@ -274,13 +277,15 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
     tc_fence_before();
     __syncthreads();   // both halves' maxima are visible, and every S column has been read
     tc_fence_after();
-    const float m_new = fmaxf(m_run, fmaxf(mb, s_red[(half ^ 1) * PT_Q + r]));   // finite: key 0 is in block 0
-    const float alpha = exp2f(m_run - m_new);
+    const float m_new = fmaxf(m_run, fmaxf(mb, s_red[(half ^ 1) * PT_Q + r]));
+    // -inf only for a row whose window has not started yet: the reference 0 keeps its state 0
+    const float m_ref = m_new == -INFINITY ? 0.0f : m_new;
+    const float alpha = exp2f(m_run - m_ref);
     m_run = m_new;
     float lsum = 0.0f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      sc[j] = exp2f(sc[j] - m_new);   // masked: exp2(-inf) = 0
+      sc[j] = exp2f(sc[j] - m_ref);   // masked: exp2(-inf) = 0
       lsum += sc[j];
     }
     l_run = l_run * alpha + lsum;
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2) k_attn_prefill_tc(const AttnPre
       }
       tc_commit(barO);
     }
-    ok = mbar_wait(barO, kb & 1, flags);
+    ok = mbar_wait(barO, (kb - kb0) & 1, flags);
     ok = __syncthreads_and(ok) != 0;
     if (!ok) break;
     tc_fence_after();

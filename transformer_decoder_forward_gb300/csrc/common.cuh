@@ -323,6 +323,9 @@ struct Epilogue {
   int rope;             // 1: rotate q and k (Llama)
   float rope_theta;
   const float2* rope_tab;  // [HD/2] inverse frequency of pair d split as (hi, lo), hi with 11 significant bits
+  const void* qn_g;     // Q/K norm: gains [HD] (weight dtype) of the q and k heads' RMSNorm, or nullptr
+  const void* kn_g;
+  float qk_eps;
   // HEAD
   float* part_val;      // [n_tiles][M]
   int* part_idx;

@@ -8,7 +8,8 @@
 //   RESID   residual add after the output / down projection;
 //   GELU    GPT-2's GELU-tanh with the tanh argument clamped to +-15 ("batch_forge");
 //   SWIGLU  silu(gate) * up;
-//   QKV     bias, RoPE on q and k (Llama), kv_write of k and v into the paged cache (fp32 or bf16);
+//   QKV     bias, Q/K norm and RoPE on q and k (Llama), kv_write of k and v into the paged cache
+//           (fp32 or bf16);
 //   HEAD    tied-LM-head logits and a per-tile greedy argmax partial.
 //
 // Latency: the per-tile bias and the per-row KV slot are staged in shared memory
@@ -247,6 +248,25 @@ __device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0,
         for (int t = 0; t < 4; ++t) {
           v0[t] = tile[m * ldt + c + t] + s_bias[c + t];
           v1[t] = tile[m * ldt + c + HD / 2 + t] + s_bias[c + HD / 2 + t];
+        }
+        if (e.qn_g && (is_q || is_k)) {
+          // Q/K norm: RMSNorm of the head over its 64 values, before RoPE. The head's 8 units
+          // are 8 consecutive i, so 8 consecutive lanes of one warp (every caller's thread index
+          // is the hardware lane mod 32 and its thread count a multiple of 32), all of them here.
+          float ss = 0.0f;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) ss += v0[t] * v0[t] + v1[t] * v1[t];
+          const unsigned gmask = 0xFFu << (threadIdx.x & 24);
+          ss += __shfl_xor_sync(gmask, ss, 1);
+          ss += __shfl_xor_sync(gmask, ss, 2);
+          ss += __shfl_xor_sync(gmask, ss, 4);
+          const float r = 1.0f / sqrtf(ss / HD + e.qk_eps);
+          const void* gw = is_q ? e.qn_g : e.kn_g;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            v0[t] = v0[t] * r * bias_at<WT>(gw, d + t);
+            v1[t] = v1[t] * r * bias_at<WT>(gw, d + HD / 2 + t);
+          }
         }
         if (e.rope && (is_q || is_k)) {
 #pragma unroll

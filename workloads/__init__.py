@@ -10,7 +10,8 @@ Seeds (numpy ``default_rng``, PCG64):
   2  context lengths
   3  block-table permutation of the paged KV pool
   4  teacher-forced decode streams
-  5  optional perturbation of norm gains / biases (tests only)
+  5  optional perturbation of norm gains / biases (tests only); Q/K-norm gains and the
+     Llama variant's attention biases are drawn after the final norm's
 
 Weights are drawn as float32 N(0, 0.02) ("weights N(0,0.02) from seed, biases
 0"); norm gains are 1 and biases 0 unless ``perturb`` asks for non-trivial
@@ -53,6 +54,13 @@ class ModelShape:
     n_ctx: int
     norm_eps: float = 1e-5
     rope_theta: float = 1e5
+    # model-feature variants (Llama variant; the window applies to either)
+    sliding_window: int = 0          # W > 0: a query at position p sees keys p-W+1 .. p
+    sliding_window_pattern: int = 0  # 0: every layer windowed; P > 0: every P-th layer (l+1 = P, 2P, ..) global
+    qk_norm: bool = False            # RMSNorm (gain [head_dim] per layer) on each q and k head before RoPE
+    rope_scaling: Optional[tuple] = None   # Llama-3 frequency scaling: (factor, low_freq_factor,
+                                           # high_freq_factor, original_max_position)
+    attn_bias: bool = False          # biases on the q, k, v projections (Llama variant)
 
     @property
     def qkv_dim(self) -> int:
@@ -172,6 +180,8 @@ class Weights:
     b_down: List[Optional[np.ndarray]]
     lnf_w: np.ndarray
     lnf_b: Optional[np.ndarray]
+    q_norm_w: Optional[List[np.ndarray]] = None   # [head_dim] per layer when shape.qk_norm
+    k_norm_w: Optional[List[np.ndarray]] = None
 
     def as_f64(self, a: Optional[np.ndarray]) -> Optional[np.ndarray]:
         """Widen one stored tensor to float64 (bf16 patterns are decoded exactly)."""
@@ -211,8 +221,8 @@ def make_weights(shape: ModelShape, scale: float = 1.0, perturb: bool = False,
             g = g + prng.standard_normal(n, dtype=np.float32) * np.float32(0.1)
         return _store(g, shape.dtype)
 
-    def bias(n: int) -> Optional[np.ndarray]:
-        if not gpt2:
+    def bias(n: int, present: bool = None) -> Optional[np.ndarray]:
+        if not (gpt2 if present is None else present):
             return None
         b = np.zeros(n, np.float32)
         if perturb:
@@ -231,13 +241,16 @@ def make_weights(shape: ModelShape, scale: float = 1.0, perturb: bool = False,
     for _ in range(L):
         lists["ln1_w"].append(gain(d))
         lists["ln1_b"].append(bias(d))
-        lists["b_qkv"].append(bias(shape.qkv_dim))
+        lists["b_qkv"].append(bias(shape.qkv_dim, gpt2 or shape.attn_bias))
         lists["b_o"].append(bias(d))
         lists["ln2_w"].append(gain(d))
         lists["ln2_b"].append(bias(d))
         lists["b_up"].append(bias(shape.up_dim))
         lists["b_down"].append(bias(d))
-    return Weights(shape=shape, tok_emb=tok, pos_emb=pos, lnf_w=gain(d), lnf_b=bias(d), **lists)
+    lnf_w, lnf_b = gain(d), bias(d)
+    qn = [gain(shape.head_dim) for _ in range(L)] if shape.qk_norm else None
+    kn = [gain(shape.head_dim) for _ in range(L)] if shape.qk_norm else None
+    return Weights(shape=shape, tok_emb=tok, pos_emb=pos, lnf_w=lnf_w, lnf_b=lnf_b, q_norm_w=qn, k_norm_w=kn, **lists)
 
 
 # ----------------------------------------------------------------------------------------------
