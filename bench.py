@@ -94,7 +94,7 @@ def job_rate(ms_local: float, units_per_rank: float, world: int, device: str = "
 
 def weight_bytes(s: wl.ModelShape) -> int:
     """Projection weights read once per step, including the tied head (vocab x d)."""
-    return (s.n_layers * s.layer_params() + s.vocab * s.d_model) * s.elt_bytes
+    return int(round((s.n_layers * s.layer_params() + s.vocab * s.d_model) * s.elt_bytes))
 
 
 def gemv_bytes(s: wl.ModelShape, B: int) -> int:

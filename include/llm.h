@@ -61,7 +61,12 @@ typedef enum {
 } llm_status;
 
 enum { LLM_ARCH_GPT2 = 0, LLM_ARCH_LLAMA = 1 };
-enum { LLM_DTYPE_F32 = 0, LLM_DTYPE_BF16 = 1 };
+/* LLM_DTYPE_Q8: Q8_0 weights ("rvllm-metal", sections "What's basic about it" and "What's
+ * next": one byte a weight): each matrix row is cut into blocks of 32 values, value j of a
+ * block being d * q_j with q an int8 quant and d the block's fp16 scale. The library takes the
+ * quants [rows][K] int8 and the scales [rows][K / 32] fp16 as two arrays (the *_scale fields of
+ * llm_weights); vectors (gains, biases) and the learned positions of such a model are fp32. */
+enum { LLM_DTYPE_F32 = 0, LLM_DTYPE_BF16 = 1, LLM_DTYPE_Q8 = 2 };
 
 /* Bits of the device error word (llm_get_error_flags). */
 #define LLM_FLAG_BAD_TOKEN     0x01u  /* token id outside [0, vocab) */
@@ -72,7 +77,7 @@ enum { LLM_DTYPE_F32 = 0, LLM_DTYPE_BF16 = 1 };
 
 typedef struct {
   int arch;               /* LLM_ARCH_GPT2 or LLM_ARCH_LLAMA */
-  int dtype;              /* LLM_DTYPE_F32 or LLM_DTYPE_BF16: element type of the weights */
+  int dtype;              /* LLM_DTYPE_F32, LLM_DTYPE_BF16 or LLM_DTYPE_Q8: the weights' type */
   int n_layers;
   int d_model;
   int n_heads;            /* query heads */
@@ -111,8 +116,8 @@ typedef struct {
 } llm_config;
 
 /*
- * Weights: DEVICE pointers, element type given by config.dtype (fp32 or bf16),
- * row-major. Per-layer fields are HOST arrays of n_layers device pointers; the
+ * Weights: DEVICE pointers, element type given by config.dtype (fp32, bf16, or for Q8_0
+ * int8 matrices with fp16 block scales and fp32 vectors and positions), row-major. Per-layer fields are HOST arrays of n_layers device pointers; the
  * library copies those arrays. Absent tensors are NULL (all biases and ln*_b /
  * pos_emb for Llama). Shapes, d = d_model, H = n_heads, Hkv = n_kv_heads,
  * hd = head_dim, F = d_ff:
@@ -149,6 +154,12 @@ typedef struct {
   const void* lnf_b;
   const void* const* q_norm_w;
   const void* const* k_norm_w;
+  /* LLM_DTYPE_Q8 only (else NULL): fp16 block scales [rows][K / 32] of the int8 matrices */
+  const void* tok_emb_scale;
+  const void* const* w_qkv_scale;
+  const void* const* w_o_scale;
+  const void* const* w_up_scale;
+  const void* const* w_down_scale;
 } llm_weights;
 
 typedef struct llm_handle llm_handle;
@@ -303,6 +314,14 @@ llm_status llm_set_linear_variant(llm_handle* h, int variant);
  * UNSUPPORTED (variant 3 with fp32), CUDA. */
 llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const void* w, const void* bias, float* y,
                          int variant, void* cuda_stream);
+
+/* llm_op_linear for Q8_0 weights: y[m][n] = sum_k x[m][k] * (wscale[n][k / 32] * wq[n][k])
+ * (+ bias[n]). wq DEVICE int8 [N][K], wscale DEVICE fp16 [N][K / 32], bias DEVICE float [N] or
+ * NULL, x DEVICE float [M][K], y DEVICE float [M][N]. variant: 1 CUDA-core GEMV (the int8
+ * weight stream, any M), 2 CUDA-core tiled GEMM. Errors: INVALID_ARG (sizes, NULL, K % 32,
+ * variant), CUDA. */
+llm_status llm_op_linear_q8(int M, int N, int K, const float* x, const void* wq, const void* wscale,
+                            const float* bias, float* y, int variant, void* cuda_stream);
 
 /* Test and diagnostic entry point (no handle): one layer of batched decode attention
  * over a paged KV pool, the split-K kernel pair of llm_decode_step ("rvllm-metal",

@@ -16,7 +16,7 @@ import math
 import struct
 from typing import List
 
-from workloads import ARCH_GPT2, DTYPE_BF16, DTYPE_F32, Weights
+from workloads import ARCH_GPT2, DTYPE_BF16, DTYPE_F32, DTYPE_Q8, Weights
 
 
 def _f(a) -> List:
@@ -32,18 +32,33 @@ def _bf16(v: float) -> float:
     return struct.unpack("<f", struct.pack("<I", bits & 0xFFFFFFFF))[0]
 
 
+def _q8(q, d):
+    """Q8_0 rows: value j of a row is (scale of its 32-value block) * (int8 quant)."""
+    out = []
+    for r in range(len(q)):
+        row = []
+        for j in range(len(q[r])):
+            row.append(float(d[r][j // 32]) * float(q[r][j]))
+        out.append(row)
+    return out
+
+
 class BruteModel:
     def __init__(self, w: Weights, kv_dtype: int = DTYPE_F32):
         s = w.shape
         self.s = s
         self.kv_bf16 = kv_dtype == DTYPE_BF16
-        self.tok = _f(w.as_f64(w.tok_emb))
+        q8 = s.dtype == DTYPE_Q8
+        self.tok = _q8(w.tok_emb.tolist(), w.tok_emb_scale.tolist()) if q8 else _f(w.as_f64(w.tok_emb))
         self.pos = _f(w.as_f64(w.pos_emb))
         self.L = []
         for l in range(s.n_layers):
             self.L.append({k: _f(w.as_f64(getattr(w, k)[l])) for k in (
                 "ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b",
                 "w_up", "b_up", "w_down", "b_down")})
+            if q8:
+                for k in ("w_qkv", "w_o", "w_up", "w_down"):
+                    self.L[l][k] = _q8(getattr(w, k)[l].tolist(), getattr(w, k + "_scale")[l].tolist())
         self.lnf_w = _f(w.as_f64(w.lnf_w))
         self.lnf_b = _f(w.as_f64(w.lnf_b))
         if s.qk_norm:

@@ -39,7 +39,7 @@ from typing import Dict, List, Optional
 
 import numpy as np
 
-from workloads import ARCH_GPT2, ARCH_LLAMA, DTYPE_BF16, DTYPE_F32, ModelShape, Weights
+from workloads import ARCH_GPT2, ARCH_LLAMA, DTYPE_BF16, DTYPE_F32, DTYPE_Q8, ModelShape, Weights
 
 GELU_C = np.sqrt(2.0 / np.pi)
 GELU_CUBIC = 0.044715
@@ -212,6 +212,15 @@ def top2_margin(z: np.ndarray) -> float:
 # model
 # ----------------------------------------------------------------------------------------------
 
+def dequant_q8_0(q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Q8_0 weights ("rvllm-metal", sections "What's basic about it" and "What's next": one
+    byte a weight): each row is cut into blocks of 32; a block's value j is d_block * q_j, d an
+    fp16 scale and q an int8."""
+    q = np.asarray(q, dtype=np.float64)
+    d = np.asarray(d, dtype=np.float64)
+    return q * np.repeat(d, q.shape[1] // d.shape[1], axis=1)
+
+
 class OracleModel:
     """A model's parameters widened to float64, plus the per-layer forward.
 
@@ -225,13 +234,17 @@ class OracleModel:
         self.shape: ModelShape = w.shape
         self.kv_dtype = kv_dtype
         f = w.as_f64
-        self.tok_emb = f(w.tok_emb)
+        q8 = self.shape.dtype == DTYPE_Q8
+        self.tok_emb = dequant_q8_0(w.tok_emb, w.tok_emb_scale) if q8 else f(w.tok_emb)
         self.pos_emb = f(w.pos_emb)
         self.layers = []
         for l in range(self.shape.n_layers):
             self.layers.append({k: f(getattr(w, k)[l]) for k in (
                 "ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b",
                 "w_up", "b_up", "w_down", "b_down")})
+            if q8:
+                for k in ("w_qkv", "w_o", "w_up", "w_down"):
+                    self.layers[l][k] = dequant_q8_0(getattr(w, k)[l], getattr(w, k + "_scale")[l])
         self.lnf_w = f(w.lnf_w)
         self.lnf_b = f(w.lnf_b)
         if self.shape.qk_norm:

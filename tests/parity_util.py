@@ -21,7 +21,9 @@ import workloads as wl
 # the same ratio as 1e-3 to 2e-3. The multiple is 3: the GPU's fp32-weight tensor-core path
 # sums three tf32 products per term (about 2^-21 relative a product, against 2^-24 for an
 # fp32 FMA), and its error measured up to 1.94x the float32 floor on these rows.
-LOGIT_TOL = {wl.DTYPE_F32: 2e-3, wl.DTYPE_BF16: 3e-2}
+LOGIT_TOL = {wl.DTYPE_F32: 2e-3, wl.DTYPE_BF16: 3e-2,
+             # Q8_0 weights are exact (scale x quant); the arithmetic is fp32, as for fp32 weights
+             wl.DTYPE_Q8: 2e-3}
 MARGIN = 1e-3
 FLOOR_MULT = 3.0
 

@@ -547,3 +547,36 @@ def test_qk_norm_gives_unit_rms_heads():
     y = od.rms_norm(q, np.ones(64), 1e-5)
     ms = (q * q).mean(-1)
     np.testing.assert_allclose(np.sqrt((y * y).mean(-1)), np.sqrt(ms / (ms + 1e-5)), rtol=1e-12)
+
+
+# ------------------------------------------------------------------------------------------------
+# Q8_0 weights ("rvllm-metal", sections "What's basic about it" and "What's next")
+# ------------------------------------------------------------------------------------------------
+
+Q8_TINY = [wl.tiny_shape(wl.ARCH_GPT2, dtype=wl.DTYPE_Q8, d_model=64, d_ff=64, n_heads=2, head_dim=32),
+           wl.tiny_shape(wl.ARCH_LLAMA, dtype=wl.DTYPE_Q8, d_model=64, d_ff=32, n_heads=2, n_kv_heads=1,
+                         head_dim=32)]
+
+
+@pytest.mark.parametrize("shape", Q8_TINY, ids=["gpt2-q8", "llama-q8"])
+def test_q8_brute_force_equals_vectorised_oracle(shape):
+    w = wl.make_weights(shape, scale=20.0, perturb=True)
+    tokens = [3, 10, 0, 7]
+    brute = np.array(oracle.BruteModel(w).run(tokens))
+    m = oracle.OracleModel(w)
+    np.testing.assert_allclose(oracle.forward_full(m, tokens), brute, rtol=RTOL, atol=1e-12)
+
+
+def test_q8_dequant_is_block_scale_times_quant_and_close_to_the_draw():
+    from dataclasses import replace
+    sq = wl.tiny_shape(wl.ARCH_GPT2, dtype=wl.DTYPE_Q8, d_model=64, d_ff=64, n_heads=2, head_dim=32)
+    wq = wl.make_weights(sq)
+    wf = wl.make_weights(replace(sq, dtype=wl.DTYPE_F32))            # the same float32 draws
+    deq = od.dequant_q8_0(wq.w_up[0], wq.w_up_scale[0])
+    # value (r, j) = d[r, j // 32] * q[r, j], written out element by element
+    r, j = 5, 45
+    assert deq[r, j] == float(wq.w_up_scale[0][r, j // 32]) * float(wq.w_up[0][r, j])
+    # within half a quantization step of the float32 draw, and the block maximum maps to +-127
+    step = np.repeat(wq.w_up_scale[0].astype(np.float64), 32, axis=1)
+    assert np.all(np.abs(deq - wf.w_up[0]) <= 0.5 * step * (1 + 1e-3) + 1e-12)
+    assert np.abs(wq.w_up[0]).max() == 127

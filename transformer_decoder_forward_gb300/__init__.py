@@ -22,7 +22,8 @@ FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIM
 
 EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_sample", "llm_decode_step_host",
            "llm_get_error_flags", "llm_selftest_wait_timeout", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
-           "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode", "llm_op_attention_decode_noalloc",
+           "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_linear_q8", "llm_op_attention_decode",
+           "llm_op_attention_decode_noalloc",
            "llm_status_string", "llm_last_error"]
 
 
@@ -50,7 +51,9 @@ class LLMWeights(ctypes.Structure):
     _fields_ = [("tok_emb", ctypes.c_void_p), ("pos_emb", ctypes.c_void_p)] + \
                [(n, _PP) for n in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b",
                                    "w_up", "b_up", "w_down", "b_down")] + \
-               [("lnf_w", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p), ("q_norm_w", _PP), ("k_norm_w", _PP)]
+               [("lnf_w", ctypes.c_void_p), ("lnf_b", ctypes.c_void_p), ("q_norm_w", _PP), ("k_norm_w", _PP),
+                ("tok_emb_scale", ctypes.c_void_p)] + \
+               [(n, _PP) for n in ("w_qkv_scale", "w_o_scale", "w_up_scale", "w_down_scale")]
 
 
 class KernelStat(ctypes.Structure):
@@ -88,6 +91,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_set_graphs.argtypes = [vp, ctypes.c_int]
     lib.llm_set_linear_variant.argtypes = [vp, ctypes.c_int]
     lib.llm_op_linear.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int, vp]
+    lib.llm_op_linear_q8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_int, vp]
     lib.llm_op_attention_decode.argtypes = [ctypes.c_int] * 4 + [vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp]
     lib.llm_op_attention_decode_noalloc.argtypes = lib.llm_op_attention_decode.argtypes
     lib.llm_status_string.argtypes = [ctypes.c_int]
@@ -96,7 +100,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_last_error.restype = ctypes.c_char_p
     for name in ("llm_create", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_sample", "llm_decode_step_host", "llm_get_error_flags",
                  "llm_set_profiling", "llm_selftest_wait_timeout", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
-                 "llm_set_linear_variant", "llm_op_linear", "llm_op_attention_decode",
+                 "llm_set_linear_variant", "llm_op_linear", "llm_op_linear_q8", "llm_op_attention_decode",
                  "llm_op_attention_decode_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -130,6 +134,18 @@ def op_linear(x, w, bias, y, variant: int, stream=None) -> None:
                              ctypes.c_void_p(s.cuda_stream)))
 
 
+def op_linear_q8(x, wq, wscale, bias, y, variant: int, stream=None) -> None:
+    """y = x . (wscale * wq)^T (+ bias) with Q8_0 weights: wq int8 [N, K], wscale float16 [N, K / 32],
+    bias float32 [N] or None, x float32 [M, K], y float32 [M, N]; variant 1 (GEMV) or 2 (tiled GEMM)."""
+    import torch
+    lib = load()
+    N, K = wq.shape
+    M = x.shape[0]
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.llm_op_linear_q8(M, N, K, _ptr(x), _ptr(wq), _ptr(wscale), _ptr(bias), _ptr(y), int(variant),
+                                ctypes.c_void_p(s.cuda_stream)))
+
+
 def op_attention_decode(q, k_pool, v_pool, positions, block_tables, out, n_kv_heads: int, stream=None,
                         noalloc: bool = False) -> None:
     """Paged decode attention of one layer (tests / diagnostics). See llm_op_attention_decode.
@@ -161,8 +177,9 @@ def upload_weights(w, device: str = "cuda"):
     out = {"tok_emb": dev(w.tok_emb), "pos_emb": dev(w.pos_emb), "lnf_w": dev(w.lnf_w), "lnf_b": dev(w.lnf_b)}
     for k in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b", "w_up", "b_up", "w_down", "b_down"):
         out[k] = [dev(a) for a in getattr(w, k)]
-    for k in ("q_norm_w", "k_norm_w"):
+    for k in ("q_norm_w", "k_norm_w", "w_qkv_scale", "w_o_scale", "w_up_scale", "w_down_scale"):
         out[k] = None if getattr(w, k) is None else [dev(a) for a in getattr(w, k)]
+    out["tok_emb_scale"] = dev(w.tok_emb_scale)
     return out
 
 
@@ -205,9 +222,10 @@ class Decoder:
             return ctypes.cast(a, _PP)
 
         w = LLMWeights(tok_emb=_ptr(dev_w["tok_emb"]), pos_emb=_ptr(dev_w["pos_emb"]),
-                       lnf_w=_ptr(dev_w["lnf_w"]), lnf_b=_ptr(dev_w["lnf_b"]))
+                       lnf_w=_ptr(dev_w["lnf_w"]), lnf_b=_ptr(dev_w["lnf_b"]),
+                       tok_emb_scale=_ptr(dev_w.get("tok_emb_scale")))
         for k in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w", "ln2_b", "w_up", "b_up", "w_down",
-                  "b_down", "q_norm_w", "k_norm_w"):
+                  "b_down", "q_norm_w", "k_norm_w", "w_qkv_scale", "w_o_scale", "w_up_scale", "w_down_scale"):
             setattr(w, k, arr(k))
         handle = ctypes.c_void_p()
         torch.cuda.synchronize()

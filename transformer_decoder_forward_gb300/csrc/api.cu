@@ -46,6 +46,7 @@ llm_status fail(llm_status s, const std::string& msg) {
 struct LayerW {
   const void *ln1_w, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o, *ln2_w, *ln2_b, *w_up, *b_up, *w_down, *b_down;
   const void *q_norm_w, *k_norm_w;   // Q/K-norm gains, or nullptr
+  const void *s_qkv, *s_o, *s_up, *s_down;   // Q8_0 block scales, or nullptr
 };
 
 struct GraphEntry {
@@ -77,6 +78,7 @@ struct llm_handle {
   int adt = DT_F32;   // activations between kernels: DT_F32, or DT_SPLIT (bf16 pairs) for bf16 weights
   int act_mul = 1;    // row stride of an activation matrix in storage elements = act_mul * width
   const void *tok_emb = nullptr, *pos_emb = nullptr, *lnf_w = nullptr, *lnf_b = nullptr;
+  const void* tok_scale = nullptr;   // Q8_0 block scales of tok_emb
   std::vector<LayerW> layers;
   // KV pool (fp32, or bf16 when cfg.kv_dtype asks for it)
   int kvdt = DT_F32;
@@ -276,7 +278,8 @@ llm_status norm_linear(llm_handle* h, const char* tag, LinearParams p, const voi
   }
   NormParams np{h->h, g, gpt2 ? b : nullptr, h->xn, h->d_args, p.M, c.d_model, gpt2 ? 1 : 0, last_row ? 1 : 0,
                 c.norm_eps};
-  RUN("norm", launch_norm(np, h->wdt, h->adt, h->stream, h->pdl));
+  // Q8_0 models keep their gains and biases in fp32
+  RUN("norm", launch_norm(np, h->wdt == DT_Q8 ? DT_F32 : h->wdt, h->adt, h->stream, h->pdl));
   p.X = h->xn;
   p.ldx = h->act_mul * c.d_model;
   return linear(h, tag, p);
@@ -295,7 +298,8 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
   const bool gpt2 = c.arch == LLM_ARCH_GPT2;
   const int qkv_n = (H + 2 * Hkv) * HD;
 
-  EmbedParams ep{h->tok_emb, gpt2 ? h->pos_emb : nullptr, h->d_args, h->h, M, d, c.vocab, c.n_ctx, h->flags};
+  EmbedParams ep{h->tok_emb, h->tok_scale, gpt2 ? h->pos_emb : nullptr, h->d_args, h->h, M, d, c.vocab, c.n_ctx,
+                 h->flags};
   RUN("embed", launch_embed(ep, h->wdt, h->stream, h->pdl));
 
   for (int l = 0; l < c.n_layers; ++l) {
@@ -305,7 +309,7 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
     lp.wdt = h->wdt; lp.xdt = h->adt; lp.adt = h->adt;
     lp.M = M;
     // norm + QKV + RoPE + kv_write
-    lp.W = w.w_qkv; lp.N = qkv_n; lp.K = d; lp.swiglu = 0;
+    lp.W = w.w_qkv; lp.Wscale = w.s_qkv; lp.N = qkv_n; lp.K = d; lp.swiglu = 0;
     lp.epi = base_epi(h);
     lp.epi.kind = EPI_QKV;
     lp.epi.bias = w.b_qkv;
@@ -341,20 +345,20 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
     }
 
     // out projection + residual
-    lp.W = w.w_o; lp.X = h->att; lp.N = d; lp.K = H * HD; lp.ldx = h->act_mul * H * HD;
+    lp.W = w.w_o; lp.Wscale = w.s_o; lp.X = h->att; lp.N = d; lp.K = H * HD; lp.ldx = h->act_mul * H * HD;
     lp.epi = base_epi(h);
     lp.epi.kind = EPI_RESID; lp.epi.bias = w.b_o; lp.epi.resid = h->h; lp.epi.ld_resid = d;
     { llm_status s_ = linear(h, "o", lp); if (s_ != LLM_OK) return s_; }
 
     // norm + FFN up (+gate) with the activation
-    lp.W = w.w_up; lp.N = F; lp.K = d; lp.swiglu = gpt2 ? 0 : 1;
+    lp.W = w.w_up; lp.Wscale = w.s_up; lp.N = F; lp.K = d; lp.swiglu = gpt2 ? 0 : 1;
     lp.epi = base_epi(h);
     lp.epi.kind = gpt2 ? EPI_GELU : EPI_SWIGLU; lp.epi.bias = w.b_up; lp.epi.out = h->ff;
     lp.epi.ld_out = h->act_mul * F;
     { llm_status s_ = norm_linear(h, "up", lp, w.ln2_w, w.ln2_b, false); if (s_ != LLM_OK) return s_; }
 
     // FFN down + residual
-    lp.W = w.w_down; lp.X = h->ff; lp.N = d; lp.K = F; lp.ldx = h->act_mul * F; lp.swiglu = 0;
+    lp.W = w.w_down; lp.Wscale = w.s_down; lp.X = h->ff; lp.N = d; lp.K = F; lp.ldx = h->act_mul * F; lp.swiglu = 0;
     lp.epi = base_epi(h);
     lp.epi.kind = EPI_RESID; lp.epi.bias = w.b_down; lp.epi.resid = h->h; lp.epi.ld_resid = d;
     { llm_status s_ = linear(h, "down", lp); if (s_ != LLM_OK) return s_; }
@@ -364,7 +368,7 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
   LinearParams hp;
   memset(&hp, 0, sizeof(hp));
   hp.wdt = h->wdt; hp.xdt = h->adt; hp.adt = h->adt;
-  hp.W = h->tok_emb; hp.M = B; hp.N = c.vocab; hp.K = d;
+  hp.W = h->tok_emb; hp.Wscale = h->tok_scale; hp.M = B; hp.N = c.vocab; hp.K = d;
   hp.epi = base_epi(h);
   hp.epi.kind = EPI_HEAD; hp.epi.part_val = h->head_val; hp.epi.part_idx = h->head_idx; hp.epi.vocab = c.vocab;
   { llm_status s_ = norm_linear(h, "head", hp, h->lnf_w, h->lnf_b, prefill); if (s_ != LLM_OK) return s_; }
@@ -505,7 +509,13 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   if (!cfgp || !wp) return fail(LLM_ERR_INVALID_ARG, "config or weights is NULL");
   const llm_config c = *cfgp;
   if (c.arch != LLM_ARCH_GPT2 && c.arch != LLM_ARCH_LLAMA) return fail(LLM_ERR_INVALID_ARG, "bad arch");
-  if (c.dtype != LLM_DTYPE_F32 && c.dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_INVALID_ARG, "bad dtype");
+  if (c.dtype != LLM_DTYPE_F32 && c.dtype != LLM_DTYPE_BF16 && c.dtype != LLM_DTYPE_Q8)
+    return fail(LLM_ERR_INVALID_ARG, "bad dtype");
+  const bool q8 = c.dtype == LLM_DTYPE_Q8;
+  if (q8 && (c.d_model % 32 != 0 || c.d_ff % 32 != 0))
+    return fail(LLM_ERR_UNSUPPORTED, "Q8_0 weights need d_model and d_ff multiples of 32");
+  if (q8 && (!wp->tok_emb_scale || !wp->w_qkv_scale || !wp->w_o_scale || !wp->w_up_scale || !wp->w_down_scale))
+    return fail(LLM_ERR_INVALID_ARG, "Q8_0 weights need every block-scale array");
   if (c.n_layers <= 0 || c.d_model <= 0 || c.n_heads <= 0 || c.n_kv_heads <= 0 || c.d_ff <= 0 || c.vocab <= 0 ||
       c.n_ctx <= 0 || c.max_batch <= 0 || c.max_blocks_per_seq <= 0 || c.max_prefill_tokens <= 0)
     return fail(LLM_ERR_INVALID_ARG, "sizes must be positive");
@@ -550,8 +560,9 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   h->stream = static_cast<cudaStream_t>(cuda_stream);
   // Only the weights take the model's dtype. Activations keep fp32 accuracy (bf16-weight
   // models store them as bf16 pairs for the tensor cores) and the KV cache is fp32.
-  h->wdt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : DT_BF16;
-  h->adt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : DT_SPLIT;
+  h->wdt = c.dtype == LLM_DTYPE_F32 ? DT_F32 : c.dtype == LLM_DTYPE_Q8 ? DT_Q8 : DT_BF16;
+  h->adt = c.dtype == LLM_DTYPE_BF16 ? DT_SPLIT : DT_F32;
+  h->tok_scale = q8 ? wp->tok_emb_scale : nullptr;
   h->act_mul = h->adt == DT_SPLIT ? 2 : 1;
   h->kvdt = c.kv_dtype == LLM_DTYPE_BF16 ? DT_BF16 : DT_F32;
   h->kv_elt = h->kvdt == DT_BF16 ? 2 : 4;
@@ -568,6 +579,14 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
     w.ln2_w = wp->ln2_w[l]; w.ln2_b = wp->ln2_b ? wp->ln2_b[l] : nullptr;
     w.w_up = wp->w_up[l]; w.b_up = wp->b_up ? wp->b_up[l] : nullptr;
     w.w_down = wp->w_down[l]; w.b_down = wp->b_down ? wp->b_down[l] : nullptr;
+    w.s_qkv = q8 ? wp->w_qkv_scale[l] : nullptr;
+    w.s_o = q8 ? wp->w_o_scale[l] : nullptr;
+    w.s_up = q8 ? wp->w_up_scale[l] : nullptr;
+    w.s_down = q8 ? wp->w_down_scale[l] : nullptr;
+    if (q8 && (!w.s_qkv || !w.s_o || !w.s_up || !w.s_down)) {
+      delete h;
+      return fail(LLM_ERR_INVALID_ARG, "NULL Q8_0 scale array in layer " + std::to_string(l));
+    }
     w.q_norm_w = c.qk_norm ? wp->q_norm_w[l] : nullptr;
     w.k_norm_w = c.qk_norm ? wp->k_norm_w[l] : nullptr;
     // the Llama variant has no biases but the optional attention (q, k, v) biases
@@ -887,6 +906,29 @@ llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const vo
                   : variant == LIN_TC   ? launch_gemm_tc(p, nsm, s, false)
                                         : launch_gemm_tc_swap(p, nsm, s, false);
   if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("llm_op_linear: ") + cudaGetErrorString(e));
+  return LLM_OK;
+}
+
+llm_status llm_op_linear_q8(int M, int N, int K, const float* x, const void* wq, const void* wscale,
+                            const float* bias, float* y, int variant, void* cuda_stream) {
+  if (M <= 0 || N <= 0 || K <= 0) return fail(LLM_ERR_INVALID_ARG, "sizes must be positive");
+  if (!x || !wq || !wscale || !y) return fail(LLM_ERR_INVALID_ARG, "NULL x, wq, wscale or y");
+  if (K % 32 != 0) return fail(LLM_ERR_INVALID_ARG, "Q8_0 needs K % 32 == 0");
+  if (variant != LIN_GEMV && variant != LIN_SIMT) return fail(LLM_ERR_INVALID_ARG, "variant must be 1 or 2");
+  int dev = 0, nsm = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+  LinearParams p;
+  memset(&p, 0, sizeof(p));
+  p.W = wq; p.Wscale = wscale; p.X = x; p.M = M; p.N = N; p.K = K; p.ldx = K;
+  p.wdt = DT_Q8; p.xdt = p.adt = DT_F32;
+  p.epi.kind = EPI_STORE_F32;
+  p.epi.bias = bias;
+  p.epi.out = y;
+  p.epi.ld_out = N;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = variant == LIN_GEMV ? launch_gemv(p, nsm, s, false) : launch_gemm_simt(p, s, false);
+  if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("llm_op_linear_q8: ") + cudaGetErrorString(e));
   return LLM_OK;
 }
 

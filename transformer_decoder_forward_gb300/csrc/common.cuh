@@ -7,8 +7,9 @@
 
 namespace llm {
 
-// DT_SPLIT: activation storage of bf16-weight models (see Split below).
-enum : int { DT_F32 = 0, DT_BF16 = 1, DT_SPLIT = 2 };
+// DT_SPLIT: activation storage of bf16-weight models (see Split below). DT_Q8: Q8_0 weights
+// (int8 quants, one fp16 scale per 32-weight block; see Q8 below).
+enum : int { DT_F32 = 0, DT_BF16 = 1, DT_SPLIT = 2, DT_Q8 = 3 };
 enum : int { ARCH_GPT2 = 0, ARCH_LLAMA = 1 };
 constexpr int HD = 64;          // head_dim (the only supported value)
 constexpr int KVB = 16;         // tokens per KV block
@@ -46,6 +47,21 @@ template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __f
 struct Split {};
 template <typename WT> struct ActOf { using type = float; };
 template <> struct ActOf<bf16> { using type = Split; };
+
+// Q8_0 weights ("rvllm-metal", sections "What's basic about it" and "What's next": one byte a
+// weight): a matrix row is cut into blocks of 32 values, value j of a block is d * q_j with q an
+// int8 quant and d the block's fp16 scale. The library keeps them as two planes: the quants
+// [rows][K] int8 (16-byte vector loads) and the scales [rows][K / 32] fp16. Q8 is the tag type
+// of such a matrix; its models keep vectors (gains, biases, learned positions) and activations
+// in fp32.
+struct Q8 {};
+constexpr int Q8_BLOCK = 32;
+template <> struct ActOf<Q8> { using type = float; };
+// element type a matrix of weight type WT is stored in, and that of its model's vectors
+template <typename WT> struct Elem { using type = WT; };
+template <> struct Elem<Q8> { using type = int8_t; };
+template <typename WT> struct VecT { using type = WT; };
+template <> struct VecT<Q8> { using type = float; };
 
 // Element n of row `row` of an activation matrix whose rows are `ld` storage elements apart
 // (fp32: ld >= n_cols; Split: ld = 2 * n_cols, the lo half starting at ld / 2).
@@ -109,6 +125,16 @@ template <> struct Vec16<float> {
   __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
     f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
     f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+};
+template <> struct Vec16<Q8> {
+  static constexpr int N = 16;
+  __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) f[4 * i + b] = (float)(int8_t)((w[i] >> (8 * b)) & 0xffu);
   }
 };
 template <> struct Vec16<bf16> {

@@ -23,9 +23,11 @@ namespace llm {
 constexpr int EPI_MAX_ROWS = 256;   // rows of one epilogue call (every projection tile fits)
 constexpr int EPI_MAX_COLS = 128;   // tile columns of one epilogue call (two 64-column sub-tiles)
 
+// Element n of a bias / gain vector of a model with weight type WT (fp32 for Q8_0 models).
 template <typename WT>
 __device__ __forceinline__ float bias_at(const void* b, int n) {
-  return b ? to_f32(reinterpret_cast<const WT*>(b)[n]) : 0.0f;
+  using VT = typename VecT<WT>::type;
+  return b ? to_f32(reinterpret_cast<const VT*>(b)[n]) : 0.0f;
 }
 
 // RoPE angle pos * inv_freq[d] reduced to about [-pi, pi] in fp32 without losing the

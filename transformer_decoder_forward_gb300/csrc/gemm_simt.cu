@@ -4,8 +4,13 @@
 // of x and W staged in threadgroup memory ("rvllm-metal", section "The matmul
 // pain story"). Here a 128 x 64 tile (64 = one head, so the shared epilogues
 // see whole heads), K in steps of 16, 256 threads each holding an 8 x 4 block.
-// This is the fp32 path and the reference path for bf16 weights (whose activations
-// arrive as bf16 pairs); bf16 prefill uses the tcgen05 kernel.
+// This is the fp32 path, the Q8_0 path (quants dequantised as they are staged) and the
+// reference path for bf16 weights (whose activations arrive as bf16 pairs); bf16 prefill uses
+// the tcgen05 kernel.
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "epilogue.cuh"
 #include "linear.cuh"
 
@@ -20,13 +25,15 @@ constexpr int AS_LD = BM + 4, BS_LD = BN + 4, OT_LD = BN + 1;
 template <typename WT>
 __global__ void __launch_bounds__(SIMT_THREADS) k_gemm_simt(const LinearParams p) {
   using AT = typename ActOf<WT>::type;   // activation storage: fp32 or a bf16 pair
+  using ST = typename Elem<WT>::type;     // stored weight element (int8 quants for Q8_0)
+  constexpr bool IS_Q8 = std::is_same<WT, Q8>::value;
   __shared__ __align__(16) float smem[BM * OT_LD];   // reused: As/Bs during the loop, output tile after
   float* As = smem;                  // [BK][AS_LD]  (k-major, m contiguous)
   float* Bs = smem + BK * AS_LD;     // [BK][BS_LD]
   const int tid = threadIdx.x;
   const int tile = blockIdx.x, m0 = blockIdx.y * BM;
   const int F = p.N;
-  const WT* W = reinterpret_cast<const WT*>(p.W);
+  const ST* W = reinterpret_cast<const ST*>(p.W);
   pdl_wait();
 
   // loader coordinates
@@ -42,7 +49,9 @@ __global__ void __launch_bounds__(SIMT_THREADS) k_gemm_simt(const LinearParams p
     b_valid = b_wrow < p.N;
   }
   const bool a_valid = m0 + a_row < p.M;
-  const WT* wb = W + (size_t)b_wrow * p.K;
+  const ST* wb = W + (size_t)b_wrow * p.K;
+  // Q8_0: this row's block scales (the value of quant k is scale[k / 32] * q[k])
+  const __half* sb = IS_Q8 ? reinterpret_cast<const __half*>(p.Wscale) + (size_t)b_wrow * (p.K / Q8_BLOCK) : nullptr;
 
   const int ty = tid >> 4, tx = tid & 15;   // rows ty*8.., cols tx*4..
   float acc[8][4];
@@ -60,7 +69,12 @@ __global__ void __launch_bounds__(SIMT_THREADS) k_gemm_simt(const LinearParams p
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int k = k0 + b_k + j;
-      Bs[(b_k + j) * BS_LD + b_col] = (b_valid && k < p.K) ? to_f32(wb[k]) : 0.0f;
+      float wv = 0.0f;
+      if (b_valid && k < p.K) {
+        if constexpr (IS_Q8) wv = (float)wb[k] * __half2float(sb[k / Q8_BLOCK]);
+        else wv = to_f32(wb[k]);
+      }
+      Bs[(b_k + j) * BS_LD + b_col] = wv;
     }
     __syncthreads();
 #pragma unroll
@@ -109,6 +123,10 @@ cudaError_t launch_gemm_simt(const LinearParams& p, cudaStream_t s, bool pdl) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
   if (p.wdt == DT_F32 && p.xdt == DT_F32 && p.adt == DT_F32) return launch_t<float>(p, s, pdl);
   if (p.wdt == DT_BF16 && p.xdt == DT_SPLIT && p.adt == DT_SPLIT) return launch_t<bf16>(p, s, pdl);
+  if (p.wdt == DT_Q8 && p.xdt == DT_F32 && p.adt == DT_F32) {
+    if (p.K % Q8_BLOCK != 0 || !p.Wscale) return cudaErrorInvalidValue;
+    return launch_t<Q8>(p, s, pdl);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -24,6 +24,7 @@
 // (programmatic dependent launch) a CTA already warms L2 with its weight slice
 // and loads its first weight vectors into registers.
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <type_traits>
@@ -65,7 +66,10 @@ __host__ __device__ constexpr size_t gemv_smem(int MT, int kcta) {
 template <typename WT, int MT>
 __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int kcta, int ks_total) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  using ST = typename Elem<WT>::type;   // stored weight element (int8 quants for Q8_0)
+  using VT = typename VecT<WT>::type;   // norm gains / biases
   constexpr bool SPLIT_X = std::is_same<WT, bf16>::value;   // bf16 weights: x is a bf16 pair
+  constexpr bool IS_Q8 = std::is_same<WT, Q8>::value;
   constexpr int VEC = Vec16<WT>::N;
   constexpr int STRIDE = 8 * VEC;
   // grid.x = row chunk (fastest, so the chunks sharing a weight slice run together), grid.y = K split,
@@ -82,8 +86,9 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 3, kl = lane & 7;
-  const WT* W = reinterpret_cast<const WT*>(p.W);
-  const WT* wp[2];
+  const ST* W = reinterpret_cast<const ST*>(p.W);
+  const ST* wp[2];
+  const __half* scl[2];   // Q8_0: the rows' block scales from k0
   bool rvalid[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -97,28 +102,35 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
       rvalid[r] = row < p.N;
     }
     wp[r] = W + (size_t)(rvalid[r] ? row : 0) * p.K + k0;
+    scl[r] = IS_Q8 ? reinterpret_cast<const __half*>(p.Wscale) + (size_t)(rvalid[r] ? row : 0) * (p.K / Q8_BLOCK) +
+                         k0 / Q8_BLOCK
+                   : nullptr;
   }
 
   // ---- before the dependency wait: weights only
   const bool vec_ok = (p.K % VEC) == 0;
   const int kvec_end = vec_ok ? (kcl / VEC) * VEC : 0;
-  if (threadIdx.x < TILE_N && kvec_end > 0 && ((p.K * sizeof(WT)) % 16) == 0) {
+  if (threadIdx.x < TILE_N && kvec_end > 0 && ((p.K * sizeof(ST)) % 16) == 0) {
     const int c = threadIdx.x;
     const int row = p.swiglu ? swiglu_row(tile * 32, c, F) : tile * TILE_N + c;
     const bool ok = p.swiglu ? (tile * 32 + (c & 31) < F) : row < p.N;
-    if (ok) bulk_prefetch_l2(W + (size_t)row * p.K + k0, (unsigned)(kvec_end * sizeof(WT)));
+    if (ok) bulk_prefetch_l2(W + (size_t)row * p.K + k0, (unsigned)(kvec_end * sizeof(ST)));
   }
   uint4 wa[U][2], wb[U][2];
-  auto load_w = [&](uint4 (&w)[U][2], int kbase) {
+  float da[U][2], db[U][2];   // Q8_0: the scale of each loaded 16-quant chunk's block
+  auto load_w = [&](uint4 (&w)[U][2], float (&dd)[U][2], int kbase) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int kk = kbase + u * STRIDE;
 #pragma unroll
-      for (int r = 0; r < 2; ++r)
-        w[u][r] = (rvalid[r] && kk < kvec_end) ? ldg_stream16(wp[r] + kk) : make_uint4(0, 0, 0, 0);
+      for (int r = 0; r < 2; ++r) {
+        const bool in = rvalid[r] && kk < kvec_end;
+        w[u][r] = in ? ldg_stream16(wp[r] + kk) : make_uint4(0, 0, 0, 0);
+        if constexpr (IS_Q8) dd[u][r] = in ? __half2float(scl[r][kk / Q8_BLOCK]) : 0.0f;
+      }
     }
   };
-  load_w(wa, kl * VEC);
+  load_w(wa, da, kl * VEC);
   pdl_trigger();
   pdl_wait();
 
@@ -127,8 +139,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
     // X = Norm(h): each warp computes its rows' statistics over the whole row, then writes the
     // CTA's K slice of the normalised row (h is fp32, K % 4 == 0, K <= 2048)
     const float* hx = reinterpret_cast<const float*>(p.X);
-    const WT* gw = reinterpret_cast<const WT*>(p.norm_g);
-    const WT* bw = reinterpret_cast<const WT*>(p.norm_b);
+    const VT* gw = reinterpret_cast<const VT*>(p.norm_g);
+    const VT* bw = reinterpret_cast<const VT*>(p.norm_b);
     for (int m = warp; m < mcount; m += GEMV_THREADS / 32) {
       float4 v[ROW_NV];
       float mean, rstd;
@@ -192,7 +204,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[r][m] = 0.0f;
 
-  auto fma_vec = [&](const uint4& w0, const uint4& w1, int k) {
+  auto fma_vec = [&](const uint4& w0, const uint4& w1, float d0, float d1, int k) {
     float f0[VEC], f1[VEC];
     Vec16<WT>::unpack(w0, f0);
     Vec16<WT>::unpack(w1, f1);
@@ -201,36 +213,52 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
       if (m < mcount) {
         float xv[VEC];
         lds_x<VEC>(xs + (size_t)m * ldxs + k, xv);
+        if constexpr (IS_Q8) {
+          // the 16 quants share their block's scale: sum q * x, then scale once
+          float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          acc[0][m] = fmaf(f0[j], xv[j], acc[0][m]);
-          acc[1][m] = fmaf(f1[j], xv[j], acc[1][m]);
+          for (int j = 0; j < VEC; ++j) {
+            s0 = fmaf(f0[j], xv[j], s0);
+            s1 = fmaf(f1[j], xv[j], s1);
+          }
+          acc[0][m] = fmaf(d0, s0, acc[0][m]);
+          acc[1][m] = fmaf(d1, s1, acc[1][m]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            acc[0][m] = fmaf(f0[j], xv[j], acc[0][m]);
+            acc[1][m] = fmaf(f1[j], xv[j], acc[1][m]);
+          }
         }
       }
     }
   };
 
   for (int k = kl * VEC; k < kvec_end; k += U * STRIDE) {
-    load_w(wb, k + U * STRIDE);
+    load_w(wb, db, k + U * STRIDE);
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (k + u * STRIDE < kvec_end) fma_vec(wa[u][0], wa[u][1], k + u * STRIDE);
+      if (k + u * STRIDE < kvec_end) fma_vec(wa[u][0], wa[u][1], da[u][0], da[u][1], k + u * STRIDE);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       wa[u][0] = wb[u][0];
       wa[u][1] = wb[u][1];
+      da[u][0] = db[u][0];
+      da[u][1] = db[u][1];
     }
   }
-  // scalar tail (K not a multiple of the vector width)
-  for (int kk = kvec_end + kl; kk < kcl; kk += 8) {
-    const float a0 = rvalid[0] ? to_f32(wp[0][kk]) : 0.0f;
-    const float a1 = rvalid[1] ? to_f32(wp[1][kk]) : 0.0f;
+  // scalar tail (K not a multiple of the vector width; never for Q8_0, whose K is a multiple of 32)
+  if constexpr (!IS_Q8) {
+    for (int kk = kvec_end + kl; kk < kcl; kk += 8) {
+      const float a0 = rvalid[0] ? to_f32(wp[0][kk]) : 0.0f;
+      const float a1 = rvalid[1] ? to_f32(wp[1][kk]) : 0.0f;
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < mcount) {
-        const float x = xs[(size_t)m * ldxs + kk];
-        acc[0][m] = fmaf(a0, x, acc[0][m]);
-        acc[1][m] = fmaf(a1, x, acc[1][m]);
+      for (int m = 0; m < MT; ++m) {
+        if (m < mcount) {
+          const float x = xs[(size_t)m * ldxs + kk];
+          acc[0][m] = fmaf(a0, x, acc[0][m]);
+          acc[1][m] = fmaf(a1, x, acc[1][m]);
+        }
       }
     }
   }
@@ -343,12 +371,15 @@ bool gemv_norm_supported(const LinearParams& p) {
 
 cudaError_t launch_gemv(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return cudaSuccess;
+  if (p.wdt == DT_Q8 && (p.K % Q8_BLOCK != 0 || !p.Wscale)) return cudaErrorInvalidValue;
   if (p.xnorm) {
     if (!gemv_norm_supported(p) || p.xdt != DT_F32) return cudaErrorInvalidValue;
     if (p.wdt == DT_F32 && p.adt == DT_F32) return launch_m<float>(p, num_sms, s, pdl);
     if (p.wdt == DT_BF16 && p.adt == DT_SPLIT) return launch_m<bf16>(p, num_sms, s, pdl);
+    if (p.wdt == DT_Q8 && p.adt == DT_F32) return launch_m<Q8>(p, num_sms, s, pdl);
     return cudaErrorInvalidValue;
   }
+  if (p.wdt == DT_Q8 && p.xdt == DT_F32 && p.adt == DT_F32) return launch_m<Q8>(p, num_sms, s, pdl);
   if (p.wdt == DT_F32 && p.xdt == DT_F32 && p.adt == DT_F32) return launch_m<float>(p, num_sms, s, pdl);
   if (p.wdt == DT_BF16 && p.xdt == DT_SPLIT && p.adt == DT_SPLIT) return launch_m<bf16>(p, num_sms, s, pdl);
   return cudaErrorInvalidValue;

@@ -8,7 +8,8 @@ namespace llm {
 constexpr int TILE_N = 64;
 
 struct LinearParams {
-  const void* W;        // [rows][K] weight, dtype wdt
+  const void* W;        // [rows][K] weight, dtype wdt (DT_Q8: the int8 quants)
+  const void* Wscale;   // DT_Q8: [rows][K / 32] fp16 block scales; otherwise unused
   const void* X;        // [M][ldx] activations, dtype xdt
   int M, N, K, ldx;     // N: output columns of the epilogue (d_ff for SWIGLU)
   int wdt, xdt, adt;    // weight / input / activation-output dtypes

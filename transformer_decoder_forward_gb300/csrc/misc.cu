@@ -1,4 +1,6 @@
 // Embedding gather, row norms, greedy-argmax reduction and the step-argument node.
+#include <cuda_fp16.h>
+
 #include <type_traits>
 
 #include "misc.cuh"
@@ -13,6 +15,8 @@ constexpr int ROW_THREADS = 256;
 // "What got built" (embedding lookup) and "Picking the model" (learned positions).
 template <typename WT>
 __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
+  using ST = typename Elem<WT>::type;   // token-embedding element (int8 quants for Q8_0)
+  using VT = typename VecT<WT>::type;   // learned positions (fp32 for Q8_0 models)
   const int m = blockIdx.x;
   pdl_wait();
   pdl_trigger();
@@ -25,10 +29,17 @@ __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
   }
   bool pos_ok = pos >= 0 && pos < p.n_ctx;
   if (!pos_ok && threadIdx.x == 0) set_flag(p.flags, FLAG_BAD_POSITION);
-  const WT* te = reinterpret_cast<const WT*>(p.tok_emb) + (size_t)(tok < 0 ? 0 : tok) * p.d;
-  const WT* pe = p.pos_emb ? reinterpret_cast<const WT*>(p.pos_emb) + (size_t)(pos_ok ? pos : 0) * p.d : nullptr;
+  const ST* te = reinterpret_cast<const ST*>(p.tok_emb) + (size_t)(tok < 0 ? 0 : tok) * p.d;
+  const VT* pe = p.pos_emb ? reinterpret_cast<const VT*>(p.pos_emb) + (size_t)(pos_ok ? pos : 0) * p.d : nullptr;
+  const __half* ts = std::is_same<WT, Q8>::value
+                         ? reinterpret_cast<const __half*>(p.tok_scale) + (size_t)(tok < 0 ? 0 : tok) * (p.d / Q8_BLOCK)
+                         : nullptr;
   for (int i = threadIdx.x; i < p.d; i += ROW_THREADS) {
-    float v = tok < 0 ? 0.0f : to_f32(te[i]);
+    float v = 0.0f;
+    if (tok >= 0) {
+      if constexpr (std::is_same<WT, Q8>::value) v = (float)te[i] * __half2float(ts[i / Q8_BLOCK]);
+      else v = to_f32(te[i]);
+    }
     if (pe && pos_ok) v += to_f32(pe[i]);
     p.h[(size_t)m * p.d + i] = v;
   }
@@ -152,6 +163,7 @@ cudaLaunchConfig_t make_launch_cfg(dim3 grid, dim3 block, size_t smem, cudaStrea
 
 cudaError_t launch_embed(const EmbedParams& p, int wdt, cudaStream_t s, bool pdl) {
   if (p.M <= 0) return cudaSuccess;
+  if (wdt == DT_Q8) return (p.d % Q8_BLOCK == 0 && p.tok_scale) ? embed_t<Q8>(p, s, pdl) : cudaErrorInvalidValue;
   return wdt == DT_F32 ? embed_t<float>(p, s, pdl) : embed_t<bf16>(p, s, pdl);
 }
 

@@ -6,6 +6,7 @@ namespace llm {
 
 struct EmbedParams {
   const void* tok_emb;     // [vocab][d]
+  const void* tok_scale;   // Q8_0 token embedding: [vocab][d / 32] fp16 block scales, else nullptr
   const void* pos_emb;     // [n_ctx][d] or nullptr
   const StepArgs* args;    // tokens, positions
   float* h;                // [M][d]

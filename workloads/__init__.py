@@ -29,7 +29,9 @@ ARCH_GPT2 = 0
 ARCH_LLAMA = 1
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+DTYPE_Q8 = 2       # matrices as Q8_0: int8 quants, one fp16 scale per 32-weight block
 KV_BLOCK = 16
+Q8_BLOCK = 32
 
 SEED_WEIGHTS = 0
 SEED_PROMPTS = 1
@@ -72,21 +74,20 @@ class ModelShape:
         return 2 * self.d_ff if self.arch == ARCH_LLAMA else self.d_ff
 
     @property
-    def elt_bytes(self) -> int:
-        return 4 if self.dtype == DTYPE_F32 else 2
+    def elt_bytes(self) -> float:
+        """Bytes a matrix weight takes: 4 (fp32), 2 (bf16), 1 + 2/32 (Q8_0 quant plus its share of a scale)."""
+        return {DTYPE_F32: 4, DTYPE_BF16: 2, DTYPE_Q8: 1 + 2 / Q8_BLOCK}[self.dtype]
 
     def layer_params(self) -> int:
         d = self.d_model
         return self.qkv_dim * d + self.n_heads * self.head_dim * d + self.up_dim * d + self.d_ff * d
-
-    def kv_bytes_per_token(self) -> int:
-        return 2 * self.n_layers * self.n_kv_heads * self.head_dim * self.elt_bytes
 
 
 GPT2_124M_F32 = ModelShape("gpt2-124m", ARCH_GPT2, DTYPE_F32, 12, 768, 12, 12, 64, 3072, 50257, 1024)
 GPT2_124M_BF16 = replace(GPT2_124M_F32, name="gpt2-124m-bf16", dtype=DTYPE_BF16)
 SMOLLM2_360M = ModelShape("smollm2-360m", ARCH_LLAMA, DTYPE_BF16, 32, 960, 15, 5, 64, 2560, 49152, 8192)
 GPT2_XL_BF16 = ModelShape("gpt2-xl", ARCH_GPT2, DTYPE_BF16, 48, 1600, 25, 25, 64, 6400, 50257, 1024)
+GPT2_124M_Q8 = replace(GPT2_124M_F32, name="gpt2-124m-q8", dtype=DTYPE_Q8)
 
 
 @dataclass(frozen=True)
@@ -126,9 +127,11 @@ W_GPT2_BF16_PREFILL = Workload("gpt2-124m-bf16-prefill-16x1024", GPT2_124M_BF16,
                                prompt_len=1024, mode="prefill")
 W_GPT2XL_B256 = Workload("gpt2-xl-bf16-b256-ctx1024", GPT2_XL_BF16, batch=256, prompt_len=960,
                          decode_steps=64, mode="teacher")
+# the batch-1 greedy workload with Q8_0 weights (the int8 weight stream)
+W_GPT2_Q8_B1 = replace(W_GPT2_F32_B1, name="gpt2-124m-q8-b1-greedy", model=GPT2_124M_Q8)
 
 WORKLOADS = {w.name: w for w in (W_GPT2_F32_B1, W_GPT2_F32_B32, W_GPT2_F32_B32_X8, W_SMOLLM2_B64,
-                                 W_GPT2_BF16_PREFILL, W_GPT2XL_B256)}
+                                 W_GPT2_BF16_PREFILL, W_GPT2XL_B256, W_GPT2_Q8_B1)}
 
 
 # ----------------------------------------------------------------------------------------------
@@ -182,9 +185,16 @@ class Weights:
     lnf_b: Optional[np.ndarray]
     q_norm_w: Optional[List[np.ndarray]] = None   # [head_dim] per layer when shape.qk_norm
     k_norm_w: Optional[List[np.ndarray]] = None
+    # Q8_0 models: the fp16 block scales [rows, K / 32] of each int8 matrix
+    tok_emb_scale: Optional[np.ndarray] = None
+    w_qkv_scale: Optional[List[np.ndarray]] = None
+    w_o_scale: Optional[List[np.ndarray]] = None
+    w_up_scale: Optional[List[np.ndarray]] = None
+    w_down_scale: Optional[List[np.ndarray]] = None
 
     def as_f64(self, a: Optional[np.ndarray]) -> Optional[np.ndarray]:
-        """Widen one stored tensor to float64 (bf16 patterns are decoded exactly)."""
+        """Widen one stored tensor to float64 (bf16 patterns are decoded exactly; int8 quants are
+        returned as their integer values, without their scales)."""
         if a is None:
             return None
         if a.dtype == np.uint16:
@@ -194,6 +204,20 @@ class Weights:
 
 def _store(x: np.ndarray, dtype: int) -> np.ndarray:
     return f32_to_bf16_bits(x) if dtype == DTYPE_BF16 else np.ascontiguousarray(x, dtype=np.float32)
+
+
+def quantize_q8_0(x: np.ndarray):
+    """Input preparation of a Q8_0 model: each row is cut into 32-value blocks, each block gets
+    the fp16 scale d = max|x| / 127 and the int8 quants round(x / d). Returns (int8 [rows, K],
+    float16 [rows, K / 32]); the model is exactly d * q."""
+    rows, K = x.shape
+    assert K % Q8_BLOCK == 0
+    b = x.reshape(rows, K // Q8_BLOCK, Q8_BLOCK).astype(np.float32)
+    d = (np.abs(b).max(axis=2) / np.float32(127)).astype(np.float16)
+    df = d.astype(np.float32)[:, :, None]
+    q = np.where(df > 0, np.rint(b / np.where(df > 0, df, 1)), 0)
+    q = np.clip(q, -127, 127).astype(np.int8)
+    return np.ascontiguousarray(q.reshape(rows, K)), np.ascontiguousarray(d)
 
 
 def make_weights(shape: ModelShape, scale: float = 1.0, perturb: bool = False,
@@ -212,14 +236,25 @@ def make_weights(shape: ModelShape, scale: float = 1.0, perturb: bool = False,
     d, L = shape.d_model, shape.n_layers
     gpt2 = shape.arch == ARCH_GPT2
 
-    def mat(rows: int, cols: int) -> np.ndarray:
-        return _store(rng.standard_normal((rows, cols), dtype=np.float32) * s, shape.dtype)
+    q8 = shape.dtype == DTYPE_Q8
+    vdt = DTYPE_F32 if q8 else shape.dtype      # Q8_0 models keep vectors and positions in fp32
+    scales: Dict[str, list] = {k: [] for k in ("w_qkv_scale", "w_o_scale", "w_up_scale", "w_down_scale")}
+
+    def mat(rows: int, cols: int, name: str = None):
+        x = rng.standard_normal((rows, cols), dtype=np.float32) * s
+        if not q8:
+            return _store(x, shape.dtype)
+        q, dsc = quantize_q8_0(x)
+        if name:
+            scales[name].append(dsc)
+            return q
+        return q, dsc
 
     def gain(n: int) -> np.ndarray:
         g = np.ones(n, np.float32)
         if perturb:
             g = g + prng.standard_normal(n, dtype=np.float32) * np.float32(0.1)
-        return _store(g, shape.dtype)
+        return _store(g, vdt)
 
     def bias(n: int, present: bool = None) -> Optional[np.ndarray]:
         if not (gpt2 if present is None else present):
@@ -227,17 +262,20 @@ def make_weights(shape: ModelShape, scale: float = 1.0, perturb: bool = False,
         b = np.zeros(n, np.float32)
         if perturb:
             b = prng.standard_normal(n, dtype=np.float32) * np.float32(0.05)
-        return _store(b, shape.dtype)
+        return _store(b, vdt)
 
     tok = mat(shape.vocab, d)
-    pos = mat(shape.n_ctx, d) if gpt2 else None
+    tok_scale = None
+    if q8:
+        tok, tok_scale = tok
+    pos = (_store(rng.standard_normal((shape.n_ctx, d), dtype=np.float32) * s, vdt) if gpt2 else None)
     lists: Dict[str, list] = {k: [] for k in ("ln1_w", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_w",
                                               "ln2_b", "w_up", "b_up", "w_down", "b_down")}
     for _ in range(L):
-        lists["w_qkv"].append(mat(shape.qkv_dim, d))
-        lists["w_o"].append(mat(d, shape.n_heads * shape.head_dim))
-        lists["w_up"].append(mat(shape.up_dim, d))
-        lists["w_down"].append(mat(d, shape.d_ff))
+        lists["w_qkv"].append(mat(shape.qkv_dim, d, "w_qkv_scale"))
+        lists["w_o"].append(mat(d, shape.n_heads * shape.head_dim, "w_o_scale"))
+        lists["w_up"].append(mat(shape.up_dim, d, "w_up_scale"))
+        lists["w_down"].append(mat(d, shape.d_ff, "w_down_scale"))
     for _ in range(L):
         lists["ln1_w"].append(gain(d))
         lists["ln1_b"].append(bias(d))
@@ -250,7 +288,9 @@ def make_weights(shape: ModelShape, scale: float = 1.0, perturb: bool = False,
     lnf_w, lnf_b = gain(d), bias(d)
     qn = [gain(shape.head_dim) for _ in range(L)] if shape.qk_norm else None
     kn = [gain(shape.head_dim) for _ in range(L)] if shape.qk_norm else None
-    return Weights(shape=shape, tok_emb=tok, pos_emb=pos, lnf_w=lnf_w, lnf_b=lnf_b, q_norm_w=qn, k_norm_w=kn, **lists)
+    extra = dict(tok_emb_scale=tok_scale, **scales) if q8 else {}
+    return Weights(shape=shape, tok_emb=tok, pos_emb=pos, lnf_w=lnf_w, lnf_b=lnf_b, q_norm_w=qn, k_norm_w=kn, **lists,
+                   **extra)
 
 
 # ----------------------------------------------------------------------------------------------
