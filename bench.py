@@ -92,6 +92,16 @@ def job_rate(ms_local: float, units_per_rank: float, world: int, device: str = "
     return ms, units, units / (ms / 1000.0)
 
 
+WEIGHTS_LABEL = {wl.DTYPE_F32: "fp32 weights", wl.DTYPE_BF16: "bf16 weights",
+                 wl.DTYPE_Q8: "Q8_0 weights (int8 quants, fp16 block scales)"}
+
+
+def dtype_label(s: wl.ModelShape) -> str:
+    """The arithmetic type of the path: the weights' type for fp32 / bf16 models; Q8_0 weights are
+    dequantised into fp32 arithmetic."""
+    return {wl.DTYPE_F32: "f32", wl.DTYPE_BF16: "bf16", wl.DTYPE_Q8: "q8_0 weights, f32 arithmetic"}[s.dtype]
+
+
 def weight_bytes(s: wl.ModelShape) -> int:
     """Projection weights read once per step, including the tied head (vocab x d)."""
     return int(round((s.n_layers * s.layer_params() + s.vocab * s.d_model) * s.elt_bytes))
@@ -434,16 +444,16 @@ def decode_part(args, W, world: int, rank: int, local: int) -> dict:
     line = {"metric": METRIC, "metric_detail": f"decode tok/s at batch {B}", "value": value,
             "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
+            "dtype": dtype_label(s), "data": "synthetic",
             "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]),
                        "decode_positions": f"{int(run.lengths.min())}..{int(run.lengths.max()) + period - 1} cycled",
                        "context_timed": f"{ctx_lo}..{ctx_hi} keys",
                        "kv": ("contiguous" if W.contiguous_kv else "paged16, shuffled tables")
                        + (", bf16" if kv_elt == 2 else ", fp32"),
-                       "precision": ("fp32 weights" if s.dtype == wl.DTYPE_F32 else "bf16 weights")
+                       "precision": WEIGHTS_LABEL[s.dtype]
                        + (", bf16 KV cache" if kv_elt == 2 else ", fp32 KV cache")
                        + ", fp32 residual, fp32 accumulation"
-                       + ("" if s.dtype == wl.DTYPE_F32 else ", activations as bf16 (hi, lo) pairs"),
+                       + (", activations as bf16 (hi, lo) pairs" if s.dtype == wl.DTYPE_BF16 else ""),
                        "l2": "inputs larger than L2: %.0f MB weights + %.0f MB KV per step" % (
                            weight_bytes(s) / 1e6, attn_bytes(s, ctx_of(0), kv_elt) / 1e6),
                        "graph": "one CUDA graph per step"},
@@ -545,8 +555,9 @@ def prefill_part(args, W, world: int, rank: int, local: int, steps: int, warmup:
     line = {"metric": METRIC, "metric_detail": f"prefill tok/s, {B} x {int(run.lengths[0])} tokens",
             "value": value, "unit": "tok/s", "n_gpus": world, "steps": steps, "warmup": warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if s.dtype == wl.DTYPE_F32 else "bf16", "data": "synthetic",
-            "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]), "kv": "paged16, fp32",
+            "dtype": dtype_label(s), "data": "synthetic",
+            "config": {"workload": W.name, "batch": B, "prompt_len": int(run.lengths[0]),
+                       "kv": "paged16, " + ("bf16" if W.kv_dtype == wl.DTYPE_BF16 else "fp32"),
                        "l2": "inputs larger than L2: %.0f MB activations per step" % (tokens_total * s.d_model * 4 / 1e6)},
             "roofline": roof,
             "attention_roofline": attn_roof,
