@@ -118,6 +118,7 @@ struct llm_handle {
   // execution options
   bool use_graphs = true;
   bool pdl = true;   // programmatic dependent launch between the step's kernels
+  bool attn_tc2 = false;   // prefill attention: the warp-specialised kernel (256-row items)
   int lin_variant = LIN_AUTO;
   std::map<int, GraphEntry> graphs;
   // profiling
@@ -340,7 +341,8 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
       ap.n_heads = H; ap.out = h->att; ap.out_dtype = h->adt; ap.flags = h->flags; ap.window = layer_window(h, l);
       // bf16-weight models: tensor cores on bf16 (hi, lo) splits (about 16 bits of every
       // operand); fp32-weight models keep fp32 FMA so their attention stays at fp32 accuracy
-      if (h->wdt == DT_BF16) RUN("attn_prefill", launch_attn_prefill_tc(ap, h->kvdt, h->stream, h->pdl));
+      if (h->attn_tc2) RUN("attn_prefill", launch_attn_prefill_tc2(ap, h->kvdt, h->stream, h->pdl));
+      else if (h->wdt == DT_BF16) RUN("attn_prefill", launch_attn_prefill_tc(ap, h->kvdt, h->stream, h->pdl));
       else RUN("attn_prefill", launch_attn_prefill(ap, h->kvdt, h->stream, h->pdl));
     }
 
@@ -678,6 +680,10 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   if (!stream_capturable(h->stream)) h->use_graphs = false;
   if (const char* env = getenv("LLM_NO_GRAPH")) h->use_graphs = h->use_graphs && env[0] != '1';
   if (const char* env = getenv("LLM_PDL")) h->pdl = env[0] != '0';
+  // bf16-weight models without a sliding window take the warp-specialised prefill attention
+  // (LLM_PREFILL_ATTN=1 keeps the earlier kernel, for comparisons)
+  h->attn_tc2 = h->wdt == DT_BF16 && c.sliding_window == 0;
+  if (const char* env = getenv("LLM_PREFILL_ATTN")) h->attn_tc2 = h->attn_tc2 && env[0] != '1';
   *out = h;
   return LLM_OK;
 }
@@ -738,7 +744,8 @@ llm_status llm_step(llm_handle* h, const int32_t* tokens, const int32_t* lengths
       return fail(LLM_ERR_OUT_OF_RANGE, "sequence needs more blocks than max_blocks_per_seq");
   }
   begin_call(h);
-  const int item_rows = h->wdt == DT_BF16 ? 128 : 64;   // query rows per prefill-attention CTA
+  // query rows per prefill-attention CTA
+  const int item_rows = h->attn_tc2 ? 256 : h->wdt == DT_BF16 ? 128 : 64;
   size_t tok_off = 0;
   int s0 = 0;
   while (s0 < B) {
@@ -762,6 +769,10 @@ llm_status llm_step(llm_handle* h, const int32_t* tokens, const int32_t* lengths
       last_row[b - s0] = r - 1;
     }
     if ((int)items.size() > h->max_items) { end_call(h); return fail(LLM_ERR_OUT_OF_RANGE, "too many attention tiles"); }
+    // longest tiles (most keys) first, so the short ones fill the last wave
+    std::stable_sort(items.begin(), items.end(), [&](const int4& x, const int4& y) {
+      return std::min(x.w, x.y + item_rows) > std::min(y.w, y.y + item_rows);
+    });
     CUDA_TRY(cudaMemcpyAsync(h->d_row_pos, row_pos.data(), rows * sizeof(int), cudaMemcpyHostToDevice, h->stream));
     CUDA_TRY(cudaMemcpyAsync(h->d_row_seq, row_seq.data(), rows * sizeof(int), cudaMemcpyHostToDevice, h->stream));
     CUDA_TRY(cudaMemcpyAsync(h->d_last_row, last_row.data(), nb * sizeof(int), cudaMemcpyHostToDevice, h->stream));

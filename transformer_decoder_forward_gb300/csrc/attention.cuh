@@ -42,7 +42,10 @@ int attn_decode_split_for(int B, int n_kv_heads, int max_ctx, int num_sms);
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int kv_dtype, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_prefill(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl);
-// Tensor-core prefill attention: items of up to 128 query rows, fp32 KV pool.
+// Tensor-core prefill attention: items of up to 128 query rows (any sliding window).
 cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl);
+// Warp-specialised tensor-core prefill attention: items of up to 256 query rows (two 128-row
+// tiles), no sliding window.
+cudaError_t launch_attn_prefill_tc2(const AttnPrefillParams& p, int kv_dtype, cudaStream_t s, bool pdl);
 
 }  // namespace llm
