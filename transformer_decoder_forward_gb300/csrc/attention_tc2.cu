@@ -8,8 +8,9 @@
 //   loader (1 thread)     1-D bulk copies of the block's raw K and V rows (4 paged 16-token
 //                         blocks each) into a two-stage raw ring;
 //   converters (4 warps)  split each raw fp32 value into bf16 hi = bf16(v), lo = bf16(v - hi)
-//                         and write the 128-byte-swizzled K-major operands: K [keys][dims] and V
-//                         transposed [dims][keys] (a bf16 pool needs no lo half), two stages;
+//                         and write K and V alike as [keys][dims] in 128-byte swizzled rows: K is
+//                         S's K-major B operand, V P.V's MN-major B operand (a bf16 pool needs no
+//                         lo half), two stages;
 //   MMA (1 thread)        S_t = Q_t K^T as hi.hi + hi.lo + lo.hi into TMEM, and O_t += P_t V with
 //                         P_t read from TMEM, for t = 0, 1, in the order S_0(j) S_1(j)
 //                         PV_0(j) S_0(j+1) PV_1(j) S_1(j+1): while one tile's softmax runs the
@@ -45,7 +46,7 @@ constexpr int Q2_TILE = 128 * 128;        // bytes of a 128-row x 64-bf16 swizzl
 constexpr int Q2_HALF = 64 * 128;         // bytes of a 64-row x 64-bf16 swizzled tile
 constexpr int OFF_Q = 0;                  // [tile][hi, lo]
 constexpr int OFF_CV = OFF_Q + 4 * Q2_TILE;
-constexpr int CV_STAGE = 4 * Q2_HALF;     // [K hi][K lo][V^T hi][V^T lo]
+constexpr int CV_STAGE = 4 * Q2_HALF;     // [K hi][K lo][V hi][V lo], rows = keys
 constexpr int CV_KHI = 0, CV_KLO = Q2_HALF, CV_VHI = 2 * Q2_HALF, CV_VLO = 3 * Q2_HALF;
 constexpr int OFF_RAW = OFF_CV + 2 * CV_STAGE;
 constexpr int RAW_STAGE = 2 * Q2_K * HD * 4;   // K rows then V rows (fp32 size; bf16 uses half)
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
     // phase read 4 different chunk columns (two lanes, keys 2m and 2m + 1, share a chunk, which the
     // V transpose needs), instead of all reading the same one.
     const int ct = tid, kr = ct & 63, dh = ct >> 6;
-    const int odd = kr & 1, ck = kr >> 3, bk = (kr & 6) * 2, rot = kr >> 1;
+    const int rot = kr >> 1;
     constexpr int EPC = 16 / (int)sizeof(KT);          // values of a 16-byte chunk
     constexpr int NCH = 32 / EPC;                       // chunks of the thread's 32 dims
     for (int j = 0; j < nkb_all; ++j) {
@@ -220,49 +221,39 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
       const bool valid = t < kend_all && pb_of(t >> 4) >= 0;   // else zeros: no stale value reaches P.V
       const KT* kraw = reinterpret_cast<const KT*>(raw) + kr * HD + 32 * dh;
       const KT* vraw = reinterpret_cast<const KT*>(raw + KREG) + kr * HD + 32 * dh;
-      // K: each chunk split into its hi / lo halves at its place in the swizzled row
+      // All of a row's chunks are loaded first (independent shared-memory reads in flight
+      // together), then converted and stored. K and V are stored alike, [keys][dims] in 128-byte
+      // swizzled rows: K is S's K-major B operand, V P.V's MN-major B operand (N = dims
+      // contiguous, K = keys along the rows), so V needs no transpose.
+      uint4 xk[NCH];
 #pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int c = (i + rot) & (NCH - 1);
-        const uint4 x = valid ? *reinterpret_cast<const uint4*>(kraw + EPC * c) : make_uint4(0, 0, 0, 0);
-        if constexpr (KV16) {
-          *reinterpret_cast<uint4*>(cv + CV_KHI + sw_off2(kr, 4 * dh + c)) = x;
-        } else {
-          const float v4[4] = {__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)};
-          uint32_t h2[2], l2[2];
+      for (int part = 0; part < 2; ++part) {
+        const KT* src = part ? vraw : kraw;
+        const int hi_off = part ? CV_VHI : CV_KHI, lo_off = part ? CV_VLO : CV_KLO;
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(v4[2 * q], v4[2 * q + 1]);
-            const __nv_bfloat162 lb = __floats2bfloat162_rn(v4[2 * q] - __low2float(hb), v4[2 * q + 1] - __high2float(hb));
-            h2[q] = *reinterpret_cast<const uint32_t*>(&hb);
-            l2[q] = *reinterpret_cast<const uint32_t*>(&lb);
-          }
-          const uint32_t o = sw_off2(kr, 4 * dh + (c >> 1)) + (c & 1) * 8;   // 4 dims = 8 bytes of bf16
-          *reinterpret_cast<uint2*>(cv + CV_KHI + o) = make_uint2(h2[0], h2[1]);
-          *reinterpret_cast<uint2*>(cv + CV_KLO + o) = make_uint2(l2[0], l2[1]);
+        for (int i = 0; i < NCH; ++i) {
+          const int c = (i + rot) & (NCH - 1);
+          xk[i] = valid ? *reinterpret_cast<const uint4*>(src + EPC * c) : make_uint4(0, 0, 0, 0);
         }
-      }
-      // V transposed (dims x keys): keys 2m, 2m + 1 (lanes kr, kr ^ 1, same chunk) pair up so every
-      // store is one 32-bit word of two keys; of a chunk's EPC dims the even lane writes the first
-      // half, the odd lane the second
 #pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int c = (i + rot) & (NCH - 1);
-        const uint4 x = valid ? *reinterpret_cast<const uint4*>(vraw + EPC * c) : make_uint4(0, 0, 0, 0);
-        float v[EPC];
-        Vec16<KT>::unpack(x, v);
+        for (int i = 0; i < NCH; ++i) {
+          const int c = (i + rot) & (NCH - 1);
+          const uint4 x = xk[i];
+          if constexpr (KV16) {
+            *reinterpret_cast<uint4*>(cv + hi_off + sw_off2(kr, 4 * dh + c)) = x;
+          } else {
+            const float v4[4] = {__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)};
+            uint32_t h2[2], l2[2];
 #pragma unroll
-        for (int e = 0; e < EPC / 2; ++e) {
-          const float mine = odd ? v[EPC / 2 + e] : v[e];
-          const float other = __shfl_xor_sync(0xffffffffu, odd ? v[e] : v[EPC / 2 + e], 1);
-          const float ke = odd ? other : mine, ko = odd ? mine : other;
-          const __nv_bfloat162 hb = __floats2bfloat162_rn(ke, ko);   // exact for a bf16 pool
-          const int d = 32 * dh + EPC * c + (EPC / 2) * odd + e;
-          const uint32_t o2 = sw_off2(d, ck) + bk;
-          *reinterpret_cast<__nv_bfloat162*>(cv + CV_VHI + o2) = hb;
-          if constexpr (!KV16) {
-            const __nv_bfloat162 lb = __floats2bfloat162_rn(ke - __low2float(hb), ko - __high2float(hb));
-            *reinterpret_cast<__nv_bfloat162*>(cv + CV_VLO + o2) = lb;
+            for (int q = 0; q < 2; ++q) {
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(v4[2 * q], v4[2 * q + 1]);
+              const __nv_bfloat162 lb = __floats2bfloat162_rn(v4[2 * q] - __low2float(hb), v4[2 * q + 1] - __high2float(hb));
+              h2[q] = *reinterpret_cast<const uint32_t*>(&hb);
+              l2[q] = *reinterpret_cast<const uint32_t*>(&lb);
+            }
+            const uint32_t o = sw_off2(kr, 4 * dh + (c >> 1)) + (c & 1) * 8;   // 4 dims = 8 bytes of bf16
+            *reinterpret_cast<uint2*>(cv + hi_off + o) = make_uint2(h2[0], h2[1]);
+            *reinterpret_cast<uint2*>(cv + lo_off + o) = make_uint2(l2[0], l2[1]);
           }
         }
       }
@@ -277,7 +268,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(Q2_T, Q2_K);
-      constexpr uint32_t idO = idesc_bf16(Q2_T, HD);
+      constexpr uint32_t idO = idesc_bf16(Q2_T, HD) | (1u << 16);   // B (V) MN-major
       bool ok = wait_ab(&q_full[0], 0, flags, abort_word) && wait_ab(&q_full[1], 0, flags, abort_word);
       auto issue_S = [&](int t, int j) {
         unsigned char* cv = base + OFF_CV + (j & 1) * CV_STAGE;
@@ -300,7 +291,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
         const uint32_t dO = tmem + (uint32_t)(128 + 64 * t), sP = tmem + (uint32_t)(64 * t);
 #pragma unroll
         for (int ks = 0; ks < Q2_K / 16; ++ks) {
-          const uint64_t o2 = (uint64_t)(ks * 2);
+          const uint64_t o2 = (uint64_t)(ks * 128);   // 16 key rows of 128 bytes a step (MN-major B)
           const uint32_t ph = sP + (uint32_t)(ks * 8), pl = sP + (uint32_t)(32 + ks * 8);
           tc_mma_ts(dO, ph, dv + o2, idO, (j > 0 || ks > 0) ? 1u : 0u);
           if constexpr (!KV16) tc_mma_ts(dO, ph, dvl + o2, idO, 1u);
