@@ -107,6 +107,96 @@ __device__ void epi_stage(const Epilogue& e, int m0, int mrows, int n0, int ncol
   }
 }
 
+// QKV: bias, Q/K norm (QKN) and RoPE on q and k, kv_write of k and v. unit = (row, head of the
+// tile, g): dims 4g..4g+3 and 32+4g..32+4g+3 of the head, so a RoPE pair (d, d + 32) stays in
+// one thread; N is a multiple of 64 (whole heads).
+template <typename WT, bool QKN>
+__device__ __forceinline__ void epi_qkv(const Epilogue& e, const float* tile, int ldt, int m0, int mrows, int n0,
+                                        int ncols, int N, int tid, int nth, const float* s_bias, const int* s_pos,
+                                        const int* s_blk) {
+  const int H = e.n_heads, Hkv = e.kv.n_kv_heads;
+  const int units_row = (ncols / HD) * 8;
+  for (int i = tid; i < mrows * units_row; i += nth) {
+    const int m = i / units_row, u = i - m * units_row;
+    const int c = (u >> 3) * HD + (u & 7) * 4;   // tile column of dim d = 4g
+    const int n = n0 + c;
+    if (n >= N) continue;
+    const int hh = n / HD, d = n - hh * HD;
+    const int row = m0 + m;
+    const int pos = s_pos[m];
+    const bool is_q = hh < H, is_k = !is_q && hh < H + Hkv;
+    float v0[4], v1[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      v0[t] = tile[m * ldt + c + t] + s_bias[c + t];
+      v1[t] = tile[m * ldt + c + HD / 2 + t] + s_bias[c + HD / 2 + t];
+    }
+    if constexpr (QKN) {
+      if (is_q || is_k) {
+        // Q/K norm: RMSNorm of the head over its 64 values, before RoPE. The head's 8 units
+        // are 8 consecutive i, so 8 consecutive lanes of one warp (every caller's thread index
+        // is the hardware lane mod 32 and its thread count a multiple of 32), all of them here.
+        float ss = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) ss += v0[t] * v0[t] + v1[t] * v1[t];
+        const unsigned gmask = 0xFFu << (threadIdx.x & 24);
+        ss += __shfl_xor_sync(gmask, ss, 1);
+        ss += __shfl_xor_sync(gmask, ss, 2);
+        ss += __shfl_xor_sync(gmask, ss, 4);
+        const float r = 1.0f / sqrtf(ss / HD + e.qk_eps);
+        const void* gw = is_q ? e.qn_g : e.kn_g;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          v0[t] = v0[t] * r * bias_at<WT>(gw, d + t);
+          v1[t] = v1[t] * r * bias_at<WT>(gw, d + HD / 2 + t);
+        }
+      }
+    }
+    if (e.rope && (is_q || is_k)) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float sn, co;
+        rope_sincos(pos, e.rope_tab[d + t], &sn, &co);
+        const float r0 = v0[t] * co - v1[t] * sn;
+        const float r1 = v1[t] * co + v0[t] * sn;
+        v0[t] = r0;
+        v1[t] = r1;
+      }
+    }
+    float* dst;
+    if (is_q) {
+      dst = e.q_out + (size_t)row * H * HD + hh * HD;
+    } else {
+      const int pb = s_blk[m];
+      if (pb < 0) continue;
+      const int g = is_k ? hh - H : hh - H - Hkv;
+      const size_t off = kv_offset(e.kv, pb, g, pos & (KVB - 1));
+      if (e.kv.dtype == DT_BF16) {
+        // a bf16 cache stores k and v rounded to nearest (ties to even)
+        bf16* kd = reinterpret_cast<bf16*>(is_k ? e.kv.k : e.kv.v) + off;
+        const __nv_bfloat162 a0 = __floats2bfloat162_rn(v0[0], v0[1]), a1 = __floats2bfloat162_rn(v0[2], v0[3]);
+        const __nv_bfloat162 b0 = __floats2bfloat162_rn(v1[0], v1[1]), b1 = __floats2bfloat162_rn(v1[2], v1[3]);
+        *reinterpret_cast<uint2*>(kd + d) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a0), *reinterpret_cast<const uint32_t*>(&a1));
+        *reinterpret_cast<uint2*>(kd + d + HD / 2) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+        continue;
+      }
+      dst = reinterpret_cast<float*>(is_k ? e.kv.k : e.kv.v) + off;
+    }
+    *reinterpret_cast<float4*>(dst + d) = make_float4(v0[0], v0[1], v0[2], v0[3]);
+    *reinterpret_cast<float4*>(dst + d + HD / 2) = make_float4(v1[0], v1[1], v1[2], v1[3]);
+  }
+}
+
+// The QKV epilogue with Q/K norm, kept out of the projection kernels' inlined code.
+template <typename WT>
+__device__ __noinline__ void epi_qkv_norm(const Epilogue& e, const float* tile, int ldt, int m0, int mrows, int n0,
+                                          int ncols, int N, int tid, int nth, const float* s_bias, const int* s_pos,
+                                          const int* s_blk) {
+  epi_qkv<WT, true>(e, tile, ldt, m0, mrows, n0, ncols, N, tid, nth, s_bias, s_pos, s_blk);
+}
+
 // The tile's outputs, from the staged values; threads tid of nth.
 template <typename WT>
 __device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0, int mrows, int n0, int ncols, int N,
@@ -231,82 +321,14 @@ __device__ void epi_apply(const Epilogue& e, const float* tile, int ldt, int m0,
       }
       break;
     }
-    case EPI_QKV: {
-      // unit = (row, head of the tile, g): dims 4g..4g+3 and 32+4g..32+4g+3 of the head, so a
-      // RoPE pair (d, d + 32) stays in one thread; N is a multiple of 64 (whole heads)
-      const int H = e.n_heads, Hkv = e.kv.n_kv_heads;
-      const int units_row = (ncols / HD) * 8;
-      for (int i = tid; i < mrows * units_row; i += nth) {
-        const int m = i / units_row, u = i - m * units_row;
-        const int c = (u >> 3) * HD + (u & 7) * 4;   // tile column of dim d = 4g
-        const int n = n0 + c;
-        if (n >= N) continue;
-        const int hh = n / HD, d = n - hh * HD;
-        const int row = m0 + m;
-        const int pos = s_pos[m];
-        const bool is_q = hh < H, is_k = !is_q && hh < H + Hkv;
-        float v0[4], v1[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          v0[t] = tile[m * ldt + c + t] + s_bias[c + t];
-          v1[t] = tile[m * ldt + c + HD / 2 + t] + s_bias[c + HD / 2 + t];
-        }
-        if (e.qn_g && (is_q || is_k)) {
-          // Q/K norm: RMSNorm of the head over its 64 values, before RoPE. The head's 8 units
-          // are 8 consecutive i, so 8 consecutive lanes of one warp (every caller's thread index
-          // is the hardware lane mod 32 and its thread count a multiple of 32), all of them here.
-          float ss = 0.0f;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) ss += v0[t] * v0[t] + v1[t] * v1[t];
-          const unsigned gmask = 0xFFu << (threadIdx.x & 24);
-          ss += __shfl_xor_sync(gmask, ss, 1);
-          ss += __shfl_xor_sync(gmask, ss, 2);
-          ss += __shfl_xor_sync(gmask, ss, 4);
-          const float r = 1.0f / sqrtf(ss / HD + e.qk_eps);
-          const void* gw = is_q ? e.qn_g : e.kn_g;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            v0[t] = v0[t] * r * bias_at<WT>(gw, d + t);
-            v1[t] = v1[t] * r * bias_at<WT>(gw, d + HD / 2 + t);
-          }
-        }
-        if (e.rope && (is_q || is_k)) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            float sn, co;
-            rope_sincos(pos, e.rope_tab[d + t], &sn, &co);
-            const float r0 = v0[t] * co - v1[t] * sn;
-            const float r1 = v1[t] * co + v0[t] * sn;
-            v0[t] = r0;
-            v1[t] = r1;
-          }
-        }
-        float* dst;
-        if (is_q) {
-          dst = e.q_out + (size_t)row * H * HD + hh * HD;
-        } else {
-          const int pb = s_blk[m];
-          if (pb < 0) continue;
-          const int g = is_k ? hh - H : hh - H - Hkv;
-          const size_t off = kv_offset(e.kv, pb, g, pos & (KVB - 1));
-          if (e.kv.dtype == DT_BF16) {
-            // a bf16 cache stores k and v rounded to nearest (ties to even)
-            bf16* kd = reinterpret_cast<bf16*>(is_k ? e.kv.k : e.kv.v) + off;
-            const __nv_bfloat162 a0 = __floats2bfloat162_rn(v0[0], v0[1]), a1 = __floats2bfloat162_rn(v0[2], v0[3]);
-            const __nv_bfloat162 b0 = __floats2bfloat162_rn(v1[0], v1[1]), b1 = __floats2bfloat162_rn(v1[2], v1[3]);
-            *reinterpret_cast<uint2*>(kd + d) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&a0), *reinterpret_cast<const uint32_t*>(&a1));
-            *reinterpret_cast<uint2*>(kd + d + HD / 2) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
-            continue;
-          }
-          dst = reinterpret_cast<float*>(is_k ? e.kv.k : e.kv.v) + off;
-        }
-        *reinterpret_cast<float4*>(dst + d) = make_float4(v0[0], v0[1], v0[2], v0[3]);
-        *reinterpret_cast<float4*>(dst + d + HD / 2) = make_float4(v1[0], v1[1], v1[2], v1[3]);
-      }
+    case EPI_QKV:
+      // The Q/K-norm instance is a separate, non-inlined function: compiled into the loop, its
+      // shuffles made every projection of the models without it about 0.4 us slower a launch.
+      if (e.qn_g)
+        epi_qkv_norm<WT>(e, tile, ldt, m0, mrows, n0, ncols, N, tid, nth, s_bias, s_pos, s_blk);
+      else
+        epi_qkv<WT, false>(e, tile, ldt, m0, mrows, n0, ncols, N, tid, nth, s_bias, s_pos, s_blk);
       break;
-    }
     case EPI_HEAD: {
       const StepArgs* a = e.args;
       float* logits = a->logits;
