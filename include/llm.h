@@ -292,12 +292,37 @@ llm_status llm_last_launch_count(llm_handle* h, int* n);
  * graphs; 0: every launch is issued eagerly. Graphs need a non-default stream. */
 llm_status llm_set_graphs(llm_handle* h, int enable);
 
+/* One-kernel decode step ("rvllm-metal", sections "What's basic about it": a step is
+ * about 900 dispatches and the GPU waits between kernels, and "What's next": fuse them).
+ * enable = 1: a decode step of B <= 8 sequences runs as one cooperative persistent
+ * kernel (one CTA per SM, grid-wide barriers between the dependent phases, every phase's
+ * weights streamed ahead into shared memory) followed by the argmax or the sampling kernel;
+ * other batch sizes, prefill and mixed steps keep one kernel a phase. 0 (default): every
+ * decode step takes one kernel a phase, the faster path on GB300 as measured (GPT-2 124M
+ * fp32 at batch 1: 0.386 against 0.371 ms a step; at batch 8 about twice as slow). The
+ * environment variable LLM_PERSISTENT=1 sets the default to 1. *supported (may be NULL) receives 1
+ * when the model's shapes allow the persistent step on this device (rows of 16-byte
+ * vectors, Q8_0 rows a multiple of 256, at most 8 query heads per KV head, one CTA per SM
+ * resident), else 0, in which case enable has no effect. Drops nothing: the cached
+ * graphs are keyed by the path they hold. */
+llm_status llm_set_persistent(llm_handle* h, int enable, int* supported);
+
+/* Self-test of the persistent step's grid barrier: launches the persistent kernel with
+ * one CTA that never arrives, so the other CTAs' bounded barrier wait gives up after its
+ * limit (about one second), sets LLM_FLAG_WAIT_TIMEOUT and every CTA leaves (the weight
+ * streamer waits for its copies in flight first). Synchronises the stream; the next
+ * llm_get_error_flags returns the flag and the context stays usable. Computes nothing
+ * and writes no output. Errors: UNSUPPORTED when the persistent step does not apply to
+ * this model (see llm_set_persistent). */
+llm_status llm_selftest_grid_barrier(llm_handle* h);
+
 /* Projection kernel choice: 0 = by row count (default), 1 = CUDA-core weight-stream
  * GEMV, 2 = CUDA-core tiled GEMM, 3 = tcgen05 GEMM with the activation rows on the
  * MMA's M side (bf16 models; falls back to 2 where it does not apply), 4 = tcgen05
  * GEMM with the weight rows on the MMA's M side (at most 256 activation rows; bf16,
  * or fp32 as three tf32 products; falls back to 3 / 2). For tests that force every
- * kernel on every shape. Drops cached graphs. Errors: INVALID_ARG for another value. */
+ * kernel on every shape: a variant other than 0 also keeps decode steps off the persistent
+ * kernel (llm_set_persistent). Drops cached graphs. Errors: INVALID_ARG for another value. */
 llm_status llm_set_linear_variant(llm_handle* h, int variant);
 
 /* Test and diagnostic entry point (no handle): one projection with a chosen kernel,

@@ -22,7 +22,7 @@ FLAG_BAD_TOKEN, FLAG_BAD_POSITION, FLAG_BAD_BLOCK, FLAG_NAN_LOGIT, FLAG_WAIT_TIM
 
 EXPORTS = ["llm_create", "llm_destroy", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_sample", "llm_decode_step_host",
            "llm_get_error_flags", "llm_selftest_wait_timeout", "llm_set_profiling", "llm_get_kernel_stats", "llm_last_launch_count",
-           "llm_set_graphs", "llm_set_linear_variant", "llm_op_linear", "llm_op_linear_q8", "llm_op_attention_decode",
+           "llm_set_graphs", "llm_set_persistent", "llm_selftest_grid_barrier", "llm_set_linear_variant", "llm_op_linear", "llm_op_linear_q8", "llm_op_attention_decode",
            "llm_op_attention_decode_noalloc",
            "llm_status_string", "llm_last_error"]
 
@@ -89,6 +89,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                          ctypes.c_int]
     lib.llm_last_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.llm_set_graphs.argtypes = [vp, ctypes.c_int]
+    lib.llm_set_persistent.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    lib.llm_selftest_grid_barrier.argtypes = [vp]
     lib.llm_set_linear_variant.argtypes = [vp, ctypes.c_int]
     lib.llm_op_linear.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int, vp]
     lib.llm_op_linear_q8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_int, vp]
@@ -100,8 +102,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.llm_last_error.restype = ctypes.c_char_p
     for name in ("llm_create", "llm_prefill", "llm_step", "llm_decode_step", "llm_decode_step_sample", "llm_decode_step_host", "llm_get_error_flags",
                  "llm_set_profiling", "llm_selftest_wait_timeout", "llm_get_kernel_stats", "llm_last_launch_count", "llm_set_graphs",
-                 "llm_set_linear_variant", "llm_op_linear", "llm_op_linear_q8", "llm_op_attention_decode",
-                 "llm_op_attention_decode_noalloc"):
+                 "llm_set_persistent", "llm_selftest_grid_barrier", "llm_set_linear_variant", "llm_op_linear",
+                 "llm_op_linear_q8", "llm_op_attention_decode", "llm_op_attention_decode_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -283,6 +285,18 @@ class Decoder:
 
     def set_graphs(self, on: bool) -> None:
         _check(self.lib.llm_set_graphs(self.handle, int(on)))
+
+    def set_persistent(self, on: bool) -> bool:
+        """Decode steps of at most 8 sequences as one persistent kernel (default off: the
+        per-phase graph measured faster); returns whether the model's shapes allow it here."""
+        sup = ctypes.c_int(0)
+        _check(self.lib.llm_set_persistent(self.handle, int(on), ctypes.byref(sup)))
+        return bool(sup.value)
+
+    def selftest_grid_barrier(self) -> None:
+        """Run the persistent kernel with one CTA withheld: the grid barrier's bounded wait runs
+        out (about one second); the next error_flags() returns LLM_FLAG_WAIT_TIMEOUT."""
+        _check(self.lib.llm_selftest_grid_barrier(self.handle))
 
     def set_linear_variant(self, v: int) -> None:
         """0 auto, 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM, 4 tcgen05 weights-on-M GEMM."""

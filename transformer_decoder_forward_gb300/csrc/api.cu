@@ -24,6 +24,7 @@
 #include "attention.cuh"
 #include "linear.cuh"
 #include "misc.cuh"
+#include "persistent.cuh"
 
 using namespace llm;
 
@@ -121,6 +122,17 @@ struct llm_handle {
   bool attn_tc2 = false;   // prefill attention: the warp-specialised kernel (256-row items)
   int lin_variant = LIN_AUTO;
   std::map<int, GraphEntry> graphs;
+  // one-kernel decode step (decode batches of at most PK_MAX_M rows)
+  bool pk_supported = false;   // shapes, alignment and residency allow it
+  bool pk_multi = false;       // the instance for more than one row fits too
+  bool pk_enabled = false;     // opt-in: measured slower than the per-phase graph (see llm.h)
+  int pk_smem_max = 0;
+  int pk_max_ch = 0;
+  PKLayer* d_pk_layers = nullptr;
+  float *pk_qkv = nullptr, *pk_att = nullptr, *pk_ff = nullptr, *pk_po = nullptr, *pk_ml = nullptr;
+  float* pk_head_val = nullptr;
+  int* pk_head_idx = nullptr;
+  unsigned* pk_sync = nullptr;
   // profiling
   bool profiling = false;
   bool prof_capture = false;   // a profiled decode step is being captured
@@ -388,6 +400,144 @@ llm_status enqueue_forward(llm_handle* h, int M, int B, bool prefill, int n_item
   return LLM_OK;
 }
 
+// ---- the one-kernel decode step -----------------------------------------------------------
+
+// Ring stages and staged-input capacity of a persistent step of M rows; false when M rows'
+// input does not leave room for two stages.
+bool pk_plan(const llm_handle* h, int M, int* nslot, int* xs_floats) {
+  const llm_config& c = h->cfg;
+  const int kmax = std::max(c.d_model, std::max(c.n_heads * HD, c.d_ff));
+  const size_t xsb = (size_t)M * kmax * sizeof(float);
+  const size_t base = pk_smem_bytes(0, 0);
+  if ((size_t)h->pk_smem_max < base + xsb) return false;
+  const int ns = (int)std::min<size_t>(PK_MAX_SLOTS, ((size_t)h->pk_smem_max - base - xsb) / PK_SLOT_BYTES);
+  if (ns < 2) return false;
+  *nslot = ns;
+  *xs_floats = M * kmax;
+  return true;
+}
+
+bool pk_usable(const llm_handle* h, int B) {
+  int ns, xs;
+  // a forced projection kernel (tests that run every kernel on every shape) keeps one kernel a phase
+  return h->pk_supported && h->pk_enabled && h->lin_variant == LIN_AUTO && B >= 1 &&
+         B <= std::min(PK_MAX_M, h->cfg.max_batch) &&
+         (B == 1 || h->pk_multi) && pk_plan(h, B, &ns, &xs);
+}
+
+PKParams pk_params(const llm_handle* h, int M) {
+  const llm_config& c = h->cfg;
+  const bool gpt2 = c.arch == LLM_ARCH_GPT2;
+  PKParams p;
+  memset(&p, 0, sizeof(p));
+  p.layers = h->d_pk_layers;
+  p.n_layers = c.n_layers; p.d = c.d_model; p.H = c.n_heads; p.Hkv = c.n_kv_heads; p.F = c.d_ff;
+  p.vocab = c.vocab; p.n_ctx = c.n_ctx; p.gpt2 = gpt2 ? 1 : 0; p.eps = c.norm_eps;
+  p.tok_emb = h->tok_emb; p.tok_scale = h->tok_scale; p.pos_emb = gpt2 ? h->pos_emb : nullptr;
+  p.lnf_g = h->lnf_w; p.lnf_b = gpt2 ? h->lnf_b : nullptr;
+  p.rope_tab = h->d_rope; p.args = h->d_args;
+  p.h = h->h; p.qkv = h->pk_qkv; p.att = h->pk_att; p.ff = h->pk_ff; p.part_o = h->pk_po; p.part_ml = h->pk_ml;
+  p.max_ch = h->pk_max_ch;
+  p.head_val = h->pk_head_val; p.head_idx = h->pk_head_idx;
+  p.sync = h->pk_sync; p.flags = h->flags; p.withhold = -1;
+  pk_plan(h, M, &p.nslot, &p.xs_floats);
+  return p;
+}
+
+// Shapes and pointers the persistent kernel handles, its scratch and its layer table. Any
+// failure here only leaves the step on the graph of per-phase kernels.
+void pk_setup(llm_handle* h) {
+  const llm_config& c = h->cfg;
+  h->pk_supported = h->pk_multi = false;
+  int coop = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev) != cudaSuccess || !coop) {
+    cudaGetLastError();
+    return;
+  }
+  h->pk_smem_max = optin;
+  const bool gpt2 = c.arch == LLM_ARCH_GPT2, q8 = h->wdt == DT_Q8;
+  const int elt = h->wdt == DT_F32 ? 4 : h->wdt == DT_BF16 ? 2 : 1;
+  const int H = c.n_heads, Hkv = c.n_kv_heads, d = c.d_model, F = c.d_ff;
+  // rows are 16-byte vectors (Q8_0: scale rows too, K a multiple of 256)
+  for (int K : {d, H * HD, F})
+    if (K % 4 != 0 || (K * elt) % 16 != 0 || (q8 && K % 256 != 0)) return;
+  if (d > PK_MAX_D || H / Hkv > PK_MAX_G) return;
+  // every CTA's share of a matrix's rows fits the staged bias and residual slices
+  for (int units : {(H + 2 * Hkv) * HD, d, F})
+    if ((units + h->num_sms - 1) / h->num_sms > PK_MAX_UNITS) return;
+  auto unit = [&](int K, int rows) { return (size_t)rows * ((size_t)K * elt + (q8 ? (size_t)K / 16 : 0)); };
+  if (unit(d, gpt2 ? 1 : 2) > PK_SLOT_BYTES || unit(H * HD, 1) > PK_SLOT_BYTES || unit(F, 1) > PK_SLOT_BYTES) return;
+  auto aligned = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (!aligned(h->tok_emb) || !aligned(h->tok_scale)) return;
+  for (const LayerW& w : h->layers)
+    for (const void* p : {w.w_qkv, w.w_o, w.w_up, w.w_down, w.s_qkv, w.s_o, w.s_up, w.s_down})
+      if (!aligned(p)) return;
+  int ns, xs, nb = 0;
+  if (!pk_plan(h, 1, &ns, &xs)) return;
+  if (pk_blocks_per_sm(h->wdt, 1, pk_smem_bytes(ns, xs), &nb) != cudaSuccess || nb < 1) {
+    cudaGetLastError();
+    return;
+  }
+  const int MM = std::min(c.max_batch, PK_MAX_M);
+  if (MM > 1 && pk_plan(h, MM, &ns, &xs)) {
+    nb = 0;
+    if (pk_blocks_per_sm(h->wdt, MM, pk_smem_bytes(ns, xs), &nb) == cudaSuccess && nb >= 1) h->pk_multi = true;
+    cudaGetLastError();
+  }
+  h->pk_max_ch = (std::min(c.n_ctx, c.max_blocks_per_seq * KVB) + PK_ATT_CH - 1) / PK_ATT_CH;
+  if (dev_alloc(h, &h->pk_qkv, (size_t)MM * (H + 2 * Hkv) * HD) != LLM_OK ||
+      dev_alloc(h, &h->pk_att, (size_t)MM * H * HD) != LLM_OK || dev_alloc(h, &h->pk_ff, (size_t)MM * F) != LLM_OK ||
+      dev_alloc(h, &h->pk_po, (size_t)MM * H * h->pk_max_ch * HD) != LLM_OK ||
+      dev_alloc(h, &h->pk_ml, (size_t)MM * H * h->pk_max_ch * 2) != LLM_OK ||
+      dev_alloc(h, &h->pk_head_val, (size_t)h->num_sms * MM) != LLM_OK ||
+      dev_alloc(h, &h->pk_head_idx, (size_t)h->num_sms * MM) != LLM_OK || dev_alloc(h, &h->pk_sync, 2) != LLM_OK ||
+      dev_alloc(h, &h->d_pk_layers, (size_t)c.n_layers) != LLM_OK)
+    return;
+  std::vector<PKLayer> tab(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& w = h->layers[l];
+    PKLayer& t = tab[l];
+    memset(&t, 0, sizeof(t));
+    t.w_qkv = w.w_qkv; t.s_qkv = w.s_qkv; t.b_qkv = w.b_qkv;
+    t.w_o = w.w_o; t.s_o = w.s_o; t.b_o = w.b_o;
+    t.w_up = w.w_up; t.s_up = w.s_up; t.b_up = w.b_up;
+    t.w_down = w.w_down; t.s_down = w.s_down; t.b_down = w.b_down;
+    t.ln1_g = w.ln1_w; t.ln1_b = gpt2 ? w.ln1_b : nullptr;
+    t.ln2_g = w.ln2_w; t.ln2_b = gpt2 ? w.ln2_b : nullptr;
+    t.qn_g = w.q_norm_w; t.kn_g = w.k_norm_w;
+    t.kv = kv_layer(h, l);
+    t.window = layer_window(h, l);
+  }
+  if (cudaMemcpy(h->d_pk_layers, tab.data(), tab.size() * sizeof(PKLayer), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  h->pk_supported = true;
+  if (const char* env = getenv("LLM_PERSISTENT")) h->pk_enabled = env[0] == '1';
+}
+
+// The step as one persistent kernel, then the argmax reduction (or the sampling kernel).
+llm_status enqueue_persistent(llm_handle* h, int B, bool sample) {
+  const PKParams p = pk_params(h, B);
+  CUDA_TRY(cudaMemsetAsync(h->pk_sync, 0, 2 * sizeof(unsigned), h->stream));
+  RUN("decode_persistent", launch_decode_persistent(p, h->wdt, B, h->num_sms, h->stream));
+  if (sample) {
+    SampleParams sp{h->d_args, h->cfg.vocab, h->flags};
+    RUN("sample", launch_sample(sp, B, h->stream, h->pdl));
+    return LLM_OK;
+  }
+  ArgmaxParams amp{h->pk_head_val, h->pk_head_idx, h->num_sms, h->d_args, h->flags};
+  RUN("argmax", launch_argmax(amp, B, h->stream, h->pdl));
+  return LLM_OK;
+}
+
+// A decode step's kernels: one persistent kernel where it applies, else one kernel a phase.
+llm_status enqueue_decode(llm_handle* h, int B, bool sample) {
+  if (pk_usable(h, B)) return enqueue_persistent(h, B, sample);
+  return enqueue_forward(h, B, B, false, 0, 0, sample);
+}
+
 llm_status check_handle(llm_handle* h) {
   if (!h) return fail(LLM_ERR_INVALID_ARG, "handle is NULL");
   cudaError_t e = cudaSetDevice(h->dev);
@@ -422,7 +572,7 @@ llm_status decode_step_impl(llm_handle* h, const StepArgs& a, bool sample) {
     if (e == cudaSuccess) {
       e = launch_set_args(h->d_args, a, h->stream);
       h->launch_counter++;
-      fs = e == cudaSuccess ? enqueue_forward(h, B, B, false, 0, 0, sample) : LLM_ERR_CUDA;
+      fs = e == cudaSuccess ? enqueue_decode(h, B, sample) : LLM_ERR_CUDA;
       const cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
       if (e == cudaSuccess) e = ee;
     }
@@ -445,20 +595,28 @@ llm_status decode_step_impl(llm_handle* h, const StepArgs& a, bool sample) {
   if (!h->use_graphs || h->profiling) {
     CUDA_TRY(launch_set_args(h->d_args, a, h->stream));
     h->launch_counter++;
-    st = enqueue_forward(h, B, B, false, 0, 0, sample);
+    st = enqueue_decode(h, B, sample);
     end_call(h);
     return st;
   }
-  const int key = B | (sample ? (1 << 24) : 0);
+  const bool pk = pk_usable(h, B);
+  const int key = B | (sample ? (1 << 24) : 0) | (pk ? (1 << 25) : 0);
   auto it = h->graphs.find(key);
   if (it == h->graphs.end()) {
     GraphEntry ge;
     CUDA_TRY(cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
     cudaError_t e = launch_set_args(h->d_args, a, h->stream);
     h->launch_counter++;
-    llm_status fs = e == cudaSuccess ? enqueue_forward(h, B, B, false, 0, 0, sample) : LLM_ERR_CUDA;
+    llm_status fs = e == cudaSuccess ? enqueue_decode(h, B, sample) : LLM_ERR_CUDA;
     cudaGraph_t g = nullptr;
     cudaError_t ee = cudaStreamEndCapture(h->stream, &g);
+    if (pk && e == cudaSuccess && (fs != LLM_OK || ee != cudaSuccess)) {
+      // the persistent kernel could not be captured: the step keeps one kernel a phase
+      if (g) cudaGraphDestroy(g);
+      cudaGetLastError();
+      h->pk_supported = false;
+      return decode_step_impl(h, a, sample);
+    }
     if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("set_args: ") + cudaGetErrorString(e));
     if (fs != LLM_OK) { if (g) cudaGraphDestroy(g); return fs; }
     if (ee != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("end capture: ") + cudaGetErrorString(ee));
@@ -688,6 +846,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   // (LLM_PREFILL_ATTN=1 keeps the earlier kernel, for comparisons)
   h->attn_tc2 = h->wdt == DT_BF16 && c.sliding_window == 0;
   if (const char* env = getenv("LLM_PREFILL_ATTN")) h->attn_tc2 = h->attn_tc2 && env[0] != '1';
+  pk_setup(h);
   *out = h;
   return LLM_OK;
 }
@@ -889,6 +1048,26 @@ llm_status llm_set_graphs(llm_handle* h, int enable) {
   llm_status st = check_handle(h);
   if (st != LLM_OK) return st;
   h->use_graphs = enable != 0 && stream_capturable(h->stream);
+  return LLM_OK;
+}
+
+llm_status llm_set_persistent(llm_handle* h, int enable, int* supported) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  h->pk_enabled = enable != 0;
+  if (supported) *supported = h->pk_supported ? 1 : 0;
+  return LLM_OK;
+}
+
+llm_status llm_selftest_grid_barrier(llm_handle* h) {
+  llm_status st = check_handle(h);
+  if (st != LLM_OK) return st;
+  if (!h->pk_supported) return fail(LLM_ERR_UNSUPPORTED, "the persistent decode step does not apply to this model");
+  PKParams p = pk_params(h, 1);
+  p.withhold = 0;
+  CUDA_TRY(cudaMemsetAsync(h->pk_sync, 0, 2 * sizeof(unsigned), h->stream));
+  CUDA_TRY(launch_decode_persistent(p, h->wdt, 1, h->num_sms, h->stream));
+  CUDA_TRY(cudaStreamSynchronize(h->stream));
   return LLM_OK;
 }
 
