@@ -525,7 +525,10 @@ def prefill_part(args, W, world: int, rank: int, local: int, steps: int, warmup:
         a[1] += t
     pk, pk_kind = peaks()
     gflops = prefill_gemm_flops(s, run.lengths)
-    label = "gemm_tc (tcgen05 projections)"
+    # the SM-pair kernel (default for prefill) or the one-SM kernel; the stored DRAM traffic
+    # belongs to the kernel it was captured on
+    pair = any(name.startswith("gemm_tc2") for name in stats)
+    label = "gemm_tc2 (tcgen05 projections on SM pairs)" if pair else "gemm_tc (tcgen05 projections)"
     roof = None
     if "gemm_tc" in fam:
         roof = family_roofline(fam, "gemm_tc", 1, ms_step, gflops, "TFLOP/s", pk["bf16_tflops"],

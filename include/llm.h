@@ -320,7 +320,9 @@ llm_status llm_selftest_grid_barrier(llm_handle* h);
  * GEMV, 2 = CUDA-core tiled GEMM, 3 = tcgen05 GEMM with the activation rows on the
  * MMA's M side (bf16 models; falls back to 2 where it does not apply), 4 = tcgen05
  * GEMM with the weight rows on the MMA's M side (at most 256 activation rows; bf16,
- * or fp32 as three tf32 products; falls back to 3 / 2). For tests that force every
+ * or fp32 as three tf32 products; falls back to 3 / 2), 5 = tcgen05 GEMM on SM pairs
+ * (cta_group::2: 256 weight rows a tile split over the two CTAs of a cluster; bf16 models,
+ * falls back to 2; the default for more than 256 rows, LLM_GEMM_PAIR=0 keeps 3). For tests that force every
  * kernel on every shape: a variant other than 0 also keeps decode steps off the persistent
  * kernel (llm_set_persistent). Drops cached graphs. Errors: INVALID_ARG for another value. */
 llm_status llm_set_linear_variant(llm_handle* h, int variant);
@@ -334,9 +336,10 @@ llm_status llm_set_linear_variant(llm_handle* h, int variant);
  * (the library keeps the activations of bf16-weight models as such pairs).
  * variant: 1 CUDA-core GEMV, 2 CUDA-core tiled GEMM, 3 tcgen05 GEMM (bf16 only),
  * 4 tcgen05 GEMM with the weights on the MMA's M side (M <= 256; bf16, or fp32 as
- * three tf32 products). Variants 3 and 4 need K % 8 == 0. Enqueued on `cuda_stream`.
- * Errors: INVALID_ARG (bad sizes, NULL, K % 8 for variants 3/4, M > 256 for 4),
- * UNSUPPORTED (variant 3 with fp32), CUDA. */
+ * three tf32 products), 5 tcgen05 GEMM on SM pairs (bf16 only). Variants 3, 4 and 5 need
+ * K % 8 == 0. Enqueued on `cuda_stream`.
+ * Errors: INVALID_ARG (bad sizes, NULL, K % 8 for variants 3/4/5, M > 256 for 4),
+ * UNSUPPORTED (variant 3 or 5 with fp32), CUDA. */
 llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const void* w, const void* bias, float* y,
                          int variant, void* cuda_stream);
 

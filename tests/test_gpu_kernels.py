@@ -31,13 +31,13 @@ def bf16_pair(x):
     return np.concatenate([hi_bits, lo_bits], axis=1), val
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3, 4], ids=["gemv", "simt", "tcgen05", "tcgen05-swap"])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5], ids=["gemv", "simt", "tcgen05", "tcgen05-swap", "tcgen05-pair"])
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_linear_kernel_matches_oracle(gpu_lib, variant, bf16, M, N, K):
     import torch
-    if variant == 3 and not bf16:
-        pytest.skip("tcgen05 path is bf16 only")
+    if variant in (3, 5) and not bf16:
+        pytest.skip("tcgen05 paths with activations on N are bf16 only")
     if variant == 1 and M > 64:
         pytest.skip("the weight-stream GEMV serves decode row counts")
     if variant == 4 and M > 256:

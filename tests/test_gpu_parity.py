@@ -38,7 +38,7 @@ def _oracle_rows(model, run, stream):
     return [oracle_teacher(model, run.prompts[b], stream[:, b]) for b in range(run.B)]
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3, 4], ids=["gemv", "simt", "tcgen05", "tcgen05-swap"])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5], ids=["gemv", "simt", "tcgen05", "tcgen05-swap", "tcgen05-pair"])
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
 def test_small_model_matches_oracle(gpu_lib, small_models, shape, variant):
     from transformer_decoder_forward_gb300.runner import WorkloadRun

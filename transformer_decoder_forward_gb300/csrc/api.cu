@@ -121,6 +121,7 @@ struct llm_handle {
   bool pdl = true;   // programmatic dependent launch between the step's kernels
   bool attn_tc2 = false;   // prefill attention: the warp-specialised kernel (256-row items)
   int lin_variant = LIN_AUTO;
+  bool gemm_pair = true;   // prefill projections on SM pairs (LLM_GEMM_PAIR=0: one SM a tile)
   std::map<int, GraphEntry> graphs;
   // one-kernel decode step (decode batches of at most PK_MAX_M rows)
   bool pk_supported = false;   // shapes, alignment and residency allow it
@@ -222,14 +223,21 @@ int pick_variant(const llm_handle* h, const LinearParams& p) {
   if (p.M >= 192 && p.N >= 32 * 128 && gemm_tc_supported(p)) return LIN_TC;
   if (p.M <= 256 && gemm_tc_swap_supported(p)) return LIN_TC_SWAP;
   if (p.M <= 64) return LIN_GEMV;
-  if (gemm_tc_supported(p)) return LIN_TC;
+  // more than 256 rows (prefill): the SM-pair kernel halves the shared-memory bytes per MMA
+  if (gemm_tc_supported(p)) return h->gemm_pair ? LIN_TC_PAIR : LIN_TC;
   return LIN_SIMT;
 }
 
 llm_status linear_v(llm_handle* h, const char* tag, const LinearParams& p, int v) {
-  std::string name = std::string(v == LIN_GEMV ? "gemv_" : v == LIN_TC ? "gemm_tc_" : v == LIN_TC_SWAP ? "gemm_tcs_" : "gemm_simt_") + tag;
+  std::string name = std::string(v == LIN_GEMV      ? "gemv_"
+                                 : v == LIN_TC      ? "gemm_tc_"
+                                 : v == LIN_TC_PAIR ? "gemm_tc2_"
+                                 : v == LIN_TC_SWAP ? "gemm_tcs_"
+                                                    : "gemm_simt_") +
+                     tag;
   if (v == LIN_GEMV) RUN(name.c_str(), launch_gemv(p, h->num_sms, h->stream, h->pdl));
   else if (v == LIN_TC) RUN(name.c_str(), launch_gemm_tc(p, h->num_sms, h->stream, h->pdl));
+  else if (v == LIN_TC_PAIR) RUN(name.c_str(), launch_gemm_tc2(p, h->num_sms, h->stream, h->pdl));
   else if (v == LIN_TC_SWAP) RUN(name.c_str(), launch_gemm_tc_swap(p, h->num_sms, h->stream, h->pdl));
   else RUN(name.c_str(), launch_gemm_simt(p, h->stream, h->pdl));
   return LLM_OK;
@@ -238,7 +246,7 @@ llm_status linear_v(llm_handle* h, const char* tag, const LinearParams& p, int v
 llm_status linear(llm_handle* h, const char* tag, LinearParams p) {
   int v = pick_variant(h, p);
   if (v == LIN_TC_SWAP && !gemm_tc_swap_supported(p)) v = gemm_tc_supported(p) ? LIN_TC : LIN_SIMT;
-  if (v == LIN_TC && !gemm_tc_supported(p)) v = LIN_SIMT;
+  if ((v == LIN_TC || v == LIN_TC_PAIR) && !gemm_tc_supported(p)) v = LIN_SIMT;
   return linear_v(h, tag, p, v);
 }
 
@@ -846,6 +854,7 @@ llm_status llm_create(const llm_config* cfgp, const llm_weights* wp, void* cuda_
   // (LLM_PREFILL_ATTN=1 keeps the earlier kernel, for comparisons)
   h->attn_tc2 = h->wdt == DT_BF16 && c.sliding_window == 0;
   if (const char* env = getenv("LLM_PREFILL_ATTN")) h->attn_tc2 = h->attn_tc2 && env[0] != '1';
+  if (const char* env = getenv("LLM_GEMM_PAIR")) h->gemm_pair = env[0] != '0';
   pk_setup(h);
   *out = h;
   return LLM_OK;
@@ -1076,9 +1085,10 @@ llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const vo
   if (M <= 0 || N <= 0 || K <= 0) return fail(LLM_ERR_INVALID_ARG, "sizes must be positive");
   if (!x || !w || !y) return fail(LLM_ERR_INVALID_ARG, "NULL x, w or y");
   if (dtype != LLM_DTYPE_F32 && dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_INVALID_ARG, "bad dtype");
-  if (variant < LIN_GEMV || variant > LIN_TC_SWAP) return fail(LLM_ERR_INVALID_ARG, "variant must be 1..4");
-  if (variant == LIN_TC && dtype != LLM_DTYPE_BF16) return fail(LLM_ERR_UNSUPPORTED, "tcgen05 path is bf16 only");
-  if ((variant == LIN_TC || variant == LIN_TC_SWAP) && K % 8 != 0)
+  if (variant < LIN_GEMV || variant > LIN_TC_PAIR) return fail(LLM_ERR_INVALID_ARG, "variant must be 1..5");
+  if ((variant == LIN_TC || variant == LIN_TC_PAIR) && dtype != LLM_DTYPE_BF16)
+    return fail(LLM_ERR_UNSUPPORTED, "tcgen05 path is bf16 only");
+  if ((variant == LIN_TC || variant == LIN_TC_SWAP || variant == LIN_TC_PAIR) && K % 8 != 0)
     return fail(LLM_ERR_INVALID_ARG, "tcgen05 paths need K % 8 == 0");
   if (variant == LIN_TC_SWAP && M > 256) return fail(LLM_ERR_INVALID_ARG, "weights-on-M tcgen05 path needs M <= 256");
   int dev = 0, nsm = 0;
@@ -1098,6 +1108,7 @@ llm_status llm_op_linear(int dtype, int M, int N, int K, const void* x, const vo
   cudaError_t e = variant == LIN_GEMV ? launch_gemv(p, nsm, s, false)
                   : variant == LIN_SIMT ? launch_gemm_simt(p, s, false)
                   : variant == LIN_TC   ? launch_gemm_tc(p, nsm, s, false)
+                  : variant == LIN_TC_PAIR ? launch_gemm_tc2(p, nsm, s, false)
                                         : launch_gemm_tc_swap(p, nsm, s, false);
   if (e != cudaSuccess) return fail(LLM_ERR_CUDA, std::string("llm_op_linear: ") + cudaGetErrorString(e));
   return LLM_OK;
@@ -1183,7 +1194,7 @@ llm_status llm_op_attention_decode(int kv_dtype, int B, int n_heads, int n_kv_he
 llm_status llm_set_linear_variant(llm_handle* h, int variant) {
   llm_status st = check_handle(h);
   if (st != LLM_OK) return st;
-  if (variant < LIN_AUTO || variant > LIN_TC_SWAP) return fail(LLM_ERR_INVALID_ARG, "variant must be 0..4");
+  if (variant < LIN_AUTO || variant > LIN_TC_PAIR) return fail(LLM_ERR_INVALID_ARG, "variant must be 0..5");
   CUDA_TRY(cudaStreamSynchronize(h->stream));
   for (auto& kv : h->graphs) {
     if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);

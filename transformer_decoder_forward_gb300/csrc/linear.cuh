@@ -35,13 +35,15 @@ inline int linear_tiles(const LinearParams& p) {
 //   LIN_SIMT     CUDA-core tiled GEMM
 //   LIN_TC       tcgen05 GEMM, activations on the MMA's M side (prefill, bf16)
 //   LIN_TC_SWAP  tcgen05 GEMM, weights on the MMA's M side (decode, M <= 256; bf16, or fp32 as 3 x tf32)
-enum : int { LIN_AUTO = 0, LIN_GEMV = 1, LIN_SIMT = 2, LIN_TC = 3, LIN_TC_SWAP = 4 };
+//   LIN_TC_PAIR  tcgen05 GEMM on SM pairs (cta_group::2), 256 weight rows a tile (prefill, bf16)
+enum : int { LIN_AUTO = 0, LIN_GEMV = 1, LIN_SIMT = 2, LIN_TC = 3, LIN_TC_SWAP = 4, LIN_TC_PAIR = 5 };
 
 // Each returns cudaSuccess or the launch error; `name` receives the kernel family name.
 cudaError_t launch_gemv(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
 bool gemv_norm_supported(const LinearParams& p);
 cudaError_t launch_gemm_simt(const LinearParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_gemm_tc(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
+cudaError_t launch_gemm_tc2(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);   // same support test
 bool gemm_tc_supported(const LinearParams& p);
 cudaError_t launch_gemm_tc_swap(const LinearParams& p, int num_sms, cudaStream_t s, bool pdl);
 bool gemm_tc_swap_supported(const LinearParams& p);
