@@ -68,7 +68,7 @@ TRAFFIC = {
     "gpt2-124m-fp32-b1-greedy": ("proj (gemv)", 10.185e6),
     "smollm2-360m-bf16-b64-ctx64to2048": ("proj (gemm_tcs)", 6.155e6),
     "gpt2-xl-bf16-b256-ctx1024": ("attn_decode", 3201.7e6),
-    "gpt2-124m-bf16-prefill-16x1024": ("gemm_tc (tcgen05 projections)", 182.1e6),
+    "gpt2-124m-bf16-prefill-16x1024": ("gemm_tc2 (tcgen05 projections on SM pairs)", 183.6e6),
 }
 
 
