@@ -589,7 +589,7 @@ def main():
     ap.add_argument("--prefill-workload", default=wl.W_GPT2_BF16_PREFILL.name,
                     choices=sorted(n for n, w in wl.WORKLOADS.items() if w.mode == "prefill") + ["none"],
                     help="prefill workload reported in the decode line's 'prefill' object")
-    ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--prefill-steps", type=int, default=20, help="timed prefills of the prefill object (0: none)")
     ap.add_argument("--cpu-steps", type=int, default=0, help="oracle decode steps of the CPU sample (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-dtype", default="f32", choices=["f32", "bf16"], help="element type of the KV cache")
@@ -618,7 +618,7 @@ def main():
         line = prefill_part(args, W, world, rank, local, args.steps, args.warmup)
     else:
         line = decode_part(args, W, world, rank, local)
-        if PW is not None:
+        if PW is not None and args.prefill_steps > 0:   # --prefill-steps 0: decode only
             line["prefill"] = prefill_part(args, PW, world, rank, local, args.prefill_steps, max(3, args.warmup))
     if rank == 0:
         print(json.dumps(line), flush=True)
