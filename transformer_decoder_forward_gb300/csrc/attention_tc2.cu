@@ -11,10 +11,9 @@
 //                         and write K and V alike as [keys][dims] in 128-byte swizzled rows: K is
 //                         S's K-major B operand, V P.V's MN-major B operand (a bf16 pool needs no
 //                         lo half), two stages;
-//   MMA (1 thread)        S_t = Q_t K^T as hi.hi + hi.lo + lo.hi into TMEM, and O_t += P_t V with
-//                         P_t read from TMEM, for t = 0, 1, in the order S_0(j) S_1(j)
-//                         PV_0(j) S_0(j+1) PV_1(j) S_1(j+1): while one tile's softmax runs the
-//                         tensor pipe works for the other;
+//   MMA (1 thread a tile) S_t = Q_t K^T as hi.hi + hi.lo + lo.hi into TMEM, and O_t += P_t V with
+//                         P_t read from TMEM, each tile in the order S_t(j) PV_t(j) S_t(j+1):
+//                         while one tile's softmax runs the tensor pipe works for the other;
 //   softmax (8 warps a tile, two threads a query row, 32 key columns each)
 //                         reads S from TMEM, masks, keeps the running maximum and sum (log2
 //                         units), writes P as bf16 pairs over S in TMEM. O accumulates in TMEM;
@@ -37,8 +36,8 @@ constexpr int Q2_T = 128;                 // query rows per tile (MMA M)
 constexpr int Q2_K = 64;                  // keys per block
 constexpr int Q2_CONV_WARPS = 4;
 constexpr int Q2_SM_WARPS = 8;            // softmax warps per tile
-constexpr int Q2_WARP_SM0 = 4, Q2_WARP_SM1 = 12, Q2_WARP_LOAD = 20, Q2_WARP_MMA = 21;
-constexpr int Q2_THREADS = 22 * 32;
+constexpr int Q2_WARP_SM0 = 4, Q2_WARP_SM1 = 12, Q2_WARP_LOAD = 20, Q2_WARP_MMA = 21;   // MMA: warps 21, 22
+constexpr int Q2_THREADS = 23 * 32;
 constexpr float Q2_TAU = 8.0f;            // log2 units: rescale O when the max grows past 2^8
 constexpr float Q2_SCALE_LOG2 = 0.125f * 1.4426950408889634f;   // log2(e) / sqrt(64), folded into Q
 
@@ -54,7 +53,7 @@ constexpr int OFF_RED = OFF_RAW + 2 * RAW_STAGE;
 constexpr int Q2_MAX_LB = 512;                 // staged block-table entries (8192 keys)
 constexpr int OFF_PB = OFF_RED + 2 * 2 * Q2_T * 4;
 constexpr int OFF_BAR = OFF_PB + Q2_MAX_LB * 4;
-constexpr int Q2_NBAR = 17;
+constexpr int Q2_NBAR = 18;
 constexpr size_t Q2_SMEM = 1024 + OFF_BAR + Q2_NBAR * 8 + 16;
 constexpr uint32_t Q2_TMEM_COLS = 256;         // S_0, S_1, O_0, O_1: 64 columns each
 
@@ -111,7 +110,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
   uint64_t* s_full = bars + 10;
   uint64_t* p_full = bars + 12;
   uint64_t* pv_full = bars + 14;
-  uint64_t* done_bar = bars + 16;
+  uint64_t* done_bar = bars + 16;   // one per MMA thread
   volatile int* abort_word = reinterpret_cast<volatile int*>(bars + Q2_NBAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Q2_NBAR) + 1;
   float* red = reinterpret_cast<float*>(base + OFF_RED);
@@ -142,13 +141,14 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], Q2_CONV_WARPS);
       mbar_init(&kv_full[i], Q2_CONV_WARPS);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_empty[i], 2);   // both tiles' MMA threads release a stage
       mbar_init(&q_full[i], Q2_SM_WARPS);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], Q2_SM_WARPS);
       mbar_init(&pv_full[i], 1);
     }
-    mbar_init(done_bar, 1);
+    mbar_init(&done_bar[0], 1);
+    mbar_init(&done_bar[1], 1);
     *abort_word = 0;
     mbar_fence_init();
   }
@@ -264,13 +264,17 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
         mbar_arrive(&kv_full[s]);
       }
     }
-  } else if (warp == Q2_WARP_MMA) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == Q2_WARP_MMA || warp == Q2_WARP_MMA + 1) {
+    // ---------------------------------------------------------------- MMA issuers, one a tile
+    // Issuing is the tile's critical resource (about 45 cycles a tcgen05.mma from one thread,
+    // 48 MMAs a block for both tiles), so each tile has its own thread: S_t(j), then for every
+    // block PV_t(j) once P_t(j) is written and S_t(j + 1) behind it (S overwrites P, the tensor
+    // pipe runs a thread's MMAs in order). The two threads' MMAs touch separate TMEM columns.
     if (lane == 0) {
+      const int t = warp - Q2_WARP_MMA;
       constexpr uint32_t idS = idesc_bf16(Q2_T, Q2_K);
       constexpr uint32_t idO = idesc_bf16(Q2_T, HD) | (1u << 16);   // B (V) MN-major
-      bool ok = wait_ab(&q_full[0], 0, flags, abort_word) && wait_ab(&q_full[1], 0, flags, abort_word);
-      auto issue_S = [&](int t, int j) {
+      auto issue_S = [&](int j) {
         unsigned char* cv = base + OFF_CV + (j & 1) * CV_STAGE;
         const uint64_t dq = sw128_desc(base + OFF_Q + (2 * t) * Q2_TILE);
         const uint64_t dql = sw128_desc(base + OFF_Q + (2 * t + 1) * Q2_TILE);
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
         }
         tc_commit(&s_full[t]);
       };
-      auto issue_PV = [&](int t, int j) {
+      auto issue_PV = [&](int j) {
         unsigned char* cv = base + OFF_CV + (j & 1) * CV_STAGE;
         const uint64_t dv = sw128_desc(cv + CV_VHI), dvl = sw128_desc(cv + CV_VLO);
         const uint32_t dO = tmem + (uint32_t)(128 + 64 * t), sP = tmem + (uint32_t)(64 * t);
@@ -299,36 +303,35 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
         }
         tc_commit(&pv_full[t]);
       };
-      if (ok && nkb_all > 0) {
+      bool ok = wait_ab(&q_full[t], 0, flags, abort_word);
+      int j = 0;
+      if (ok && nkb[t] > 0) {
         ok = wait_ab(&kv_full[0], 0, flags, abort_word);
         if (ok) {
           tc_fence_after();
-          if (nkb[0] > 0) issue_S(0, 0);
-          if (nkb[1] > 0) issue_S(1, 0);
+          issue_S(0);
         }
-        for (int j = 0; ok && j < nkb_all; ++j) {
-          if (j < nkb[0]) {
-            if (!(ok = wait_ab(&p_full[0], j & 1, flags, abort_word))) break;
-            tc_fence_after();
-            issue_PV(0, j);
-          }
-          if (j + 1 < nkb_all) {
+        for (; ok && j < nkb[t]; ++j) {
+          if (!(ok = wait_ab(&p_full[t], j & 1, flags, abort_word))) break;
+          tc_fence_after();
+          issue_PV(j);
+          tc_commit(&kv_empty[j & 1]);   // this tile's reads of the stage are done when these complete
+          if (j + 1 < nkb[t]) {
             if (!(ok = wait_ab(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, flags, abort_word))) break;
             tc_fence_after();
+            issue_S(j + 1);
           }
-          if (j + 1 < nkb[0]) issue_S(0, j + 1);
-          if (j < nkb[1]) {
-            if (!(ok = wait_ab(&p_full[1], j & 1, flags, abort_word))) break;
-            tc_fence_after();
-            issue_PV(1, j);
-          }
-          tc_commit(&kv_empty[j & 1]);
-          if (j + 1 < nkb[1]) issue_S(1, j + 1);
         }
       }
+      // blocks only the other tile needs: release each stage in order, once it is filled (the
+      // fill waited for this thread's earlier release of that stage)
+      for (; ok && j < nkb_all; ++j) {
+        if (!(ok = wait_ab(&kv_full[j & 1], (j >> 1) & 1, flags, abort_word))) break;
+        mbar_arrive(&kv_empty[j & 1]);
+      }
       // every MMA issued completes before the tensor memory is freed
-      tc_commit(done_bar);
-      mbar_wait(done_bar, 0, flags);
+      tc_commit(&done_bar[t]);
+      mbar_wait(&done_bar[t], 0, flags);
     }
   } else {
     // ---------------------------------------------------------------- softmax, tile t
