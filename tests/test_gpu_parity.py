@@ -73,6 +73,32 @@ def test_small_model_bf16_kv_matches_oracle(gpu_lib, small_models, shape, varian
         check_ids(ids[:, b], ref, f"{shape.name} bf16 KV seq {b}")
 
 
+# Prompts long enough that the prefill projections span several 128-row token tiles (the
+# SM-pair GEMM above 256 rows, the one-SM kernel below): SwiGLU, RoPE and the KV writes of every
+# tile, against the oracle, then a few decode steps reading those KV entries.
+LONG_LENGTHS = {"small-gpt2": np.array([120, 100, 90], dtype=np.int32),
+                "small-gpt2-bf16": np.array([120, 100, 90], dtype=np.int32),
+                "small-llama": np.array([300, 17, 200], dtype=np.int32),
+                "small-llama-f32": np.array([300, 17, 200], dtype=np.int32)}
+
+
+@pytest.mark.parametrize("variant", [0, 3], ids=["auto", "tcgen05-one-sm"])
+@pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
+def test_long_prompt_prefill_matches_oracle(gpu_lib, small_models, shape, variant):
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, model = small_models[shape.name]
+    lengths = LONG_LENGTHS[shape.name]
+    run = WorkloadRun(small_workload(shape), host_weights=w, lengths=lengths)
+    stream = wl.draw_stream(run.B, 3, shape.vocab)
+    ids, z = run_gpu_teacher(run, stream, variant=variant)
+    assert run.dec.error_flags() == 0
+    for b in range(run.B):
+        ref = oracle_teacher(model, run.prompts[b], stream[:, b])
+        check_logits(z[:, b], ref, shape.dtype, f"{shape.name} long prompt seq {b}")
+        check_ids(ids[:, b], ref, f"{shape.name} long prompt seq {b}")
+    run.close()
+
+
 def test_graph_replay_equals_eager_bitwise(gpu_lib, small_models):
     from transformer_decoder_forward_gb300.runner import WorkloadRun
     w, _ = small_models[SMALL_LLAMA.name]
