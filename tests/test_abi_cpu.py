@@ -108,6 +108,8 @@ def test_control_calls_on_a_null_handle_fail_cleanly(lib):
     assert lib.llm_set_linear_variant(None, 1) == 1
     assert lib.llm_last_launch_count(None, ctypes.byref(n)) == 1
     assert lib.llm_get_kernel_stats(None, None, 0, ctypes.byref(n), 0) == 1
+    assert lib.llm_set_persistent(None, 1, ctypes.byref(n)) == 1
+    assert lib.llm_selftest_grid_barrier(None) == 1
 
 
 def test_op_linear_checks_arguments_on_the_host(lib):
@@ -118,6 +120,9 @@ def test_op_linear_checks_arguments_on_the_host(lib):
     assert lib.llm_op_linear(7, 4, 8, 8, p, p, None, p, 1, None) == 1         # dtype
     assert lib.llm_op_linear(F32, 4, 8, 8, p, p, None, p, 0, None) == 1       # variant
     assert lib.llm_op_linear(F32, 4, 8, 8, p, p, None, p, 3, None) == 4       # tcgen05 prefill GEMM is bf16 only
+    assert lib.llm_op_linear(F32, 4, 8, 8, p, p, None, p, 5, None) == 4       # so is the SM-pair GEMM
+    assert lib.llm_op_linear(BF16, 4, 8, 8, p, p, None, p, 6, None) == 1      # no variant 6
+    assert lib.llm_op_linear(BF16, 4, 8, 12, p, p, None, p, 5, None) == 1     # K % 8
     assert lib.llm_op_linear(BF16, 4, 8, 12, p, p, None, p, 4, None) == 1     # K % 8
     assert lib.llm_op_linear(BF16, 300, 8, 16, p, p, None, p, 4, None) == 1   # weights-on-M path: M <= 256
     assert b"256" in lib.llm_last_error()
