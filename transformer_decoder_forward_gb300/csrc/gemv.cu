@@ -131,6 +131,19 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
     }
   };
   load_w(wa, da, kl * VEC);
+  // The epilogue's constants (the tile's bias, and for QKV the rows' positions and KV blocks)
+  // depend on no kernel of the step either (the step arguments were written by its first node,
+  // which has completed before any projection starts): staged before the wait, for the rows
+  // this CTA's epilogue will handle.
+  const int n0 = p.swiglu ? tile * 32 : tile * TILE_N;
+  int er0 = 0, er1 = mcount;
+  if (ks_total > 1) {
+    const int rank = (int)cg::this_cluster().block_rank();
+    const int rp = (mcount + ks_total - 1) / ks_total;
+    er0 = min(mcount, rank * rp);
+    er1 = min(mcount, er0 + rp);
+  }
+  if (er1 > er0) epi_stage<WT>(p.epi, mbase + er0, er1 - er0, n0, TILE_N, p.N, threadIdx.x, GEMV_THREADS);
   pdl_trigger();
   pdl_wait();
 
@@ -276,18 +289,15 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
     }
   }
 
-  const int n0 = p.swiglu ? tile * 32 : tile * TILE_N;
   if (ks_total == 1) {
     __syncthreads();
-    run_epilogue<WT>(p.epi, tl, TL_LD, mbase, mcount, n0, TILE_N, p.N);
+    epi_apply<WT>(p.epi, tl, TL_LD, mbase, mcount, n0, TILE_N, p.N, threadIdx.x, GEMV_THREADS);
     return;
   }
   // ---- split-K reduction across the cluster through distributed shared memory
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  const int rank = (int)cluster.block_rank();
-  const int rp = (mcount + ks_total - 1) / ks_total;
-  const int r0 = min(mcount, rank * rp), r1 = min(mcount, r0 + rp);
+  const int r0 = er0, r1 = er1;
   for (int i = threadIdx.x; i < (r1 - r0) * TILE_N; i += GEMV_THREADS) {
     const int m = r0 + i / TILE_N, c = i % TILE_N;
     float s = 0.0f;
@@ -296,7 +306,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
     red[(m - r0) * TL_LD + c] = s;
   }
   cluster.sync();   // every rank has finished reading the others' partials
-  if (r1 > r0) run_epilogue<WT>(p.epi, red, TL_LD, mbase + r0, r1 - r0, n0, TILE_N, p.N);
+  if (r1 > r0) epi_apply<WT>(p.epi, red, TL_LD, mbase + r0, r1 - r0, n0, TILE_N, p.N, threadIdx.x, GEMV_THREADS);
 }
 
 // K split (cluster size) from the weight shape only: enough CTAs to cover the SMs and an
