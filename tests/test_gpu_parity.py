@@ -54,6 +54,26 @@ def test_small_model_matches_oracle(gpu_lib, small_models, shape, variant):
     run.close()
 
 
+@pytest.mark.parametrize("shape", [SMALL_GPT2, SMALL_LLAMA], ids=["small-gpt2", "small-llama"])
+def test_many_sequences_split_decode_attention_matches_oracle(gpu_lib, small_models, shape):
+    """17 sequences of 1..110 tokens: the decode attention cuts the longer ones into 64-token
+    chunks (split kernel plus merge launch) next to sequences that fit one chunk; every sequence
+    agrees with the oracle."""
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, model = small_models[shape.name]
+    lengths = np.array([5, 17, 70, 33, 64, 65, 1, 100, 47, 16, 80, 2, 90, 31, 58, 110, 9], dtype=np.int32)
+    W = wl.Workload("small-many", shape, batch=len(lengths), prompt_len=0, decode_steps=STEPS, mode="teacher")
+    run = WorkloadRun(W, host_weights=w, lengths=lengths)
+    stream = wl.draw_stream(run.B, STEPS, shape.vocab)
+    ids, z = run_gpu_teacher(run, stream)
+    assert run.dec.error_flags() == 0
+    for b in range(run.B):
+        ref = oracle_teacher(model, run.prompts[b], stream[:, b])
+        check_logits(z[:, b], ref, shape.dtype, f"{shape.name} seq {b}")
+        check_ids(ids[:, b], ref, f"{shape.name} seq {b}")
+    run.close()
+
+
 @pytest.mark.parametrize("variant", [0, 2], ids=["auto", "simt"])
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
 def test_small_model_bf16_kv_matches_oracle(gpu_lib, small_models, shape, variant):

@@ -18,8 +18,13 @@
 //     each stage's commit is multicast to both CTAs' "empty" barriers, each tile's last to both
 //     "accumulator full" barriers.
 //   - warps 2-17: read the accumulator of this CTA's rows, hand it back by arriving on the even
-//     CTA's "accumulator empty" barrier (which counts both CTAs' epilogue warps), stage the tile
-//     transposed in shared memory and run the shared epilogue.
+//     CTA's "accumulator empty" barrier (which counts both CTAs' epilogue warps), and apply the
+//     epilogue. The element-wise kinds (stores, GELU, residual add, and the QKV epilogue without
+//     RoPE or Q/K norm) apply it straight from registers: a thread holds one output column (its
+//     TMEM lane) for 32 tokens, so for every token a warp stores 32 consecutive columns. The
+//     other kinds (SwiGLU pairs gate and up rows of different warps, RoPE pairs dims d and d + 32)
+//     stage the tile transposed in shared memory and run the shared epilogue; without the staging
+//     tile the element-wise instance keeps a 6-stage ring instead of 4.
 // Every wait is bounded (FLAG_WAIT_TIMEOUT); a cluster barrier precedes the release of the
 // tensor memory, so no CTA leaves while the pair's MMAs may still read its shared memory.
 #include <algorithm>
@@ -35,7 +40,6 @@ namespace {
 constexpr int P_BM = 128;    // tokens per tile
 constexpr int P_BN = 128;    // weight rows per CTA (256 per pair)
 constexpr int P_BK = 64;
-constexpr int P_STAGES = 4;
 constexpr int P_THREADS = 576;   // producer warp, MMA warp, 16 epilogue warps
 constexpr int P_EPI_THREADS = 512;
 constexpr int P_EPI_WARPS = P_EPI_THREADS / 32;
@@ -43,11 +47,91 @@ constexpr int P_W_STAGE = P_BN * P_BK * 2;   // bytes
 constexpr int P_X_STAGE = P_BM * P_BK * 2;
 constexpr int P_STAGE = P_W_STAGE + P_X_STAGE;   // [W rows][x_hi or x_lo rows]
 constexpr int P_OT_LD = P_BN + 1;
-constexpr size_t P_OT_BYTES = (size_t)P_BM * P_OT_LD * 4;
 constexpr int P_ACC = 2;
 constexpr int P_ACC_COLS = 2 * P_BM;   // x_hi tokens, then x_lo tokens
 constexpr uint32_t P_TMEM_COLS = P_ACC * P_ACC_COLS;
-constexpr size_t P_SMEM = 1024 + (size_t)P_STAGES * P_STAGE + P_OT_BYTES + 256;
+
+// Ring depth and the transposed staging tile of the two instances.
+template <bool DIRECT>
+struct PairCfg {
+  static constexpr int STAGES = DIRECT ? 6 : 4;
+  static constexpr size_t OT_BYTES = DIRECT ? 0 : (size_t)P_BM * P_OT_LD * 4;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * P_STAGE + OT_BYTES + 256;
+  static_assert(SMEM <= 220 * 1024, "shared memory of one CTA, with the epilogue's static staging");
+};
+
+// The epilogue kinds that need no staging tile (see the file comment).
+inline bool epi_direct_ok(const Epilogue& e) {
+  return e.kind == EPI_STORE_F32 || e.kind == EPI_STORE_ACT || e.kind == EPI_GELU || e.kind == EPI_RESID ||
+         (e.kind == EPI_QKV && !e.rope && e.qn_g == nullptr);
+}
+
+// Element-wise epilogue from registers: this thread's output column n0 + col (its TMEM lane) for
+// tokens m0 + c0 + j, j < 32, with acc[j] = x_hi.W + x_lo.W. Same arithmetic, in the same order,
+// as the staged path (epi_apply): (x_hi.W + x_lo.W) + bias.
+__device__ __forceinline__ void epi_direct(const Epilogue& e, const float* acc, int m0, int mrows, int c0, int col,
+                                           int n0, int N) {
+  const int n = n0 + col;
+  if (n >= N) return;
+  const EpiStaging& st = epi_staging();
+  const float b = st.bias[col];
+  const int jn = min(32, mrows - c0);   // tokens of this thread's quarter inside the tile
+  switch (e.kind) {
+    case EPI_STORE_F32:
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < jn) reinterpret_cast<float*>(e.out)[(size_t)(m0 + c0 + j) * e.ld_out + n] = acc[j] + b;
+      break;
+    case EPI_STORE_ACT:
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < jn) act_store<Split>(e.out, m0 + c0 + j, e.ld_out, n, acc[j] + b);
+      break;
+    case EPI_GELU:
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < jn) act_store<Split>(e.out, m0 + c0 + j, e.ld_out, n, gelu_tanh_clamped(acc[j] + b));
+      break;
+    case EPI_RESID: {
+#pragma unroll
+      for (int h = 0; h < 32; h += 16) {   // 16 loads in flight, then their stores
+        float hv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) hv[j] = h + j < jn ? e.resid[(size_t)(m0 + c0 + h + j) * e.ld_resid + n] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (h + j < jn) e.resid[(size_t)(m0 + c0 + h + j) * e.ld_resid + n] = hv[j] + acc[h + j] + b;
+      }
+      break;
+    }
+    case EPI_QKV: {   // no RoPE, no Q/K norm: q to q_out, k and v to the row's KV slot
+      const int H = e.n_heads, Hkv = e.kv.n_kv_heads;
+      const int hh = n / HD, d = n - hh * HD;
+      if (hh < H) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < jn) e.q_out[(size_t)(m0 + c0 + j) * H * HD + n] = acc[j] + b;
+        break;
+      }
+      const bool is_k = hh < H + Hkv;
+      const int g = is_k ? hh - H : hh - H - Hkv;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j >= jn) break;
+        const int m = c0 + j;
+        const int pb = st.blk[m];
+        if (pb < 0) continue;
+        const size_t off = kv_offset(e.kv, pb, g, st.pos[m] & (KVB - 1)) + d;
+        const float y = acc[j] + b;
+        if (e.kv.dtype == DT_BF16) reinterpret_cast<bf16*>(is_k ? e.kv.k : e.kv.v)[off] = __float2bfloat16_rn(y);
+        else reinterpret_cast<float*>(is_k ? e.kv.k : e.kv.v)[off] = y;
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
 
 __device__ __forceinline__ void epi_bar2() { asm volatile("bar.sync 1, %0;" ::"r"(P_EPI_THREADS) : "memory"); }
 __device__ __forceinline__ bool epi_bar2_all(bool v) {
@@ -65,15 +149,17 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
+template <bool DIRECT>
 __global__ void __launch_bounds__(P_THREADS, 1)
     k_gemm_tc2(const LinearParams p, const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo,
                const __grid_constant__ CUtensorMap tmW, int tiles_m, int tiles_n2) {
+  constexpr int P_STAGES = PairCfg<DIRECT>::STAGES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto sW = [&](int s) { return base + (size_t)s * P_STAGE; };
   auto sX = [&](int s) { return base + (size_t)s * P_STAGE + P_W_STAGE; };
-  float* ot = reinterpret_cast<float*>(base + (size_t)P_STAGES * P_STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)P_STAGES * P_STAGE + P_OT_BYTES);
+  float* ot = reinterpret_cast<float*>(base + (size_t)P_STAGES * P_STAGE);   // staged instance only
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)P_STAGES * P_STAGE + PairCfg<DIRECT>::OT_BYTES);
   uint64_t* empty = full + P_STAGES;
   uint64_t* acc_full = empty + P_STAGES;
   uint64_t* acc_empty = acc_full + P_ACC;
@@ -201,21 +287,30 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       if (!epi_bar2_all(ok)) break;   // the epilogue warps leave together
       tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * P_ACC_COLS);
+      const int c0 = quarter * 32;
+      float acc[32];
       {
-        const int c0 = quarter * 32;
         uint32_t rh[32], rl[32];
         tmem_ld32(ta + (uint32_t)c0, rh);             // x_hi . W
         tmem_ld32(ta + (uint32_t)(P_BM + c0), rl);    // x_lo . W
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ot[(c0 + j) * P_OT_LD + wrow] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+        for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+      }
+      if constexpr (!DIRECT) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ot[(c0 + j) * P_OT_LD + wrow] = acc[j];
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)(a * 8));   // the MMA may refill it
-      epi_bar2();
-      epi_apply<bf16>(p.epi, ot, P_OT_LD, m0, mrows, n0, P_BN, p.N, et, P_EPI_THREADS);
-      epi_bar2();
+      if constexpr (DIRECT) {
+        epi_direct(p.epi, acc, m0, mrows, c0, wrow, n0, p.N);
+      } else {
+        epi_bar2();
+        epi_apply<bf16>(p.epi, ot, P_OT_LD, m0, mrows, n0, P_BN, p.N, et, P_EPI_THREADS);
+      }
+      epi_bar2();   // the staging arrays (and tile) are free for the next tile
     }
   }
   tc_fence_before();
@@ -243,17 +338,20 @@ cudaError_t launch_gemm_tc2(const LinearParams& p, int num_sms, cudaStream_t s, 
   const int tiles_m = (p.M + P_BM - 1) / P_BM;
   const int pairs = std::min(tiles_m * tiles_n2, num_sms / 2);
   if (pairs < 1) return cudaErrorInvalidValue;
-  static bool attr_set_dev[MAX_DEVICES] = {};
-  bool& attr_set = attr_set_dev[current_device()];
+  const bool direct = epi_direct_ok(p.epi);
+  auto kern = direct ? k_gemm_tc2<true> : k_gemm_tc2<false>;
+  const size_t smem = direct ? PairCfg<true>::SMEM : PairCfg<false>::SMEM;
+  static bool attr_set_dev[MAX_DEVICES][2] = {};
+  bool& attr_set = attr_set_dev[current_device()][direct ? 1 : 0];
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(P_THREADS);
-  cfg.dynamicSmemBytes = P_SMEM;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -264,7 +362,7 @@ cudaError_t launch_gemm_tc2(const LinearParams& p, int num_sms, cudaStream_t s, 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_gemm_tc2, p, mx, mxl, mw, tiles_m, tiles_n2);
+  return cudaLaunchKernelEx(&cfg, kern, p, mx, mxl, mw, tiles_m, tiles_n2);
 }
 
 }  // namespace llm
