@@ -6,17 +6,21 @@
 // two 128-row query tiles of one sequence (256 consecutive query positions); 64-key blocks.
 // The roles run concurrently, joined by mbarriers:
 //   loader (1 thread)     1-D bulk copies of the block's raw K and V rows (4 paged 16-token
-//                         blocks each) into a two-stage raw ring;
+//                         blocks each) into a three-stage raw ring;
 //   converters (4 warps)  split each raw fp32 value into bf16 hi = bf16(v), lo = bf16(v - hi)
 //                         and write K and V alike as [keys][dims] in 128-byte swizzled rows: K is
 //                         S's K-major B operand, V P.V's MN-major B operand (a bf16 pool needs no
-//                         lo half), two stages;
-//   MMA (1 thread a tile) S_t = Q_t K^T as hi.hi + hi.lo + lo.hi into TMEM, and O_t += P_t V with
-//                         P_t read from TMEM, each tile in the order S_t(j) PV_t(j) S_t(j+1):
-//                         while one tile's softmax runs the tensor pipe works for the other;
+//                         lo half), three stages: S(j + 1) reads block j + 1 before P(j).V has
+//                         released block j;
+//   MMA (1 thread a tile) S_t = Q_t K^T as hi.hi + hi.lo + lo.hi into TMEM, with Q_t's hi and lo
+//                         halves as the A operand in TMEM, and O_t += P_t V with P_t read from
+//                         TMEM. S_t(j + 1) is issued as soon as the softmax has read S_t(j), so it
+//                         runs while the softmax of block j does; P_t(j).V follows once P_t(j) is
+//                         written;
 //   softmax (8 warps a tile, two threads a query row, 32 key columns each)
 //                         reads S from TMEM, masks, keeps the running maximum and sum (log2
-//                         units), writes P as bf16 pairs over S in TMEM. O accumulates in TMEM;
+//                         units), writes P as bf16 pairs into its own TMEM columns once the
+//                         previous P.V has read them. O accumulates in TMEM;
 //                         it is rescaled (read, multiplied, written back) only when a row's
 //                         maximum grows by more than 2^8 over the reference the exponentials
 //                         use, so most blocks touch O not at all.
@@ -41,21 +45,23 @@ constexpr int Q2_THREADS = 23 * 32;
 constexpr float Q2_TAU = 8.0f;            // log2 units: rescale O when the max grows past 2^8
 constexpr float Q2_SCALE_LOG2 = 0.125f * 1.4426950408889634f;   // log2(e) / sqrt(64), folded into Q
 
-constexpr int Q2_TILE = 128 * 128;        // bytes of a 128-row x 64-bf16 swizzled tile
 constexpr int Q2_HALF = 64 * 128;         // bytes of a 64-row x 64-bf16 swizzled tile
-constexpr int OFF_Q = 0;                  // [tile][hi, lo]
-constexpr int OFF_CV = OFF_Q + 4 * Q2_TILE;
+constexpr int Q2_NS = 3;                  // stages of the raw and of the converted K/V rings
+constexpr int OFF_CV = 0;
 constexpr int CV_STAGE = 4 * Q2_HALF;     // [K hi][K lo][V hi][V lo], rows = keys
 constexpr int CV_KHI = 0, CV_KLO = Q2_HALF, CV_VHI = 2 * Q2_HALF, CV_VLO = 3 * Q2_HALF;
-constexpr int OFF_RAW = OFF_CV + 2 * CV_STAGE;
+constexpr int OFF_RAW = OFF_CV + Q2_NS * CV_STAGE;
 constexpr int RAW_STAGE = 2 * Q2_K * HD * 4;   // K rows then V rows (fp32 size; bf16 uses half)
-constexpr int OFF_RED = OFF_RAW + 2 * RAW_STAGE;
+constexpr int OFF_RED = OFF_RAW + Q2_NS * RAW_STAGE;
 constexpr int Q2_MAX_LB = 512;                 // staged block-table entries (8192 keys)
-constexpr int OFF_PB = OFF_RED + 2 * 2 * Q2_T * 4;
+constexpr int OFF_PB = OFF_RED + 2 * 2 * 2 * Q2_T * 4;   // [block parity][tile][half][row]
 constexpr int OFF_BAR = OFF_PB + Q2_MAX_LB * 4;
-constexpr int Q2_NBAR = 18;
+constexpr int Q2_NBAR = 4 * Q2_NS + 12;
 constexpr size_t Q2_SMEM = 1024 + OFF_BAR + Q2_NBAR * 8 + 16;
-constexpr uint32_t Q2_TMEM_COLS = 256;         // S_0, S_1, O_0, O_1: 64 columns each
+// tensor memory: tile t owns columns 256 t .. 256 t + 255: S (fp32, 64 keys), P (bf16 pairs: hi
+// in 32 columns, lo in 32), O (fp32, 64 dims), Q (bf16 pairs: hi 32 columns, lo 32)
+constexpr uint32_t Q2_TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_P = 64, TM_O = 128, TM_Q = 192;
 
 __device__ __forceinline__ uint32_t sw_off2(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -103,14 +109,15 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + OFF_BAR);
   uint64_t* raw_full = bars + 0;
-  uint64_t* raw_empty = bars + 2;
-  uint64_t* kv_full = bars + 4;
-  uint64_t* kv_empty = bars + 6;
-  uint64_t* q_full = bars + 8;
-  uint64_t* s_full = bars + 10;
-  uint64_t* p_full = bars + 12;
-  uint64_t* pv_full = bars + 14;
-  uint64_t* done_bar = bars + 16;   // one per MMA thread
+  uint64_t* raw_empty = raw_full + Q2_NS;
+  uint64_t* kv_full = raw_empty + Q2_NS;
+  uint64_t* kv_empty = kv_full + Q2_NS;
+  uint64_t* q_full = kv_empty + Q2_NS;   // per tile, from here on
+  uint64_t* s_full = q_full + 2;
+  uint64_t* s_free = s_full + 2;         // the softmax has read S(j): S(j + 1) may overwrite it
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_full = p_full + 2;
+  uint64_t* done_bar = pv_full + 2;      // one per MMA thread
   volatile int* abort_word = reinterpret_cast<volatile int*>(bars + Q2_NBAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Q2_NBAR) + 1;
   float* red = reinterpret_cast<float*>(base + OFF_RED);
@@ -137,13 +144,16 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
     tmem_relinquish();
   }
   if (tid == 32) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < Q2_NS; ++i) {
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], Q2_CONV_WARPS);
       mbar_init(&kv_full[i], Q2_CONV_WARPS);
       mbar_init(&kv_empty[i], 2);   // both tiles' MMA threads release a stage
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], Q2_SM_WARPS);
       mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], Q2_SM_WARPS);
       mbar_init(&p_full[i], Q2_SM_WARPS);
       mbar_init(&pv_full[i], 1);
     }
@@ -173,10 +183,10 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
     if (lane == 0) {
       const KT* kpool = reinterpret_cast<const KT*>(p.kv.k);
       const KT* vpool = reinterpret_cast<const KT*>(p.kv.v);
-      int last[2] = {-1, -1};
+      int last[Q2_NS] = {-1, -1, -1};
       for (int j = 0; j < nkb_all; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !wait_ab(&raw_empty[s], ((j >> 1) - 1) & 1, flags, abort_word)) break;
+        const int s = j % Q2_NS;
+        if (j >= Q2_NS && !wait_ab(&raw_empty[s], ((j / Q2_NS) - 1) & 1, flags, abort_word)) break;
         unsigned char* raw = base + OFF_RAW + s * RAW_STAGE;
         int pbs[4];
         unsigned bytes = 0;
@@ -197,8 +207,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
         last[s] = j;
       }
       // copies still in flight must land before the CTA's shared memory goes away
-      for (int s = 0; s < 2; ++s)
-        if (last[s] >= 0) mbar_wait(&raw_full[s], (last[s] >> 1) & 1, flags);
+      for (int s = 0; s < Q2_NS; ++s)
+        if (last[s] >= 0) mbar_wait(&raw_full[s], (last[s] / Q2_NS) & 1, flags);
     }
   } else if (warp < Q2_CONV_WARPS) {
     // ---------------------------------------------------------------- converters
@@ -212,9 +222,10 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
     constexpr int EPC = 16 / (int)sizeof(KT);          // values of a 16-byte chunk
     constexpr int NCH = 32 / EPC;                       // chunks of the thread's 32 dims
     for (int j = 0; j < nkb_all; ++j) {
-      const int s = j & 1;
-      if (j >= 2 && !__all_sync(0xffffffffu, wait_ab(&kv_empty[s], ((j >> 1) - 1) & 1, flags, abort_word))) break;
-      if (!__all_sync(0xffffffffu, wait_ab(&raw_full[s], (j >> 1) & 1, flags, abort_word))) break;
+      const int s = j % Q2_NS;
+      if (j >= Q2_NS && !__all_sync(0xffffffffu, wait_ab(&kv_empty[s], ((j / Q2_NS) - 1) & 1, flags, abort_word)))
+        break;
+      if (!__all_sync(0xffffffffu, wait_ab(&raw_full[s], (j / Q2_NS) & 1, flags, abort_word))) break;
       const unsigned char* raw = base + OFF_RAW + s * RAW_STAGE;
       unsigned char* cv = base + OFF_CV + s * CV_STAGE;
       const int t = j * Q2_K + kr;
@@ -267,32 +278,34 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
   } else if (warp == Q2_WARP_MMA || warp == Q2_WARP_MMA + 1) {
     // ---------------------------------------------------------------- MMA issuers, one a tile
     // Issuing is the tile's critical resource (about 45 cycles a tcgen05.mma from one thread,
-    // 48 MMAs a block for both tiles), so each tile has its own thread: S_t(j), then for every
-    // block PV_t(j) once P_t(j) is written and S_t(j + 1) behind it (S overwrites P, the tensor
-    // pipe runs a thread's MMAs in order). The two threads' MMAs touch separate TMEM columns.
+    // 48 MMAs a block for both tiles), so each tile has its own thread: S_t(j + 1) as soon as the
+    // softmax has read S_t(j), P_t(j).V once P_t(j) is written. The tensor pipe runs a thread's
+    // MMAs in order, so S_t(j + 2) completing means P_t(j).V has too. The two threads' MMAs touch
+    // separate TMEM columns.
     if (lane == 0) {
       const int t = warp - Q2_WARP_MMA;
       constexpr uint32_t idS = idesc_bf16(Q2_T, Q2_K);
       constexpr uint32_t idO = idesc_bf16(Q2_T, HD) | (1u << 16);   // B (V) MN-major
+      const uint32_t tt = tmem + (uint32_t)(256 * t);
       auto issue_S = [&](int j) {
-        unsigned char* cv = base + OFF_CV + (j & 1) * CV_STAGE;
-        const uint64_t dq = sw128_desc(base + OFF_Q + (2 * t) * Q2_TILE);
-        const uint64_t dql = sw128_desc(base + OFF_Q + (2 * t + 1) * Q2_TILE);
+        unsigned char* cv = base + OFF_CV + (j % Q2_NS) * CV_STAGE;
+        const uint32_t qh = tt + TM_Q, ql = tt + TM_Q + 32;   // A: Q hi / lo, 8 columns a K step
         const uint64_t dk = sw128_desc(cv + CV_KHI), dkl = sw128_desc(cv + CV_KLO);
-        const uint32_t d = tmem + (uint32_t)(64 * t);
+        const uint32_t d = tt + TM_S;
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint64_t o2 = (uint64_t)(ks * 2);   // 32 bytes of K a step
-          tc_mma(d, dq + o2, dk + o2, idS, ks > 0 ? 1u : 0u);
-          if constexpr (!KV16) tc_mma(d, dq + o2, dkl + o2, idS, 1u);
-          tc_mma(d, dql + o2, dk + o2, idS, 1u);
+          const uint32_t ak = (uint32_t)(ks * 8);
+          tc_mma_ts(d, qh + ak, dk + o2, idS, ks > 0 ? 1u : 0u);
+          if constexpr (!KV16) tc_mma_ts(d, qh + ak, dkl + o2, idS, 1u);
+          tc_mma_ts(d, ql + ak, dk + o2, idS, 1u);
         }
         tc_commit(&s_full[t]);
       };
       auto issue_PV = [&](int j) {
-        unsigned char* cv = base + OFF_CV + (j & 1) * CV_STAGE;
+        unsigned char* cv = base + OFF_CV + (j % Q2_NS) * CV_STAGE;
         const uint64_t dv = sw128_desc(cv + CV_VHI), dvl = sw128_desc(cv + CV_VLO);
-        const uint32_t dO = tmem + (uint32_t)(128 + 64 * t), sP = tmem + (uint32_t)(64 * t);
+        const uint32_t dO = tt + TM_O, sP = tt + TM_P;
 #pragma unroll
         for (int ks = 0; ks < Q2_K / 16; ++ks) {
           const uint64_t o2 = (uint64_t)(ks * 128);   // 16 key rows of 128 bytes a step (MN-major B)
@@ -312,22 +325,24 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
           issue_S(0);
         }
         for (; ok && j < nkb[t]; ++j) {
-          if (!(ok = wait_ab(&p_full[t], j & 1, flags, abort_word))) break;
-          tc_fence_after();
-          issue_PV(j);
-          tc_commit(&kv_empty[j & 1]);   // this tile's reads of the stage are done when these complete
           if (j + 1 < nkb[t]) {
-            if (!(ok = wait_ab(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, flags, abort_word))) break;
+            const int s1 = (j + 1) % Q2_NS;
+            if (!(ok = wait_ab(&s_free[t], j & 1, flags, abort_word))) break;
+            if (!(ok = wait_ab(&kv_full[s1], ((j + 1) / Q2_NS) & 1, flags, abort_word))) break;
             tc_fence_after();
             issue_S(j + 1);
           }
+          if (!(ok = wait_ab(&p_full[t], j & 1, flags, abort_word))) break;
+          tc_fence_after();
+          issue_PV(j);
+          tc_commit(&kv_empty[j % Q2_NS]);   // this tile's reads of the stage are done when these complete
         }
       }
       // blocks only the other tile needs: release each stage in order, once it is filled (the
       // fill waited for this thread's earlier release of that stage)
       for (; ok && j < nkb_all; ++j) {
-        if (!(ok = wait_ab(&kv_full[j & 1], (j >> 1) & 1, flags, abort_word))) break;
-        mbar_arrive(&kv_empty[j & 1]);
+        if (!(ok = wait_ab(&kv_full[j % Q2_NS], (j / Q2_NS) & 1, flags, abort_word))) break;
+        mbar_arrive(&kv_empty[j % Q2_NS]);
       }
       // every MMA issued completes before the tensor memory is freed
       tc_commit(&done_bar[t]);
@@ -356,24 +371,34 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
       }
+      // dims 32 half + 2i, 2i + 1 -> column 16 half + i of the hi and of the lo half (TMEM lane r)
+      uint32_t qh[16], ql[16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint4 hi, lo;
         split8b(v + 8 * c, hi, lo);
-        *reinterpret_cast<uint4*>(base + OFF_Q + (2 * t) * Q2_TILE + sw_off2(r, 4 * half + c)) = hi;
-        *reinterpret_cast<uint4*>(base + OFF_Q + (2 * t + 1) * Q2_TILE + sw_off2(r, 4 * half + c)) = lo;
+        qh[4 * c] = hi.x; qh[4 * c + 1] = hi.y; qh[4 * c + 2] = hi.z; qh[4 * c + 3] = hi.w;
+        ql[4 * c] = lo.x; ql[4 * c + 1] = lo.y; ql[4 * c + 2] = lo.z; ql[4 * c + 3] = lo.w;
       }
-      fence_async_smem();
+      const uint32_t tq = tmem + t_lane + (uint32_t)(256 * t) + TM_Q + (uint32_t)(16 * half);
+      tmem_st16(tq, qh);
+      tmem_st16(tq + 32, ql);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full[t]);
     }
     const int qpos = qp0 + Q2_T * t + min(r, max(nqt, 1) - 1);   // rows beyond the tile repeat its last
     float m_ref = -INFINITY, l_run = 0.0f;                        // l_run: this thread's 32 key columns
     bool ok = true;
-    const uint32_t tS = tmem + t_lane + (uint32_t)(64 * t);
-    const uint32_t tO = tmem + t_lane + (uint32_t)(128 + 64 * t + 32 * half);
-    float* red_mine = red + (2 * t + half) * Q2_T;
-    float* red_other = red + (2 * t + (half ^ 1)) * Q2_T;
+    const uint32_t tS = tmem + t_lane + (uint32_t)(256 * t) + TM_S;
+    const uint32_t tP = tmem + t_lane + (uint32_t)(256 * t) + TM_P;
+    const uint32_t tO = tmem + t_lane + (uint32_t)(256 * t) + TM_O + (uint32_t)(32 * half);
+    // the maxima exchange alternates between two buffers by block parity: S(j + 1) can complete
+    // before the other half of a row has read block j's maximum, and a thread that runs ahead
+    // then writes block j + 1's into the other buffer
+    auto red_mine = [&](int j) { return red + ((j & 1) * 4 + 2 * t + half) * Q2_T; };
+    auto red_other = [&](int j) { return red + ((j & 1) * 4 + 2 * t + (half ^ 1)) * Q2_T; };
     // Every warp of the group runs every iteration and every group barrier, also after a wait
     // gave up (ok false: the work is skipped), so no warp is left waiting at a named barrier.
     for (int j = 0; j < nkb[t]; ++j) {
@@ -385,6 +410,9 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
         uint32_t sr[32];
         tmem_ld32(tS + (uint32_t)(32 * half), sr);
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[t]);   // S(j + 1) may now overwrite S(j)
         // only blocks reaching past the tile's first query need the causal mask (warp-uniform)
         if (j * Q2_K + Q2_K - 1 <= qp0 + Q2_T * t) {
 #pragma unroll
@@ -401,10 +429,10 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
           }
         }
       }
-      red_mine[r] = mb;
+      red_mine(j)[r] = mb;
       named_bar(1 + t, Q2_SM_WARPS * 32);   // both halves' maxima written; both have read S
       if (!ok) continue;
-      const float m_blk = fmaxf(mb, red_other[r]);
+      const float m_blk = fmaxf(mb, red_other(j)[r]);
       // the exponentials use the reference m_ref; it moves (and O is rescaled) only when the
       // block's maximum passes it by more than 2^8, or on the first block (key 0 is visible to
       // every row). Both threads of a row decide alike; the TMEM accesses are warp-wide, so a
@@ -412,19 +440,6 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
       const bool grow = m_blk > m_ref + Q2_TAU;
       const float m_new = grow ? m_blk : m_ref;
       const float alpha = grow ? ex2(m_ref - m_new) : 1.0f;   // m_ref = -inf: 0
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        ok = __all_sync(0xffffffffu, wait_ab(&pv_full[t], (j - 1) & 1, flags, abort_word));
-        if (!ok) continue;
-        tc_fence_after();
-        uint32_t ov[32];
-        tmem_ld32(tO, ov);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-        tmem_st16(tO, ov);
-        tmem_st16(tO + 16, ov + 16);
-        tmem_st_wait();
-      }
       l_run *= alpha;
       m_ref = m_new;
       float lsum = 0.0f;
@@ -434,19 +449,34 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
         lsum += sc[c];
       }
       l_run += lsum;
-      {   // P row r, keys 32 half .. + 31 as bf16 pairs: P_hi columns 16 half .., P_lo 32 + 16 half ..
-        uint32_t ph[16], pl[16];
+      if (j > 0) {
+        // P(j - 1).V has read the P columns and added into O before they are rewritten or O
+        // is rescaled
+        ok = __all_sync(0xffffffffu, wait_ab(&pv_full[t], (j - 1) & 1, flags, abort_word));
+        if (!ok) continue;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {
+          uint32_t ov[32];
+          tmem_ld32(tO, ov);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(sc[2 * i], sc[2 * i + 1]);
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(sc[2 * i] - __low2float(hi), sc[2 * i + 1] - __high2float(hi));
-          ph[i] = *reinterpret_cast<const uint32_t*>(&hi);
-          pl[i] = *reinterpret_cast<const uint32_t*>(&lo);
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st16(tO, ov);
+          tmem_st16(tO + 16, ov + 16);
         }
-        tmem_st16(tS + (uint32_t)(16 * half), ph);
-        tmem_st16(tS + (uint32_t)(32 + 16 * half), pl);
-        tmem_st_wait();
       }
+      uint32_t ph[16], pl[16];   // P row r, keys 32 half .. + 31 as bf16 pairs
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(sc[2 * i], sc[2 * i + 1]);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(sc[2 * i] - __low2float(hi), sc[2 * i + 1] - __high2float(hi));
+        ph[i] = *reinterpret_cast<const uint32_t*>(&hi);
+        pl[i] = *reinterpret_cast<const uint32_t*>(&lo);
+      }
+      // P_hi in columns 16 half .., P_lo in 32 + 16 half .. of the tile's P block
+      tmem_st16(tP + (uint32_t)(16 * half), ph);
+      tmem_st16(tP + (uint32_t)(32 + 16 * half), pl);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
@@ -464,10 +494,10 @@ __global__ void __launch_bounds__(Q2_THREADS, 1) k_attn_prefill_tc2(const AttnPr
         for (int c = 0; c < 32; ++c) o[c] = __uint_as_float(ov[c]);
       }
       named_bar(1 + t, Q2_SM_WARPS * 32);   // every thread is done with the maxima
-      red_mine[r] = l_run;
+      red_mine(0)[r] = l_run;
       named_bar(1 + t, Q2_SM_WARPS * 32);
       if (ok && !*abort_word && r < nqt) {
-        const float inv = 1.0f / (l_run + red_other[r]);
+        const float inv = 1.0f / (l_run + red_other(0)[r]);
         const int ld = (std::is_same<AT, Split>::value ? 2 : 1) * H * HD;
 #pragma unroll
         for (int d = 0; d < 32; d += 4) {
