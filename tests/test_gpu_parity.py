@@ -74,11 +74,13 @@ def test_many_sequences_split_decode_attention_matches_oracle(gpu_lib, small_mod
     run.close()
 
 
-@pytest.mark.parametrize("variant", [0, 2], ids=["auto", "simt"])
+@pytest.mark.parametrize("variant", [0, 2, 5], ids=["auto", "simt", "tcgen05-pair"])
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
 def test_small_model_bf16_kv_matches_oracle(gpu_lib, small_models, shape, variant):
     """A bf16 KV cache: every attention kernel (decode split-K, fp32-weight prefill tiles, tcgen05
-    prefill) reads bf16 K/V, against the oracle that stores K and V rounded to bf16."""
+    prefill) reads bf16 K/V, against the oracle that stores K and V rounded to bf16. The SM-pair
+    projections write the bf16 K/V of the QKV epilogue (straight from tensor memory for GPT-2,
+    through the staged tile with RoPE for the Llama variant)."""
     from transformer_decoder_forward_gb300.runner import WorkloadRun
     w, _ = small_models[shape.name]
     model = oracle.OracleModel(w, kv_dtype=wl.DTYPE_BF16)
