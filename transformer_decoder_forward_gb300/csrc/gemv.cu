@@ -41,7 +41,12 @@ namespace {
 constexpr int GEMV_THREADS = 256;
 constexpr int TL_LD = TILE_N + 1;   // padded row stride of the output tiles in smem
 constexpr int GEMV_MT = 16;         // rows per CTA (larger M: more CTAs along grid.x)
-constexpr int U = 2;                // weight vectors per row in flight per thread and stage
+// weight vectors per row in flight per thread and stage. One fp32 or bf16 row's accumulators
+// leave registers free for four (qkv's and o's whole slice is then loaded before the dependency
+// wait, the down projection's in three rounds instead of six: the batch-1 GPT-2 124M step 0.350 ->
+// 0.318 ms). Two otherwise, so two CTAs an SM stay resident; for Q8_0 (16 weights a vector) three
+// measured slower and four spill.
+template <typename WT, int MT> constexpr int gemv_u() { return (MT == 1 && !std::is_same<WT, Q8>::value) ? 4 : 2; }
 
 // 4 or 8 staged activations (fp32 in shared memory) into registers
 template <int VEC>
@@ -72,6 +77,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(const LinearParams p, int
   constexpr bool IS_Q8 = std::is_same<WT, Q8>::value;
   constexpr int VEC = Vec16<WT>::N;
   constexpr int STRIDE = 8 * VEC;
+  constexpr int U = gemv_u<WT, MT>();
   // grid.x = row chunk (fastest, so the chunks sharing a weight slice run together), grid.y = K split,
   // grid.z = output tile
   const int tile = blockIdx.z, ks = blockIdx.y, mbase = blockIdx.x * MT;
