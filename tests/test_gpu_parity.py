@@ -265,6 +265,42 @@ def test_device_error_flags_and_host_status(gpu_lib, small_models):
     with pytest.raises(L.LLMError) as e:
         run.dec.prefill(run.tokens, [SMALL_GPT2.n_ctx + 1], run.tables, run.next_ids)
     assert e.value.status == 2
+    # empty inputs (no sequence at all) are argument errors, refused before any launch
+    empty = torch.zeros(0, dtype=torch.int32, device=dev)
+    with pytest.raises(L.LLMError) as e:
+        run.dec.decode_step(empty, empty, run.tables, empty)
+    assert e.value.status == 1
+    with pytest.raises(L.LLMError) as e:
+        run.dec.prefill(empty, [], run.tables, run.next_ids)
+    assert e.value.status == 1
+    with pytest.raises(L.LLMError) as e:
+        run.dec.step(empty, [], [], run.tables, run.next_ids)
+    assert e.value.status == 1
+    # and the handle still runs a valid step afterwards
+    with torch.cuda.stream(run.stream):
+        run.dec.decode_step(ok_tok, run.step_positions[0], run.tables, run.next_ids)
+    torch.cuda.synchronize()
+    assert run.dec.error_flags() == 0
+    run.close()
+
+
+@pytest.mark.parametrize("shape", [SMALL_GPT2, SMALL_LLAMA], ids=["small-gpt2", "small-llama"])
+def test_context_filled_to_n_ctx_matches_oracle(gpu_lib, small_models, shape):
+    """The largest context: a prompt of n_ctx - 1 tokens, then one decode step at position
+    n_ctx - 1 (the last learned position of GPT-2, the last slot of the block table), with the
+    last 16-token block ragged for the Llama shape's prompt."""
+    from transformer_decoder_forward_gb300.runner import WorkloadRun
+    w, model = small_models[shape.name]
+    lengths = np.array([shape.n_ctx - 1, 37], dtype=np.int32)
+    W = wl.Workload("small-full", shape, batch=len(lengths), prompt_len=0, decode_steps=1, mode="teacher")
+    run = WorkloadRun(W, host_weights=w, lengths=lengths)
+    stream = wl.draw_stream(run.B, 1, shape.vocab)
+    ids, z = run_gpu_teacher(run, stream)
+    assert run.dec.error_flags() == 0
+    for b in range(run.B):
+        ref = oracle_teacher(model, run.prompts[b], stream[:, b])
+        check_logits(z[:, b], ref, shape.dtype, f"{shape.name} full-context seq {b}")
+        check_ids(ids[:, b], ref, f"{shape.name} full-context seq {b}")
     run.close()
 
 
