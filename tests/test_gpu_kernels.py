@@ -107,8 +107,11 @@ def oracle_decode_attention(q, k, v, pos, tables, H, Hkv):
 
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 @pytest.mark.parametrize("B,H,Hkv,ctx", [(1, 12, 12, 1), (3, 12, 12, 200), (5, 15, 5, 2049), (4, 8, 1, 700),
-                                         (64, 25, 25, 300)])
+                                         (64, 25, 25, 300), (80, 32, 16, 261)])
 def test_decode_attention_matches_oracle(gpu_lib, bf16, B, H, Hkv, ctx):
+    """Against the oracle on shuffled paged pools. The last two cases have enough (sequence, KV
+    head) pairs for 1024-token chunks, where one or two query heads a KV head take the 8-warp,
+    half-block instance (ctx 261: a ragged last half block)."""
     import torch
     q, k, v, pos, tables, d = make_attention_case(B, H, Hkv, ctx, bf16, seed=B + H + ctx)
     out = torch.full((B, H * 64), float("nan"), dtype=torch.float32, device="cuda")

@@ -24,20 +24,19 @@ namespace llm {
 namespace {
 
 constexpr int AD_WARPS = 4;
-constexpr int AD_THREADS = AD_WARPS * 32;
 constexpr int MAX_G = 8;
 constexpr int AD_MAX_BLOCKS_PER_WARP = 32;   // a split spans at most 4 * 32 blocks = 2048 tokens
 constexpr float SM_SCALE = 0.125f;          // 1/sqrt(64)
 constexpr float LOG2E = 1.4426950408889634f;
 
-// Shared-memory ring of one warp: NST stages, each one 16-token block of one KV head,
-// K then V (4 KB each in fp32, 2 KB in bf16), filled by 1-D TMA bulk copies.
-template <typename KT>
+// Shared-memory ring of one warp: NST stages, each TOK tokens (a 16-token block, or half of
+// one) of one KV head, K then V, filled by 1-D TMA bulk copies. NW warps a CTA.
+template <typename KT, int NW = AD_WARPS, int TOK = KVB>
 struct AttnRing {
-  static constexpr int BLK = KVB * HD * (int)sizeof(KT);
+  static constexpr int BLK = TOK * HD * (int)sizeof(KT);
   static constexpr int NST = sizeof(KT) == 4 ? 2 : 3;   // 64 KB (fp32) / 48 KB per CTA: three CTAs an SM
   static constexpr int WARP_BYTES = NST * 2 * BLK;
-  static constexpr size_t SMEM = (size_t)AD_WARPS * WARP_BYTES + (size_t)AD_WARPS * NST * 8;
+  static constexpr size_t SMEM = (size_t)NW * WARP_BYTES + (size_t)NW * NST * 8;
 };
 
 // Eight elements of one K or V row that lane dg (0..7) of a token row handles, as
@@ -58,7 +57,9 @@ template <> __device__ __forceinline__ void lds_row8<bf16>(const bf16* row, int 
 }
 
 // Decode attention, one CTA per (sequence b, KV head g, chunk of `split` tokens).
-// The chunk's 16-token KV blocks are dealt to the 4 warps in turn. Each warp runs its
+// The chunk's KV blocks are dealt to the NW warps in turn: 16-token blocks to 4 warps, or, for
+// many long sequences with one query head per KV head (the G = 1 GPT-2 XL shape), 8-token half
+// blocks to 8 warps (the same 64 KB ring a CTA, twice the warps streaming). Each warp runs its
 // own pipeline: lane 0 streams the warp's blocks into a ring of shared-memory stages
 // with 1-D TMA bulk copies (one mbarrier per stage), so several blocks per warp are
 // in flight without holding them in registers, while the warp computes on the oldest
@@ -68,11 +69,11 @@ template <> __device__ __forceinline__ void lds_row8<bf16>(const bf16* row, int 
 // its value row, so no probability is broadcast. Scores are kept in log2 units (q is
 // pre-scaled by log2(e)/sqrt(64)) so every exponential is one exp2. The 4 warps'
 // states are merged in shared memory at the end.
-template <typename KT, typename AT, int GMAX>
-__global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDecodeParams p) {
-  using R = AttnRing<KT>;
-  constexpr int NW = AD_WARPS, NST = R::NST;
-  constexpr int TG = 4, IT = KVB / TG;        // 4 token rows per step, 4 steps per block
+template <typename KT, typename AT, int GMAX, int NW = AD_WARPS, int TOK = KVB>
+__global__ void __launch_bounds__(NW * 32) k_attn_decode_split(const AttnDecodeParams p) {
+  using R = AttnRing<KT, NW, TOK>;
+  constexpr int NST = R::NST, NTH = NW * 32;
+  constexpr int TG = 4, IT = TOK / TG;        // 4 token rows per step, TOK / 4 steps per stage
   constexpr bool F32 = sizeof(KT) == 4;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ float s_m[NW][GMAX], s_l[NW][GMAX];
@@ -112,11 +113,11 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
     return;
   }
   const int nt = min(chunk, ctx - t0);
-  const int nblk = (nt + KVB - 1) / KVB;
-  const int nj = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;   // this warp's blocks: warp + NW*j
-  // physical block of this warp's j-th block, held by lane j
+  const int nblk = (nt + TOK - 1) / TOK;
+  const int nj = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;   // this warp's stages: warp + NW*j
+  // physical block of this warp's j-th stage, held by lane j
   int my_pb = -1;
-  if (lane < nj) my_pb = kv_block(p.kv, a->block_tables, b, t0 + (warp + NW * lane) * KVB, p.flags);
+  if (lane < nj) my_pb = kv_block(p.kv, a->block_tables, b, t0 + (warp + NW * lane) * TOK, p.flags);
 
   const KT* kbase = reinterpret_cast<const KT*>(p.kv.k);
   const KT* vbase = reinterpret_cast<const KT*>(p.kv.v);
@@ -125,7 +126,8 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
     if (lane == 0) {
       uint64_t* bar = &bars[j % NST];
       if (pb >= 0) {
-        const size_t off = kv_offset(p.kv, pb, g, 0);
+        // t0 is a multiple of 16: a half-block stage starts at slot 0 or 8 of its block
+        const size_t off = kv_offset(p.kv, pb, g, ((warp + NW * j) * TOK) & (KVB - 1));
         mbar_arrive_expect_tx(bar, 2 * R::BLK);
         bulk_g2s(const_cast<KT*>(kst(j % NST)), kbase + off, R::BLK, bar);
         bulk_g2s(const_cast<KT*>(vst(j % NST)), vbase + off, R::BLK, bar);
@@ -135,8 +137,8 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
     }
   };
   const int pre = min(NST, nj);
-  const int new_blk = (ctx - 1) / KVB - t0 / KVB;   // chunk-relative block of the new token
-  int early = 0;                                     // this warp's leading blocks older than it
+  const int new_blk = (ctx - 1 - t0) / TOK;   // chunk-relative stage of the new token
+  int early = 0;                               // this warp's leading stages older than it
   while (early < pre && warp + NW * early < new_blk) ++early;
   for (int j = 0; j < early; ++j) issue(j);
   pdl_wait();   // q and the new token's K/V come from the preceding projection
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
     if (pb >= 0) {
       const KT* K = kst(s);
       const KT* V = vst(s);
-      const int tok0 = (warp + NW * j) * KVB;   // first token of the block inside the chunk
+      const int tok0 = (warp + NW * j) * TOK;   // first token of the stage inside the chunk
       float sc[GMAX][IT];
 #pragma unroll
       for (int it = 0; it < IT; ++it) {
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode_split(const AttnDeco
   // final; otherwise the chunk's (max, sum, output) goes to the partial buffer for the
   // merge kernel.
   const int ldo = (std::is_same<AT, Split>::value ? 2 : 1) * H * HD;
-  for (int i = tid; i < G * HD; i += AD_THREADS) {
+  for (int i = tid; i < G * HD; i += NTH) {
     const int jj = i / HD, d = i - jj * HD;
     float M = -INFINITY;
 #pragma unroll
@@ -493,29 +495,41 @@ int attn_decode_split_for(int B, int n_kv_heads, int max_ctx, int num_sms) {
 
 namespace {
 
-template <typename KT, typename AT>
-cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
-  const int G = p.n_heads / p.kv.n_kv_heads;
-  auto kern = G == 1 ? k_attn_decode_split<KT, AT, 1>
-              : G == 2 ? k_attn_decode_split<KT, AT, 2>
-              : G == 3 ? k_attn_decode_split<KT, AT, 3>
-              : G == 4 ? k_attn_decode_split<KT, AT, 4>
-                       : k_attn_decode_split<KT, AT, 8>;
-  static bool attr_set_dev[MAX_DEVICES][9] = {};
-  bool* attr_set = attr_set_dev[current_device()];
-  if (!attr_set[G]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AttnRing<KT>::SMEM);
+// One split-kernel instance: set its shared-memory limit once per device, launch it and, when a
+// sequence spans several chunks, the merge.
+template <typename KT, typename AT, int GMAX, int NW, int TOK>
+cudaError_t decode_launch(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
+  using R = AttnRing<KT, NW, TOK>;
+  auto kern = k_attn_decode_split<KT, AT, GMAX, NW, TOK>;
+  static bool attr_set_dev[MAX_DEVICES] = {};
+  bool& attr_set = attr_set_dev[current_device()];
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)R::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[G] = true;
+    attr_set = true;
   }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t c1 =
-      make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(AD_THREADS), AttnRing<KT>::SMEM, s, attr, pdl);
+  cudaLaunchConfig_t c1 = make_cfg(dim3(p.B * p.kv.n_kv_heads, p.max_splits), dim3(NW * 32), R::SMEM, s, attr, pdl);
   cudaError_t e = cudaLaunchKernelEx(&c1, kern, p);
   if (e != cudaSuccess || p.max_splits == 1) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t c2 = make_cfg(dim3(p.B * p.n_heads), dim3(HD), 0, s, attr2, pdl);
   return cudaLaunchKernelEx(&c2, k_attn_decode_merge<AT>, p);
+}
+
+template <typename KT, typename AT>
+cudaError_t decode_t(const AttnDecodeParams& p, cudaStream_t s, bool pdl) {
+  const int G = p.n_heads / p.kv.n_kv_heads;
+  // 1024-token chunks (the (sequence, KV head) pairs fill the GPU several times) with one or two
+  // query heads a KV head: 8 warps on half blocks (GPT-2 XL batch 256: attention about 2% faster);
+  // elsewhere the per-stage cost of half blocks outweighs the extra warps
+  if (p.split >= 1024 && G <= 2)
+    return G == 1 ? decode_launch<KT, AT, 1, 8, KVB / 2>(p, s, pdl) : decode_launch<KT, AT, 2, 8, KVB / 2>(p, s, pdl);
+  return G == 1   ? decode_launch<KT, AT, 1, AD_WARPS, KVB>(p, s, pdl)
+         : G == 2 ? decode_launch<KT, AT, 2, AD_WARPS, KVB>(p, s, pdl)
+         : G == 3 ? decode_launch<KT, AT, 3, AD_WARPS, KVB>(p, s, pdl)
+         : G == 4 ? decode_launch<KT, AT, 4, AD_WARPS, KVB>(p, s, pdl)
+                  : decode_launch<KT, AT, 8, AD_WARPS, KVB>(p, s, pdl);
 }
 
 template <typename KT, typename AT>
