@@ -67,7 +67,7 @@ TRAFFIC = {
     "gpt2-124m-fp32-b32-teacher": ("proj (gemm_tcs)", 10.392e6),
     "gpt2-124m-fp32-b1-greedy": ("proj (gemv)", 10.17e6),
     "smollm2-360m-bf16-b64-ctx64to2048": ("proj (gemm_tcs)", 6.155e6),
-    "gpt2-xl-bf16-b256-ctx1024": ("attn_decode", 3201.7e6),
+    "gpt2-xl-bf16-b256-ctx1024": ("attn_decode", 3175.5e6),
     "gpt2-124m-bf16-prefill-16x1024": ("gemm_tc2 (tcgen05 projections on SM pairs)", 184.6e6),
 }
 
