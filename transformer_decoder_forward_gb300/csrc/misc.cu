@@ -52,26 +52,24 @@ __global__ void __launch_bounds__(ROW_THREADS) k_embed(const EmbedParams p) {
 // read with 16-byte loads; the variance pass re-reads it from L1.
 constexpr int NORM_ROWS = 8;   // rows (warps) per CTA
 
-// NORM_NV float4 per lane are held in registers: d <= 128 NORM_NV.
+// NORM_NV float4 per lane of the row are held in registers: d <= 128 NORM_NV. The gains and
+// biases sit in shared memory, so the registers hold only the row and a prefill's norm keeps
+// four CTAs (32 rows) an SM in flight instead of two.
 template <typename WT, typename AT, int NORM_NV>
 __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
+  __shared__ __align__(16) float s_g[NORM_NV * 128], s_b[NORM_NV * 128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * NORM_ROWS + warp;
   const int d4 = p.d >> 2;
   const WT* gw = reinterpret_cast<const WT*>(p.g);
   const WT* bw = reinterpret_cast<const WT*>(p.b);
   const int ld = std::is_same<AT, Split>::value ? 2 * p.d : p.d;
-  // gains / biases of this lane's columns: weights, so loaded before waiting on the producer
-  float gv[NORM_NV][4], bv[NORM_NV][4];
-#pragma unroll
-  for (int j = 0; j < NORM_NV; ++j) {
-    const int i = lane + 32 * j;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      gv[j][t] = i < d4 ? to_f32(gw[4 * i + t]) : 0.0f;
-      bv[j][t] = (i < d4 && bw) ? to_f32(bw[4 * i + t]) : 0.0f;
-    }
+  // gains / biases: weights, so staged before waiting on the producer
+  for (int i = threadIdx.x; i < p.d; i += NORM_ROWS * 32) {
+    s_g[i] = to_f32(gw[i]);
+    s_b[i] = bw ? to_f32(bw[i]) : 0.0f;
   }
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
   if (r >= p.rows) return;
@@ -85,9 +83,12 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) k_norm(const NormParams p) {
     const int i = lane + 32 * j;
     if (i >= d4) continue;
     const float xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    const float4 g4 = *reinterpret_cast<const float4*>(s_g + 4 * i);
+    const float4 b4 = *reinterpret_cast<const float4*>(s_b + 4 * i);
+    const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
     float y[4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) y[t] = norm_apply(xv[t], mean, scale, gv[j][t], bv[j][t]);
+    for (int t = 0; t < 4; ++t) y[t] = norm_apply(xv[t], mean, scale, gv[t], bv[t]);
     act_store4<AT>(p.out, r, ld, 4 * i, y);
   }
 }
@@ -140,6 +141,7 @@ cudaError_t norm_t(const NormParams& p, cudaStream_t s, bool pdl) {
   const int nv = (p.d + 127) / 128;   // registers sized for the row width
   if (nv <= 2) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 2>, p);
   if (nv <= 4) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 4>, p);
+  if (nv <= 6) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 6>, p);
   if (nv <= 8) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 8>, p);
   if (nv <= 13) return cudaLaunchKernelEx(&c, k_norm<WT, AT, 13>, p);
   return cudaLaunchKernelEx(&c, k_norm<WT, AT, ROW_NV>, p);
