@@ -58,7 +58,7 @@ template <> __device__ __forceinline__ void lds_row8<bf16>(const bf16* row, int 
 
 // Decode attention, one CTA per (sequence b, KV head g, chunk of `split` tokens).
 // The chunk's KV blocks are dealt to the NW warps in turn: 16-token blocks to 4 warps, or, for
-// many long sequences with one query head per KV head (the G = 1 GPT-2 XL shape), 8-token half
+// many long sequences with one or two query heads per KV head (the GPT-2 XL shape), 8-token half
 // blocks to 8 warps (the same 64 KB ring a CTA, twice the warps streaming). Each warp runs its
 // own pipeline: lane 0 streams the warp's blocks into a ring of shared-memory stages
 // with 1-D TMA bulk copies (one mbarrier per stage), so several blocks per warp are
@@ -67,7 +67,7 @@ template <> __device__ __forceinline__ void lds_row8<bf16>(const bf16* row, int 
 // for every query head of the group in registers. A token row is 8 lanes wide (8
 // values a lane), four token rows per warp step; the lanes that score a token weight
 // its value row, so no probability is broadcast. Scores are kept in log2 units (q is
-// pre-scaled by log2(e)/sqrt(64)) so every exponential is one exp2. The 4 warps'
+// pre-scaled by log2(e)/sqrt(64)) so every exponential is one exp2. The warps'
 // states are merged in shared memory at the end.
 template <typename KT, typename AT, int GMAX, int NW = AD_WARPS, int TOK = KVB>
 __global__ void __launch_bounds__(NW * 32) k_attn_decode_split(const AttnDecodeParams p) {
